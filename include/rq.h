@@ -1,0 +1,237 @@
+/*
+ * rq.h -- C ABI of librq.so, the quantized linear layer for GB300 (sm_103a).
+ *
+ * The operations follow the three source pages of realizar 0.8.4 (docs.rs):
+ *   [gemm.rs]  src/cuda/executor/layers/cublas_prefill/gemm.rs
+ *   [mod.rs]   src/cuda/executor/layers/cublas_prefill/mod.rs
+ *   [q6k.rs]   src/cuda/executor/q6k_gemv_indexed.rs
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers are DEVICE pointers (cudaMalloc / torch CUDA tensors) unless
+ *    the name ends in _host.  The caller owns every pointer it passes in.
+ *  - `stream` is a cudaStream_t (0 = legacy default stream).  Every call is
+ *    asynchronous and stream-ordered: nothing synchronises the host, except
+ *    rq_get_device_status and allocations on a cache miss (documented below).
+ *  - Arguments are validated on the host before anything is launched; on a
+ *    validation error nothing is launched or written and the status says why.
+ *    A failed launch returns RQ_ERR_CUDA.  No entry point traps or aborts.
+ *  - Matrices are row-major and densely packed (row stride = row length).
+ *  - Shapes: M = tokens (rows of x and y), N = output features (weight rows),
+ *    K = input features.  Quantized weights need K % 256 == 0.
+ *  - Not thread-safe per rq_ctx: one thread and one stream at a time per ctx.
+ */
+#ifndef RQ_H
+#define RQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RQ_ABI_VERSION 1
+
+typedef enum {
+    RQ_OK = 0,
+    RQ_ERR_NULL = 1,       /* a required pointer is NULL                      */
+    RQ_ERR_SHAPE = 2,      /* a size is out of range or misaligned            */
+    RQ_ERR_QTYPE = 3,      /* unsupported weight quantization type            */
+    RQ_ERR_NOT_CACHED = 4, /* reserved: a weight has no FP8 cache entry       */
+    RQ_ERR_ALLOC = 5,      /* device or host allocation failed                */
+    RQ_ERR_CUDA = 6,       /* a CUDA call or kernel launch failed             */
+    RQ_ERR_TIMEOUT = 7,    /* a kernel gave up on a pipeline wait (see below) */
+    RQ_ERR_ARCH = 8        /* device lacks sm_103 features (tcgen05, TMA)     */
+} rq_status;
+
+/* GGUF tensor type ids. */
+typedef enum { RQ_Q4K = 12, RQ_Q6K = 14 } rq_qtype;
+
+/* ABI-identical to cudaStream_t. */
+typedef struct CUstream_st *rq_stream_t;
+
+/* Opaque context: owns the FP8 weight cache, the activation FP8 scratch and
+ * the device scalars of the prefill path. */
+typedef struct rq_ctx rq_ctx;
+
+int rq_abi_version(void);
+const char *rq_status_string(rq_status s);
+
+/* ------------------------------------------------------------ context -- */
+
+/* Create a context on the current CUDA device.  Default GEMM threshold 4,
+ * or the value of the environment variable RQ_GEMM_THRESHOLD (read once,
+ * here), mirroring [mod.rs] cublas_gemm_threshold.
+ * Errors: RQ_ERR_NULL (out == NULL), RQ_ERR_ALLOC. */
+rq_status rq_ctx_create(rq_ctx **out);
+
+/* Free every buffer the context owns (FP8 weights, scratch, scalars).  The
+ * caller must make sure no work using them is still in flight.  NULL is a
+ * no-op. */
+void rq_ctx_destroy(rq_ctx *ctx);
+
+/* M at or above the threshold goes to the FP8 GEMM, below it to the GEMV
+ * ([mod.rs], cublas_gemm_threshold: "Minimum M ... to use GEMM instead of
+ * batched GEMV", default 4).  Errors: RQ_ERR_NULL, RQ_ERR_SHAPE (< 1). */
+rq_status rq_ctx_set_gemm_threshold(rq_ctx *ctx, int m_threshold);
+int rq_ctx_get_gemm_threshold(const rq_ctx *ctx);
+
+/* Host-side counters: activation-cache hits and misses of rq_linear, number
+ * of cached FP8 weights and the device bytes they hold.  Any out pointer may
+ * be NULL.  Errors: RQ_ERR_NULL (ctx). */
+rq_status rq_ctx_get_stats(const rq_ctx *ctx, int64_t *act_hits_host,
+                           int64_t *act_misses_host, int64_t *weights_host,
+                           int64_t *weight_bytes_host);
+
+/* ---------------------------------------------------- absmax + E4M3 ---- */
+
+/* Per-tensor absmax ([mod.rs], ABSMAX_REDUCE_PTX and gpu_absmax_device):
+ * *absmax_bits = IEEE bits of max_i |x[i]| over the n floats of x, starting
+ * from +0; NaNs are skipped, +-Inf count as +Inf.  The word is zeroed on
+ * `stream` first (no host copy from a stack temporary), then reduced with an
+ * unsigned atomic max, which orders non-negative floats correctly.
+ *   x: n floats (any alignment).  absmax_bits: one device word (4-aligned).
+ * Errors: RQ_ERR_NULL, RQ_ERR_SHAPE (n < 0).  n == 0 yields 0. */
+rq_status rq_absmax(const float *x, int64_t n, uint32_t *absmax_bits,
+                    rq_stream_t stream);
+
+/* Scaled FP32 -> E4M3 ([mod.rs], F32_TO_E4M3_DEVICE_SCALED_PTX): reads the
+ * absmax word A from the device, uses A' = (A == 0 ? 1 : A), s = 448 / A'
+ * (correctly rounded fp32 division), writes out[i] = E4M3(fl32(x[i] * s)) and
+ * *dequant_out = A' / 448.  Encoder rules: exponent rebias 127 -> 7, mantissa
+ * round-to-nearest-even 23 -> 3 bits, values below 2^-6 flush to 0x00,
+ * overflow saturates to sign|0x7E (+-448), 0x7F/0xFF are never produced,
+ * NaN/Inf inputs give sign(x)|0x7E and +-0 gives 0x00 (decided before the
+ * multiply).  Bit-exact with the CPU reference.
+ *   x: n floats.  out: n bytes.  dequant_out: one device float.
+ * Errors: RQ_ERR_NULL, RQ_ERR_SHAPE (n < 0). */
+rq_status rq_quant_e4m3(const float *x, int64_t n, const uint32_t *absmax_bits,
+                        uint8_t *out, float *dequant_out, rq_stream_t stream);
+
+/* ------------------------------------------------------------- GEMV ---- */
+
+/* Decode GEMV on GGUF Q4_K weights, dequantized inside the dot product
+ * ([q6k.rs], q4k_gemv_into; [mod.rs] cublas_gemm_threshold doc: batched GEMV
+ * for small M reads Q4_K directly at 0.5625 B/weight):
+ *   y[m, n] = sum_k x[m, k] * w(n, k),  0 <= m < M, 0 <= n < N.
+ *   w: N rows of K/256 Q4_K super-blocks, 144 B each (fp16 d, fp16 dmin,
+ *      12 packed 6-bit scale/min bytes, 128 bytes of 4-bit quants), rows
+ *      contiguous; 16-byte aligned.
+ *   x: f32 [M x K], 16-byte aligned.  y: f32 [M x N] (written, not added to).
+ * fp32 accumulation; agrees with the fp64 reference within
+ * 1e-4 * sum_k |x[m,k] * w(n,k)| per element.
+ * Errors: RQ_ERR_NULL, RQ_ERR_SHAPE (M not in 1..8, N < 1, K < 256,
+ * K % 256 != 0, misaligned w or x). */
+rq_status rq_q4k_gemv(const void *w, const float *x, float *y, int M, int N,
+                      int K, rq_stream_t stream);
+
+/* The same on GGUF Q6_K weights ([q6k.rs], q6k_gemv_indexed_async, which
+ * returns InvalidLaunchConfig for a null weight pointer; here the output is
+ * caller-owned, nothing is allocated):
+ *   w: N rows of K/256 Q6_K super-blocks, 210 B each (ql[128], qh[64],
+ *      16 int8 scales, fp16 d), rows contiguous; 4-byte aligned.
+ *   weight = d * scale * (q - 32), q the 6-bit quant.
+ * Errors: as rq_q4k_gemv (w need only be 4-byte aligned). */
+rq_status rq_q6k_gemv(const void *w, const float *x, float *y, int M, int N,
+                      int K, rq_stream_t stream);
+
+/* ------------------------------------------------------- FP8 prefill --- */
+
+/* FP8 weight cache ([gemm.rs], get_or_cache_fp8_weight): on the first call
+ * for (w, qtype, N, K) the packed weight is dequantized to fp32 in the fixed
+ * order w = (d*sc)*q - dmin*m (Q4_K) or (d*scale)*(q-32) (Q6_K), its absmax
+ * A_w is taken, and every weight is encoded as in rq_quant_e4m3 with
+ * 448 / A_w'.  Unlike the pages, the dequant scale A_w'/448 stays in device
+ * memory (no host read-back, no host sync); no fp32 scratch is used (the
+ * weight is decoded twice instead).  Later calls return the cached pointers.
+ *   *w_fp8: device E4M3 bytes [N x K] owned by ctx, valid until
+ *           rq_ctx_destroy.  *w_dequant: one device float owned by ctx.
+ * A miss allocates with cudaMalloc (which may synchronise the device).
+ * Errors: RQ_ERR_NULL, RQ_ERR_QTYPE, RQ_ERR_SHAPE, RQ_ERR_ALLOC. */
+rq_status rq_fp8_weight_cache(rq_ctx *ctx, rq_qtype qtype, const void *w,
+                              int N, int K, const uint8_t **w_fp8,
+                              const float **w_dequant, rq_stream_t stream);
+
+/* FP8 E4M3 GEMM with a fused fp32 epilogue ([gemm.rs],
+ * cublas_prefill_fp8_gemm: raw FP8 products, then the activation scale
+ * act_absmax/448 and the weight scale w_absmax/448, both read from device
+ * memory, with no host sync):
+ *   y[m, n] = (sum_k e4m3(x_fp8[m, k]) * e4m3(w_fp8[n, k]))
+ *             * (*x_dequant) * (*w_dequant)            for m < M, n < N.
+ * Tensor cores (tcgen05 kind::f8f6f4), fp32 accumulation; agrees with the
+ * exact reference within 2e-3*|ref| + 1e-3*rms(row of ref).
+ *   x_fp8: E4M3 [M_pad x K], M_pad = (M + 15) / 16 * 16; rows M..M_pad-1
+ *          are read but do not affect y.  16-byte aligned.
+ *   w_fp8: E4M3 [N x K], 16-byte aligned.   y: f32 [M x N]; rows >= M and
+ *          columns >= N are never written.
+ * Errors: RQ_ERR_NULL, RQ_ERR_SHAPE (M, N < 1, K < 128, K % 128 != 0,
+ * misaligned operands), RQ_ERR_CUDA. */
+rq_status rq_fp8_gemm(const uint8_t *x_fp8, const float *x_dequant,
+                      const uint8_t *w_fp8, const float *w_dequant, float *y,
+                      int M, int N, int K, rq_stream_t stream);
+
+/* Quantized linear layer with M-threshold routing ([mod.rs],
+ * cublas_gemm_threshold; [gemm.rs], cublas_prefill_gemm FP8 branch):
+ *   M <  threshold: Q4_K / Q6_K GEMV straight from the packed weights
+ *                   (M > 8 is processed 8 rows at a time);
+ *   M >= threshold: FP8 weight cache (a hit after the first call), then, on
+ *                   an activation-cache miss, absmax + E4M3 quantization of
+ *                   x into the ctx's [M_pad x K] scratch (pad rows zeroed),
+ *                   then the FP8 GEMM.
+ * The activation cache ([gemm.rs], PMAT-084 reuse across Q/K/V and gate/up)
+ * is keyed by (x, M, K, generation); rq_act_cache_invalidate bumps the
+ * generation and must be called when x's contents change in place.
+ * Errors: those of the routes taken. */
+rq_status rq_linear(rq_ctx *ctx, rq_qtype qtype, const void *w, const float *x,
+                    float *y, int M, int N, int K, rq_stream_t stream);
+
+/* Forget the cached FP8 activation (bump the generation). */
+rq_status rq_act_cache_invalidate(rq_ctx *ctx);
+
+/* ----------------------------------------------------------- tracing --- */
+
+/* Kernel-level tracing of rq_linear, the device-side counterpart of the
+ * pages' PREFILL_DETAIL_TRACE phases ([gemm.rs], cublas_prefill_fp8_gemm:
+ * absmax+convert / gemm / convert) without their host synchronisations:
+ * while tracing is on, every kernel rq_linear launches is bracketed by two
+ * CUDA events recorded on the call's stream (as external event nodes when the
+ * stream is being captured).  Kinds: */
+typedef enum {
+    RQ_TRACE_GEMV = 0,    /* Q4_K / Q6_K GEMV                         */
+    RQ_TRACE_ABSMAX = 1,  /* zeroing + absmax of the activation       */
+    RQ_TRACE_QUANT = 2,   /* activation E4M3 quantization             */
+    RQ_TRACE_GEMM = 3,    /* FP8 GEMM                                 */
+    RQ_TRACE_WCACHE = 4,  /* FP8 weight-cache build (a miss)          */
+    RQ_TRACE_KINDS = 5
+} rq_trace_kind;
+
+/* Start tracing with room for `capacity` kernels (events are created here,
+ * reused across begin/end pairs).  Kernels beyond the capacity are not
+ * traced.  Errors: RQ_ERR_NULL, RQ_ERR_SHAPE (capacity < 1),
+ * RQ_ERR_ALLOC. */
+rq_status rq_ctx_trace_begin(rq_ctx *ctx, int capacity);
+
+/* Stop tracing, wait for the traced events, and return per kind the number
+ * of kernels and their summed device time in milliseconds (arrays of
+ * RQ_TRACE_KINDS host entries; either may be NULL).  Errors: RQ_ERR_NULL,
+ * RQ_ERR_CUDA. */
+rq_status rq_ctx_trace_end(rq_ctx *ctx, int64_t *counts_host, double *ms_host);
+
+/* Synchronise `stream`, then report and clear the library's device error
+ * word: RQ_ERR_TIMEOUT if a GEMM pipeline wait exceeded its time limit (the
+ * kernel then stopped early and its output is incomplete), RQ_ERR_CUDA if
+ * the synchronisation itself failed, RQ_OK otherwise. */
+rq_status rq_get_device_status(rq_stream_t stream);
+
+/* Test hook for the timeout path: launches one block that waits on an
+ * mbarrier nothing will ever complete, with a wait limit of `limit_ns`
+ * nanoseconds, and records a timeout exactly like the GEMM would.  The
+ * caller then reads it with rq_get_device_status.  Errors: RQ_ERR_SHAPE
+ * (limit_ns outside 1 .. 10^10), RQ_ERR_CUDA. */
+rq_status rq_debug_wait_timeout(int64_t limit_ns, rq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RQ_H */

@@ -1,0 +1,442 @@
+// rq_gemm.cu -- FP8 E4M3 prefill GEMM on sm_103a tensor cores.
+//
+// realizar 0.8.4, cublas_prefill/gemm.rs, cublas_prefill_fp8_gemm: the GEMM
+// multiplies raw E4M3 codes, and the activation scale act_absmax/448 and the
+// weight scale w_absmax/448 are applied afterwards from device memory (no host
+// sync).  The pages call cuBLASLt into an f16 buffer and rescale in a second
+// kernel; here both scales are applied to the fp32 accumulator in the GEMM's
+// own epilogue, and the GEMM is hand-written:
+//
+//   Y[m, n] = (sum_k e4m3(X[m, k]) * e4m3(W[n, k])) * x_deq * w_deq
+//
+// Roles (192 threads, one CTA per SM, persistent over output tiles):
+//   warp 0      TMA producer: 128 x 128 B tiles of W and BN x 128 B tiles of
+//               X (SWIZZLE_128B) into a 4-stage shared-memory ring;
+//   warp 1      allocates TMEM, and one thread issues tcgen05.mma
+//               (kind::f8f6f4, E4M3 x E4M3 -> f32, M = 128, N = BN, K = 32)
+//               into one of two TMEM accumulators (2 x BN columns);
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//               lanes 32*(w%4)...), scale, masked coalesced f32 stores.
+// The tile's MMA M dimension is the weight rows (N of the problem) and its
+// MMA N dimension is the tokens, so M padded to 16 is a valid MMA width.
+// Every mbarrier wait is bounded by a time limit; on expiry the kernel
+// records RQ_ERR_TIMEOUT in a device word, drains its own copies and MMAs,
+// frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "rq_device.cuh"
+#include "rq_internal.h"
+
+namespace rq {
+
+__device__ unsigned int g_rq_device_error;  // bit 0: a pipeline wait timed out
+
+namespace {
+
+constexpr int kBM = 128;               // weight rows per tile (MMA M)
+constexpr int kBK = 128;               // K bytes per stage = one swizzle row
+constexpr int kStages = 4;
+constexpr int kMaxBN = 256;
+constexpr int kThreads = 192;
+constexpr int kABytes = kBM * kBK;           // 16 KB
+constexpr int kBBytesMax = kMaxBN * kBK;     // 32 KB
+constexpr int kSmemBytes = kStages * (kABytes + kBBytesMax) + 1024 /*barriers*/ +
+                           1024 /*alignment slack*/;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// --------------------------------------------------------- PTX wrappers --
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete, at most limit_ns.
+// Returns false (and records the timeout) if the limit expired.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer() - t0 > limit_ns) {
+      atomicOr(&g_rq_device_error, 1u);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map,
+                                            uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, K-major operand with 128-byte swizzle:
+// start address >> 4 (bits 0-13), leading byte offset 16 B (unused for this
+// layout, bits 16-29), stride byte offset 1024 B between 8-row groups
+// (bits 32-45), descriptor version 1 (bit 46), swizzle mode 2 = 128 B
+// (bits 61-63).  Tile bases are 1024-byte aligned, so the base offset is 0;
+// the K step inside the 128-byte row advances the start address by 32 B.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(16u >> 4) << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f8f6f4: D = f32 (bits 4-5 = 1), A = B = E4M3
+// (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bits
+// 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t instr_desc(int mma_m, int mma_n) {
+  return (1u << 4) | ((uint32_t)(mma_n >> 3) << 17) | ((uint32_t)(mma_m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f8(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
+        "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]),
+        "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ------------------------------------------------------------- kernel ----
+
+struct GemmArgs {
+  const float* x_deq;
+  const float* w_deq;
+  float* y;
+  int M, N, K;
+  int bn;          // tokens per tile: multiple of 16, <= 256
+  int tiles_n;     // ceil(N / 128)
+  int tiles_m;     // ceil(M_pad / bn)
+  uint32_t tmem_cols;
+  uint64_t wait_limit_ns;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                const __grid_constant__ CUtensorMap tmap_x, const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;                                  // kStages x 16 KB
+  uint8_t* sB = smem + kStages * kABytes;              // kStages x 32 KB
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBBytesMax);
+  // bars: full[kStages], empty[kStages], tfull[2], tempty[2], done[1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
+  const uint32_t tfull0 = smem_u32(bars + 2 * kStages);
+  const uint32_t tempty0 = smem_u32(bars + 2 * kStages + 2);
+  const uint32_t done_bar = smem_u32(bars + 2 * kStages + 4);
+  const int bn = args.bn;
+  const int kblocks = args.K / kBK;
+  const int ntiles = args.tiles_n * args.tiles_m;
+  const uint32_t stage_tx = (uint32_t)(kABytes + bn * kBK);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull0 + 8 * b, 1);
+      mbar_init(tempty0 + 8 * b, 4);
+    }
+    mbar_init(done_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_x)) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(args.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, last_parity = 0;  // per stage: issued, parity
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        const int tn = t / args.tiles_m, tm = t - tn * args.tiles_m;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, args.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full0 + 8 * stage;
+          mbar_arrive_expect_tx(fb, stage_tx);
+          tma_load_2d(smem_u32(sA + stage * kABytes), &tmap_w, fb, kb * kBK, tn * kBM);
+          tma_load_2d(smem_u32(sB + stage * kBBytesMax), &tmap_x, fb, kb * kBK, tm * bn);
+          issued_mask |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+      }
+      // Drain: every issued copy has landed before the CTA can exit.
+      for (int s = 0; s < kStages; ++s)
+        if (issued_mask & (1u << s))
+          mbar_wait(full0 + 8 * s, (last_parity >> s) & 1u, args.wait_limit_ns);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      const uint32_t idesc = instr_desc(kBM, bn);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, args.wait_limit_ns)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * bn);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(full0 + 8 * stage, phase, args.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + stage * kABytes);
+          const uint32_t b_addr = smem_u32(sB + stage * kBBytesMax);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 32; ++kk)
+            mma_f8(d_tmem, smem_desc(a_addr + 32 * kk), smem_desc(b_addr + 32 * kk), idesc,
+                   (kb | kk) != 0);
+          mma_commit(empty0 + 8 * stage);  // frees the stage when these MMAs finish
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        mma_commit(tfull0 + 8 * acc);  // accumulator ready for the epilogue
+        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      }
+      // Drain: all issued MMAs have completed before TMEM is released.
+      mma_commit(done_bar);
+      mbar_wait(done_bar, 0, args.wait_limit_ns);
+    }
+  } else {
+    // --------------------------------------------------------- epilogue --
+    const int quad = warp & 3;  // TMEM lanes 32*quad .. +31
+    const float scale_x = *args.x_deq, scale_w = *args.w_deq;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+      const int tn = t / args.tiles_m, tm = t - tn * args.tiles_m;
+      // every lane polls; the outcome is made warp-uniform before the
+      // .sync.aligned TMEM loads below
+      const bool ready = mbar_wait(tfull0 + 8 * acc, acc_phase, args.wait_limit_ns);
+      if (!__all_sync(0xFFFFFFFFu, ready)) break;
+      tc_fence_after();
+      const int n = tn * kBM + quad * 32 + lane;
+      const int m0 = tm * bn;
+      const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * bn);
+      for (int c = 0; c < bn; c += 16) {
+        uint32_t v[16];
+        tmem_ld16(taddr + (uint32_t)c, v);
+        if (n < args.N) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int m = m0 + c + j;
+            if (m < args.M)
+              args.y[(size_t)m * args.N + n] = (__uint_as_float(v[j]) * scale_x) * scale_w;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(args.tmem_cols)
+                 : "memory");
+  }
+}
+
+// A block that waits on an mbarrier nothing completes (timeout test hook).
+__global__ void wait_timeout_kernel(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    const uint32_t b = smem_u32(&bar);
+    mbar_init(b, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_wait(b, 0, limit_ns);
+  }
+}
+
+// ----------------------------------------------------------- host side --
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D map over a row-major [rows x K] byte matrix, box = box_rows x 128 B,
+// 128-byte swizzle, out-of-range rows read as zero.
+bool make_map(CUtensorMap* map, const void* base, int rows, int K, int box_rows) {
+  auto fn = get_encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)K};
+  const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+uint32_t tmem_columns(int bn) {
+  uint32_t need = (uint32_t)(2 * bn), c = 32;
+  while (c < need) c <<= 1;
+  return c;
+}
+
+}  // namespace
+
+rq_status launch_fp8_gemm(const uint8_t* x_fp8, const float* x_deq,
+                          const uint8_t* w_fp8, const float* w_deq, float* y,
+                          int M, int N, int K, cudaStream_t st) {
+  const int m_pad = (M + 15) / 16 * 16;
+  const int bn = m_pad < kMaxBN ? m_pad : kMaxBN;
+  CUtensorMap tw, tx;
+  if (!make_map(&tw, w_fp8, N, K, kBM) || !make_map(&tx, x_fp8, m_pad, K, bn))
+    return RQ_ERR_CUDA;
+  GemmArgs a;
+  a.x_deq = x_deq;
+  a.w_deq = w_deq;
+  a.y = y;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.bn = bn;
+  a.tiles_n = (N + kBM - 1) / kBM;
+  a.tiles_m = (m_pad + bn - 1) / bn;
+  a.tmem_cols = tmem_columns(bn);
+  a.wait_limit_ns = kWaitLimitNs;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(fp8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess)
+      return RQ_ERR_CUDA;
+    attr_done = true;
+  }
+  const int tiles = a.tiles_n * a.tiles_m;
+  const int sms = device_sm_count();
+  const int grid = tiles < sms ? tiles : sms;
+  fp8_gemm_kernel<<<grid, kThreads, kSmemBytes, st>>>(tw, tx, a);
+  return launch_status();
+}
+
+rq_status read_and_clear_device_error(cudaStream_t st) {
+  if (cudaStreamSynchronize(st) != cudaSuccess) return RQ_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_rq_device_error, sizeof(v)) != cudaSuccess)
+    return RQ_ERR_CUDA;
+  if (v == 0) return RQ_OK;
+  const unsigned int zero = 0;
+  if (cudaMemcpyToSymbol(g_rq_device_error, &zero, sizeof(zero)) != cudaSuccess)
+    return RQ_ERR_CUDA;
+  return RQ_ERR_TIMEOUT;
+}
+
+rq_status launch_debug_wait_timeout(int64_t limit_ns, cudaStream_t st) {
+  wait_timeout_kernel<<<1, 32, 0, st>>>((uint64_t)limit_ns);
+  return launch_status();
+}
+
+}  // namespace rq

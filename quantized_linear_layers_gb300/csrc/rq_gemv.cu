@@ -1,0 +1,467 @@
+// rq_gemv.cu -- decode GEMV on GGUF Q4_K / Q6_K weights, M = 1..8 tokens.
+//
+// realizar 0.8.4, q6k_gemv_indexed.rs (q4k_gemv_into and its variants,
+// q6k_gemv_indexed_async) and cublas_prefill/mod.rs (cublas_gemm_threshold:
+// the batched GEMV reads Q4_K directly at 0.5625 B/weight).  The kernel
+// bodies are not on the pages; this design is written for sm_103a:
+//
+//  * Persistent grid (SM count x resident CTAs).  Each warp owns groups of R
+//    consecutive weight rows; within a group, lane l handles the 64-weight
+//    quant groups u = l, l+32, ... of every row (one 16-byte header load and
+//    two 16-byte quant loads per row, all coalesced across the warp).  The
+//    next item's loads are issued before the current one is decoded, so two
+//    items of weight bytes are in flight per warp.
+//  * x is read through L1 (16-byte loads) once per item and reused by all R
+//    rows; the per-32-weight sums of x are computed once per CTA into shared
+//    memory (they carry the dmin*m term of Q4_K and the -32 offset of Q6_K).
+//  * Nibble -> float without int->float conversions: a byte permute places
+//    the quant q in the mantissa of 0.5 (0x3F000000), giving 0.5 + q*2^-p
+//    exactly; sum x*(0.5 + q*2^-p) - 0.5*sum x = 2^-p * sum x*q, so each
+//    weight costs one PRMT and one FFMA, and the 2^p is folded into d*sc.
+//  * fp32 accumulation, one warp-shuffle reduction per row.
+#include "rq_device.cuh"
+#include "rq_internal.h"
+
+namespace rq {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+// 0.5 + b * 2^-8 for byte b (0..63) of v placed in bits 16..23.
+__device__ __forceinline__ float mag_b2(uint32_t v, uint32_t sel) {
+  return __uint_as_float(__byte_perm(v, 0x3F000000u, sel));
+}
+// Selectors 0x7j44 give [0x3F][byte j of v][0][0] (bits 31..0) = 0.5 + b*2^-8;
+// selectors 0x74j4 give [0x3F][0][byte j][0]: a high-nibble byte 16q in bits
+// 8..15 is 0.5 + q*2^-12.
+
+template <int M>
+__device__ void x_sums(const float* __restrict__ x, int K, int span,
+                       float* __restrict__ sums) {
+  // sums[m * (K/span) + s] = sum_{i<span} x[m, s*span + i], span in {8, 32}
+  const int per = K / span;
+  for (int i = threadIdx.x; i < M * per; i += blockDim.x) {
+    const int m = i / per, s = i - m * per;
+    const float4* p = reinterpret_cast<const float4*>(x + (size_t)m * K + (size_t)s * span);
+    float acc = 0.f;
+    for (int j = 0; j < span / 4; ++j) {
+      const float4 v = __ldg(p + j);
+      acc += (v.x + v.y) + (v.z + v.w);
+    }
+    sums[i] = acc;
+  }
+}
+
+// ------------------------------------------------------------------ Q4_K --
+
+struct Q4Item {
+  uint4 h;   // d, dmin (fp16 pair) and the 12 packed scale/min bytes
+  uint4 a;   // quant bytes 0..15 of the 64-weight group
+  uint4 b;   // quant bytes 16..31
+};
+
+template <int R>
+__device__ __forceinline__ void q4_load(Q4Item (&it)[R], const uint8_t* __restrict__ W,
+                                        size_t rowbytes, int row0, int N, int u,
+                                        bool valid) {
+  const int sb = u >> 2, g = u & 3;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    if (valid && row0 + r < N) {
+      const uint8_t* p = W + (size_t)(row0 + r) * rowbytes + (size_t)sb * kQ4KBytes;
+      it[r].h = ldg_nc_v4(p);
+      it[r].a = ldg_nc_v4(p + 16 + 32 * g);
+      it[r].b = ldg_nc_v4(p + 32 + 32 * g);
+    } else {
+      it[r].h = make_uint4(0, 0, 0, 0);
+      it[r].a = it[r].h;
+      it[r].b = it[r].h;
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t q4_word(const Q4Item& it, int w) {
+  switch (w) {
+    case 0: return it.a.x; case 1: return it.a.y;
+    case 2: return it.a.z; case 3: return it.a.w;
+    case 4: return it.b.x; case 5: return it.b.y;
+    case 6: return it.b.z; default: return it.b.w;
+  }
+}
+
+// Accumulate the contribution of 64-weight group u of R rows into acc.
+template <int M, int R>
+__device__ __forceinline__ void q4_compute(const Q4Item (&it)[R], int u,
+                                           const float* __restrict__ x, int K,
+                                           const float* __restrict__ xs, int nsub,
+                                           float (&acc)[R][M]) {
+  const int sb = u >> 2, g = u & 3;
+  const int k0 = sb * kQK + 64 * g;
+  const int sh = (g & 1) * 16;     // byte pair of sub-blocks 2g, 2g+1
+  const bool upper = g >= 2;       // sub-blocks 4..7 use the split packing
+  float Alo[R], Ahi[R], Dlo[R], Dhi[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const uint32_t A = it[r].h.y, B = it[r].h.z, C = it[r].h.w;
+    const uint32_t a16 = A >> sh, b16 = B >> sh, c16 = C >> sh;
+    // 6-bit scales (scp) and mins (mp) of sub-blocks 2g (low byte), 2g+1
+    const uint32_t scp = upper ? ((c16 & 0x0F0Fu) | ((a16 >> 2) & 0x3030u)) : (a16 & 0x3F3Fu);
+    const uint32_t mp = upper ? (((c16 >> 4) & 0x0F0Fu) | ((b16 >> 2) & 0x3030u)) : (b16 & 0x3F3Fu);
+    const float2 dd = half_pair(it[r].h.x);  // .x = d, .y = dmin
+    Alo[r] = (dd.x * 256.0f) * (float)(scp & 0xFFu);
+    Ahi[r] = (dd.x * 4096.0f) * (float)((scp >> 8) & 0xFFu);
+    Dlo[r] = dd.y * (float)(mp & 0xFFu);
+    Dhi[r] = dd.y * (float)((mp >> 8) & 0xFFu);
+  }
+  float Tlo[R][M], Thi[R][M];
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int m = 0; m < M; ++m) Tlo[r][m] = Thi[r][m] = 0.f;
+
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    float4 xl[M], xh[M];
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+      const float* xr = x + (size_t)m * K + k0 + 4 * w;
+      xl[m] = __ldg(reinterpret_cast<const float4*>(xr));
+      xh[m] = __ldg(reinterpret_cast<const float4*>(xr + 32));
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const uint32_t v = q4_word(it[r], w);
+      const uint32_t lo = v & 0x0F0F0F0Fu, hi = v & 0xF0F0F0F0u;
+      const float l0 = mag_b2(lo, 0x7044u), l1 = mag_b2(lo, 0x7144u);
+      const float l2 = mag_b2(lo, 0x7244u), l3 = mag_b2(lo, 0x7344u);
+      const float h0 = mag_b2(hi, 0x7404u), h1 = mag_b2(hi, 0x7414u);
+      const float h2 = mag_b2(hi, 0x7424u), h3 = mag_b2(hi, 0x7434u);
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        float t = Tlo[r][m];
+        t = fmaf(xl[m].x, l0, t); t = fmaf(xl[m].y, l1, t);
+        t = fmaf(xl[m].z, l2, t); t = fmaf(xl[m].w, l3, t);
+        Tlo[r][m] = t;
+        float s = Thi[r][m];
+        s = fmaf(xh[m].x, h0, s); s = fmaf(xh[m].y, h1, s);
+        s = fmaf(xh[m].z, h2, s); s = fmaf(xh[m].w, h3, s);
+        Thi[r][m] = s;
+      }
+    }
+  }
+  const int sub = k0 >> 5;
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    const float Slo = xs[m * nsub + sub], Shi = xs[m * nsub + sub + 1];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      float c = Alo[r] * (Tlo[r][m] - 0.5f * Slo);
+      c = fmaf(Ahi[r], Thi[r][m] - 0.5f * Shi, c);
+      c = fmaf(-Dlo[r], Slo, c);
+      c = fmaf(-Dhi[r], Shi, c);
+      acc[r][m] += c;
+    }
+  }
+}
+
+template <int M, int R>
+__global__ void __launch_bounds__(kThreads)
+q4k_gemv_kernel(const uint8_t* __restrict__ W, const float* __restrict__ x,
+                float* __restrict__ y, int N, int K) {
+  extern __shared__ float xs[];  // [M][K/32] sums of x per 32-weight sub-block
+  const int nsb = K >> 8, U = nsb * 4, nsub = K >> 5;
+  const size_t rowbytes = (size_t)nsb * kQ4KBytes;
+  const int lane = threadIdx.x & 31;
+  const int gwarp = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  const int nwarps = gridDim.x * kWarps;
+  const int ngroups = (N + R - 1) / R;
+  const int iters = (U + 31) >> 5;
+
+  int rg = gwarp, it = 0;
+  const bool active = rg < ngroups;
+  Q4Item cur[R];
+  if (active) q4_load<R>(cur, W, rowbytes, rg * R, N, lane, lane < U);
+  x_sums<M>(x, K, 32, xs);
+  __syncthreads();
+  if (!active) return;
+
+  float acc[R][M];
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int m = 0; m < M; ++m) acc[r][m] = 0.f;
+
+  while (true) {
+    int nrg = rg, nit = it + 1;
+    if (nit == iters) { nit = 0; nrg += nwarps; }
+    const bool has_next = nrg < ngroups;
+    Q4Item nxt[R];
+    if (has_next) {
+      const int nu = nit * 32 + lane;
+      q4_load<R>(nxt, W, rowbytes, nrg * R, N, nu, nu < U);
+    }
+    const int u = it * 32 + lane;
+    if (u < U) q4_compute<M, R>(cur, u, x, K, xs, nsub, acc);
+    if (nit == 0) {  // row group rg complete
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          const float v = warp_sum(acc[r][m]);
+          acc[r][m] = 0.f;
+          if (lane == 0 && rg * R + r < N) y[(size_t)m * N + rg * R + r] = v;
+        }
+    }
+    if (!has_next) break;
+#pragma unroll
+    for (int r = 0; r < R; ++r) cur[r] = nxt[r];
+    rg = nrg;
+    it = nit;
+  }
+}
+
+// ------------------------------------------------------------------ Q6_K --
+//
+// Unit = (super-block sb, half h, l-quad lq): the 32 weights
+// 128h + 32i + 8lq + j (i = 0..3, j = 0..7), built from 8 bytes of ql at
+// 64h + 8lq, 8 bytes of ql at 64h + 32 + 8lq and 8 bytes of qh at 32h + 8lq,
+// with scales sc[8h + lq/2 + 2i].  Super-blocks are 210 bytes, so fields are
+// only 2-byte aligned; each 8-byte quant field is read as three aligned 32-bit
+// words and funnel-shifted (the third word ends at most at byte 196 of the
+// block, so it never leaves the block); the scales are read as 16-bit pairs.
+
+struct Q6Item {
+  uint32_t qa[2], qb[2], qh[2];  // ql(64h+8lq..), ql(64h+32+8lq..), qh(32h+8lq..)
+  uint32_t sc[2];                // scales 8h .. 8h+7
+  uint32_t d;                    // fp16 d in the low half
+};
+
+__device__ __forceinline__ void ld8_unaligned(const uint8_t* p, uint32_t (&out)[2]) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  const uint8_t* base = reinterpret_cast<const uint8_t*>(a & ~uintptr_t(3));
+  const uint32_t shift = (uint32_t)(a & 3) * 8;  // 0 or 16
+  const uint32_t w0 = ldg_nc_u32(base), w1 = ldg_nc_u32(base + 4), w2 = ldg_nc_u32(base + 8);
+  out[0] = __funnelshift_r(w0, w1, shift);
+  out[1] = __funnelshift_r(w1, w2, shift);
+}
+
+template <int R>
+__device__ __forceinline__ void q6_load(Q6Item (&it)[R], const uint8_t* __restrict__ W,
+                                        size_t rowbytes, int row0, int N, int u,
+                                        bool valid) {
+  const int sb = u >> 3, h = (u >> 2) & 1, lq = u & 3;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    if (valid && row0 + r < N) {
+      const uint8_t* p = W + (size_t)(row0 + r) * rowbytes + (size_t)sb * kQ6KBytes;
+      ld8_unaligned(p + 64 * h + 8 * lq, it[r].qa);
+      ld8_unaligned(p + 64 * h + 32 + 8 * lq, it[r].qb);
+      ld8_unaligned(p + 128 + 32 * h + 8 * lq, it[r].qh);
+      const uint8_t* ps = p + 192 + 8 * h;  // 8 scale bytes, 2-byte aligned
+      it[r].sc[0] = ldg_nc_u16(ps) | (ldg_nc_u16(ps + 2) << 16);
+      it[r].sc[1] = ldg_nc_u16(ps + 4) | (ldg_nc_u16(ps + 6) << 16);
+      it[r].d = ldg_nc_u16(p + 208);
+    } else {
+      it[r].qa[0] = it[r].qa[1] = it[r].qb[0] = it[r].qb[1] = 0;
+      it[r].qh[0] = it[r].qh[1] = it[r].sc[0] = it[r].sc[1] = 0;
+      it[r].d = 0;
+    }
+  }
+}
+
+__device__ __forceinline__ float sbyte(uint32_t w2[2], int i) {
+  const uint32_t word = i < 4 ? w2[0] : w2[1];
+  return (float)(int)(int8_t)((word >> (8 * (i & 3))) & 0xFFu);
+}
+
+template <int M, int R>
+__device__ __forceinline__ void q6_compute(Q6Item (&it)[R], int u,
+                                           const float* __restrict__ x, int K,
+                                           const float* __restrict__ xs, int nsub8,
+                                           float (&acc)[R][M]) {
+  const int sb = u >> 3, h = (u >> 2) & 1, lq = u & 3;
+  const int kbase = sb * kQK + 128 * h + 8 * lq;  // + 32 i + j
+  float T[R][M][4];
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int m = 0; m < M; ++m)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) T[r][m][i] = 0.f;
+
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {      // bytes j = 4*half .. 4*half+3
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {             // quarter i: weights 32i + j
+      float4 xv[M];
+#pragma unroll
+      for (int m = 0; m < M; ++m)
+        xv[m] = __ldg(reinterpret_cast<const float4*>(x + (size_t)m * K + kbase + 32 * i + 4 * half));
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const uint32_t la = it[r].qa[half], lb = it[r].qb[half], hb = it[r].qh[half];
+        uint32_t q;
+        if (i == 0) q = (la & 0x0F0F0F0Fu) | ((hb << 4) & 0x30303030u);
+        else if (i == 1) q = (lb & 0x0F0F0F0Fu) | ((hb << 2) & 0x30303030u);
+        else if (i == 2) q = ((la >> 4) & 0x0F0F0F0Fu) | (hb & 0x30303030u);
+        else q = ((lb >> 4) & 0x0F0F0F0Fu) | ((hb >> 2) & 0x30303030u);
+        const float f0 = mag_b2(q, 0x7044u), f1 = mag_b2(q, 0x7144u);
+        const float f2 = mag_b2(q, 0x7244u), f3 = mag_b2(q, 0x7344u);
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          float t = T[r][m][i];
+          t = fmaf(xv[m].x, f0, t); t = fmaf(xv[m].y, f1, t);
+          t = fmaf(xv[m].z, f2, t); t = fmaf(xv[m].w, f3, t);
+          T[r][m][i] = t;
+        }
+      }
+    }
+  }
+  // weight = d*sc*(q-32); sum_j x*(0.5 + q/256) = 0.5*S + sum x q / 256, so
+  // sum_j x*w = d*sc*(256*T - 128*S - 32*S) = d*sc*(256*T - 160*S).
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const float d = __half2float(__ushort_as_half((unsigned short)(it[r].d & 0xFFFFu)));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float dsc = d * sbyte(it[r].sc, lq / 2 + 2 * i);
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        const float S = xs[m * nsub8 + ((kbase + 32 * i) >> 3)];
+        acc[r][m] = fmaf(dsc, fmaf(256.0f, T[r][m][i], -160.0f * S), acc[r][m]);
+      }
+    }
+  }
+}
+
+template <int M, int R>
+__global__ void __launch_bounds__(kThreads)
+q6k_gemv_kernel(const uint8_t* __restrict__ W, const float* __restrict__ x,
+                float* __restrict__ y, int N, int K) {
+  extern __shared__ float xs[];  // [M][K/8] sums of x per 8 weights
+  const int nsb = K >> 8, U = nsb * 8, nsub8 = K >> 3;
+  const size_t rowbytes = (size_t)nsb * kQ6KBytes;
+  const int lane = threadIdx.x & 31;
+  const int gwarp = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  const int nwarps = gridDim.x * kWarps;
+  const int ngroups = (N + R - 1) / R;
+  const int iters = (U + 31) >> 5;
+
+  int rg = gwarp, it = 0;
+  const bool active = rg < ngroups;
+  Q6Item cur[R];
+  if (active) q6_load<R>(cur, W, rowbytes, rg * R, N, lane, lane < U);
+  x_sums<M>(x, K, 8, xs);
+  __syncthreads();
+  if (!active) return;
+
+  float acc[R][M];
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int m = 0; m < M; ++m) acc[r][m] = 0.f;
+
+  while (true) {
+    int nrg = rg, nit = it + 1;
+    if (nit == iters) { nit = 0; nrg += nwarps; }
+    const bool has_next = nrg < ngroups;
+    Q6Item nxt[R];
+    if (has_next) {
+      const int nu = nit * 32 + lane;
+      q6_load<R>(nxt, W, rowbytes, nrg * R, N, nu, nu < U);
+    }
+    const int u = it * 32 + lane;
+    if (u < U) q6_compute<M, R>(cur, u, x, K, xs, nsub8, acc);
+    if (nit == 0) {
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          const float v = warp_sum(acc[r][m]);
+          acc[r][m] = 0.f;
+          if (lane == 0 && rg * R + r < N) y[(size_t)m * N + rg * R + r] = v;
+        }
+    }
+    if (!has_next) break;
+#pragma unroll
+    for (int r = 0; r < R; ++r) cur[r] = nxt[r];
+    rg = nrg;
+    it = nit;
+  }
+}
+
+// ---------------------------------------------------------------- launch --
+
+template <typename KernelT>
+int persistent_grid(KernelT kernel, size_t smem, int ngroups) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem) !=
+          cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  const int want = (ngroups + kWarps - 1) / kWarps;
+  const int cap = device_sm_count() * per_sm;
+  return want < cap ? (want < 1 ? 1 : want) : cap;
+}
+
+template <int M, int R>
+rq_status run_q4k(const uint8_t* w, const float* x, float* y, int N, int K,
+                  cudaStream_t st) {
+  const size_t smem = (size_t)M * (K / 32) * sizeof(float);
+  auto kern = q4k_gemv_kernel<M, R>;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return RQ_ERR_CUDA;
+  const int grid = persistent_grid(kern, smem, (N + R - 1) / R);
+  kern<<<grid, kThreads, smem, st>>>(w, x, y, N, K);
+  return launch_status();
+}
+
+template <int M, int R>
+rq_status run_q6k(const uint8_t* w, const float* x, float* y, int N, int K,
+                  cudaStream_t st) {
+  const size_t smem = (size_t)M * (K / 8) * sizeof(float);
+  auto kern = q6k_gemv_kernel<M, R>;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return RQ_ERR_CUDA;
+  const int grid = persistent_grid(kern, smem, (N + R - 1) / R);
+  kern<<<grid, kThreads, smem, st>>>(w, x, y, N, K);
+  return launch_status();
+}
+
+}  // namespace
+
+rq_status launch_q4k_gemv(const uint8_t* w, const float* x, float* y, int M,
+                          int N, int K, cudaStream_t st) {
+  switch (M) {
+    case 1: return run_q4k<1, 2>(w, x, y, N, K, st);
+    case 2: return run_q4k<2, 2>(w, x, y, N, K, st);
+    case 3: return run_q4k<3, 2>(w, x, y, N, K, st);
+    case 4: return run_q4k<4, 2>(w, x, y, N, K, st);
+    case 5: return run_q4k<5, 1>(w, x, y, N, K, st);
+    case 6: return run_q4k<6, 1>(w, x, y, N, K, st);
+    case 7: return run_q4k<7, 1>(w, x, y, N, K, st);
+    case 8: return run_q4k<8, 1>(w, x, y, N, K, st);
+    default: return RQ_ERR_SHAPE;
+  }
+}
+
+rq_status launch_q6k_gemv(const uint8_t* w, const float* x, float* y, int M,
+                          int N, int K, cudaStream_t st) {
+  switch (M) {
+    case 1: return run_q6k<1, 2>(w, x, y, N, K, st);
+    case 2: return run_q6k<2, 2>(w, x, y, N, K, st);
+    case 3: return run_q6k<3, 1>(w, x, y, N, K, st);
+    case 4: return run_q6k<4, 1>(w, x, y, N, K, st);
+    case 5: return run_q6k<5, 1>(w, x, y, N, K, st);
+    case 6: return run_q6k<6, 1>(w, x, y, N, K, st);
+    case 7: return run_q6k<7, 1>(w, x, y, N, K, st);
+    case 8: return run_q6k<8, 1>(w, x, y, N, K, st);
+    default: return RQ_ERR_SHAPE;
+  }
+}
+
+}  // namespace rq

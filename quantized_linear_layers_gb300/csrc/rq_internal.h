@@ -1,0 +1,52 @@
+// rq_internal.h -- host-side interfaces between the librq translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/rq.h"
+
+namespace rq {
+
+// Map a CUDA error (or a pending launch error) to a status.
+inline rq_status cuda_status(cudaError_t e) {
+  return e == cudaSuccess ? RQ_OK : RQ_ERR_CUDA;
+}
+inline rq_status launch_status() { return cuda_status(cudaGetLastError()); }
+
+int device_sm_count();
+
+// rq_quant.cu ---------------------------------------------------------------
+// Zero *absmax_bits on the stream, then reduce max|x| into it.
+rq_status launch_absmax(const float* x, int64_t n, uint32_t* absmax_bits,
+                        cudaStream_t st);
+// Encode n elements of x with the device absmax, zero-fill out[n..n_out),
+// write the dequant scale (if non-null).
+rq_status launch_quant(const float* x, int64_t n, int64_t n_out,
+                       const uint32_t* absmax_bits, uint8_t* out,
+                       float* dequant_out, cudaStream_t st);
+
+// rq_gemv.cu ----------------------------------------------------------------
+rq_status launch_q4k_gemv(const uint8_t* w, const float* x, float* y, int M,
+                          int N, int K, cudaStream_t st);
+rq_status launch_q6k_gemv(const uint8_t* w, const float* x, float* y, int M,
+                          int N, int K, cudaStream_t st);
+
+// rq_wcache.cu --------------------------------------------------------------
+// Decode the packed weight (fixed fp32 order) and reduce its absmax into
+// *absmax_bits (which the caller zeroed on the stream).
+rq_status launch_dequant_absmax(int qtype, const uint8_t* w, int N, int K,
+                                uint32_t* absmax_bits, cudaStream_t st);
+// Decode again and encode with 448/absmax'; write the dequant scale.
+rq_status launch_dequant_encode(int qtype, const uint8_t* w, int N, int K,
+                                const uint32_t* absmax_bits, uint8_t* out,
+                                float* dequant_out, cudaStream_t st);
+
+// rq_gemm.cu ----------------------------------------------------------------
+rq_status launch_fp8_gemm(const uint8_t* x_fp8, const float* x_deq,
+                          const uint8_t* w_fp8, const float* w_deq, float* y,
+                          int M, int N, int K, cudaStream_t st);
+rq_status read_and_clear_device_error(cudaStream_t st);
+rq_status launch_debug_wait_timeout(int64_t limit_ns, cudaStream_t st);
+
+}  // namespace rq

@@ -1,0 +1,84 @@
+"""GPU parity: Q4_K / Q6_K decode GEMV against the fp64 oracle, within
+|gpu - oracle| <= 1e-4 * sum_k |x_k w_k| per element."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+from gpu_util import empty, gemv_ok, to_dev
+
+pytestmark = pytest.mark.gpu
+
+Q4K, Q6K = 12, 14
+
+
+@pytest.fixture(scope="module")
+def rq():
+    import quantized_linear_layers_gb300 as rq
+    return rq
+
+
+def gpu_gemv(rq, qtype, W, x, N, K):
+    M = x.shape[0]
+    y = empty((M, N), torch.float32)
+    y.fill_(float("nan"))
+    fn = rq.rq_q4k_gemv if qtype == Q4K else rq.rq_q6k_gemv
+    fn(to_dev(W), to_dev(x), y, M, N, K)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+@pytest.mark.parametrize("qtype", [Q4K, Q6K])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("N,K", [(1, 256), (67, 768), (130, 2560), (33, 8448)])
+def test_small_shapes_all_m(rq, qtype, M, N, K):
+    W = synthetic.weight_matrix(1000 + N + K, qtype, N, K)
+    x = synthetic.activation(M + K, M, K)
+    got = gpu_gemv(rq, qtype, W, x, N, K)
+    ref, absdot = oracle.gemv(qtype, W, x, N, K)
+    ok, worst = gemv_ok(got, ref, absdot)
+    assert ok, "worst error / bound = %.3g" % worst
+
+
+def test_c1_q4k_gemv_full(rq):
+    """Single Q4_K GEMV, M=1, N=512, K=1024, every output checked."""
+    N, K = 512, 1024
+    W = synthetic.q4k_matrix(1, N, K)
+    x = synthetic.activation(2, 1, K)
+    got = gpu_gemv(rq, Q4K, W, x, N, K)
+    ref, absdot = oracle.gemv(Q4K, W, x, N, K)
+    ok, worst = gemv_ok(got, ref, absdot)
+    assert ok, worst
+
+
+C3_SHAPES = [(Q4K, 3584, 3584), (Q4K, 512, 3584), (Q6K, 512, 3584),
+             (Q4K, 18944, 3584), (Q4K, 3584, 18944)]
+
+
+@pytest.mark.parametrize("qtype,N,K", C3_SHAPES)
+@pytest.mark.parametrize("M", [1, 4, 8])
+def test_c3_full_size_sampled_rows(rq, qtype, N, K, M):
+    """Decoder shapes at full size; the oracle checks 48 sampled rows
+    (first, last, and seeded picks) of the launch the benchmark times."""
+    W = synthetic.weight_matrix(31 * N + K, qtype, N, K)
+    x = synthetic.activation(7 + M, M, K)
+    got = gpu_gemv(rq, qtype, W, x, N, K)
+    assert np.all(np.isfinite(got))
+    rng = np.random.default_rng(N + K + M)
+    rows = np.unique(np.concatenate([[0, 1, N - 2, N - 1], rng.integers(0, N, 44)]))
+    ref, absdot = oracle.gemv_rows(qtype, W, x, N, K, rows)
+    ok, worst = gemv_ok(got[:, rows], ref, absdot)
+    assert ok, worst
+
+
+def test_gemv_writes_only_its_outputs(rq):
+    N, K, M = 37, 512, 3
+    W = synthetic.q4k_matrix(3, N, K)
+    x = synthetic.activation(3, M, K)
+    buf = empty(M * N + 64, torch.float32)
+    buf.fill_(12345.0)
+    rq.rq_q4k_gemv(to_dev(W), to_dev(x), buf, M, N, K)
+    torch.cuda.synchronize()
+    tail = buf[M * N:].cpu().numpy()
+    assert np.all(tail == 12345.0)

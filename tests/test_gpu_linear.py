@@ -1,0 +1,131 @@
+"""GPU: rq_linear routing by the M threshold, FP8 activation reuse across
+linears that share an input, and the bounded-wait timeout path."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+from gpu_util import empty, gemm_ok, gemv_ok, to_dev
+
+pytestmark = pytest.mark.gpu
+
+Q4K, Q6K = 12, 14
+
+
+@pytest.fixture(scope="module")
+def rq():
+    import quantized_linear_layers_gb300 as rq
+    return rq
+
+
+def gemm_route_ref(qtype, W, x, N, K):
+    wb, wd = oracle.fp8_weight_cache(qtype, W, N, K)
+    xb, xd = oracle.quant_e4m3(x, oracle.absmax_bits(x))
+    return oracle.fp8_gemm(xb, xd, wb, wd)
+
+
+def check_gemm(got, ref):
+    rms = np.sqrt(np.mean(ref ** 2, axis=1, keepdims=True))
+    ok, worst = gemm_ok(got, ref, rms)
+    assert ok, worst
+
+
+@pytest.mark.parametrize("qtype", [Q4K, Q6K])
+def test_routing_around_threshold(rq, qtype):
+    N, K = 160, 1024
+    W = synthetic.weight_matrix(4, qtype, N, K)
+    Wd = to_dev(W)
+    ctx = rq.Context()
+    assert ctx.gemm_threshold == 4
+    for M in (1, 2, 3, 4, 5):
+        x = synthetic.activation(40 + M, M, K, outlier_frac=1e-3)
+        y = empty((M, N), torch.float32)
+        before = ctx.stats()
+        ctx.rq_linear(qtype, Wd, to_dev(x), y, M, N, K)
+        torch.cuda.synchronize()
+        after = ctx.stats()
+        got = y.cpu().numpy()
+        if oracle.route_is_gemm(M, 4):
+            assert after["act_misses"] == before["act_misses"] + 1
+            check_gemm(got, gemm_route_ref(qtype, W, x, N, K))
+        else:
+            assert after == before
+            ref, absdot = oracle.gemv(qtype, W, x, N, K)
+            assert gemv_ok(got, ref, absdot)[0]
+    ctx.close()
+
+
+def test_raised_threshold_runs_gemv_in_chunks_of_8(rq):
+    N, K, M = 96, 512, 13
+    W = synthetic.q4k_matrix(8, N, K)
+    x = synthetic.activation(8, M, K)
+    ctx = rq.Context(gemm_threshold=32)
+    y = empty((M, N), torch.float32)
+    ctx.rq_linear(Q4K, to_dev(W), to_dev(x), y, M, N, K)
+    torch.cuda.synchronize()
+    ref, absdot = oracle.gemv(Q4K, W, x[:8], N, K)
+    ref2, absdot2 = oracle.gemv(Q4K, W, x[8:], N, K)
+    assert gemv_ok(y.cpu().numpy(), np.vstack([ref, ref2]), np.vstack([absdot, absdot2]))[0]
+    assert ctx.stats()["act_misses"] == 0
+    ctx.close()
+
+
+def test_threshold_from_environment(rq, monkeypatch):
+    monkeypatch.setenv("RQ_GEMM_THRESHOLD", "9")
+    ctx = rq.Context()
+    assert ctx.gemm_threshold == 9
+    ctx.set_gemm_threshold(2)
+    assert ctx.gemm_threshold == 2
+    ctx.close()
+
+
+def test_activation_reuse_counts_and_results(rq):
+    """q/k/v share x and gate/up share h: 3 reuses per layer as on the pages
+    (Q computes, K and V reuse; gate computes, up reuses)."""
+    K, M = 512, 40
+    shapes = [("q", Q4K, 256), ("k", Q4K, 128), ("v", Q6K, 128), ("o", Q4K, 256),
+              ("gate", Q4K, 384), ("up", Q4K, 384)]
+    host = {n: synthetic.weight_matrix(70 + i, qt, N, K) for i, (n, qt, N) in enumerate(shapes)}
+    dev_w = {n: to_dev(w) for n, w in host.items()}
+    acts = {"x": synthetic.activation(1, M, K, outlier_frac=1e-3),
+            "a": synthetic.activation(2, M, K), "h": synthetic.activation(3, M, K)}
+    dev_a = {k: to_dev(v) for k, v in acts.items()}
+    src = {"q": "x", "k": "x", "v": "x", "o": "a", "gate": "h", "up": "h"}
+    ctx = rq.Context()
+    for layer in range(2):
+        for name, qt, N in shapes:
+            y = empty((M, N), torch.float32)
+            ctx.rq_linear(qt, dev_w[name], dev_a[src[name]], y, M, N, K)
+            torch.cuda.synchronize()
+            check_gemm(y.cpu().numpy(), gemm_route_ref(qt, host[name], acts[src[name]], N, K))
+    st = ctx.stats()
+    # per layer: q miss, k hit, v hit, o miss, gate miss, up hit
+    assert st["act_hits"] == 6 and st["act_misses"] == 6
+    assert st["weights"] == 6
+    # rewriting x in place requires an explicit invalidation
+    new_x = synthetic.activation(9, M, K)
+    dev_a["x"].copy_(to_dev(new_x))
+    ctx.rq_act_cache_invalidate()
+    y = empty((M, 256), torch.float32)
+    ctx.rq_linear(Q4K, dev_w["q"], dev_a["x"], y, M, 256, K)
+    torch.cuda.synchronize()
+    assert ctx.stats()["act_misses"] == 7
+    check_gemm(y.cpu().numpy(), gemm_route_ref(Q4K, host["q"], new_x, 256, K))
+    ctx.close()
+
+
+def test_wait_timeout_is_reported_and_cleared(rq):
+    rq.rq_debug_wait_timeout(20_000_000)  # 20 ms on a barrier nobody completes
+    assert rq.rq_get_device_status() == 7  # RQ_ERR_TIMEOUT
+    assert rq.rq_get_device_status() == 0  # cleared
+    # the context is still usable
+    N, K, M = 128, 256, 16
+    W = synthetic.q4k_matrix(2, N, K)
+    x = synthetic.activation(2, M, K)
+    ctx = rq.Context()
+    y = empty((M, N), torch.float32)
+    ctx.rq_linear(Q4K, to_dev(W), to_dev(x), y, M, N, K)
+    assert rq.rq_get_device_status() == 0
+    check_gemm(y.cpu().numpy(), gemm_route_ref(Q4K, W, x, N, K))
+    ctx.close()

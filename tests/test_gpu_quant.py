@@ -1,0 +1,140 @@
+"""GPU parity: rq_absmax and rq_quant_e4m3 are bit-exact with the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+from gpu_util import empty, to_dev, u32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def rq():
+    import quantized_linear_layers_gb300 as rq
+    return rq
+
+
+def run_gpu(rq, x, absmax_override=None):
+    xd = to_dev(x.ravel())
+    n = x.size
+    bits = empty(1, torch.int32)
+    out = empty(max(n, 1), torch.uint8)
+    deq = empty(1, torch.float32)
+    rq.rq_absmax(xd, n, bits)
+    if absmax_override is not None:
+        bits.fill_(int(np.array([absmax_override], np.uint32).view(np.int32)[0]))
+    rq.rq_quant_e4m3(xd, n, bits, out, deq)
+    torch.cuda.synchronize()
+    return u32(bits), out.cpu().numpy()[:n], np.float32(deq.item())
+
+
+def special_tail():
+    """Special values: signed zeros, infinities, NaNs, fp32 subnormals, the
+    flush boundary, every exact midpoint between adjacent normal E4M3 values
+    (from the format: 2^(e-7) * (1 + (2m+1)/16)), 464, and 447..480."""
+    bits = [0x00000000, 0x80000000, 0x7F800000, 0xFF800000, 0x7FC00000, 0xFFC00000,
+            0x7F800001, 0xFF800001, 0x00000001, 0x007FFFFF, 0x80000001, 0x807FFFFF,
+            0x3C7FFFFF, 0xBC7FFFFF]
+    vals = [2.0 ** -7, -2.0 ** -7, 2.0 ** -6, -2.0 ** -6]
+    mids = []
+    for e in range(1, 16):
+        for m in range(8):
+            if e == 15 and m == 7:
+                continue
+            mids.append(2.0 ** (e - 7) * (1 + (2 * m + 1) / 16.0))
+    mids = sorted(mids)
+    vals += mids + [-v for v in mids] + [float(v) for v in range(447, 481)]
+    vals += [-float(v) for v in range(447, 481)] + [463.99, 464.01, 479.9, 495.9, 496.0]
+    arr = np.concatenate([np.array(bits, np.uint32).view(np.float32),
+                          np.array(vals, np.float32)])
+    return arr
+
+
+def test_c2_body_and_special_tail_bit_exact(rq):
+    # 512 x 3584 activation, N(0,1) with 0.1% of positions x50
+    x = synthetic.activation(20240601, 512, 3584, outlier_frac=1e-3)
+    bits, out, deq = run_gpu(rq, x)
+    a = oracle.absmax_bits(x)
+    ob, od = oracle.quant_e4m3(x, a)
+    assert bits == a
+    assert np.array_equal(out, ob.ravel())
+    assert deq == od
+    # the special tail is its own segment with absmax forced to 448 (scale 1)
+    tail = special_tail()
+    f448 = int(np.float32(448.0).view(np.uint32))
+    _, tout, tdeq = run_gpu(rq, tail, absmax_override=f448)
+    ob2, od2 = oracle.quant_e4m3(tail, f448)
+    assert np.array_equal(tout, ob2)
+    assert tdeq == od2 == np.float32(1.0)
+    assert not np.any((tout & 0x7F) == 0x7F)
+
+
+@pytest.mark.parametrize("n", [0, 1, 3, 5, 1023, 4097, 100003])
+@pytest.mark.parametrize("offset", [0, 1, 3])
+def test_ragged_and_unaligned(rq, n, offset):
+    base = synthetic.normal_f32(n + 7, n + offset) * np.float32(3.0)
+    x = base[offset:]
+    xd_full = to_dev(base)
+    xd = xd_full[offset:]
+    bits = empty(1, torch.int32)
+    out_full = empty(n + 8, torch.uint8)
+    out = out_full[offset:offset + n] if n else out_full
+    deq = empty(1, torch.float32)
+    rq.rq_absmax(xd, n, bits)
+    rq.rq_quant_e4m3(xd, n, bits, out, deq)
+    torch.cuda.synchronize()
+    a = oracle.absmax_bits(x)
+    assert u32(bits) == a
+    ob, od = oracle.quant_e4m3(x, a)
+    assert np.array_equal(out.cpu().numpy()[:n], ob)
+    assert np.float32(deq.item()) == od
+
+
+def test_absmax_ignores_nan_and_counts_inf(rq):
+    x = synthetic.normal_f32(5, 10000)
+    x[17] = np.nan
+    x[18] = np.float32(-1e5)
+    bits, _, _ = run_gpu(rq, x)
+    assert bits == oracle.absmax_bits(x) == int(np.float32(1e5).view(np.uint32))
+    x[19] = -np.inf
+    bits, out, deq = run_gpu(rq, x)
+    assert bits == int(np.float32(np.inf).view(np.uint32))
+    ob, od = oracle.quant_e4m3(x, bits)
+    assert np.array_equal(out, ob) and np.isinf(deq) and np.isinf(od)
+
+
+def test_all_zero_tensor_uses_unit_absmax(rq):
+    x = np.zeros(1000, np.float32)
+    x[::3] = -0.0
+    bits, out, deq = run_gpu(rq, x)
+    assert bits == 0 and np.all(out == 0)
+    assert deq == np.float32(1.0) / np.float32(448.0)
+
+
+def test_every_fp32_exponent_and_mantissa_pattern(rq):
+    """A sweep over sign x exponent x mantissa-tail patterns through the
+    device encoder with scale 1 (absmax forced to 448)."""
+    e = np.arange(256, dtype=np.uint32) << 23
+    m = np.array([0, 1, 0x7FFFF, 0x80000, 0x80001, 0xFFFFF, 0x100000, 0x17FFFF,
+                  0x180000, 0x280000, 0x380000, 0x3FFFFF, 0x400000, 0x480000,
+                  0x500000, 0x580000, 0x600000, 0x680000, 0x700000, 0x780000,
+                  0x7FFFFF], dtype=np.uint32)
+    bits = (e[:, None] | m[None, :]).ravel()
+    bits = np.concatenate([bits, bits | 0x80000000])
+    x = bits.view(np.float32)
+    f448 = int(np.float32(448.0).view(np.uint32))
+    _, out, _ = run_gpu(rq, x, absmax_override=f448)
+    ob, _ = oracle.quant_e4m3(x, f448)
+    assert np.array_equal(out, ob)
+
+
+def test_large_scaled_variant_bit_exact(rq):
+    """4096 x 18944 activation (310 MB): the bandwidth-sized variant."""
+    x = synthetic.activation(77, 4096, 18944, outlier_frac=1e-3)
+    bits, out, deq = run_gpu(rq, x)
+    a = oracle.absmax_bits(x)
+    ob, od = oracle.quant_e4m3(x, a)
+    assert bits == a and deq == od
+    assert np.array_equal(out, ob.ravel())
