@@ -345,6 +345,7 @@ def run_gpu(args, world, rank, local):
     sampler.start()
     t_wall = time.perf_counter()
     for _ in range(args.steps):
+        torch.cuda.nvtx.range_push("timed_step")
         e0, e1, e2 = ev(), ev(), ev()
         e0.record(stream)
         graph.replay()
@@ -353,6 +354,7 @@ def run_gpu(args, world, rank, local):
         st.run_pass(M_PREFILL, stream)
         e2.record(stream)
         tr = st.ctx.rq_ctx_trace_end()  # waits for the pass's events
+        torch.cuda.nvtx.range_pop()
         for k, (n, ms) in tr.items():
             c = traced.setdefault(k, [0, 0.0])
             c[0] += n
@@ -381,7 +383,7 @@ def run_gpu(args, world, rank, local):
     traffic = gemm_traffic_per_launch()
 
     # ----------------------------------------------------------- e2e leg --
-    e2e = run_e2e(args, st, torch, rq, dev, stream, world)
+    e2e = None if args.no_e2e else run_e2e(args, st, torch, rq, dev, stream, world)
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -479,6 +481,63 @@ def run_e2e(args, st, torch, rq, dev, stream, world):
             "note": "prefill FLOPs / (decode + prefill eager step with copies)"}
 
 
+def run_case(args):
+    """One kernel on one shape, `--launches` times after 3 warm-up launches:
+    the small, self-contained command the ncu captures use."""
+    import torch
+    import quantized_linear_layers_gb300 as rq
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    M, N, K = args.M, args.N, args.K
+    if args.case in ("gemv_q4k", "gemv_q6k"):
+        qt = synthetic.Q4K if args.case == "gemv_q4k" else synthetic.Q6K
+        W = torch.from_numpy(synthetic.weight_matrix(1, qt, N, K)).to(dev)
+        x = torch.from_numpy(synthetic.activation(2, M, K)).to(dev)
+        y = torch.empty(M, N, device=dev)
+        fn = rq.rq_q4k_gemv if qt == synthetic.Q4K else rq.rq_q6k_gemv
+        call = lambda: fn(W, x, y, M, N, K)  # noqa: E731
+    elif args.case in ("absmax", "quant"):
+        x = torch.from_numpy(synthetic.activation(3, M, K, outlier_frac=1e-3)).to(dev)
+        bits = torch.zeros(1, dtype=torch.int32, device=dev)
+        out = torch.empty(M * K, dtype=torch.uint8, device=dev)
+        deq = torch.empty(1, device=dev)
+        rq.rq_absmax(x, M * K, bits)
+        if args.case == "absmax":
+            call = lambda: rq.rq_absmax(x, M * K, bits)  # noqa: E731
+        else:
+            call = lambda: rq.rq_quant_e4m3(x, M * K, bits, out, deq)  # noqa: E731
+    elif args.case == "gemm":
+        ctx = rq.Context()
+        W = torch.from_numpy(synthetic.q4k_matrix(4, N, K)).to(dev)
+        wq, wd = ctx.rq_fp8_weight_cache(synthetic.Q4K, W, N, K)
+        x = torch.from_numpy(synthetic.activation(5, M, K, outlier_frac=1e-3)).to(dev)
+        m_pad = (M + 15) // 16 * 16
+        bits = torch.zeros(1, dtype=torch.int32, device=dev)
+        xq = torch.zeros(m_pad * K, dtype=torch.uint8, device=dev)
+        xd = torch.empty(1, device=dev)
+        rq.rq_absmax(x, M * K, bits)
+        rq.rq_quant_e4m3(x, M * K, bits, xq, xd)
+        y = torch.empty(M, N, device=dev)
+        call = lambda: rq.rq_fp8_gemm(xq, xd, wq, wd, y, M, N, K)  # noqa: E731
+    else:
+        raise SystemExit("unknown case " + args.case)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(args.launches):
+        call()
+    e.record()
+    torch.cuda.synchronize()
+    status = rq.rq_get_device_status()
+    ms = s.elapsed_time(e) / args.launches
+    print(json.dumps({"case": args.case, "M": M, "N": N, "K": K, "ms_per_launch": ms,
+                      "status": status}), flush=True)
+    if status != 0:
+        raise SystemExit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -487,7 +546,17 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--ref-rows", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end leg (profiling runs only)")
+    ap.add_argument("--case", default=None,
+                    help="single-kernel mode: gemv_q4k, gemv_q6k, absmax, quant, gemm")
+    ap.add_argument("--M", type=int, default=2048)
+    ap.add_argument("--N", type=int, default=3584)
+    ap.add_argument("--K", type=int, default=3584)
+    ap.add_argument("--launches", type=int, default=3)
     args = ap.parse_args()
+    if args.case:
+        return run_case(args)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup()

@@ -19,6 +19,9 @@
 //    exactly; sum x*(0.5 + q*2^-p) - 0.5*sum x = 2^-p * sum x*q, so each
 //    weight costs one PRMT and one FFMA, and the 2^p is folded into d*sc.
 //  * fp32 accumulation, one warp-shuffle reduction per row.
+#include <map>
+#include <utility>
+
 #include "rq_device.cuh"
 #include "rq_internal.h"
 
@@ -393,12 +396,25 @@ q6k_gemv_kernel(const uint8_t* __restrict__ W, const float* __restrict__ x,
 
 // ---------------------------------------------------------------- launch --
 
+// Resident CTAs per SM for a kernel at a dynamic shared-memory size; the
+// occupancy query is cached per (kernel, smem) since it costs host time.
 template <typename KernelT>
-int persistent_grid(KernelT kernel, size_t smem, int ngroups) {
+int blocks_per_sm(KernelT kernel, size_t smem) {
+  static std::map<std::pair<const void*, size_t>, int> cache;
+  const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), smem);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem) !=
           cudaSuccess || per_sm < 1)
     per_sm = 1;
+  cache.emplace(key, per_sm);
+  return per_sm;
+}
+
+template <typename KernelT>
+int persistent_grid(KernelT kernel, size_t smem, int ngroups) {
+  const int per_sm = blocks_per_sm(kernel, smem);
   const int want = (ngroups + kWarps - 1) / kWarps;
   const int cap = device_sm_count() * per_sm;
   return want < cap ? (want < 1 ? 1 : want) : cap;
@@ -409,10 +425,13 @@ rq_status run_q4k(const uint8_t* w, const float* x, float* y, int N, int K,
                   cudaStream_t st) {
   const size_t smem = (size_t)M * (K / 32) * sizeof(float);
   auto kern = q4k_gemv_kernel<M, R>;
-  if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
-    return RQ_ERR_CUDA;
+  static size_t smem_set = 48 * 1024;
+  if (smem > smem_set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+      return RQ_ERR_CUDA;
+    smem_set = smem;
+  }
   const int grid = persistent_grid(kern, smem, (N + R - 1) / R);
   kern<<<grid, kThreads, smem, st>>>(w, x, y, N, K);
   return launch_status();
@@ -423,10 +442,13 @@ rq_status run_q6k(const uint8_t* w, const float* x, float* y, int N, int K,
                   cudaStream_t st) {
   const size_t smem = (size_t)M * (K / 8) * sizeof(float);
   auto kern = q6k_gemv_kernel<M, R>;
-  if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
-    return RQ_ERR_CUDA;
+  static size_t smem_set = 48 * 1024;
+  if (smem > smem_set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+      return RQ_ERR_CUDA;
+    smem_set = smem;
+  }
   const int grid = persistent_grid(kern, smem, (N + R - 1) / R);
   kern<<<grid, kThreads, smem, st>>>(w, x, y, N, K);
   return launch_status();

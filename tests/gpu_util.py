@@ -51,7 +51,7 @@ class _DevBuf:
 
     def __init__(self, ptr, n, typestr):
         self.__cuda_array_interface__ = {
-            "shape": (n,), "typestr": typestr, "data": (int(ptr), True),
+            "shape": (n,), "typestr": typestr, "data": (int(ptr), False),
             "version": 3, "strides": None}
 
 
