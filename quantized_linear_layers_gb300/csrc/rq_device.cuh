@@ -19,32 +19,53 @@ constexpr int kQ6KBytes = 210;    // Q6_K super-block size
 // NaN / Inf / overflow saturated to sign|0x7E, and (the one deviation from
 // that code) 0x7F / 0xFF never produced.
 //
-// Formulation used here: for 2^-6 <= |v| < Inf, (|v|bits - 120<<23) >> 20 is
-// exactly the 7-bit code exponent:mantissa; rounding that integer to nearest
-// even on the 20 dropped bits also performs the mantissa carry into the
-// exponent, and one clamp to 0x7E covers both 0x7F and exponent overflow.
-__device__ __forceinline__ uint32_t e4m3_from_bits(uint32_t bits) {
-  const uint32_t sign = (bits >> 24) & 0x80u;
-  const uint32_t mag = bits & 0x7FFFFFFFu;
-  if (mag >= 0x7F800000u) return sign | 0x7Eu;   // NaN, +-Inf
-  if (mag < 0x3C800000u) return 0u;               // below 2^-6 (incl. +-0)
-  const uint32_t r = mag - 0x3C000000u;           // exponent rebias by 120
-  uint32_t code = r >> 20;
-  const uint32_t rem = r & 0xFFFFFu;
-  code += (rem > 0x80000u) | ((rem == 0x80000u) & (code & 1u));
-  code = code < 0x7Eu ? code : 0x7Eu;
-  return sign | code;
+// Formulation used here: the sm_89+ conversion cvt.rn.satfinite.e4m3x2.f32
+// rounds to nearest even among E4M3FN values and saturates finite overflow
+// and +-Inf to +-448, which is exactly the rule for 2^-6 <= |v|; values below
+// 2^-6 (and NaN, which only arises from 0 * Inf here) are replaced by +0
+// before the conversion, and non-finite inputs are handled before the
+// multiply by the callers below.
+
+// Two codes: low byte from `lo`, high byte from `hi`.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// +0 unless 2^-6 <= |v| (NaN fails the comparison too).
+__device__ __forceinline__ float flush_small(float v) {
+  return fabsf(v) >= 0x1p-6f ? v : 0.0f;
+}
+
+__device__ __forceinline__ bool non_finite(float x) {
+  return (__float_as_uint(x) & 0x7F800000u) == 0x7F800000u;
+}
+
+__device__ __forceinline__ uint32_t saturated_code(float x) {
+  return ((__float_as_uint(x) >> 24) & 0x80u) | 0x7Eu;
 }
 
 // Scaled element encode: non-finite inputs keep their own sign and saturate,
 // +-0 gives 0x00 (both decided before the multiply); otherwise one
 // correctly rounded fp32 multiply by s (no FMA contraction) and the encoder.
 __device__ __forceinline__ uint32_t e4m3_scaled(float x, float s) {
-  const uint32_t b = __float_as_uint(x);
-  const uint32_t mag = b & 0x7FFFFFFFu;
-  if (mag >= 0x7F800000u) return ((b >> 24) & 0x80u) | 0x7Eu;
-  if (mag == 0u) return 0u;
-  return e4m3_from_bits(__float_as_uint(__fmul_rn(x, s)));
+  if (non_finite(x)) return saturated_code(x);
+  return cvt_e4m3x2(0.0f, flush_small(__fmul_rn(x, s))) & 0xFFu;
+}
+
+// Four elements -> four codes (element i in byte i).
+__device__ __forceinline__ uint32_t e4m3_scaled4(float4 v, float s) {
+  const float a = flush_small(__fmul_rn(v.x, s)), b = flush_small(__fmul_rn(v.y, s));
+  const float c = flush_small(__fmul_rn(v.z, s)), d = flush_small(__fmul_rn(v.w, s));
+  uint32_t r = cvt_e4m3x2(b, a) | (cvt_e4m3x2(d, c) << 16);
+  if (non_finite(v.x) | non_finite(v.y) | non_finite(v.z) | non_finite(v.w)) {
+    if (non_finite(v.x)) r = (r & 0xFFFFFF00u) | saturated_code(v.x);
+    if (non_finite(v.y)) r = (r & 0xFFFF00FFu) | (saturated_code(v.y) << 8);
+    if (non_finite(v.z)) r = (r & 0xFF00FFFFu) | (saturated_code(v.z) << 16);
+    if (non_finite(v.w)) r = (r & 0x00FFFFFFu) | (saturated_code(v.w) << 24);
+  }
+  return r;
 }
 
 // Quantization scale from the absmax word: A' = (A == 0 ? 1 : A),
@@ -87,6 +108,76 @@ __device__ __forceinline__ float2 half_pair(uint32_t v) {
   return make_float2(__half2float(__ushort_as_half((unsigned short)(v & 0xFFFFu))),
                      __half2float(__ushort_as_half((unsigned short)(v >> 16))));
 }
+
+// ------------------------------------------------------ mbarrier / TMA ----
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete, at most limit_ns
+// nanoseconds.  On expiry, sets bit 0 of *err and returns false.
+__device__ __noinline__ inline bool mbar_wait(uint32_t bar, uint32_t parity,
+                                              uint64_t limit_ns, unsigned int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer() - t0 > limit_ns) {
+      atomicOr(err, 1u);
+      return false;
+    }
+  }
+}
+
+// 1-D bulk copy global -> shared, completing `bytes` of transaction on bar.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s for any pipeline wait
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

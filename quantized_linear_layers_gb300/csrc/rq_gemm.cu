@@ -25,6 +25,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
+
 #include "rq_device.cuh"
 #include "rq_internal.h"
 
@@ -43,59 +45,8 @@ constexpr int kABytes = kBM * kBK;           // 16 KB
 constexpr int kBBytesMax = kMaxBN * kBK;     // 32 KB
 constexpr int kSmemBytes = kStages * (kABytes + kBBytesMax) + 1024 /*barriers*/ +
                            1024 /*alignment slack*/;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 // --------------------------------------------------------- PTX wrappers --
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t globaltimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-               "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Wait for the phase with the given parity to complete, at most limit_ns.
-// Returns false (and records the timeout) if the limit expired.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer() - t0 > limit_ns) {
-      atomicOr(&g_rq_device_error, 1u);
-      return false;
-    }
-  }
-}
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map,
                                             uint32_t bar, int c0, int c1) {
@@ -236,7 +187,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
         const int tn = t / args.tiles_m, tm = t - tn * args.tiles_m;
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, args.wait_limit_ns)) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, args.wait_limit_ns, &g_rq_device_error)) {
             ok = false;
             break;
           }
@@ -252,7 +203,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
       // Drain: every issued copy has landed before the CTA can exit.
       for (int s = 0; s < kStages; ++s)
         if (issued_mask & (1u << s))
-          mbar_wait(full0 + 8 * s, (last_parity >> s) & 1u, args.wait_limit_ns);
+          mbar_wait(full0 + 8 * s, (last_parity >> s) & 1u, args.wait_limit_ns,
+                    &g_rq_device_error);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer --
@@ -264,11 +216,11 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-        if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, args.wait_limit_ns)) break;
+        if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, args.wait_limit_ns, &g_rq_device_error)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * bn);
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(full0 + 8 * stage, phase, args.wait_limit_ns)) {
+          if (!mbar_wait(full0 + 8 * stage, phase, args.wait_limit_ns, &g_rq_device_error)) {
             ok = false;
             break;
           }
@@ -288,7 +240,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
       }
       // Drain: all issued MMAs have completed before TMEM is released.
       mma_commit(done_bar);
-      mbar_wait(done_bar, 0, args.wait_limit_ns);
+      mbar_wait(done_bar, 0, args.wait_limit_ns, &g_rq_device_error);
     }
   } else {
     // --------------------------------------------------------- epilogue --
@@ -300,7 +252,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
       const int tn = t / args.tiles_m, tm = t - tn * args.tiles_m;
       // every lane polls; the outcome is made warp-uniform before the
       // .sync.aligned TMEM loads below
-      const bool ready = mbar_wait(tfull0 + 8 * acc, acc_phase, args.wait_limit_ns);
+      const bool ready =
+          mbar_wait(tfull0 + 8 * acc, acc_phase, args.wait_limit_ns, &g_rq_device_error);
       if (!__all_sync(0xFFFFFFFFu, ready)) break;
       tc_fence_after();
       const int n = tn * kBM + quad * 32 + lane;
@@ -342,8 +295,8 @@ __global__ void wait_timeout_kernel(uint64_t limit_ns) {
   if (threadIdx.x == 0) {
     const uint32_t b = smem_u32(&bar);
     mbar_init(b, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    mbar_wait(b, 0, limit_ns);
+    mbar_fence_init();
+    mbar_wait(b, 0, limit_ns, &g_rq_device_error);
   }
 }
 
@@ -386,13 +339,41 @@ uint32_t tmem_columns(int bn) {
   return c;
 }
 
+// Tokens per tile.  Every CTA is resident at once (one per SM), so a launch
+// takes ceil(tiles / SMs) rounds and a round costs about the time of one tile,
+// which grows with BN plus a fixed part (pipeline fill, epilogue tail).
+// Candidates are multiples of 16 up to 256; the cheapest estimate wins, ties
+// going to the wider tile.  RQ_GEMM_BN (a multiple of 16, 16..256) forces a
+// width, for tuning measurements.
+int choose_bn(int m_pad, int N, int sms) {
+  const char* env = std::getenv("RQ_GEMM_BN");
+  const int v = env ? std::atoi(env) : 0;
+  const int forced = (v >= 16 && v <= kMaxBN && v % 16 == 0) ? v : 0;
+  if (forced) return forced < m_pad ? forced : m_pad;
+  if (m_pad <= kMaxBN) return m_pad;
+  const long tiles_n = (N + kBM - 1) / kBM;
+  int best = kMaxBN;
+  long best_cost = -1;
+  for (int bn = kMaxBN; bn >= 64; bn -= 16) {
+    const long tiles = tiles_n * ((m_pad + bn - 1) / bn);
+    const long rounds = (tiles + sms - 1) / sms;
+    const long cost = rounds * (bn + 48);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
 }  // namespace
 
 rq_status launch_fp8_gemm(const uint8_t* x_fp8, const float* x_deq,
                           const uint8_t* w_fp8, const float* w_deq, float* y,
                           int M, int N, int K, cudaStream_t st) {
   const int m_pad = (M + 15) / 16 * 16;
-  const int bn = m_pad < kMaxBN ? m_pad : kMaxBN;
+  const int sms = device_sm_count();
+  const int bn = choose_bn(m_pad, N, sms);
   CUtensorMap tw, tx;
   if (!make_map(&tw, w_fp8, N, K, kBM) || !make_map(&tx, x_fp8, m_pad, K, bn))
     return RQ_ERR_CUDA;
@@ -416,7 +397,6 @@ rq_status launch_fp8_gemm(const uint8_t* x_fp8, const float* x_deq,
     attr_done = true;
   }
   const int tiles = a.tiles_n * a.tiles_m;
-  const int sms = device_sm_count();
   const int grid = tiles < sms ? tiles : sms;
   fp8_gemm_kernel<<<grid, kThreads, kSmemBytes, st>>>(tw, tx, a);
   return launch_status();
@@ -424,10 +404,12 @@ rq_status launch_fp8_gemm(const uint8_t* x_fp8, const float* x_deq,
 
 rq_status read_and_clear_device_error(cudaStream_t st) {
   if (cudaStreamSynchronize(st) != cudaSuccess) return RQ_ERR_CUDA;
+  const rq_status gemv = read_and_clear_gemv_error();
+  if (gemv == RQ_ERR_CUDA) return gemv;
   unsigned int v = 0;
   if (cudaMemcpyFromSymbol(&v, g_rq_device_error, sizeof(v)) != cudaSuccess)
     return RQ_ERR_CUDA;
-  if (v == 0) return RQ_OK;
+  if (v == 0) return gemv;
   const unsigned int zero = 0;
   if (cudaMemcpyToSymbol(g_rq_device_error, &zero, sizeof(zero)) != cudaSuccess)
     return RQ_ERR_CUDA;

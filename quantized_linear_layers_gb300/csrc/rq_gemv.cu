@@ -394,6 +394,173 @@ q6k_gemv_kernel(const uint8_t* __restrict__ W, const float* __restrict__ x,
   }
 }
 
+// ------------------------------------------------- Q4_K, one token ---------
+//
+// M = 1 is the decode hot path.  Each lane owns one 64-weight quant group u
+// of every row and keeps x[64u .. 64u+63] (and its two 32-weight sums) in
+// registers for the whole kernel, so x costs no memory traffic per weight.
+// A team of ceil(K/64/32) warps covers K; a CTA runs `teams` teams and one
+// producer warp.  Each CTA owns a contiguous block of rows (the row blocks of
+// all CTAs differ by at most one row); the producer streams the block into a
+// shared-memory ring, `rows_per_stage` consecutive rows (one contiguous
+// cp.async.bulk copy) per stage, and the teams take the stage's rows in turn.
+// Per row a lane reads its 48 bytes (header + 32 quant bytes) from shared
+// memory -- conflict-free 16-byte loads -- decodes and accumulates; a warp
+// shuffle reduction and one shared atomic per warp and row complete the dot
+// product.  Every mbarrier wait is bounded.
+
+__device__ unsigned int g_gemv_error;  // bit 0: a pipeline wait timed out
+
+struct M1Args {
+  const uint8_t* W;
+  const float* x;
+  float* y;
+  int N, K;
+  int team_warps;      // warps per team: ceil(K / 64 / 32)
+  int teams;           // teams per CTA
+  int rows_per_stage;  // 2 * teams
+  int stages;
+  uint32_t ring_bytes;  // stages * rows_per_stage * rowbytes
+  uint64_t wait_limit_ns;
+};
+
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+
+// Dot product of one lane's 64 weights (header h, quants qa/qb of group g)
+// with the lane's x registers.
+__device__ __forceinline__ float q4_group_dot(const uint4& h, const uint4& qa,
+                                              const uint4& qb, int sh, bool upper,
+                                              const float (&xl)[32], const float (&xh)[32],
+                                              float hs_lo, float hs_hi, float s_lo,
+                                              float s_hi) {
+  const uint32_t a16 = h.y >> sh, b16 = h.z >> sh, c16 = h.w >> sh;
+  const uint32_t scp = upper ? ((c16 & 0x0F0Fu) | ((a16 >> 2) & 0x3030u)) : (a16 & 0x3F3Fu);
+  const uint32_t mp = upper ? (((c16 >> 4) & 0x0F0Fu) | ((b16 >> 2) & 0x3030u)) : (b16 & 0x3F3Fu);
+  const float2 dd = half_pair(h.x);
+  const float a_lo = (dd.x * 256.0f) * (float)(scp & 0xFFu);
+  const float a_hi = (dd.x * 4096.0f) * (float)((scp >> 8) & 0xFFu);
+  const float d_lo = dd.y * (float)(mp & 0xFFu);
+  const float d_hi = dd.y * (float)((mp >> 8) & 0xFFu);
+  const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+  float tl0 = 0.f, tl1 = 0.f, th0 = 0.f, th1 = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const uint32_t lo = q[w] & 0x0F0F0F0Fu, hi = q[w] & 0xF0F0F0F0u;
+    tl0 = fmaf(xl[4 * w + 0], mag_b2(lo, 0x7044u), tl0);
+    tl1 = fmaf(xl[4 * w + 1], mag_b2(lo, 0x7144u), tl1);
+    tl0 = fmaf(xl[4 * w + 2], mag_b2(lo, 0x7244u), tl0);
+    tl1 = fmaf(xl[4 * w + 3], mag_b2(lo, 0x7344u), tl1);
+    th0 = fmaf(xh[4 * w + 0], mag_b2(hi, 0x7404u), th0);
+    th1 = fmaf(xh[4 * w + 1], mag_b2(hi, 0x7414u), th1);
+    th0 = fmaf(xh[4 * w + 2], mag_b2(hi, 0x7424u), th0);
+    th1 = fmaf(xh[4 * w + 3], mag_b2(hi, 0x7434u), th1);
+  }
+  float c = a_lo * ((tl0 + tl1) - hs_lo);
+  c = fmaf(a_hi, (th0 + th1) - hs_hi, c);
+  c = fmaf(-d_lo, s_lo, c);
+  return fmaf(-d_hi, s_hi, c);
+}
+
+__global__ void __launch_bounds__(384, 1) q4k_gemv_m1_kernel(const M1Args a) {
+  extern __shared__ __align__(128) uint8_t smem_m1[];
+  const int nsb = a.K >> 8, U = nsb * 4;
+  const int rowbytes = nsb * kQ4KBytes;
+  const int rps = a.rows_per_stage;
+  const uint32_t stage_bytes = (uint32_t)(rps * rowbytes);
+  uint8_t* ring = smem_m1;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + a.ring_bytes);  // full[], empty[]
+  float* acc = reinterpret_cast<float*>(bars + 2 * a.stages);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + a.stages);
+
+  const int compute_warps = a.teams * a.team_warps;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r0 = (int)((int64_t)blockIdx.x * a.N / gridDim.x);
+  const int r1 = (int)((int64_t)(blockIdx.x + 1) * a.N / gridDim.x);
+  const int rows = r1 - r0;
+  const int iters = (rows + rps - 1) / rps;
+
+  for (int i = threadIdx.x; i < rows; i += blockDim.x) acc[i] = 0.f;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, compute_warps);
+    }
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  if (warp == compute_warps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t issued = 0, parity_bits = 0;
+      for (int it = 0; it < iters; ++it) {
+        const int s = it % a.stages;
+        const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
+        if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, a.wait_limit_ns, &g_gemv_error)) break;
+        const int nr = min(rps, rows - it * rps);
+        const uint32_t bytes = (uint32_t)(nr * rowbytes);
+        mbar_arrive_expect_tx(full0 + 8 * s, bytes);
+        bulk_g2s(smem_u32(ring + s * stage_bytes),
+                 a.W + (size_t)(r0 + it * rps) * rowbytes, bytes, full0 + 8 * s);
+        issued |= 1u << s;
+        parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
+      }
+      // every issued copy has landed before the CTA can exit
+      for (int s = 0; s < a.stages; ++s)
+        if (issued & (1u << s))
+          mbar_wait(full0 + 8 * s, (parity_bits >> s) & 1u, a.wait_limit_ns, &g_gemv_error);
+    }
+  } else if (warp < compute_warps) {
+    // ------------------------------------------------------------- compute
+    const int team = warp / a.team_warps, wt = warp - team * a.team_warps;
+    const int u = wt * 32 + lane;
+    const bool active = u < U;
+    const int sb = u >> 2, g = u & 3;
+    const int sh = (g & 1) * 16;
+    const bool upper = g >= 2;
+    float xl[32], xh[32];
+    float s_lo = 0.f, s_hi = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float4 vl = make_float4(0.f, 0.f, 0.f, 0.f), vh = vl;
+      if (active) {
+        const float4* px = reinterpret_cast<const float4*>(a.x + 64 * u);
+        vl = __ldg(px + j);
+        vh = __ldg(px + 8 + j);
+      }
+      xl[4 * j] = vl.x; xl[4 * j + 1] = vl.y; xl[4 * j + 2] = vl.z; xl[4 * j + 3] = vl.w;
+      xh[4 * j] = vh.x; xh[4 * j + 1] = vh.y; xh[4 * j + 2] = vh.z; xh[4 * j + 3] = vh.w;
+      s_lo += (vl.x + vl.y) + (vl.z + vl.w);
+      s_hi += (vh.x + vh.y) + (vh.z + vh.w);
+    }
+    const float hs_lo = 0.5f * s_lo, hs_hi = 0.5f * s_hi;
+    const int off_h = sb * kQ4KBytes, off_a = off_h + 16 + 32 * g, off_b = off_a + 16;
+    for (int it = 0; it < iters; ++it) {
+      const int s = it % a.stages;
+      const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
+      const bool ok = mbar_wait(full0 + 8 * s, ph, a.wait_limit_ns, &g_gemv_error);
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      const int nr = min(rps, rows - it * rps);
+      const uint8_t* stage = ring + s * stage_bytes;
+      for (int rr = team; rr < nr; rr += a.teams) {
+        const uint8_t* rp = stage + rr * rowbytes;
+        float part = 0.f;
+        if (active)
+          part = q4_group_dot(lds128(rp + off_h), lds128(rp + off_a), lds128(rp + off_b), sh,
+                              upper, xl, xh, hs_lo, hs_hi, s_lo, s_hi);
+        part = warp_sum(part);
+        if (lane == 0) atomicAdd(&acc[it * rps + rr], part);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < rows; i += blockDim.x) a.y[r0 + i] = acc[i];
+}
+
 // ---------------------------------------------------------------- launch --
 
 // Resident CTAs per SM for a kernel at a dynamic shared-memory size; the
@@ -454,12 +621,62 @@ rq_status run_q6k(const uint8_t* w, const float* x, float* y, int N, int K,
   return launch_status();
 }
 
+// One-token Q4_K launch: team_warps = ceil(K/64/32), ~8 compute warps per
+// CTA, one CTA per SM, a ring of up to 8 stages within ~150 KB.
+rq_status run_q4k_m1(const uint8_t* w, const float* x, float* y, int N, int K,
+                     cudaStream_t st) {
+  const int U = K / 64;
+  M1Args a;
+  a.W = w;
+  a.x = x;
+  a.y = y;
+  a.N = N;
+  a.K = K;
+  a.team_warps = (U + 31) / 32;
+  a.teams = a.team_warps >= 8 ? 1 : 8 / a.team_warps;
+  a.rows_per_stage = 2 * a.teams;
+  const int rowbytes = (K / kQK) * kQ4KBytes;
+  const int stage_bytes = a.rows_per_stage * rowbytes;
+  int stages = (150 * 1024) / stage_bytes;
+  stages = stages > 8 ? 8 : (stages < 2 ? 2 : stages);
+  a.stages = stages;
+  a.ring_bytes = (uint32_t)(stages * stage_bytes);
+  a.wait_limit_ns = kWaitLimitNs;
+  const int sms = device_sm_count();
+  const int grid = N < sms ? N : sms;
+  const int max_rows = (N + grid - 1) / grid;
+  const size_t smem = a.ring_bytes + 16 * (size_t)stages + 4 * (size_t)max_rows;
+  const int threads = (a.teams * a.team_warps + 1) * 32;
+  static size_t smem_set = 48 * 1024;
+  if (smem > smem_set) {
+    if (cudaFuncSetAttribute(q4k_gemv_m1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+      return RQ_ERR_CUDA;
+    smem_set = smem;
+  }
+  q4k_gemv_m1_kernel<<<grid, threads, smem, st>>>(a);
+  return launch_status();
+}
+
 }  // namespace
+
+rq_status read_and_clear_gemv_error() {
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_gemv_error, sizeof(v)) != cudaSuccess) return RQ_ERR_CUDA;
+  if (v == 0) return RQ_OK;
+  const unsigned int zero = 0;
+  if (cudaMemcpyToSymbol(g_gemv_error, &zero, sizeof(zero)) != cudaSuccess) return RQ_ERR_CUDA;
+  return RQ_ERR_TIMEOUT;
+}
 
 rq_status launch_q4k_gemv(const uint8_t* w, const float* x, float* y, int M,
                           int N, int K, cudaStream_t st) {
   switch (M) {
-    case 1: return run_q4k<1, 2>(w, x, y, N, K, st);
+    case 1:
+      // the one-token kernel keeps 64 x values per lane in registers; its
+      // team of ceil(K/2048) warps plus the producer warp fit 384 threads
+      if (K <= 11 * 2048) return run_q4k_m1(w, x, y, N, K, st);
+      return run_q4k<1, 2>(w, x, y, N, K, st);
     case 2: return run_q4k<2, 2>(w, x, y, N, K, st);
     case 3: return run_q4k<3, 2>(w, x, y, N, K, st);
     case 4: return run_q4k<4, 2>(w, x, y, N, K, st);

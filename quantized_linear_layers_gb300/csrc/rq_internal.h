@@ -31,6 +31,8 @@ rq_status launch_q4k_gemv(const uint8_t* w, const float* x, float* y, int M,
                           int N, int K, cudaStream_t st);
 rq_status launch_q6k_gemv(const uint8_t* w, const float* x, float* y, int M,
                           int N, int K, cudaStream_t st);
+// Read and clear the GEMV kernels' device error word (after a sync).
+rq_status read_and_clear_gemv_error();
 
 // rq_wcache.cu --------------------------------------------------------------
 // Decode the packed weight (fixed fp32 order) and reduce its absmax into

@@ -136,3 +136,14 @@ def test_full_size_prefill_shapes(rq, N, K, M):
         ok, worst = gemm_ok(got[m], ref, rms)
         assert ok, (m, worst)
     ctx.close()
+
+
+@pytest.mark.parametrize("bn", [16, 48, 112, 208, 256])
+def test_forced_tile_widths(rq, bn, monkeypatch):
+    """Every tile width the shape heuristic can pick gives the same result."""
+    monkeypatch.setenv("RQ_GEMM_BN", str(bn))
+    M, N, K = 300, 200, 384
+    Xb = random_e4m3(77, (M, K))
+    Wb = random_e4m3(78, (N, K))
+    got = gpu_gemm(rq, Xb, 0.01, Wb, 0.02, M)
+    check_full(got, oracle.fp8_gemm(Xb, 0.01, Wb, 0.02))
