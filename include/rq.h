@@ -185,6 +185,40 @@ rq_status rq_fp8_gemm(const uint8_t *x_fp8, const float *x_dequant,
 rq_status rq_linear(rq_ctx *ctx, rq_qtype qtype, const void *w, const float *x,
                     float *y, int M, int N, int K, rq_stream_t stream);
 
+/* FP8 linear layer that allocates nothing.  The source pages have no
+ * counterpart to this entry point.
+ *
+ * For callers that cannot call cudaMalloc while serving: code that runs
+ * inside a host framework which owns and pre-reserves all device memory (an
+ * inference engine's plugin or operator callback, say), or a process under a
+ * fixed device-memory budget where a new allocation would fail or stall.
+ * Given an E4M3 weight and its dequant scale (for example the pointers
+ * rq_fp8_weight_cache returns), it computes the same result as the FP8 route
+ * of rq_linear: absmax of x, E4M3 quantization of x, FP8 GEMM with both
+ * scales applied to the fp32 accumulator:
+ *   y[m, n] = (sum_k e4m3(xq[m, k]) * e4m3(w_fp8[n, k])) * x_deq * (*w_dequant)
+ *   x: f32 [M x K], 16-byte aligned.  w_fp8: E4M3 [N x K], 16-byte aligned.
+ *   w_dequant: one device float.  y: f32 [M x N].
+ * The quantized activation (M_pad x K bytes, M_pad = M rounded up to 16) and
+ * two device scalars live in one fixed array inside the library, of
+ * RQ_NOALLOC_MAX_ACT_BYTES + 256 bytes, which every GPU that loads the
+ * library holds until the process exits.  No call allocates: no cudaMalloc,
+ * cudaFree or allocating library routine.
+ *   - The first call on a device looks up that array's device address (once
+ *     per device, with that device current); make that first call before
+ *     any stream capture.
+ *   - Each GPU has its own copy of the array.  All calls on a GPU share it,
+ *     and it keeps the last call's contents; each call re-zeroes what must
+ *     start at zero.  Calls whose work overlaps on the same GPU (on two
+ *     streams, say) race on the array: serialise them.
+ * Errors: RQ_ERR_NULL; RQ_ERR_SHAPE for M, N < 1, K < 128, K % 128 != 0,
+ * misaligned pointers, or M_pad * K > RQ_NOALLOC_MAX_ACT_BYTES (the array
+ * is too small for this activation); RQ_ERR_CUDA. */
+#define RQ_NOALLOC_MAX_ACT_BYTES (8u * 1024u * 1024u)
+rq_status rq_fp8_linear_noalloc(const float *x, const uint8_t *w_fp8,
+                                const float *w_dequant, float *y, int M, int N,
+                                int K, rq_stream_t stream);
+
 /* Forget the cached FP8 activation (bump the generation). */
 rq_status rq_act_cache_invalidate(rq_ctx *ctx);
 

@@ -56,6 +56,7 @@ _SIGS = {
                              ctypes.POINTER(_vp), _vp], _i32),
     "rq_fp8_gemm": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp], _i32),
     "rq_linear": ([_vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _vp], _i32),
+    "rq_fp8_linear_noalloc": ([_vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp], _i32),
     "rq_act_cache_invalidate": ([_vp], _i32),
     "rq_ctx_trace_begin": ([_vp, _i32], _i32),
     "rq_ctx_trace_end": ([_vp, _vp, _vp], _i32),
@@ -123,6 +124,19 @@ def rq_q6k_gemv(w, x, y, M, N, K, stream=None):
 def rq_fp8_gemm(x_fp8, x_dequant, w_fp8, w_dequant, y, M, N, K, stream=None):
     _check(_lib.rq_fp8_gemm(_ptr(x_fp8), _ptr(x_dequant), _ptr(w_fp8), _ptr(w_dequant),
                             _ptr(y), M, N, K, _stream(stream)), "rq_fp8_gemm")
+
+
+NOALLOC_MAX_ACT_BYTES = 8 * 1024 * 1024
+
+
+def rq_fp8_linear_noalloc(x, w_fp8, w_dequant, y, M, N, K, stream=None):
+    """FP8 linear layer that allocates nothing (for callers that may not call
+    cudaMalloc while serving): the activation's E4M3 copy lives in a fixed
+    array inside the library, so (M rounded up to 16) * K must not exceed
+    NOALLOC_MAX_ACT_BYTES.  w_fp8 / w_dequant are device tensors or the
+    addresses Context.rq_fp8_weight_cache returns."""
+    _check(_lib.rq_fp8_linear_noalloc(_ptr(x), _ptr(w_fp8), _ptr(w_dequant), _ptr(y), M, N,
+                                      K, _stream(stream)), "rq_fp8_linear_noalloc")
 
 
 def rq_get_device_status(stream=None):
