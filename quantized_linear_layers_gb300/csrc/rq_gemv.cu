@@ -428,42 +428,66 @@ __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
   return *reinterpret_cast<const uint4*>(p);
 }
 
-// Dot product of one lane's 64 weights (header h, quants qa/qb of group g)
-// with the lane's x registers.
-__device__ __forceinline__ float q4_group_dot(const uint4& h, const uint4& qa,
-                                              const uint4& qb, int sh, bool upper,
-                                              const float (&xl)[32], const float (&xh)[32],
-                                              float hs_lo, float hs_hi, float s_lo,
-                                              float s_hi) {
+// Group coefficients from a header: (256 d sc_lo, 4096 d sc_hi, dmin m_lo,
+// dmin m_hi) for sub-blocks 2g, 2g+1.
+__device__ __forceinline__ float4 q4_coeffs(const uint4& h, int sh, bool upper) {
   const uint32_t a16 = h.y >> sh, b16 = h.z >> sh, c16 = h.w >> sh;
   const uint32_t scp = upper ? ((c16 & 0x0F0Fu) | ((a16 >> 2) & 0x3030u)) : (a16 & 0x3F3Fu);
   const uint32_t mp = upper ? (((c16 >> 4) & 0x0F0Fu) | ((b16 >> 2) & 0x3030u)) : (b16 & 0x3F3Fu);
   const float2 dd = half_pair(h.x);
-  const float a_lo = (dd.x * 256.0f) * (float)(scp & 0xFFu);
-  const float a_hi = (dd.x * 4096.0f) * (float)((scp >> 8) & 0xFFu);
-  const float d_lo = dd.y * (float)(mp & 0xFFu);
-  const float d_hi = dd.y * (float)((mp >> 8) & 0xFFu);
-  const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-  float tl0 = 0.f, tl1 = 0.f, th0 = 0.f, th1 = 0.f;
-#pragma unroll
-  for (int w = 0; w < 8; ++w) {
-    const uint32_t lo = q[w] & 0x0F0F0F0Fu, hi = q[w] & 0xF0F0F0F0u;
-    tl0 = fmaf(xl[4 * w + 0], mag_b2(lo, 0x7044u), tl0);
-    tl1 = fmaf(xl[4 * w + 1], mag_b2(lo, 0x7144u), tl1);
-    tl0 = fmaf(xl[4 * w + 2], mag_b2(lo, 0x7244u), tl0);
-    tl1 = fmaf(xl[4 * w + 3], mag_b2(lo, 0x7344u), tl1);
-    th0 = fmaf(xh[4 * w + 0], mag_b2(hi, 0x7404u), th0);
-    th1 = fmaf(xh[4 * w + 1], mag_b2(hi, 0x7414u), th1);
-    th0 = fmaf(xh[4 * w + 2], mag_b2(hi, 0x7424u), th0);
-    th1 = fmaf(xh[4 * w + 3], mag_b2(hi, 0x7434u), th1);
-  }
-  float c = a_lo * ((tl0 + tl1) - hs_lo);
-  c = fmaf(a_hi, (th0 + th1) - hs_hi, c);
-  c = fmaf(-d_lo, s_lo, c);
-  return fmaf(-d_hi, s_hi, c);
+  return make_float4((dd.x * 256.0f) * (float)(scp & 0xFFu),
+                     (dd.x * 4096.0f) * (float)((scp >> 8) & 0xFFu),
+                     dd.y * (float)(mp & 0xFFu), dd.y * (float)((mp >> 8) & 0xFFu));
 }
 
-__global__ void __launch_bounds__(384, 1) q4k_gemv_m1_kernel(const M1Args a) {
+// Two rows' 64-weight dot products with the same x registers, interleaved so
+// that their loads and FMA chains overlap.
+__device__ __forceinline__ float2 q4_group_dot2(const uint8_t* r0, const uint8_t* r1,
+                                                int off_h, int off_a, int sh, bool upper,
+                                                const float (&xl)[32], const float (&xh)[32],
+                                                float hs_lo, float hs_hi, float s_lo,
+                                                float s_hi) {
+  const uint4 h0 = lds128(r0 + off_h), h1 = lds128(r1 + off_h);
+  const uint4 a0 = lds128(r0 + off_a), a1 = lds128(r1 + off_a);
+  const uint4 b0 = lds128(r0 + off_a + 16), b1 = lds128(r1 + off_a + 16);
+  const uint32_t q0[8] = {a0.x, a0.y, a0.z, a0.w, b0.x, b0.y, b0.z, b0.w};
+  const uint32_t q1[8] = {a1.x, a1.y, a1.z, a1.w, b1.x, b1.y, b1.z, b1.w};
+  float l0 = 0.f, l1 = 0.f, g0 = 0.f, g1 = 0.f;  // row 0: lo, hi chains
+  float m0 = 0.f, m1 = 0.f, k0 = 0.f, k1 = 0.f;  // row 1
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const uint32_t lo0 = q0[w] & 0x0F0F0F0Fu, hi0 = q0[w] & 0xF0F0F0F0u;
+    const uint32_t lo1 = q1[w] & 0x0F0F0F0Fu, hi1 = q1[w] & 0xF0F0F0F0u;
+    l0 = fmaf(xl[4 * w + 0], mag_b2(lo0, 0x7044u), l0);
+    m0 = fmaf(xl[4 * w + 0], mag_b2(lo1, 0x7044u), m0);
+    l1 = fmaf(xl[4 * w + 1], mag_b2(lo0, 0x7144u), l1);
+    m1 = fmaf(xl[4 * w + 1], mag_b2(lo1, 0x7144u), m1);
+    l0 = fmaf(xl[4 * w + 2], mag_b2(lo0, 0x7244u), l0);
+    m0 = fmaf(xl[4 * w + 2], mag_b2(lo1, 0x7244u), m0);
+    l1 = fmaf(xl[4 * w + 3], mag_b2(lo0, 0x7344u), l1);
+    m1 = fmaf(xl[4 * w + 3], mag_b2(lo1, 0x7344u), m1);
+    g0 = fmaf(xh[4 * w + 0], mag_b2(hi0, 0x7404u), g0);
+    k0 = fmaf(xh[4 * w + 0], mag_b2(hi1, 0x7404u), k0);
+    g1 = fmaf(xh[4 * w + 1], mag_b2(hi0, 0x7414u), g1);
+    k1 = fmaf(xh[4 * w + 1], mag_b2(hi1, 0x7414u), k1);
+    g0 = fmaf(xh[4 * w + 2], mag_b2(hi0, 0x7424u), g0);
+    k0 = fmaf(xh[4 * w + 2], mag_b2(hi1, 0x7424u), k0);
+    g1 = fmaf(xh[4 * w + 3], mag_b2(hi0, 0x7434u), g1);
+    k1 = fmaf(xh[4 * w + 3], mag_b2(hi1, 0x7434u), k1);
+  }
+  const float4 c0 = q4_coeffs(h0, sh, upper), c1 = q4_coeffs(h1, sh, upper);
+  float p0 = c0.x * ((l0 + l1) - hs_lo);
+  p0 = fmaf(c0.y, (g0 + g1) - hs_hi, p0);
+  p0 = fmaf(-c0.z, s_lo, p0);
+  p0 = fmaf(-c0.w, s_hi, p0);
+  float p1 = c1.x * ((m0 + m1) - hs_lo);
+  p1 = fmaf(c1.y, (k0 + k1) - hs_hi, p1);
+  p1 = fmaf(-c1.z, s_lo, p1);
+  p1 = fmaf(-c1.w, s_hi, p1);
+  return make_float2(p0, p1);
+}
+
+__global__ void __launch_bounds__(544, 1) q4k_gemv_m1_kernel(const M1Args a) {
   extern __shared__ __align__(128) uint8_t smem_m1[];
   const int nsb = a.K >> 8, U = nsb * 4;
   const int rowbytes = nsb * kQ4KBytes;
@@ -536,7 +560,7 @@ __global__ void __launch_bounds__(384, 1) q4k_gemv_m1_kernel(const M1Args a) {
       s_hi += (vh.x + vh.y) + (vh.z + vh.w);
     }
     const float hs_lo = 0.5f * s_lo, hs_hi = 0.5f * s_hi;
-    const int off_h = sb * kQ4KBytes, off_a = off_h + 16 + 32 * g, off_b = off_a + 16;
+    const int off_h = sb * kQ4KBytes, off_a = off_h + 16 + 32 * g;
     for (int it = 0; it < iters; ++it) {
       const int s = it % a.stages;
       const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
@@ -544,14 +568,23 @@ __global__ void __launch_bounds__(384, 1) q4k_gemv_m1_kernel(const M1Args a) {
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
       const int nr = min(rps, rows - it * rps);
       const uint8_t* stage = ring + s * stage_bytes;
-      for (int rr = team; rr < nr; rr += a.teams) {
-        const uint8_t* rp = stage + rr * rowbytes;
-        float part = 0.f;
+      // this team's rows of the stage: team and team + teams (rps = 2 teams)
+      const int ra = team, rb = team + a.teams;
+      if (ra < nr) {
+        const bool two = rb < nr;
+        float2 part = make_float2(0.f, 0.f);
         if (active)
-          part = q4_group_dot(lds128(rp + off_h), lds128(rp + off_a), lds128(rp + off_b), sh,
-                              upper, xl, xh, hs_lo, hs_hi, s_lo, s_hi);
-        part = warp_sum(part);
-        if (lane == 0) atomicAdd(&acc[it * rps + rr], part);
+          part = q4_group_dot2(stage + ra * rowbytes, stage + (two ? rb : ra) * rowbytes, off_h,
+                               off_a, sh, upper, xl, xh, hs_lo, hs_hi, s_lo, s_hi);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          part.x += __shfl_xor_sync(0xFFFFFFFFu, part.x, o);
+          part.y += __shfl_xor_sync(0xFFFFFFFFu, part.y, o);
+        }
+        if (lane == 0) {
+          atomicAdd(&acc[it * rps + ra], part.x);
+          if (two) atomicAdd(&acc[it * rps + rb], part.y);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * s);
@@ -633,7 +666,7 @@ rq_status run_q4k_m1(const uint8_t* w, const float* x, float* y, int N, int K,
   a.N = N;
   a.K = K;
   a.team_warps = (U + 31) / 32;
-  a.teams = a.team_warps >= 8 ? 1 : 8 / a.team_warps;
+  a.teams = a.team_warps >= 16 ? 1 : 16 / a.team_warps;
   a.rows_per_stage = 2 * a.teams;
   const int rowbytes = (K / kQK) * kQ4KBytes;
   const int stage_bytes = a.rows_per_stage * rowbytes;
@@ -674,8 +707,8 @@ rq_status launch_q4k_gemv(const uint8_t* w, const float* x, float* y, int M,
   switch (M) {
     case 1:
       // the one-token kernel keeps 64 x values per lane in registers; its
-      // team of ceil(K/2048) warps plus the producer warp fit 384 threads
-      if (K <= 11 * 2048) return run_q4k_m1(w, x, y, N, K, st);
+      // team of ceil(K/2048) warps plus the producer warp fit 544 threads
+      if (K <= 16 * 2048) return run_q4k_m1(w, x, y, N, K, st);
       return run_q4k<1, 2>(w, x, y, N, K, st);
     case 2: return run_q4k<2, 2>(w, x, y, N, K, st);
     case 3: return run_q4k<3, 2>(w, x, y, N, K, st);
