@@ -19,6 +19,7 @@
 //    exactly; sum x*(0.5 + q*2^-p) - 0.5*sum x = 2^-p * sum x*q, so each
 //    weight costs one PRMT and one FFMA, and the 2^p is folded into d*sc.
 //  * fp32 accumulation, one warp-shuffle reduction per row.
+#include <cstdlib>
 #include <map>
 #include <utility>
 
@@ -397,8 +398,15 @@ q6k_gemv_kernel(const uint8_t* __restrict__ W, const float* __restrict__ x,
 // ------------------------------------------------- Q4_K, one token ---------
 //
 // M = 1 is the decode hot path.  Each lane owns one 64-weight quant group u
-// of every row and keeps x[64u .. 64u+63] (and its two 32-weight sums) in
-// registers for the whole kernel, so x costs no memory traffic per weight.
+// of every row and keeps x[64u .. 64u+63] in registers for the whole kernel,
+// so x costs no memory traffic per weight.  At the start the lane splits each
+// 32-value half of its x into three int8 planes, x = s (x1 + x2/128 +
+// x3/16384) to within max|x| / (127 * 32768); the 4-bit quants, masked to one
+// nibble per byte, then enter 4-way byte dot products (dp4a) against the
+// planes, three per four weights, and the sub-block sums are put back
+// together in fp32.  This is not an activation quantization: the planes
+// reproduce x to ~2^-22 of its sub-block maximum, far inside the GEMV
+// tolerance.
 // A team of ceil(K/64/32) warps covers K; a CTA runs `teams` teams and one
 // producer warp.  Each CTA owns a contiguous block of rows (the row blocks of
 // all CTAs differ by at most one row); the producer streams the block into a
@@ -440,61 +448,131 @@ __device__ __forceinline__ float4 q4_coeffs(const uint4& h, int sh, bool upper) 
                      dd.y * (float)(mp & 0xFFu), dd.y * (float)((mp >> 8) & 0xFFu));
 }
 
-// Two rows' 64-weight dot products with the same x registers, interleaved so
-// that their loads and FMA chains overlap.
-__device__ __forceinline__ float2 q4_group_dot2(const uint8_t* r0, const uint8_t* r1,
-                                                int off_h, int off_a, int sh, bool upper,
-                                                const float (&xl)[32], const float (&xh)[32],
-                                                float hs_lo, float hs_hi, float s_lo,
-                                                float s_hi) {
+// x of one 32-weight sub-block as three int8 planes: with s = max|x| / 127,
+// x = s * (x1 + x2 / 128 + x3 / 16384) + e, |e| <= max|x| / (127 * 32768).
+// t = x / s is rounded once (fp32 multiply); x1 = rint(t) and the residuals
+// t - x1 (|.| <= 1/2) and their x128 scalings are exact, so the only errors
+// are that rounding and the final residual.  Each plane holds values in
+// [-127, 127] resp. [-64, 64] packed four per register (byte j = element j).
+struct XSplit {
+  int p1[8], p2[8], p3[8];  // planes, 4 int8 per register
+  float scale;              // s
+  float sum;                // sum of the 32 x values (fp32)
+};
+
+// sum_l x_l * q_l for the 32 quants of one nibble plane (byte j of word w =
+// quant 4w + j), from the three integer plane products.
+struct Dot3 {
+  int a1, a2, a3;
+};
+
+__device__ __forceinline__ float dot3_value(const Dot3& d, float scale) {
+  const float v = fmaf((float)d.a3, 1.0f / 16384.0f, fmaf((float)d.a2, 1.0f / 128.0f, (float)d.a1));
+  return v * scale;
+}
+
+// Two rows' 64-weight dot products (integer path), interleaved.
+__device__ __forceinline__ float2 q4_group_dot2i(const uint8_t* r0, const uint8_t* r1,
+                                                 int off_h, int off_a, int sh, bool upper,
+                                                 const XSplit& xl, const XSplit& xh) {
   const uint4 h0 = lds128(r0 + off_h), h1 = lds128(r1 + off_h);
   const uint4 a0 = lds128(r0 + off_a), a1 = lds128(r1 + off_a);
   const uint4 b0 = lds128(r0 + off_a + 16), b1 = lds128(r1 + off_a + 16);
   const uint32_t q0[8] = {a0.x, a0.y, a0.z, a0.w, b0.x, b0.y, b0.z, b0.w};
   const uint32_t q1[8] = {a1.x, a1.y, a1.z, a1.w, b1.x, b1.y, b1.z, b1.w};
-  float l0 = 0.f, l1 = 0.f, g0 = 0.f, g1 = 0.f;  // row 0: lo, hi chains
-  float m0 = 0.f, m1 = 0.f, k0 = 0.f, k1 = 0.f;  // row 1
+  Dot3 l0 = {0, 0, 0}, g0 = {0, 0, 0}, l1 = {0, 0, 0}, g1 = {0, 0, 0};
 #pragma unroll
   for (int w = 0; w < 8; ++w) {
-    const uint32_t lo0 = q0[w] & 0x0F0F0F0Fu, hi0 = q0[w] & 0xF0F0F0F0u;
-    const uint32_t lo1 = q1[w] & 0x0F0F0F0Fu, hi1 = q1[w] & 0xF0F0F0F0u;
-    l0 = fmaf(xl[4 * w + 0], mag_b2(lo0, 0x7044u), l0);
-    m0 = fmaf(xl[4 * w + 0], mag_b2(lo1, 0x7044u), m0);
-    l1 = fmaf(xl[4 * w + 1], mag_b2(lo0, 0x7144u), l1);
-    m1 = fmaf(xl[4 * w + 1], mag_b2(lo1, 0x7144u), m1);
-    l0 = fmaf(xl[4 * w + 2], mag_b2(lo0, 0x7244u), l0);
-    m0 = fmaf(xl[4 * w + 2], mag_b2(lo1, 0x7244u), m0);
-    l1 = fmaf(xl[4 * w + 3], mag_b2(lo0, 0x7344u), l1);
-    m1 = fmaf(xl[4 * w + 3], mag_b2(lo1, 0x7344u), m1);
-    g0 = fmaf(xh[4 * w + 0], mag_b2(hi0, 0x7404u), g0);
-    k0 = fmaf(xh[4 * w + 0], mag_b2(hi1, 0x7404u), k0);
-    g1 = fmaf(xh[4 * w + 1], mag_b2(hi0, 0x7414u), g1);
-    k1 = fmaf(xh[4 * w + 1], mag_b2(hi1, 0x7414u), k1);
-    g0 = fmaf(xh[4 * w + 2], mag_b2(hi0, 0x7424u), g0);
-    k0 = fmaf(xh[4 * w + 2], mag_b2(hi1, 0x7424u), k0);
-    g1 = fmaf(xh[4 * w + 3], mag_b2(hi0, 0x7434u), g1);
-    k1 = fmaf(xh[4 * w + 3], mag_b2(hi1, 0x7434u), k1);
+    const int lo0 = (int)(q0[w] & 0x0F0F0F0Fu), hi0 = (int)((q0[w] >> 4) & 0x0F0F0F0Fu);
+    const int lo1 = (int)(q1[w] & 0x0F0F0F0Fu), hi1 = (int)((q1[w] >> 4) & 0x0F0F0F0Fu);
+    l0.a1 = __dp4a(lo0, xl.p1[w], l0.a1);
+    l1.a1 = __dp4a(lo1, xl.p1[w], l1.a1);
+    l0.a2 = __dp4a(lo0, xl.p2[w], l0.a2);
+    l1.a2 = __dp4a(lo1, xl.p2[w], l1.a2);
+    l0.a3 = __dp4a(lo0, xl.p3[w], l0.a3);
+    l1.a3 = __dp4a(lo1, xl.p3[w], l1.a3);
+    g0.a1 = __dp4a(hi0, xh.p1[w], g0.a1);
+    g1.a1 = __dp4a(hi1, xh.p1[w], g1.a1);
+    g0.a2 = __dp4a(hi0, xh.p2[w], g0.a2);
+    g1.a2 = __dp4a(hi1, xh.p2[w], g1.a2);
+    g0.a3 = __dp4a(hi0, xh.p3[w], g0.a3);
+    g1.a3 = __dp4a(hi1, xh.p3[w], g1.a3);
   }
+  // coefficients with the 2^p factors of the float path removed: (d sc_lo,
+  // d sc_hi, dmin m_lo, dmin m_hi)
   const float4 c0 = q4_coeffs(h0, sh, upper), c1 = q4_coeffs(h1, sh, upper);
-  float p0 = c0.x * ((l0 + l1) - hs_lo);
-  p0 = fmaf(c0.y, (g0 + g1) - hs_hi, p0);
-  p0 = fmaf(-c0.z, s_lo, p0);
-  p0 = fmaf(-c0.w, s_hi, p0);
-  float p1 = c1.x * ((m0 + m1) - hs_lo);
-  p1 = fmaf(c1.y, (k0 + k1) - hs_hi, p1);
-  p1 = fmaf(-c1.z, s_lo, p1);
-  p1 = fmaf(-c1.w, s_hi, p1);
+  const float dl0 = dot3_value(l0, xl.scale), dh0 = dot3_value(g0, xh.scale);
+  const float dl1 = dot3_value(l1, xl.scale), dh1 = dot3_value(g1, xh.scale);
+  float p0 = (c0.x * (1.0f / 256.0f)) * dl0;
+  p0 = fmaf(c0.y * (1.0f / 4096.0f), dh0, p0);
+  p0 = fmaf(-c0.z, xl.sum, p0);
+  p0 = fmaf(-c0.w, xh.sum, p0);
+  float p1 = (c1.x * (1.0f / 256.0f)) * dl1;
+  p1 = fmaf(c1.y * (1.0f / 4096.0f), dh1, p1);
+  p1 = fmaf(-c1.z, xl.sum, p1);
+  p1 = fmaf(-c1.w, xh.sum, p1);
   return make_float2(p0, p1);
 }
 
+// Round to the nearest integer with the fp32 magic constant 1.5 * 2^23
+// (valid for |t| < 2^22): returns the rounded value as a float and as an int.
+__device__ __forceinline__ float round_magic(float t, int& i) {
+  const float f = t + 12582912.0f;
+  i = __float_as_int(f) - 0x4B400000;
+  return f - 12582912.0f;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+// Sum each of the 8 per-lane values over the warp: afterwards lane l holds the
+// total of slot (l >> 2) & 7 (4 + 2 + 1 exchanging levels, then 2 plain).
+__device__ __forceinline__ float reduce8(float (&v)[8], int lane) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const bool up = lane & 16;
+    const float send = up ? v[i] : v[i + 4], keep = up ? v[i + 4] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const bool up = lane & 8;
+    const float send = up ? v[i] : v[i + 2], keep = up ? v[i + 2] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
+  }
+  {
+    const bool up = lane & 4;
+    const float send = up ? v[0] : v[1], keep = up ? v[1] : v[0];
+    v[0] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 4);
+  }
+  v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], 2);
+  v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], 1);
+  return v[0];
+}
+
+// Shared-memory layout of the x planes: per 64-weight unit u, 208 bytes:
+// plane p (0..2) half h (0 = low nibbles, 1 = high) byte l at p*64 + h*32 + l;
+// the 16 padding bytes make 16-byte reads of consecutive units conflict-free.
+constexpr int kPlaneStride = 208;
+
+template <int RPT>
 __global__ void __launch_bounds__(544, 1) q4k_gemv_m1_kernel(const M1Args a) {
+  static_assert(RPT == 2 || RPT == 4 || RPT == 8, "rows per team per stage");
+  constexpr int SPB = 8 / RPT;  // stages per 8-row reduction batch
   extern __shared__ __align__(128) uint8_t smem_m1[];
-  const int nsb = a.K >> 8, U = nsb * 4;
+  const int nsb = a.K >> 8, U = nsb * 4, nsub = a.K >> 5;
   const int rowbytes = nsb * kQ4KBytes;
-  const int rps = a.rows_per_stage;
+  const int rps = a.rows_per_stage;  // teams * RPT
   const uint32_t stage_bytes = (uint32_t)(rps * rowbytes);
   uint8_t* ring = smem_m1;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + a.ring_bytes);  // full[], empty[]
+  uint8_t* planes = ring + a.ring_bytes;                              // U * 208
+  const int nsub2 = (nsub + 1) & ~1;  // keeps the barriers 8-byte aligned
+  float* xscale = reinterpret_cast<float*>(planes + U * kPlaneStride);  // nsub2
+  float* xsum = xscale + nsub2;                                        // nsub2
+  uint64_t* bars = reinterpret_cast<uint64_t*>(xsum + nsub2);
   float* acc = reinterpret_cast<float*>(bars + 2 * a.stages);
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + a.stages);
 
@@ -504,6 +582,7 @@ __global__ void __launch_bounds__(544, 1) q4k_gemv_m1_kernel(const M1Args a) {
   const int r1 = (int)((int64_t)(blockIdx.x + 1) * a.N / gridDim.x);
   const int rows = r1 - r0;
   const int iters = (rows + rps - 1) / rps;
+  const int first = iters < a.stages ? iters : a.stages;
 
   for (int i = threadIdx.x; i < rows; i += blockDim.x) acc[i] = 0.f;
   if (threadIdx.x == 0) {
@@ -515,79 +594,158 @@ __global__ void __launch_bounds__(544, 1) q4k_gemv_m1_kernel(const M1Args a) {
   }
   __syncthreads();
 
-  if (warp == compute_warps) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t issued = 0, parity_bits = 0;
-      for (int it = 0; it < iters; ++it) {
-        const int s = it % a.stages;
-        const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
-        if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, a.wait_limit_ns, &g_gemv_error)) break;
-        const int nr = min(rps, rows - it * rps);
-        const uint32_t bytes = (uint32_t)(nr * rowbytes);
-        mbar_arrive_expect_tx(full0 + 8 * s, bytes);
-        bulk_g2s(smem_u32(ring + s * stage_bytes),
-                 a.W + (size_t)(r0 + it * rps) * rowbytes, bytes, full0 + 8 * s);
-        issued |= 1u << s;
-        parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
-      }
-      // every issued copy has landed before the CTA can exit
-      for (int s = 0; s < a.stages; ++s)
-        if (issued & (1u << s))
-          mbar_wait(full0 + 8 * s, (parity_bits >> s) & 1u, a.wait_limit_ns, &g_gemv_error);
+  // ------------------------------------------------------------ producer --
+  uint32_t issued = 0, parity_bits = 0;
+  bool prod_ok = true;
+  auto produce = [&](int it) {
+    const int s = it % a.stages;
+    const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
+    if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, a.wait_limit_ns, &g_gemv_error)) {
+      prod_ok = false;
+      return;
     }
+    const int nr = min(rps, rows - it * rps);
+    const uint32_t bytes = (uint32_t)(nr * rowbytes);
+    mbar_arrive_expect_tx(full0 + 8 * s, bytes);
+    bulk_g2s(smem_u32(ring + s * stage_bytes), a.W + (size_t)(r0 + it * rps) * rowbytes, bytes,
+             full0 + 8 * s);
+    issued |= 1u << s;
+    parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
+  };
+  const bool producer = warp == compute_warps && lane == 0;
+  // the first ring's worth of copies is in flight while x is prepared
+  if (producer)
+    for (int it = 0; it < first && prod_ok; ++it) produce(it);
+
+  // ------------------------------------------------ x planes (all compute warps)
+  // Four lanes per 32-value sub-block, eight values each: coalesced 16-byte
+  // loads, a two-level shuffle for the sub-block's max and sum, and 8-byte
+  // stores of each plane's bytes.
+  if (warp < compute_warps) {
+    const int q = lane & 3;
+    for (int sb32 = warp * 8 + (lane >> 2); sb32 < nsub; sb32 += compute_warps * 8) {
+      const float4* px = reinterpret_cast<const float4*>(a.x + 32 * sb32 + 8 * q);
+      const float4 va = __ldg(px), vb = __ldg(px + 1);
+      const float v[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+      float mx = 0.f, sm = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        mx = fmaxf(mx, fabsf(v[i]));
+        sm += v[i];
+      }
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+      sm += __shfl_xor_sync(0xFFFFFFFFu, sm, 1);
+      sm += __shfl_xor_sync(0xFFFFFFFFu, sm, 2);
+      const float inv = mx > 0.f ? 127.0f / mx : 0.0f;
+      uint32_t b1[2] = {0, 0}, b2[2] = {0, 0}, b3[2] = {0, 0};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float t = fminf(fmaxf(v[i] * inv, -127.0f), 127.0f);
+        int i1, i2, i3;
+        const float f1 = round_magic(t, i1);
+        const float u2 = (t - f1) * 128.0f;
+        const float f2 = round_magic(u2, i2);
+        round_magic((u2 - f2) * 128.0f, i3);
+        const int sh8 = 8 * (i & 3);
+        b1[i >> 2] |= ((uint32_t)i1 & 0xFFu) << sh8;
+        b2[i >> 2] |= ((uint32_t)i2 & 0xFFu) << sh8;
+        b3[i >> 2] |= ((uint32_t)i3 & 0xFFu) << sh8;
+      }
+      uint8_t* pl = planes + (sb32 >> 1) * kPlaneStride + (sb32 & 1) * 32 + 8 * q;
+      *reinterpret_cast<uint2*>(pl) = make_uint2(b1[0], b1[1]);
+      *reinterpret_cast<uint2*>(pl + 64) = make_uint2(b2[0], b2[1]);
+      *reinterpret_cast<uint2*>(pl + 128) = make_uint2(b3[0], b3[1]);
+      if (q == 0) {
+        xscale[sb32] = mx > 0.f ? mx / 127.0f : 1.0f;
+        xsum[sb32] = sm;
+      }
+    }
+  }
+  __syncthreads();
+
+  if (producer) {
+    for (int it = first; it < iters && prod_ok; ++it) produce(it);
+    // every issued copy has landed before the CTA can exit
+    for (int s = 0; s < a.stages; ++s)
+      if (issued & (1u << s))
+        mbar_wait(full0 + 8 * s, (parity_bits >> s) & 1u, a.wait_limit_ns, &g_gemv_error);
   } else if (warp < compute_warps) {
-    // ------------------------------------------------------------- compute
+    // ------------------------------------------------------------ compute --
     const int team = warp / a.team_warps, wt = warp - team * a.team_warps;
     const int u = wt * 32 + lane;
     const bool active = u < U;
     const int sb = u >> 2, g = u & 3;
     const int sh = (g & 1) * 16;
     const bool upper = g >= 2;
-    float xl[32], xh[32];
-    float s_lo = 0.f, s_hi = 0.f;
+    XSplit xsl, xsh;
+    if (active) {
+      const uint8_t* pu = planes + u * kPlaneStride;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float4 vl = make_float4(0.f, 0.f, 0.f, 0.f), vh = vl;
-      if (active) {
-        const float4* px = reinterpret_cast<const float4*>(a.x + 64 * u);
-        vl = __ldg(px + j);
-        vh = __ldg(px + 8 + j);
+      for (int h = 0; h < 2; ++h) {
+        XSplit& xs = h ? xsh : xsl;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const uint4 v1 = lds128(pu + 0 + 32 * h + 16 * c);
+          const uint4 v2 = lds128(pu + 64 + 32 * h + 16 * c);
+          const uint4 v3 = lds128(pu + 128 + 32 * h + 16 * c);
+          xs.p1[4 * c] = v1.x; xs.p1[4 * c + 1] = v1.y; xs.p1[4 * c + 2] = v1.z; xs.p1[4 * c + 3] = v1.w;
+          xs.p2[4 * c] = v2.x; xs.p2[4 * c + 1] = v2.y; xs.p2[4 * c + 2] = v2.z; xs.p2[4 * c + 3] = v2.w;
+          xs.p3[4 * c] = v3.x; xs.p3[4 * c + 1] = v3.y; xs.p3[4 * c + 2] = v3.z; xs.p3[4 * c + 3] = v3.w;
+        }
+        xs.scale = xscale[2 * u + h];
+        xs.sum = xsum[2 * u + h];
       }
-      xl[4 * j] = vl.x; xl[4 * j + 1] = vl.y; xl[4 * j + 2] = vl.z; xl[4 * j + 3] = vl.w;
-      xh[4 * j] = vh.x; xh[4 * j + 1] = vh.y; xh[4 * j + 2] = vh.z; xh[4 * j + 3] = vh.w;
-      s_lo += (vl.x + vl.y) + (vl.z + vl.w);
-      s_hi += (vh.x + vh.y) + (vh.z + vh.w);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        xsl.p1[i] = xsl.p2[i] = xsl.p3[i] = xsh.p1[i] = xsh.p2[i] = xsh.p3[i] = 0;
+      }
+      xsl.scale = xsh.scale = 1.f;
+      xsl.sum = xsh.sum = 0.f;
     }
-    const float hs_lo = 0.5f * s_lo, hs_hi = 0.5f * s_hi;
     const int off_h = sb * kQ4KBytes, off_a = off_h + 16 + 32 * g;
-    for (int it = 0; it < iters; ++it) {
-      const int s = it % a.stages;
-      const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
-      const bool ok = mbar_wait(full0 + 8 * s, ph, a.wait_limit_ns, &g_gemv_error);
-      if (!__all_sync(0xFFFFFFFFu, ok)) break;
-      const int nr = min(rps, rows - it * rps);
-      const uint8_t* stage = ring + s * stage_bytes;
-      // this team's rows of the stage: team and team + teams (rps = 2 teams)
-      const int ra = team, rb = team + a.teams;
-      if (ra < nr) {
-        const bool two = rb < nr;
-        float2 part = make_float2(0.f, 0.f);
-        if (active)
-          part = q4_group_dot2(stage + ra * rowbytes, stage + (two ? rb : ra) * rowbytes, off_h,
-                               off_a, sh, upper, xl, xh, hs_lo, hs_hi, s_lo, s_hi);
+    bool ok = true;
+    for (int it0 = 0; it0 < iters && ok; it0 += SPB) {
+      float pa[8];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          part.x += __shfl_xor_sync(0xFFFFFFFFu, part.x, o);
-          part.y += __shfl_xor_sync(0xFFFFFFFFu, part.y, o);
-        }
-        if (lane == 0) {
-          atomicAdd(&acc[it * rps + ra], part.x);
-          if (two) atomicAdd(&acc[it * rps + rb], part.y);
+      for (int i = 0; i < 8; ++i) pa[i] = 0.f;
+#pragma unroll
+      for (int q = 0; q < SPB; ++q) {
+        const int it = it0 + q;
+        if (it < iters && ok) {
+          const int s = it % a.stages;
+          const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * s, ph, a.wait_limit_ns, &g_gemv_error));
+          if (ok) {
+            const int nr = min(rps, rows - it * rps);
+            const uint8_t* stage = ring + s * stage_bytes + (size_t)team * RPT * rowbytes;
+#pragma unroll
+            for (int j = 0; j < RPT; j += 2) {
+              const int ra = team * RPT + j;
+              if (active && ra < nr) {
+                const bool two = ra + 1 < nr;
+                const float2 p2 = q4_group_dot2i(stage + j * rowbytes,
+                                                 stage + (two ? j + 1 : j) * rowbytes, off_h,
+                                                 off_a, sh, upper, xsl, xsh);
+                pa[q * RPT + j] = p2.x;
+                pa[q * RPT + j + 1] = two ? p2.y : 0.f;
+              }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * s);
+          }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+      // slot (lane >> 2) & 7 of this warp's 8 rows: stage it0 + slot / RPT,
+      // team row slot % RPT
+      const float tot = reduce8(pa, lane);
+      const int slot = (lane >> 2) & 7;
+      const int it = it0 + slot / RPT;
+      if ((lane & 3) == 0 && it < iters) {
+        const int rr = team * RPT + slot % RPT;
+        if (rr < min(rps, rows - it * rps)) atomicAdd(&acc[it * rps + rr], tot);
+      }
     }
   }
   __syncthreads();
@@ -654,11 +812,23 @@ rq_status run_q6k(const uint8_t* w, const float* x, float* y, int N, int K,
   return launch_status();
 }
 
-// One-token Q4_K launch: team_warps = ceil(K/64/32), ~8 compute warps per
-// CTA, one CTA per SM, a ring of up to 8 stages within ~150 KB.
+// One-token Q4_K launch: team_warps = ceil(K/64/32), up to 16 compute warps
+// per CTA, one CTA per SM, shared memory split between the x planes and a
+// ring of weight stages.  The RQ_GEMV_* environment variables override the
+// launch shape for tuning runs.
 rq_status run_q4k_m1(const uint8_t* w, const float* x, float* y, int N, int K,
                      cudaStream_t st) {
-  const int U = K / 64;
+  auto knob = [](const char* name, int dflt, int lo, int hi) {
+    const char* e = std::getenv(name);
+    const int v = e ? std::atoi(e) : dflt;
+    return v < lo ? lo : (v > hi ? hi : v);
+  };
+  const int warps_per_cta = knob("RQ_GEMV_WARPS", 16, 1, 16);
+  int rpt = knob("RQ_GEMV_RPT", 4, 2, 8);
+  rpt = rpt >= 8 ? 8 : (rpt >= 4 ? 4 : 2);
+  const int ring_kb = knob("RQ_GEMV_RING_KB", 150, 16, 200);
+  const int max_stages = knob("RQ_GEMV_STAGES", 8, 2, 16);
+  const int U = K / 64, nsub = K / 32;
   M1Args a;
   a.W = w;
   a.x = x;
@@ -666,28 +836,40 @@ rq_status run_q4k_m1(const uint8_t* w, const float* x, float* y, int N, int K,
   a.N = N;
   a.K = K;
   a.team_warps = (U + 31) / 32;
-  a.teams = a.team_warps >= 16 ? 1 : 16 / a.team_warps;
-  a.rows_per_stage = 2 * a.teams;
+  a.teams = a.team_warps >= warps_per_cta ? 1 : warps_per_cta / a.team_warps;
+  a.rows_per_stage = rpt * a.teams;
   const int rowbytes = (K / kQK) * kQ4KBytes;
   const int stage_bytes = a.rows_per_stage * rowbytes;
-  int stages = (150 * 1024) / stage_bytes;
-  stages = stages > 8 ? 8 : (stages < 2 ? 2 : stages);
-  a.stages = stages;
-  a.ring_bytes = (uint32_t)(stages * stage_bytes);
-  a.wait_limit_ns = kWaitLimitNs;
   const int sms = device_sm_count();
   const int grid = N < sms ? N : sms;
   const int max_rows = (N + grid - 1) / grid;
-  const size_t smem = a.ring_bytes + 16 * (size_t)stages + 4 * (size_t)max_rows;
+  const size_t nsub2 = (size_t)((nsub + 1) & ~1);
+  const size_t fixed = (size_t)U * kPlaneStride + 8 * nsub2 +
+                       16 * (size_t)max_stages + 4 * (size_t)max_rows;
+  const size_t limit = 227 * 1024;
+  if (fixed + 2 * (size_t)stage_bytes > limit) return RQ_ERR_SHAPE;
+  size_t ring = (size_t)ring_kb * 1024;
+  if (ring > limit - fixed) ring = limit - fixed;
+  int stages = (int)(ring / stage_bytes);
+  stages = stages > max_stages ? max_stages : (stages < 2 ? 2 : stages);
+  a.stages = stages;
+  a.ring_bytes = (uint32_t)(stages * stage_bytes);
+  a.wait_limit_ns = kWaitLimitNs;
+  const size_t smem = a.ring_bytes + (size_t)U * kPlaneStride + 8 * nsub2 +
+                      16 * (size_t)stages +
+                      4 * (size_t)max_rows;
   const int threads = (a.teams * a.team_warps + 1) * 32;
-  static size_t smem_set = 48 * 1024;
-  if (smem > smem_set) {
-    if (cudaFuncSetAttribute(q4k_gemv_m1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
+  auto kern = rpt == 8 ? q4k_gemv_m1_kernel<8>
+                       : (rpt == 4 ? q4k_gemv_m1_kernel<4> : q4k_gemv_m1_kernel<2>);
+  static size_t smem_set[3] = {48 * 1024, 48 * 1024, 48 * 1024};
+  size_t& set = smem_set[rpt == 8 ? 2 : (rpt == 4 ? 1 : 0)];
+  if (smem > set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
       return RQ_ERR_CUDA;
-    smem_set = smem;
+    set = smem;
   }
-  q4k_gemv_m1_kernel<<<grid, threads, smem, st>>>(a);
+  kern<<<grid, threads, smem, st>>>(a);
   return launch_status();
 }
 
@@ -708,7 +890,12 @@ rq_status launch_q4k_gemv(const uint8_t* w, const float* x, float* y, int M,
     case 1:
       // the one-token kernel keeps 64 x values per lane in registers; its
       // team of ceil(K/2048) warps plus the producer warp fit 544 threads
-      if (K <= 16 * 2048) return run_q4k_m1(w, x, y, N, K, st);
+      if (K <= 16 * 2048) {
+        // RQ_ERR_SHAPE here means the launch shape does not fit shared
+        // memory; nothing was launched, so the generic kernel takes it
+        const rq_status s1 = run_q4k_m1(w, x, y, N, K, st);
+        if (s1 != RQ_ERR_SHAPE) return s1;
+      }
       return run_q4k<1, 2>(w, x, y, N, K, st);
     case 2: return run_q4k<2, 2>(w, x, y, N, K, st);
     case 3: return run_q4k<3, 2>(w, x, y, N, K, st);
