@@ -433,19 +433,23 @@ def run_gpu(args, world, rank, local):
 
 
 def gemm_traffic_per_launch():
-    """DRAM bytes per GEMM launch from the committed ncu capture, if it was
-    taken on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", "fp8_gemm_traffic.json")
+    """DRAM bytes per GEMM launch (stack average) from the committed ncu
+    summary, if it was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "fp8_gemm_traffic.txt")
     src = os.path.join(ROOT, "quantized_linear_layers_gb300", "csrc", "rq_gemm.cu")
     if not os.path.exists(path):
         return None
+    rec = {}
     with open(path) as f:
-        rec = json.load(f)
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                rec[k.strip()] = v.strip()
     with open(src, "rb") as f:
         h = hashlib.sha256(f.read()).hexdigest()
     if rec.get("kernel_source_sha256") != h:
         return None
-    return rec.get("traffic_bytes_per_launch")
+    return int(rec["traffic_bytes_per_launch"])
 
 
 def run_e2e(args, st, torch, rq, dev, stream, world):
