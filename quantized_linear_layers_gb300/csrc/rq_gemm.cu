@@ -289,6 +289,257 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
   }
 }
 
+// ------------------------------------------------------ 2-CTA variant ----
+//
+// A cluster of two CTAs (a "pair") computes a 256 x BN output tile with
+// tcgen05.mma.cta_group::2 (M = 256): CTA r of the pair holds weight rows
+// 128r .. 128r+127 of the tile (A) and token rows r*BN/2 .. of the tile (B),
+// so each SM streams half of the B tile the 1-CTA kernel needs and the
+// tensor cores read half the shared-memory operand bytes per MAC.  Only the
+// leader (rank 0) issues MMAs; both CTAs' TMA loads complete on the leader's
+// "full" barriers, the leader's commits arrive on both CTAs' "empty" and
+// "tmem full" barriers (multicast), and both CTAs' epilogue warps arrive on
+// the leader's "tmem empty" barriers.  Each CTA's TMEM holds its 128 rows of
+// the accumulator.  All waits are bounded as in the 1-CTA kernel.
+
+constexpr int kStages2 = 6;
+constexpr int kBHalfMax = kMaxBN / 2 * kBK;  // 16 KB: this CTA's half of B
+constexpr int kSmemBytes2 = kStages2 * (kABytes + kBHalfMax) + 1024 + 1024;
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// shared::cluster address of the same shared variable in CTA `rank`.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx_cluster(uint32_t cluster_bar, uint32_t bytes) {
+  asm volatile(
+      "mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
+          cluster_bar),
+      "r"(bytes)
+      : "memory");
+}
+
+// TMA load into this CTA's shared memory, completing on the pair leader's
+// barrier (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t leader_bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(leader_bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_f8_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on the barrier at this shared offset in both CTAs of the pair
+// when this thread's earlier tcgen05 operations complete.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(bar),
+      "h"((unsigned short)3)
+      : "memory");
+}
+
+// Arrive on this CTA's own barrier when this thread's earlier tcgen05
+// operations complete (pair granularity).
+__device__ __forceinline__ void mma_commit_pair_local(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                     const __grid_constant__ CUtensorMap tmap_x, const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;                            // kStages2 x 16 KB
+  uint8_t* sB = smem + kStages2 * kABytes;       // kStages2 x 16 KB (half the token tile)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages2 * kBHalfMax);
+  // bars: full[kStages2], empty[kStages2], tfull[2], tempty[2], done[1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages2 + 5);
+
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages2);
+  const uint32_t tfull0 = smem_u32(bars + 2 * kStages2);
+  const uint32_t tempty0 = smem_u32(bars + 2 * kStages2 + 2);
+  const uint32_t done_bar = smem_u32(bars + 2 * kStages2 + 4);
+  const int bn = args.bn, half = bn / 2;
+  const int kblocks = args.K / kBK;
+  const int ntiles = args.tiles_n * args.tiles_m;  // tiles_n counts 256-row tiles
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const uint32_t stage_tx = (uint32_t)(kABytes + half * kBK);  // per CTA
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages2; ++s) {
+      mbar_init(full0 + 8 * s, 2);   // one expect_tx arrival per CTA (leader's is used)
+      mbar_init(empty0 + 8 * s, 1);  // the leader's commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull0 + 8 * b, 1);
+      mbar_init(tempty0 + 8 * b, 8);  // 4 epilogue warps x 2 CTAs (leader's is used)
+    }
+    mbar_init(done_bar, 1);
+    mbar_fence_init();
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_x)) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(args.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers are initialised before any remote use
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------- TMA producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = pair; t < ntiles && ok; t += npairs) {
+        const int tn = t / args.tiles_m, tm = t - tn * args.tiles_m;
+        const int wrow = tn * 256 + (int)rank * kBM;
+        const int trow = tm * bn + (int)rank * half;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, args.wait_limit_ns, &g_rq_device_error)) {
+            ok = false;
+            break;
+          }
+          const uint32_t lead_full = peer_addr(full0 + 8 * stage, 0);
+          mbar_expect_tx_cluster(lead_full, stage_tx);
+          tma_load_2d_pair(smem_u32(sA + stage * kABytes), &tmap_w, lead_full, kb * kBK, wrow);
+          tma_load_2d_pair(smem_u32(sB + stage * kBHalfMax), &tmap_x, lead_full, kb * kBK, trow);
+          if (++stage == kStages2) { stage = 0; phase ^= 1; }
+        }
+      }
+      // Drain: this CTA's last copies have landed once the leader's MMAs
+      // that consume them have freed the stages (seen on our own "empty").
+      for (int i = 0; i < kStages2 && ok; ++i) {
+        if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, args.wait_limit_ns, &g_rq_device_error))
+          break;
+        if (++stage == kStages2) { stage = 0; phase ^= 1; }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------- MMA issuer (leader)
+    if (leader && lane == 0) {
+      const uint32_t idesc = instr_desc(256, bn);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = pair; t < ntiles && ok; t += npairs) {
+        if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, args.wait_limit_ns, &g_rq_device_error))
+          break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * bn);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(full0 + 8 * stage, phase, args.wait_limit_ns, &g_rq_device_error)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + stage * kABytes);
+          const uint32_t b_addr = smem_u32(sB + stage * kBHalfMax);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 32; ++kk)
+            mma_f8_pair(d_tmem, smem_desc(a_addr + 32 * kk), smem_desc(b_addr + 32 * kk), idesc,
+                        (kb | kk) != 0);
+          mma_commit_pair(empty0 + 8 * stage);
+          if (++stage == kStages2) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        mma_commit_pair(tfull0 + 8 * acc);
+        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      }
+      mma_commit_pair_local(done_bar);
+      mbar_wait(done_bar, 0, args.wait_limit_ns, &g_rq_device_error);
+    }
+  } else {
+    // --------------------------------------------------- epilogue (both)
+    const int quad = warp & 3;
+    const float scale_x = *args.x_deq, scale_w = *args.w_deq;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = pair; t < ntiles; t += npairs) {
+      const int tn = t / args.tiles_m, tm = t - tn * args.tiles_m;
+      const bool ready =
+          mbar_wait(tfull0 + 8 * acc, acc_phase, args.wait_limit_ns, &g_rq_device_error);
+      if (!__all_sync(0xFFFFFFFFu, ready)) break;
+      tc_fence_after();
+      const int n = tn * 256 + (int)rank * kBM + quad * 32 + lane;
+      const int m0 = tm * bn;
+      const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * bn);
+      for (int c = 0; c < bn; c += 16) {
+        uint32_t v[16];
+        tmem_ld16(taddr + (uint32_t)c, v);
+        if (n < args.N) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int m = m0 + c + j;
+            if (m < args.M)
+              args.y[(size_t)m * args.N + n] = (__uint_as_float(v[j]) * scale_x) * scale_w;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(peer_addr(tempty0 + 8 * acc, 0));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // neither CTA leaves while its peer may still touch its memory
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(args.tmem_cols)
+                 : "memory");
+  }
+}
+
 // A block that waits on an mbarrier nothing completes (timeout test hook).
 __global__ void wait_timeout_kernel(uint64_t limit_ns) {
   __shared__ uint64_t bar;
@@ -366,6 +617,57 @@ int choose_bn(int m_pad, int N, int sms) {
   return best;
 }
 
+// Tokens per tile for the pair kernel: multiples of 32 (each CTA holds half),
+// same round-based cost model over the SM pairs.
+int choose_bn_pair(int m_pad, int N, int pairs) {
+  const char* env = std::getenv("RQ_GEMM_BN");
+  const int v = env ? std::atoi(env) : 0;
+  const int m32 = (m_pad + 31) / 32 * 32;
+  if (v >= 32 && v <= kMaxBN && v % 32 == 0) return v < m32 ? v : m32;
+  if (m32 <= kMaxBN) return m32;
+  const long tiles_n = (N + 255) / 256;
+  int best = kMaxBN;
+  long best_cost = -1;
+  for (int bn = kMaxBN; bn >= 64; bn -= 32) {
+    const long tiles = tiles_n * ((m_pad + bn - 1) / bn);
+    const long rounds = (tiles + pairs - 1) / pairs;
+    const long cost = rounds * (bn + 48);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+// Number of CTA pairs of the pair kernel that fit on the GPU at once.
+int resident_pairs(int sms) {
+  static int cached = 0;
+  if (cached == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (sms / 2));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes2;
+    int n = 0;
+    cudaFuncSetAttribute(fp8_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         kSmemBytes2);
+    if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_pair_kernel, &cfg) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = 1;
+    }
+    cached = n;
+  }
+  return cached;
+}
+
+// The pair kernel is opt-in (RQ_GEMM_PAIR=1) until it outruns the
+// one-CTA kernel on the prefill shapes.
+bool use_pair_kernel(int N) {
+  const char* env = std::getenv("RQ_GEMM_PAIR");
+  if (env == nullptr || std::atoi(env) == 0) return false;
+  return N > kBM;
+}
+
 }  // namespace
 
 rq_status launch_fp8_gemm(const uint8_t* x_fp8, const float* x_deq,
@@ -373,9 +675,10 @@ rq_status launch_fp8_gemm(const uint8_t* x_fp8, const float* x_deq,
                           int M, int N, int K, cudaStream_t st) {
   const int m_pad = (M + 15) / 16 * 16;
   const int sms = device_sm_count();
-  const int bn = choose_bn(m_pad, N, sms);
+  const bool pair = use_pair_kernel(N) && sms >= 2;
+  const int bn = pair ? choose_bn_pair(m_pad, N, resident_pairs(sms)) : choose_bn(m_pad, N, sms);
   CUtensorMap tw, tx;
-  if (!make_map(&tw, w_fp8, N, K, kBM) || !make_map(&tx, x_fp8, m_pad, K, bn))
+  if (!make_map(&tw, w_fp8, N, K, kBM) || !make_map(&tx, x_fp8, m_pad, K, pair ? bn / 2 : bn))
     return RQ_ERR_CUDA;
   GemmArgs a;
   a.x_deq = x_deq;
@@ -385,10 +688,26 @@ rq_status launch_fp8_gemm(const uint8_t* x_fp8, const float* x_deq,
   a.N = N;
   a.K = K;
   a.bn = bn;
-  a.tiles_n = (N + kBM - 1) / kBM;
+  a.tiles_n = pair ? (N + 255) / 256 : (N + kBM - 1) / kBM;
   a.tiles_m = (m_pad + bn - 1) / bn;
   a.tmem_cols = tmem_columns(bn);
   a.wait_limit_ns = kWaitLimitNs;
+  const int tiles = a.tiles_n * a.tiles_m;
+  if (pair) {
+    static bool attr2 = false;
+    if (!attr2) {
+      if (cudaFuncSetAttribute(fp8_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmemBytes2) != cudaSuccess)
+        return RQ_ERR_CUDA;
+      attr2 = true;
+    }
+    // A persistent grid must be resident at once: not every SM can be
+    // paired inside its GPC, so the grid is the number of pairs that fit.
+    const int max_pairs = resident_pairs(sms);
+    const int grid = 2 * (tiles < max_pairs ? tiles : max_pairs);
+    fp8_gemm_pair_kernel<<<grid, kThreads, kSmemBytes2, st>>>(tw, tx, a);
+    return launch_status();
+  }
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(fp8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -396,7 +715,6 @@ rq_status launch_fp8_gemm(const uint8_t* x_fp8, const float* x_deq,
       return RQ_ERR_CUDA;
     attr_done = true;
   }
-  const int tiles = a.tiles_n * a.tiles_m;
   const int grid = tiles < sms ? tiles : sms;
   fp8_gemm_kernel<<<grid, kThreads, kSmemBytes, st>>>(tw, tx, a);
   return launch_status();

@@ -147,3 +147,19 @@ def test_forced_tile_widths(rq, bn, monkeypatch):
     Wb = random_e4m3(78, (N, K))
     got = gpu_gemm(rq, Xb, 0.01, Wb, 0.02, M)
     check_full(got, oracle.fp8_gemm(Xb, 0.01, Wb, 0.02))
+
+
+@pytest.mark.parametrize("pair", ["0", "1"])
+@pytest.mark.parametrize("M,N,K,bn", [(17, 256, 256, 0), (300, 384, 512, 0), (64, 1000, 384, 0),
+                                      (512, 640, 1024, 128), (2048, 512, 3584, 0),
+                                      (700, 3584, 256, 224)])
+def test_single_and_pair_kernels(rq, monkeypatch, pair, M, N, K, bn):
+    """The one-CTA and the CTA-pair (cta_group::2) kernels agree with the
+    oracle on ragged shapes, including weight-row tiles that straddle N."""
+    monkeypatch.setenv("RQ_GEMM_PAIR", pair)
+    if bn:
+        monkeypatch.setenv("RQ_GEMM_BN", str(bn))
+    Xb = random_e4m3(M + 3 * N, (M, K))
+    Wb = random_e4m3(N + 5 * K, (N, K))
+    got = gpu_gemm(rq, Xb, 0.01, Wb, 0.02, M)
+    check_full(got, oracle.fp8_gemm(Xb, 0.01, Wb, 0.02))
