@@ -324,17 +324,12 @@ __device__ __forceinline__ void cluster_sync() {
                    : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+// Remote arrive without release semantics: a release at cluster scope would
+// make the arriving thread wait for all its earlier global stores.  Callers
+// order what must be ordered (tcgen05 reads) with tcgen05 fences.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx_cluster(uint32_t cluster_bar, uint32_t bytes) {
-  asm volatile(
-      "mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
-          cluster_bar),
-      "r"(bytes)
-      : "memory");
 }
 
 // TMA load into this CTA's shared memory, completing on the pair leader's
@@ -399,11 +394,11 @@ fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
   const int kblocks = args.K / kBK;
   const int ntiles = args.tiles_n * args.tiles_m;  // tiles_n counts 256-row tiles
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-  const uint32_t stage_tx = (uint32_t)(kABytes + half * kBK);  // per CTA
+  const uint32_t stage_tx = (uint32_t)(kABytes + half * kBK);  // bytes per CTA per stage
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages2; ++s) {
-      mbar_init(full0 + 8 * s, 2);   // one expect_tx arrival per CTA (leader's is used)
+      mbar_init(full0 + 8 * s, 1);   // the leader's expect_tx for both CTAs' bytes
       mbar_init(empty0 + 8 * s, 1);  // the leader's commit
     }
     for (int b = 0; b < 2; ++b) {
@@ -443,8 +438,10 @@ fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
             ok = false;
             break;
           }
+          // the leader arms its barrier for both CTAs' bytes; the peer's
+          // copies may land first (the transaction count may run negative)
           const uint32_t lead_full = peer_addr(full0 + 8 * stage, 0);
-          mbar_expect_tx_cluster(lead_full, stage_tx);
+          if (leader) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * stage_tx);
           tma_load_2d_pair(smem_u32(sA + stage * kABytes), &tmap_w, lead_full, kb * kBK, wrow);
           tma_load_2d_pair(smem_u32(sB + stage * kBHalfMax), &tmap_x, lead_full, kb * kBK, trow);
           if (++stage == kStages2) { stage = 0; phase ^= 1; }
@@ -523,7 +520,12 @@ fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(peer_addr(tempty0 + 8 * acc, 0));
+      if (lane == 0) {
+        if (leader)
+          mbar_arrive(tempty0 + 8 * acc);
+        else
+          mbar_arrive_cluster_relaxed(peer_addr(tempty0 + 8 * acc, 0));
+      }
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
   }
@@ -660,12 +662,15 @@ int resident_pairs(int sms) {
   return cached;
 }
 
-// The pair kernel is opt-in (RQ_GEMM_PAIR=1) until it outruns the
-// one-CTA kernel on the prefill shapes.
-bool use_pair_kernel(int N) {
+// The pair kernel wins when its 256-row tiles come in wide token tiles
+// (BN >= 224); where N is small the 256-row tiles quantize badly and the
+// one-CTA kernel with narrower tiles is faster (measured on GB300).
+// RQ_GEMM_PAIR=0 / 1 forces the one-CTA / pair kernel.
+bool use_pair_kernel(int N, int bn_pair) {
+  if (N <= kBM) return false;
   const char* env = std::getenv("RQ_GEMM_PAIR");
-  if (env == nullptr || std::atoi(env) == 0) return false;
-  return N > kBM;
+  if (env != nullptr) return std::atoi(env) != 0;
+  return bn_pair >= 224;
 }
 
 }  // namespace
@@ -675,8 +680,9 @@ rq_status launch_fp8_gemm(const uint8_t* x_fp8, const float* x_deq,
                           int M, int N, int K, cudaStream_t st) {
   const int m_pad = (M + 15) / 16 * 16;
   const int sms = device_sm_count();
-  const bool pair = use_pair_kernel(N) && sms >= 2;
-  const int bn = pair ? choose_bn_pair(m_pad, N, resident_pairs(sms)) : choose_bn(m_pad, N, sms);
+  const int bn_pair = sms >= 2 ? choose_bn_pair(m_pad, N, resident_pairs(sms)) : 0;
+  const bool pair = sms >= 2 && use_pair_kernel(N, bn_pair);
+  const int bn = pair ? bn_pair : choose_bn(m_pad, N, sms);
   CUtensorMap tw, tx;
   if (!make_map(&tw, w_fp8, N, K, kBM) || !make_map(&tx, x_fp8, m_pad, K, pair ? bn / 2 : bn))
     return RQ_ERR_CUDA;
