@@ -291,10 +291,6 @@ class Stack:
             for name, qt, N, K, W in self.weights[layer]:
                 ctx.rq_linear(qt, W, a[SOURCE[name]], self.out[M][name], M, N, K, stream)
 
-    def kernels_per_prefill_pass(self):
-        # per layer: 4 activation misses x (absmax + quant) + 7 GEMMs
-        return synthetic.N_LAYERS * (4 * 2 + 7)
-
 
 def run_gpu(args, world, rank, local):
     import torch
@@ -415,7 +411,7 @@ def run_gpu(args, world, rank, local):
                      "flops_per_launch_avg": flops / 196.0,
                      "avg_launch_ms": gemm_trace_ms / gemm_calls if gemm_calls else None},
         "trace_ms_per_step": {k: v[1] / K for k, v in traced.items()},
-        "gpu_launches": K * (196 + st.kernels_per_prefill_pass()),
+        "gpu_launches": K * 196 + sum(c for c, _ in traced.values()),
         "clocks": clocks, "e2e": e2e, "setup_s": setup_s, "wall_s": wall_s,
         "act_cache": st.ctx.stats(),
     }
@@ -510,6 +506,13 @@ def run_case(args):
             call = lambda: rq.rq_absmax(x, M * K, bits)  # noqa: E731
         else:
             call = lambda: rq.rq_quant_e4m3(x, M * K, bits, out, deq)  # noqa: E731
+    elif args.case == "act_cache":
+        ctx = rq.Context()
+        x = torch.from_numpy(synthetic.activation(3, M, K, outlier_frac=1e-3)).to(dev)
+
+        def call():
+            ctx.rq_act_cache_invalidate()
+            ctx.rq_fp8_act_cache(x, M, K)
     elif args.case == "gemm":
         ctx = rq.Context()
         W = torch.from_numpy(synthetic.q4k_matrix(4, N, K)).to(dev)
@@ -536,7 +539,11 @@ def run_case(args):
     torch.cuda.synchronize()
     status = rq.rq_get_device_status()
     ms = s.elapsed_time(e) / args.launches
+    m_pad = (M + 15) // 16 * 16
+    moved = {"absmax": 4 * M * K, "quant": 5 * M * K,
+             "act_cache": 4 * M * K + m_pad * K}.get(args.case)
     print(json.dumps({"case": args.case, "M": M, "N": N, "K": K, "ms_per_launch": ms,
+                      "gbs": moved / ms / 1e6 if moved else None,
                       "status": status}), flush=True)
     if status != 0:
         raise SystemExit(1)
@@ -553,7 +560,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the end-to-end leg (profiling runs only)")
     ap.add_argument("--case", default=None,
-                    help="single-kernel mode: gemv_q4k, gemv_q6k, absmax, quant, gemm")
+                    help="single-kernel mode: gemv_q4k, gemv_q6k, absmax, quant, "
+                         "act_cache, gemm")
     ap.add_argument("--M", type=int, default=2048)
     ap.add_argument("--N", type=int, default=3584)
     ap.add_argument("--K", type=int, default=3584)

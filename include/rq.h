@@ -170,6 +170,26 @@ rq_status rq_fp8_gemm(const uint8_t *x_fp8, const float *x_dequant,
                       const uint8_t *w_fp8, const float *w_dequant, float *y,
                       int M, int N, int K, rq_stream_t stream);
 
+/* FP8 activation cache ([gemm.rs], cublas_prefill_fp8_gemm: the
+ * activation's per-tensor absmax and E4M3 conversion, and the PMAT-084
+ * reuse of that FP8 copy by the next linears that read the same input):
+ * returns device pointers to the E4M3 form of x and its dequant scale
+ * absmax'/448 (absmax' = absmax, or 1 for an all-zero x), quantizing x into
+ * the ctx's scratch on a miss.  The bytes are those of rq_absmax followed by
+ * rq_quant_e4m3, with rows M..M_pad-1 zero (M_pad = M rounded up to 16), so
+ * the result feeds rq_fp8_gemm directly.  The key is (x, M, K, generation),
+ * as for rq_linear, which calls this on its FP8 route.
+ *   x: f32 [M x K], 16-byte aligned.   *x_fp8: E4M3 [M_pad x K] (owned by
+ *   ctx).   *x_dequant: one device float (owned by ctx).
+ * The pointers stay valid until a later miss on this ctx needs a larger
+ * scratch, or the ctx is destroyed; a later miss of the same or smaller size
+ * overwrites the bytes in stream order.  Allocates on a miss that needs a
+ * larger scratch.  Errors: RQ_ERR_NULL, RQ_ERR_SHAPE (M, K < 1, x
+ * misaligned), RQ_ERR_ALLOC, RQ_ERR_CUDA. */
+rq_status rq_fp8_act_cache(rq_ctx *ctx, const float *x, int M, int K,
+                           const uint8_t **x_fp8, const float **x_dequant,
+                           rq_stream_t stream);
+
 /* Quantized linear layer with M-threshold routing ([mod.rs],
  * cublas_gemm_threshold; [gemm.rs], cublas_prefill_gemm FP8 branch):
  *   M <  threshold: Q4_K / Q6_K GEMV straight from the packed weights
@@ -177,7 +197,12 @@ rq_status rq_fp8_gemm(const uint8_t *x_fp8, const float *x_dequant,
  *   M >= threshold: FP8 weight cache (a hit after the first call), then, on
  *                   an activation-cache miss, absmax + E4M3 quantization of
  *                   x into the ctx's [M_pad x K] scratch (pad rows zeroed),
- *                   then the FP8 GEMM.
+ *                   then the FP8 GEMM.  When x is 16-byte aligned and fits
+ *                   the shared memory of one wave of CTAs (about 220 KB per
+ *                   SM), absmax and quantization are one cooperative kernel
+ *                   that reads x once (same bytes as the two-kernel form;
+ *                   environment RQ_ONE_PASS_QUANT=0 at ctx creation turns it
+ *                   off).
  * The activation cache ([gemm.rs], PMAT-084 reuse across Q/K/V and gate/up)
  * is keyed by (x, M, K, generation); rq_act_cache_invalidate bumps the
  * generation and must be called when x's contents change in place.
@@ -233,7 +258,8 @@ rq_status rq_act_cache_invalidate(rq_ctx *ctx);
 typedef enum {
     RQ_TRACE_GEMV = 0,    /* Q4_K / Q6_K GEMV                         */
     RQ_TRACE_ABSMAX = 1,  /* zeroing + absmax of the activation       */
-    RQ_TRACE_QUANT = 2,   /* activation E4M3 quantization             */
+    RQ_TRACE_QUANT = 2,   /* activation E4M3 quantization (or the
+                             one-pass absmax + quantization kernel)   */
     RQ_TRACE_GEMM = 3,    /* FP8 GEMM                                 */
     RQ_TRACE_WCACHE = 4,  /* FP8 weight-cache build (a miss)          */
     RQ_TRACE_KINDS = 5
@@ -252,8 +278,9 @@ rq_status rq_ctx_trace_begin(rq_ctx *ctx, int capacity);
 rq_status rq_ctx_trace_end(rq_ctx *ctx, int64_t *counts_host, double *ms_host);
 
 /* Synchronise `stream`, then report and clear the library's device error
- * word: RQ_ERR_TIMEOUT if a GEMM pipeline wait exceeded its time limit (the
- * kernel then stopped early and its output is incomplete), RQ_ERR_CUDA if
+ * word: RQ_ERR_TIMEOUT if a GEMM or GEMV pipeline wait, or the one-pass
+ * quantization's grid barrier, exceeded its time limit (the kernel then
+ * stopped early and its output is incomplete), RQ_ERR_CUDA if
  * the synchronisation itself failed, RQ_OK otherwise. */
 rq_status rq_get_device_status(rq_stream_t stream);
 

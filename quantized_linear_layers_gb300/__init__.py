@@ -55,6 +55,8 @@ _SIGS = {
     "rq_fp8_weight_cache": ([_vp, _i32, _vp, _i32, _i32, ctypes.POINTER(_vp),
                              ctypes.POINTER(_vp), _vp], _i32),
     "rq_fp8_gemm": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp], _i32),
+    "rq_fp8_act_cache": ([_vp, _vp, _i32, _i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+                          _vp], _i32),
     "rq_linear": ([_vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _vp], _i32),
     "rq_fp8_linear_noalloc": ([_vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp], _i32),
     "rq_act_cache_invalidate": ([_vp], _i32),
@@ -196,6 +198,15 @@ class Context:
                                         ctypes.byref(wd), _stream(stream)),
                "rq_fp8_weight_cache")
         return wq.value, wd.value
+
+    def rq_fp8_act_cache(self, x, M, K, stream=None):
+        """-> (device address of E4M3 [M_pad x K], device address of the scale)."""
+        xq = _vp()
+        xd = _vp()
+        _check(_lib.rq_fp8_act_cache(self._h, _ptr(x), M, K, ctypes.byref(xq),
+                                     ctypes.byref(xd), _stream(stream)),
+               "rq_fp8_act_cache")
+        return xq.value, xd.value
 
     def rq_linear(self, qtype, w, x, y, M, N, K, stream=None):
         _check(_lib.rq_linear(self._h, qtype, _ptr(w), _ptr(x), _ptr(y), M, N, K,

@@ -80,6 +80,8 @@ struct rq_ctx {
   size_t act_cap = 0;
   uint32_t* absmax = nullptr;  // device word
   float* act_deq = nullptr;    // device float
+  unsigned int* fused = nullptr;  // one-pass quantization state (4 device words)
+  bool fused_ok = true;           // RQ_ONE_PASS_QUANT=0 keeps the two-kernel path
   // activation cache key
   bool act_valid = false;
   const float* act_x = nullptr;
@@ -160,6 +162,14 @@ rq_status rq_ctx_create(rq_ctx** out) {
   }
   c->absmax = static_cast<uint32_t*>(p);
   c->act_deq = reinterpret_cast<float*>(static_cast<uint8_t*>(p) + 128);
+  c->fused = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(p) + 192);
+  if (cudaMemset(p, 0, 256) != cudaSuccess) {
+    cudaFree(p);
+    delete c;
+    return RQ_ERR_CUDA;
+  }
+  const char* one_pass = std::getenv("RQ_ONE_PASS_QUANT");
+  if (one_pass != nullptr && std::atoi(one_pass) == 0) c->fused_ok = false;
   *out = c;
   return RQ_OK;
 }
@@ -293,6 +303,65 @@ rq_status rq_fp8_gemm(const uint8_t* x_fp8, const float* x_dequant, const uint8_
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
+rq_status rq_fp8_act_cache(rq_ctx* ctx, const float* x, int M, int K,
+                           const uint8_t** x_fp8, const float** x_dequant,
+                           rq_stream_t stream) {
+  if (ctx == nullptr || x == nullptr || x_fp8 == nullptr || x_dequant == nullptr)
+    return RQ_ERR_NULL;
+  if (M < 1 || K < 1 || !aligned(x, 16)) return RQ_ERR_SHAPE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  rq_status s = RQ_OK;
+  const bool hit = ctx->act_valid && ctx->act_x == x && ctx->act_M == M &&
+                   ctx->act_K == K && ctx->act_gen == ctx->gen;
+  if (hit) {
+    ++ctx->hits;
+  } else {
+    const int m_pad = (M + 15) / 16 * 16;
+    const size_t need = (size_t)m_pad * (size_t)K;
+    if (need > ctx->act_cap) {
+      if (ctx->act) cudaFree(ctx->act);
+      ctx->act = nullptr;
+      ctx->act_cap = 0;
+      ctx->act_valid = false;
+      void* p = nullptr;
+      if (cudaMalloc(&p, need) != cudaSuccess) {
+        cudaGetLastError();
+        return RQ_ERR_ALLOC;
+      }
+      ctx->act = static_cast<uint8_t*>(p);
+      ctx->act_cap = need;
+    }
+    const int64_t n = (int64_t)M * K;
+    if (ctx->fused_ok && act_quant_fused_fits(x, n, ctx->act)) {
+      TraceScope ts(ctx, RQ_TRACE_QUANT, st);
+      s = launch_act_quant_fused(x, n, (int64_t)need, ctx->act, ctx->absmax, ctx->act_deq,
+                                 ctx->fused, st);
+    } else {
+      {
+        TraceScope ts(ctx, RQ_TRACE_ABSMAX, st);
+        s = launch_absmax(x, n, ctx->absmax, st);
+      }
+      if (s == RQ_OK) {
+        TraceScope ts(ctx, RQ_TRACE_QUANT, st);
+        s = launch_quant(x, n, (int64_t)need, ctx->absmax, ctx->act, ctx->act_deq, st);
+      }
+    }
+    if (s != RQ_OK) {
+      ctx->act_valid = false;
+      return s;
+    }
+    ctx->act_valid = true;
+    ctx->act_x = x;
+    ctx->act_M = M;
+    ctx->act_K = K;
+    ctx->act_gen = ctx->gen;
+    ++ctx->misses;
+  }
+  *x_fp8 = ctx->act;
+  *x_dequant = ctx->act_deq;
+  return RQ_OK;
+}
+
 rq_status rq_linear(rq_ctx* ctx, rq_qtype qtype, const void* w, const float* x, float* y,
                     int M, int N, int K, rq_stream_t stream) {
   if (ctx == nullptr || w == nullptr || x == nullptr || y == nullptr) return RQ_ERR_NULL;
@@ -325,48 +394,12 @@ rq_status rq_linear(rq_ctx* ctx, rq_qtype qtype, const void* w, const float* x, 
   }
   if (s != RQ_OK) return s;
 
-  const bool hit = ctx->act_valid && ctx->act_x == x && ctx->act_M == M &&
-                   ctx->act_K == K && ctx->act_gen == ctx->gen;
-  if (hit) {
-    ++ctx->hits;
-  } else {
-    const int m_pad = (M + 15) / 16 * 16;
-    const size_t need = (size_t)m_pad * (size_t)K;
-    if (need > ctx->act_cap) {
-      if (ctx->act) cudaFree(ctx->act);
-      ctx->act = nullptr;
-      ctx->act_cap = 0;
-      ctx->act_valid = false;
-      void* p = nullptr;
-      if (cudaMalloc(&p, need) != cudaSuccess) {
-        cudaGetLastError();
-        return RQ_ERR_ALLOC;
-      }
-      ctx->act = static_cast<uint8_t*>(p);
-      ctx->act_cap = need;
-    }
-    const int64_t n = (int64_t)M * K;
-    {
-      TraceScope ts(ctx, RQ_TRACE_ABSMAX, st);
-      s = launch_absmax(x, n, ctx->absmax, st);
-    }
-    if (s == RQ_OK) {
-      TraceScope ts(ctx, RQ_TRACE_QUANT, st);
-      s = launch_quant(x, n, (int64_t)need, ctx->absmax, ctx->act, ctx->act_deq, st);
-    }
-    if (s != RQ_OK) {
-      ctx->act_valid = false;
-      return s;
-    }
-    ctx->act_valid = true;
-    ctx->act_x = x;
-    ctx->act_M = M;
-    ctx->act_K = K;
-    ctx->act_gen = ctx->gen;
-    ++ctx->misses;
-  }
+  const uint8_t* xq = nullptr;
+  const float* xdeq = nullptr;
+  s = rq_fp8_act_cache(ctx, x, M, K, &xq, &xdeq, stream);
+  if (s != RQ_OK) return s;
   TraceScope ts(ctx, RQ_TRACE_GEMM, st);
-  return launch_fp8_gemm(ctx->act, ctx->act_deq, wq, wdeq, y, M, N, K, st);
+  return launch_fp8_gemm(xq, xdeq, wq, wdeq, y, M, N, K, st);
 }
 
 rq_status rq_ctx_trace_begin(rq_ctx* ctx, int capacity) {

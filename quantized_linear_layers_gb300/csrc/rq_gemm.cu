@@ -730,10 +730,12 @@ rq_status read_and_clear_device_error(cudaStream_t st) {
   if (cudaStreamSynchronize(st) != cudaSuccess) return RQ_ERR_CUDA;
   const rq_status gemv = read_and_clear_gemv_error();
   if (gemv == RQ_ERR_CUDA) return gemv;
+  const rq_status quant = read_and_clear_quant_error();
+  if (quant == RQ_ERR_CUDA) return quant;
   unsigned int v = 0;
   if (cudaMemcpyFromSymbol(&v, g_rq_device_error, sizeof(v)) != cudaSuccess)
     return RQ_ERR_CUDA;
-  if (v == 0) return gemv;
+  if (v == 0) return gemv != RQ_OK ? gemv : quant;
   const unsigned int zero = 0;
   if (cudaMemcpyToSymbol(g_rq_device_error, &zero, sizeof(zero)) != cudaSuccess)
     return RQ_ERR_CUDA;

@@ -26,6 +26,18 @@ rq_status launch_quant(const float* x, int64_t n, int64_t n_out,
                        const uint32_t* absmax_bits, uint8_t* out,
                        float* dequant_out, cudaStream_t st);
 
+// One-pass absmax + encode (one cooperative wave, tensor staged in shared
+// memory).  Needs x 16-byte and out 4-byte aligned and n small enough for
+// one wave; `state` is 4 device words, zero before the first launch and
+// used by one stream at a time.  absmax_out / dequant_out may be null.
+bool act_quant_fused_fits(const float* x, int64_t n, const uint8_t* out);
+rq_status launch_act_quant_fused(const float* x, int64_t n, int64_t n_out,
+                                 uint8_t* out, uint32_t* absmax_out,
+                                 float* dequant_out, unsigned int* state,
+                                 cudaStream_t st);
+// Read and clear the one-pass kernel's device error word (after a sync).
+rq_status read_and_clear_quant_error();
+
 // rq_gemv.cu ----------------------------------------------------------------
 rq_status launch_q4k_gemv(const uint8_t* w, const float* x, float* y, int M,
                           int N, int K, cudaStream_t st);

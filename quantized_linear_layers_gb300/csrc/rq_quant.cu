@@ -101,6 +101,123 @@ quant_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
   for (int64_t i = n + tid; i < n_out; i += nthreads) out[i] = 0;
 }
 
+// ------------------------------------------------------ one-pass variant --
+//
+// When the whole activation fits in the shared memory of one wave of CTAs
+// (one CTA per SM), it is read from HBM once: each CTA bulk-copies its chunk
+// into shared memory, reduces its max, all CTAs meet at a grid barrier that
+// publishes the tensor max, and each CTA encodes its chunk from shared memory.
+// Same arithmetic as absmax_kernel + quant_kernel, so the bytes are identical.
+//
+// state[0..1]: absmax words, used alternately by consecutive launches (the
+//              one for launch g is zero when it starts);
+// state[2]:    arrival count (zero between launches);
+// state[3]:    launch generation g.
+// Launches that share a state word block run one after another (one stream).
+
+__device__ unsigned int g_quant_error;
+
+constexpr int kFusedThreads = 1024;
+constexpr int kFusedParts = 4;               // bulk copies (and barriers) per CTA
+constexpr int64_t kFusedMinChunk = 4096;     // floats: fewer CTAs for small tensors
+constexpr int64_t kFusedSmemMax = 220 * 1024;
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned int* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__global__ void __launch_bounds__(kFusedThreads, 1)
+act_quant_fused_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
+                       int64_t chunk, uint8_t* __restrict__ out,
+                       uint32_t* __restrict__ absmax_out, float* __restrict__ dequant_out,
+                       unsigned int* state) {
+  extern __shared__ __align__(128) float4 stash[];
+  __shared__ __align__(8) uint64_t bars[kFusedParts];
+  __shared__ uint32_t warp_max[kFusedThreads / 32];
+  __shared__ uint32_t gen_s, absmax_s;
+
+  const int64_t begin = (int64_t)blockIdx.x * chunk;
+  const int64_t len = min(chunk, n - begin);
+  const int64_t cnt4 = len >> 2;  // float4s moved by the bulk copies
+  const int tid = threadIdx.x;
+
+  if (tid == 0) {
+    gen_s = ld_acquire_u32(state + 3);
+    for (int p = 0; p < kFusedParts; ++p) mbar_init(smem_u32(&bars[p]), 1);
+    mbar_fence_init();
+    for (int p = 0; p < kFusedParts; ++p) {
+      const int64_t lo = cnt4 * p / kFusedParts, hi = cnt4 * (p + 1) / kFusedParts;
+      const uint32_t bytes = (uint32_t)((hi - lo) * 16);
+      mbar_arrive_expect_tx(smem_u32(&bars[p]), bytes);
+      if (bytes != 0) bulk_g2s(smem_u32(stash + lo), x + begin + 4 * lo, bytes, smem_u32(&bars[p]));
+    }
+  }
+  __syncthreads();
+
+  uint32_t m = 0;
+  for (int p = 0; p < kFusedParts; ++p) {
+    mbar_wait(smem_u32(&bars[p]), 0, kWaitLimitNs, &g_quant_error);
+    const int64_t lo = cnt4 * p / kFusedParts, hi = cnt4 * (p + 1) / kFusedParts;
+    for (int64_t i = lo + tid; i < hi; i += kFusedThreads) m = max4(m, stash[i]);
+  }
+  for (int64_t i = (cnt4 << 2) + tid; i < len; i += kFusedThreads)
+    m = max(m, abs_bits_skip_nan(__ldg(x + begin + i)));
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  const int lane = tid & 31, warp = tid >> 5;
+  if (lane == 0) warp_max[warp] = m;
+  __syncthreads();
+
+  if (warp == 0) {
+    m = __reduce_max_sync(0xFFFFFFFFu, warp_max[lane]);
+    if (lane == 0) {
+      const uint32_t g = gen_s;
+      unsigned int* word = state + (g & 1u);
+      if (m != 0u) atomicMax(word, m);
+      __threadfence();
+      const unsigned int arrived = atomicAdd(state + 2, 1u);
+      if (arrived == gridDim.x - 1) {
+        state[2] = 0u;
+        state[(g + 1u) & 1u] = 0u;
+        __threadfence();
+        atomicExch(state + 3, g + 1u);
+      } else {
+        const uint64_t t0 = globaltimer();
+        while (ld_acquire_u32(state + 3) == g) {
+          if (globaltimer() - t0 > kWaitLimitNs) {
+            atomicOr(&g_quant_error, 2u);
+            break;
+          }
+        }
+      }
+      absmax_s = ld_acquire_u32(word);
+    }
+  }
+  __syncthreads();
+
+  const float a = absmax_prime(absmax_s);
+  const float s = __fdiv_rn(448.0f, a);
+  if (blockIdx.x == 0 && tid == 0) {
+    if (absmax_out != nullptr) *absmax_out = absmax_s;
+    if (dequant_out != nullptr) *dequant_out = __fdiv_rn(a, 448.0f);
+  }
+  uint32_t* o4 = reinterpret_cast<uint32_t*>(out + begin);
+  for (int64_t i = tid; i < cnt4; i += kFusedThreads) o4[i] = pack4(stash[i], s);
+  for (int64_t i = (cnt4 << 2) + tid; i < len; i += kFusedThreads)
+    out[begin + i] = (uint8_t)e4m3_scaled(__ldg(x + begin + i), s);
+  const int64_t stride = (int64_t)gridDim.x * kFusedThreads;
+  for (int64_t i = n + (int64_t)blockIdx.x * kFusedThreads + tid; i < n_out; i += stride)
+    out[i] = 0;
+}
+
+int64_t fused_chunk(int64_t n) {
+  const int64_t sms = device_sm_count();
+  int64_t c = (n + sms - 1) / sms;
+  c = (c + 3) & ~int64_t(3);
+  return c < kFusedMinChunk ? kFusedMinChunk : c;
+}
+
 int grid_for(int64_t work_items) {
   const int64_t per_wave = (int64_t)device_sm_count() * 4;  // 4 CTAs / SM
   int64_t blocks = (work_items + kThreads - 1) / kThreads;
@@ -137,6 +254,49 @@ rq_status launch_quant(const float* x, int64_t n, int64_t n_out,
     quant_kernel<false><<<grid, kThreads, 0, st>>>(x, n, n_out, absmax_bits,
                                                    out, dequant_out);
   return launch_status();
+}
+
+bool act_quant_fused_fits(const float* x, int64_t n, const uint8_t* out) {
+  return n > 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
+         (reinterpret_cast<uintptr_t>(out) & 3) == 0 &&
+         fused_chunk(n) * 4 <= kFusedSmemMax;
+}
+
+rq_status launch_act_quant_fused(const float* x, int64_t n, int64_t n_out,
+                                 uint8_t* out, uint32_t* absmax_out,
+                                 float* dequant_out, unsigned int* state,
+                                 cudaStream_t st) {
+  if (!act_quant_fused_fits(x, n, out)) return RQ_ERR_SHAPE;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(act_quant_fused_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kFusedSmemMax) != cudaSuccess)
+      return launch_status();
+    attr_set = true;
+  }
+  int64_t chunk = fused_chunk(n);
+  const int grid = (int)((n + chunk - 1) / chunk);
+  const size_t smem = (size_t)((chunk + 3) / 4) * 16;
+  void* args[] = {(void*)&x, (void*)&n, (void*)&n_out, (void*)&chunk, (void*)&out,
+                  (void*)&absmax_out, (void*)&dequant_out, (void*)&state};
+  const cudaError_t e = cudaLaunchCooperativeKernel((const void*)act_quant_fused_kernel,
+                                                    dim3(grid), dim3(kFusedThreads), args,
+                                                    smem, st);
+  if (e == cudaErrorCooperativeLaunchTooLarge) {
+    cudaGetLastError();
+    return RQ_ERR_SHAPE;
+  }
+  return cuda_status(e);
+}
+
+rq_status read_and_clear_quant_error() {
+  unsigned int v = 0;
+  const unsigned int zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_quant_error, sizeof(v)) != cudaSuccess) return RQ_ERR_CUDA;
+  if (v == 0) return RQ_OK;
+  if (cudaMemcpyToSymbol(g_quant_error, &zero, sizeof(zero)) != cudaSuccess) return RQ_ERR_CUDA;
+  return RQ_ERR_TIMEOUT;
 }
 
 }  // namespace rq

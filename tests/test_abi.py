@@ -71,6 +71,10 @@ def test_null_pointers_rejected_before_launch(rq):
     assert lib.rq_fp8_gemm(fake, fake, NULL, fake, fake, 16, 128, 128, NULL) == 1
     assert lib.rq_linear(NULL, 12, fake, fake, fake, 1, 8, 256, NULL) == 1
     assert lib.rq_fp8_weight_cache(NULL, 12, fake, 8, 256, NULL, NULL, NULL) == 1
+    out = ctypes.byref(ctypes.c_void_p())
+    assert lib.rq_fp8_act_cache(NULL, fake, 16, 128, out, out, NULL) == 1
+    assert lib.rq_fp8_act_cache(fake, NULL, 16, 128, out, out, NULL) == 1
+    assert lib.rq_fp8_act_cache(fake, fake, 16, 128, NULL, out, NULL) == 1
     assert lib.rq_ctx_create(NULL) == 1
     assert lib.rq_act_cache_invalidate(NULL) == 1
     assert lib.rq_ctx_set_gemm_threshold(NULL, 4) == 1
@@ -95,6 +99,11 @@ def test_bad_shapes_rejected_before_launch(rq):
         assert lib.rq_fp8_gemm(a, a, a, a, a, M, N, K, NULL) == 2, (M, N, K)
     assert lib.rq_fp8_gemm(a + 8, a, a, a, a, 16, 128, 128, NULL) == 2  # TMA: 16 B
     assert lib.rq_debug_wait_timeout(0, NULL) == 2
+    out = ctypes.byref(ctypes.c_void_p())
+    fake_ctx = ctypes.c_void_p(a)  # not dereferenced: shape checks come first
+    assert lib.rq_fp8_act_cache(fake_ctx, a, 0, 128, out, out, NULL) == 2
+    assert lib.rq_fp8_act_cache(fake_ctx, a, 16, 0, out, out, NULL) == 2
+    assert lib.rq_fp8_act_cache(fake_ctx, a + 4, 16, 128, out, out, NULL) == 2
 
 
 def test_bad_qtype_rejected(rq):

@@ -6,7 +6,7 @@ import torch
 
 import oracle
 import synthetic
-from gpu_util import empty, gemm_ok, gemv_ok, to_dev
+from gpu_util import device_view, empty, gemm_ok, gemv_ok, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -112,6 +112,66 @@ def test_activation_reuse_counts_and_results(rq):
     torch.cuda.synchronize()
     assert ctx.stats()["act_misses"] == 7
     check_gemm(y.cpu().numpy(), gemm_route_ref(Q4K, host["q"], new_x, 256, K))
+    ctx.close()
+
+
+def act_cache_bytes(ctx, xd, M, K):
+    xq, xdq = ctx.rq_fp8_act_cache(xd, M, K)
+    torch.cuda.synchronize()
+    m_pad = (M + 15) // 16 * 16
+    b = device_view(xq, m_pad * K, torch.uint8).cpu().numpy()
+    d = np.float32(device_view(xdq, 1, torch.float32).item())
+    return b, d
+
+
+def oracle_act_bytes(x, M, K):
+    m_pad = (M + 15) // 16 * 16
+    ob, od = oracle.quant_e4m3(x, oracle.absmax_bits(x))
+    want = np.zeros(m_pad * K, np.uint8)
+    want[:M * K] = ob.ravel()
+    return want, od
+
+
+@pytest.mark.parametrize("one_pass", ["1", "0"])
+@pytest.mark.parametrize("M,K", [(2048, 3584), (611, 1024), (37, 3584), (5, 256),
+                                 (16, 128), (3, 4101), (2048, 18944)])
+def test_activation_cache_bytes_bit_exact(rq, monkeypatch, one_pass, M, K):
+    """The FP8 activation (one-pass kernel or absmax + quant kernels) is the
+    oracle's bytes, pad rows zero, over three successive misses with
+    different maxima (the one-pass kernel alternates its absmax words)."""
+    monkeypatch.setenv("RQ_ONE_PASS_QUANT", one_pass)
+    ctx = rq.Context()
+    x = synthetic.activation(5000 + M + K, M, K, outlier_frac=1e-3)
+    x.ravel()[min(4, x.size - 1)] = np.nan
+    xd = to_dev(x)
+    for scale in (1.0, 0.25, 3.0):
+        xs = (x * np.float32(scale)).astype(np.float32)
+        xd.copy_(to_dev(xs))
+        ctx.rq_act_cache_invalidate()
+        ctx.rq_ctx_trace_begin(8)
+        got, gd = act_cache_bytes(ctx, xd, M, K)
+        tr = ctx.rq_ctx_trace_end()
+        assert rq.rq_get_device_status() == 0
+        want, wd = oracle_act_bytes(xs, M, K)
+        assert gd == wd
+        assert np.array_equal(got, want), np.flatnonzero(got != want)[:8]
+        # 16-byte aligned x of <= 220 KB per SM takes the one-pass kernel
+        fused = one_pass == "1" and M * K <= 152 * 56320
+        assert tr["absmax"][0] == (0 if fused else 1) and tr["quant"][0] == 1
+    # a hit returns the same bytes without launching anything
+    ctx.rq_ctx_trace_begin(8)
+    got2, _ = act_cache_bytes(ctx, xd, M, K)
+    assert sum(c for c, _ in ctx.rq_ctx_trace_end().values()) == 0
+    assert np.array_equal(got2, got)
+    ctx.close()
+
+
+def test_activation_cache_all_zero_input(rq):
+    M, K = 64, 512
+    ctx = rq.Context()
+    xd = to_dev(np.zeros((M, K), np.float32))
+    got, gd = act_cache_bytes(ctx, xd, M, K)
+    assert not got.any() and gd == np.float32(1.0) / np.float32(448.0)
     ctx.close()
 
 
