@@ -491,28 +491,35 @@ def run_case(args):
     M, N, K = args.M, args.N, args.K
     if args.case in ("gemv_q4k", "gemv_q6k"):
         qt = synthetic.Q4K if args.case == "gemv_q4k" else synthetic.Q6K
-        W = torch.from_numpy(synthetic.weight_matrix(1, qt, N, K)).to(dev)
+        W0 = torch.from_numpy(synthetic.weight_matrix(1, qt, N, K)).to(dev)
+        # copies of the weight so that successive launches read HBM, not L2
+        Ws = [W0] + [W0.clone() for _ in range(-(-(512 << 20) // W0.numel()) - 1)]
         x = torch.from_numpy(synthetic.activation(2, M, K)).to(dev)
         y = torch.empty(M, N, device=dev)
         fn = rq.rq_q4k_gemv if qt == synthetic.Q4K else rq.rq_q6k_gemv
-        call = lambda: fn(W, x, y, M, N, K)  # noqa: E731
-    elif args.case in ("absmax", "quant"):
-        x = torch.from_numpy(synthetic.activation(3, M, K, outlier_frac=1e-3)).to(dev)
+        wit = iter(range(1 << 62))
+        call = lambda: fn(Ws[next(wit) % len(Ws)], x, y, M, N, K)  # noqa: E731
+    elif args.case in ("absmax", "quant", "act_cache"):
+        # enough copies of the activation that successive launches read
+        # HBM, not L2 (at least 512 MB in all)
+        x0 = torch.from_numpy(synthetic.activation(3, M, K, outlier_frac=1e-3)).to(dev)
+        xs = [x0] + [x0.clone() for _ in range(max(0, -(-(512 << 20) // (4 * M * K)) - 1))]
+        it = iter(range(1 << 62))
         bits = torch.zeros(1, dtype=torch.int32, device=dev)
         out = torch.empty(M * K, dtype=torch.uint8, device=dev)
         deq = torch.empty(1, device=dev)
-        rq.rq_absmax(x, M * K, bits)
-        if args.case == "absmax":
-            call = lambda: rq.rq_absmax(x, M * K, bits)  # noqa: E731
-        else:
-            call = lambda: rq.rq_quant_e4m3(x, M * K, bits, out, deq)  # noqa: E731
-    elif args.case == "act_cache":
+        rq.rq_absmax(x0, M * K, bits)
         ctx = rq.Context()
-        x = torch.from_numpy(synthetic.activation(3, M, K, outlier_frac=1e-3)).to(dev)
 
         def call():
-            ctx.rq_act_cache_invalidate()
-            ctx.rq_fp8_act_cache(x, M, K)
+            x = xs[next(it) % len(xs)]
+            if args.case == "absmax":
+                rq.rq_absmax(x, M * K, bits)
+            elif args.case == "quant":
+                rq.rq_quant_e4m3(x, M * K, bits, out, deq)
+            else:
+                ctx.rq_act_cache_invalidate()
+                ctx.rq_fp8_act_cache(x, M, K)
     elif args.case == "gemm":
         ctx = rq.Context()
         W = torch.from_numpy(synthetic.q4k_matrix(4, N, K)).to(dev)
@@ -532,16 +539,35 @@ def run_case(args):
         call()
     torch.cuda.synchronize()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(args.launches):
-        call()
-    e.record()
+    if args.graph:
+        # the launches replayed from a CUDA graph: device time without the
+        # host's per-call cost
+        g = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream(dev)
+        cs.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(cs):
+            with torch.cuda.graph(g, stream=cs):
+                for _ in range(args.launches):
+                    call()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        s.record()
+        g.replay()
+        e.record()
+    else:
+        s.record()
+        for _ in range(args.launches):
+            call()
+        e.record()
     torch.cuda.synchronize()
     status = rq.rq_get_device_status()
     ms = s.elapsed_time(e) / args.launches
     m_pad = (M + 15) // 16 * 16
     moved = {"absmax": 4 * M * K, "quant": 5 * M * K,
-             "act_cache": 4 * M * K + m_pad * K}.get(args.case)
+             "act_cache": 4 * M * K + m_pad * K,
+             "gemv_q4k": N * (K // 256) * 144 + 4 * M * (K + N),
+             "gemv_q6k": N * (K // 256) * 210 + 4 * M * (K + N)}.get(args.case)
     print(json.dumps({"case": args.case, "M": M, "N": N, "K": K, "ms_per_launch": ms,
                       "gbs": moved / ms / 1e6 if moved else None,
                       "status": status}), flush=True)
@@ -566,6 +592,8 @@ def main():
     ap.add_argument("--N", type=int, default=3584)
     ap.add_argument("--K", type=int, default=3584)
     ap.add_argument("--launches", type=int, default=3)
+    ap.add_argument("--graph", action="store_true",
+                    help="single-kernel mode: time the launches as one CUDA graph replay")
     args = ap.parse_args()
     if args.case:
         return run_case(args)

@@ -897,6 +897,16 @@ rq_status launch_q4k_gemv(const uint8_t* w, const float* x, float* y, int M,
         if (s1 != RQ_ERR_SHAPE) return s1;
       }
       return run_q4k<1, 2>(w, x, y, N, K, st);
+    default:
+      break;
+  }
+  if (M >= 2 && M <= 8 && std::getenv("RQ_GEMV_NO_MMA") == nullptr) {
+    // RQ_ERR_SHAPE: the shape does not fit the tensor-core kernel and
+    // nothing was launched
+    const rq_status s2 = launch_q4k_gemv_mma(w, x, y, M, N, K, st);
+    if (s2 != RQ_ERR_SHAPE) return s2;
+  }
+  switch (M) {
     case 2: return run_q4k<2, 2>(w, x, y, N, K, st);
     case 3: return run_q4k<3, 2>(w, x, y, N, K, st);
     case 4: return run_q4k<4, 2>(w, x, y, N, K, st);

@@ -46,6 +46,13 @@ rq_status launch_q6k_gemv(const uint8_t* w, const float* x, float* y, int M,
 // Read and clear the GEMV kernels' device error word (after a sync).
 rq_status read_and_clear_gemv_error();
 
+// rq_gemv_mma.cu ------------------------------------------------------------
+// Q4_K GEMV for M = 2..8 tokens on the tensor cores.  RQ_ERR_SHAPE (nothing
+// launched) when the shape does not fit the kernel.
+rq_status launch_q4k_gemv_mma(const uint8_t* w, const float* x, float* y, int M, int N, int K,
+                              cudaStream_t st);
+rq_status read_and_clear_gemv_mma_error();
+
 // rq_wcache.cu --------------------------------------------------------------
 // Decode the packed weight (fixed fp32 order) and reduce its absmax into
 // *absmax_bits (which the caller zeroed on the stream).

@@ -82,3 +82,55 @@ def test_gemv_writes_only_its_outputs(rq):
     torch.cuda.synchronize()
     tail = buf[M * N:].cpu().numpy()
     assert np.all(tail == 12345.0)
+
+
+@pytest.mark.parametrize("ks", ["", "2", "3", "5", "8"])
+@pytest.mark.parametrize("M", [2, 5, 8])
+def test_tensor_core_gemv_k_slices(rq, monkeypatch, ks, M):
+    """M = 2..8 Q4_K GEMV (tensor-core kernel): every split of K across the
+    CTAs of a cluster gives the oracle's result, including a last tile that
+    straddles N and slices whose last super-blocks lie past K."""
+    if ks:
+        monkeypatch.setenv("RQ_GEMV_MMA_KS", ks)
+    N, K = 203, 4096
+    W = synthetic.q4k_matrix(77 + M, N, K)
+    x = synthetic.activation(78 + M, M, K, outlier_frac=1e-3)
+    got = gpu_gemv(rq, Q4K, W, x, N, K)
+    ref, absdot = oracle.gemv(Q4K, W, x, N, K)
+    ok, worst = gemv_ok(got, ref, absdot)
+    assert ok, worst
+
+
+def test_tensor_core_gemv_per_token_magnitudes(rq):
+    """Tokens of very different magnitude, an all-zero token and a token
+    below fp16's normal range: each token's own power-of-two scale keeps
+    the split x = hi + lo exact to 2^-22."""
+    N, K, M = 96, 3584, 8
+    W = synthetic.q4k_matrix(5, N, K)
+    x = synthetic.activation(6, M, K)
+    x[0] *= np.float32(1e-7)
+    x[1] *= np.float32(3e4)
+    x[2] = 0
+    x[3] *= np.float32(2.0 ** -30)
+    x[4, ::7] = 0
+    got = gpu_gemv(rq, Q4K, W, x, N, K)
+    ref, absdot = oracle.gemv(Q4K, W, x, N, K)
+    ok, worst = gemv_ok(got[[0, 1, 3, 4, 5, 6, 7]], ref[[0, 1, 3, 4, 5, 6, 7]],
+                        absdot[[0, 1, 3, 4, 5, 6, 7]])
+    assert ok, worst
+    assert np.all(got[2] == 0)
+
+
+@pytest.mark.parametrize("M", [2, 4, 8])
+def test_tensor_core_and_generic_kernels_agree(rq, monkeypatch, M):
+    """The generic Q4_K kernel (tensor-core kernel switched off) and the
+    tensor-core kernel both meet the bound on the same launch."""
+    N, K = 512, 3584
+    W = synthetic.q4k_matrix(40 + M, N, K)
+    x = synthetic.activation(41 + M, M, K, outlier_frac=1e-3)
+    ref, absdot = oracle.gemv(Q4K, W, x, N, K)
+    got = gpu_gemv(rq, Q4K, W, x, N, K)
+    assert gemv_ok(got, ref, absdot)[0]
+    monkeypatch.setenv("RQ_GEMV_NO_MMA", "1")
+    got2 = gpu_gemv(rq, Q4K, W, x, N, K)
+    assert gemv_ok(got2, ref, absdot)[0]
