@@ -16,6 +16,14 @@
 
 namespace rq {
 
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("RQ_PDL");
+    return e == nullptr || std::atoi(e) != 0;
+  }();
+  return on;
+}
+
 int device_sm_count() {
   static int cached[64] = {0};
   int dev = 0;

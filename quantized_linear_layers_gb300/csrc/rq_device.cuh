@@ -179,6 +179,20 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s for any pipeline wait
 
+// Programmatic dependent launch.  pdl_wait: block until the grids this
+// launch depends on have completed and their memory operations are visible;
+// pdl_trigger: let the next launch in the stream start being scheduled.
+// Both are no-ops for launches made without programmatic serialization.
+// Every kernel of the library calls pdl_wait before it reads anything an
+// earlier launch may write (activations, scales, outputs) and calls
+// pdl_trigger only after its own pdl_wait, so that whatever a kernel may
+// read before its wait (constant weights) was written by launches that
+// completed before its predecessor passed its own wait.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);

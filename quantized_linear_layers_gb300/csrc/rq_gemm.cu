@@ -140,6 +140,10 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBBytesMax);
   // bars: full[kStages], empty[kStages], tfull[2], tempty[2], done[1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  // nothing global is read before the previous launch has completed: the
+  // weight operand may have been written by the launch just before
+  pdl_wait();
+  pdl_trigger();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
@@ -382,6 +386,8 @@ fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages2 * kBHalfMax);
   // bars: full[kStages2], empty[kStages2], tfull[2], tempty[2], done[1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages2 + 5);
+  pdl_wait();
+  pdl_trigger();
 
   const uint32_t rank = cluster_rank();
   const bool leader = rank == 0;
@@ -711,8 +717,7 @@ rq_status launch_fp8_gemm(const uint8_t* x_fp8, const float* x_deq,
     // paired inside its GPC, so the grid is the number of pairs that fit.
     const int max_pairs = resident_pairs(sms);
     const int grid = 2 * (tiles < max_pairs ? tiles : max_pairs);
-    fp8_gemm_pair_kernel<<<grid, kThreads, kSmemBytes2, st>>>(tw, tx, a);
-    return launch_status();
+    return launch_kernel(fp8_gemm_pair_kernel, grid, kThreads, kSmemBytes2, st, tw, tx, a);
   }
   static bool attr_done = false;
   if (!attr_done) {
@@ -722,8 +727,7 @@ rq_status launch_fp8_gemm(const uint8_t* x_fp8, const float* x_deq,
     attr_done = true;
   }
   const int grid = tiles < sms ? tiles : sms;
-  fp8_gemm_kernel<<<grid, kThreads, kSmemBytes, st>>>(tw, tx, a);
-  return launch_status();
+  return launch_kernel(fp8_gemm_kernel, grid, kThreads, kSmemBytes, st, tw, tx, a);
 }
 
 rq_status read_and_clear_device_error(cudaStream_t st) {

@@ -186,6 +186,8 @@ q4k_gemv_kernel(const uint8_t* __restrict__ W, const float* __restrict__ x,
   const bool active = rg < ngroups;
   Q4Item cur[R];
   if (active) q4_load<R>(cur, W, rowbytes, rg * R, N, lane, lane < U);
+  pdl_wait();  // x and y only after the previous launch has completed
+  pdl_trigger();
   x_sums<M>(x, K, 32, xs);
   __syncthreads();
   if (!active) return;
@@ -356,6 +358,8 @@ q6k_gemv_kernel(const uint8_t* __restrict__ W, const float* __restrict__ x,
   const bool active = rg < ngroups;
   Q6Item cur[R];
   if (active) q6_load<R>(cur, W, rowbytes, rg * R, N, lane, lane < U);
+  pdl_wait();  // x and y only after the previous launch has completed
+  pdl_trigger();
   x_sums<M>(x, K, 8, xs);
   __syncthreads();
   if (!active) return;
@@ -430,6 +434,7 @@ struct M1Args {
   int stages;
   uint32_t ring_bytes;  // stages * rows_per_stage * rowbytes
   uint64_t wait_limit_ns;
+  int row_align;        // Q6_K: rows per 16-byte-aligned group of rows
 };
 
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
@@ -613,9 +618,12 @@ __global__ void __launch_bounds__(544, 1) q4k_gemv_m1_kernel(const M1Args a) {
     parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
   };
   const bool producer = warp == compute_warps && lane == 0;
-  // the first ring's worth of copies is in flight while x is prepared
+  // the first ring's worth of weight copies is in flight while the previous
+  // launch finishes and x is prepared
   if (producer)
     for (int it = 0; it < first && prod_ok; ++it) produce(it);
+  pdl_wait();  // x and y only after the previous launch has completed
+  pdl_trigger();
 
   // ------------------------------------------------ x planes (all compute warps)
   // Four lanes per 32-value sub-block, eight values each: coalesced 16-byte
@@ -752,6 +760,268 @@ __global__ void __launch_bounds__(544, 1) q4k_gemv_m1_kernel(const M1Args a) {
   for (int i = threadIdx.x; i < rows; i += blockDim.x) a.y[r0 + i] = acc[i];
 }
 
+// ------------------------------------------------- Q6_K, one token ---------
+//
+// Same structure as the one-token Q4_K kernel (bulk-copy ring of row stages,
+// teams of warps, x as three int8 planes in registers, dp4a inner products,
+// 8-row transpose reductions, shared atomics per row).  A lane owns the
+// 64 weights 128hh + 32i + 16lq + j (i = 0..3, j = 0..15) of super-block sb
+// (unit u = 4 sb + 2 hh + lq): 16 bytes of ql at 64hh + 16lq (i = 0, 2),
+// 16 at 64hh + 32 + 16lq (i = 1, 3) and 16 of qh at 128 + 32hh + 16lq,
+// with the scale of 16-weight sub-block 8hh + 2i + lq for quarter i.  The
+// 6-bit quant q (0..63) enters dp4a as a non-negative int8 and the offset
+// is applied once per sub-block: sum x (q - 32) = sum x q - 32 sum x.
+// Super-blocks are 210 bytes, so fields are only 2-byte aligned in shared
+// memory: each 16-byte field is read as five aligned words and
+// funnel-shifted.  Rows are 16-byte aligned only in groups of `row_align`,
+// so each CTA's row block and every stage start on such a group; the bytes
+// of a final stage past the last 16-byte boundary are copied by the
+// producer with plain loads.
+
+struct XSplit16 {
+  int p1[4], p2[4], p3[4];  // planes of one 16-weight sub-block
+  float scale, sum;
+};
+
+// 16 bytes at a 2-byte aligned shared-memory address (the word after the
+// field is read and discarded; it lies inside the CTA's shared memory).
+__device__ __forceinline__ void lds16u(const uint8_t* p, uint32_t (&w)[4]) {
+  const uint32_t mis = smem_u32(p) & 3u;
+  const uint32_t* b = reinterpret_cast<const uint32_t*>(p - mis);
+  const uint32_t sh = mis * 8u;
+  const uint32_t v0 = b[0], v1 = b[1], v2 = b[2], v3 = b[3], v4 = b[4];
+  w[0] = __funnelshift_r(v0, v1, sh);
+  w[1] = __funnelshift_r(v1, v2, sh);
+  w[2] = __funnelshift_r(v2, v3, sh);
+  w[3] = __funnelshift_r(v3, v4, sh);
+}
+
+// One row's dot product over a lane's unit.  blk: the super-block in shared
+// memory.
+__device__ __forceinline__ float q6_unit_dot(const uint8_t* blk, int hh, int lq,
+                                             const XSplit16 (&xs)[4]) {
+  uint32_t qa[4], qb[4], qh[4], sc[4];
+  lds16u(blk + 64 * hh + 16 * lq, qa);
+  lds16u(blk + 64 * hh + 32 + 16 * lq, qb);
+  lds16u(blk + 128 + 32 * hh + 16 * lq, qh);
+  lds16u(blk + 192, sc);  // the 16 int8 scales
+  const float d = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(blk + 208)));
+  Dot3 t[4] = {{0, 0, 0}, {0, 0, 0}, {0, 0, 0}, {0, 0, 0}};
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const uint32_t h = qh[w];
+    const int q0 = (int)((qa[w] & 0x0F0F0F0Fu) | ((h << 4) & 0x30303030u));
+    const int q1 = (int)((qb[w] & 0x0F0F0F0Fu) | ((h << 2) & 0x30303030u));
+    const int q2 = (int)(((qa[w] >> 4) & 0x0F0F0F0Fu) | (h & 0x30303030u));
+    const int q3 = (int)(((qb[w] >> 4) & 0x0F0F0F0Fu) | ((h >> 2) & 0x30303030u));
+    t[0].a1 = __dp4a(q0, xs[0].p1[w], t[0].a1);
+    t[1].a1 = __dp4a(q1, xs[1].p1[w], t[1].a1);
+    t[2].a1 = __dp4a(q2, xs[2].p1[w], t[2].a1);
+    t[3].a1 = __dp4a(q3, xs[3].p1[w], t[3].a1);
+    t[0].a2 = __dp4a(q0, xs[0].p2[w], t[0].a2);
+    t[1].a2 = __dp4a(q1, xs[1].p2[w], t[1].a2);
+    t[2].a2 = __dp4a(q2, xs[2].p2[w], t[2].a2);
+    t[3].a2 = __dp4a(q3, xs[3].p2[w], t[3].a2);
+    t[0].a3 = __dp4a(q0, xs[0].p3[w], t[0].a3);
+    t[1].a3 = __dp4a(q1, xs[1].p3[w], t[1].a3);
+    t[2].a3 = __dp4a(q2, xs[2].p3[w], t[2].a3);
+    t[3].a3 = __dp4a(q3, xs[3].p3[w], t[3].a3);
+  }
+  // scale of sub-block 8hh + 2i + lq: byte 8hh + lq + 2i of the 16
+  const uint32_t sw0 = hh ? sc[2] : sc[0], sw1 = hh ? sc[3] : sc[1];
+  float r = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t word = i < 2 ? sw0 : sw1;
+    const int bsel = lq + 2 * (i & 1);
+    const float s8 = (float)(int)(int8_t)((word >> (8 * bsel)) & 0xFFu);
+    r = fmaf(s8, dot3_value(t[i], xs[i].scale) - 32.0f * xs[i].sum, r);
+  }
+  return d * r;
+}
+
+// Shared-memory layout of the Q6_K x planes: per unit u, 208 bytes: plane p
+// (0..2), quarter i (0..3), byte j (0..15) at p*64 + i*16 + j.
+
+template <int RPT>
+__global__ void __launch_bounds__(544, 1) q6k_gemv_m1_kernel(const M1Args a) {
+  static_assert(RPT == 2 || RPT == 4 || RPT == 8, "rows per team per stage");
+  constexpr int SPB = 8 / RPT;
+  extern __shared__ __align__(128) uint8_t smem_q6[];
+  const int nsb = a.K >> 8, U = nsb * 4, nsub16 = a.K >> 4;
+  const int rowbytes = nsb * kQ6KBytes;
+  const int rps = a.rows_per_stage;
+  const uint32_t stage_bytes = (uint32_t)(rps * rowbytes);
+  uint8_t* ring = smem_q6;
+  uint8_t* planes = ring + a.ring_bytes;                              // U * 208
+  float* xscale = reinterpret_cast<float*>(planes + U * kPlaneStride);  // nsub16
+  float* xsum = xscale + nsub16;                                       // nsub16
+  uint64_t* bars = reinterpret_cast<uint64_t*>(xsum + nsub16);
+  float* acc = reinterpret_cast<float*>(bars + 2 * a.stages);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + a.stages);
+
+  const int compute_warps = a.teams * a.team_warps;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ra = a.row_align;
+  const int ngrp = (a.N + ra - 1) / ra;
+  const int r0 = min(a.N, (int)((int64_t)blockIdx.x * ngrp / gridDim.x) * ra);
+  const int r1 = min(a.N, (int)((int64_t)(blockIdx.x + 1) * ngrp / gridDim.x) * ra);
+  const int rows = r1 - r0;
+  const int iters = (rows + rps - 1) / rps;
+  const int first = iters < a.stages ? iters : a.stages;
+
+  for (int i = threadIdx.x; i < rows; i += blockDim.x) acc[i] = 0.f;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, compute_warps);
+    }
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  // ------------------------------------------------------------ producer --
+  uint32_t issued = 0, parity_bits = 0;
+  bool prod_ok = true;
+  auto produce = [&](int it) {
+    const int s = it % a.stages;
+    const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
+    if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, a.wait_limit_ns, &g_gemv_error)) {
+      prod_ok = false;
+      return;
+    }
+    const int nr = min(rps, rows - it * rps);
+    const uint32_t bytes = (uint32_t)(nr * rowbytes);
+    const uint32_t bulk = bytes & ~15u;
+    const uint8_t* src = a.W + (size_t)(r0 + it * rps) * rowbytes;
+    uint8_t* dst = ring + s * stage_bytes;
+    // the last stage of the matrix may end off a 16-byte boundary
+    for (uint32_t b = bulk; b < bytes; b += 2)
+      *reinterpret_cast<unsigned short*>(dst + b) = (unsigned short)ldg_nc_u16(src + b);
+    mbar_arrive_expect_tx(full0 + 8 * s, bulk);
+    if (bulk != 0) bulk_g2s(smem_u32(dst), src, bulk, full0 + 8 * s);
+    issued |= 1u << s;
+    parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
+  };
+  const bool producer = warp == compute_warps && lane == 0;
+  if (producer)
+    for (int it = 0; it < first && prod_ok; ++it) produce(it);
+  pdl_wait();  // x and y only after the previous launch has completed
+  pdl_trigger();
+
+  // ------------------------------------------------ x planes (all compute warps)
+  // Two lanes per 16-value sub-block, eight values each.
+  if (warp < compute_warps) {
+    const int half = lane & 1;
+    for (int s16 = warp * 16 + (lane >> 1); s16 < nsub16; s16 += compute_warps * 16) {
+      const float4* px = reinterpret_cast<const float4*>(a.x + 16 * s16 + 8 * half);
+      const float4 va = __ldg(px), vb = __ldg(px + 1);
+      const float v[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+      float mx = 0.f, sm = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        mx = fmaxf(mx, fabsf(v[i]));
+        sm += v[i];
+      }
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+      sm += __shfl_xor_sync(0xFFFFFFFFu, sm, 1);
+      const float inv = mx > 0.f ? 127.0f / mx : 0.0f;
+      uint32_t b1[2] = {0, 0}, b2[2] = {0, 0}, b3[2] = {0, 0};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float t = fminf(fmaxf(v[i] * inv, -127.0f), 127.0f);
+        int i1, i2, i3;
+        const float f1 = round_magic(t, i1);
+        const float u2 = (t - f1) * 128.0f;
+        const float f2 = round_magic(u2, i2);
+        round_magic((u2 - f2) * 128.0f, i3);
+        const int sh8 = 8 * (i & 3);
+        b1[i >> 2] |= ((uint32_t)i1 & 0xFFu) << sh8;
+        b2[i >> 2] |= ((uint32_t)i2 & 0xFFu) << sh8;
+        b3[i >> 2] |= ((uint32_t)i3 & 0xFFu) << sh8;
+      }
+      // sub-block s16 = 16 sb + 8 hh + 2 i + lq belongs to unit 4 sb + 2 hh + lq
+      const int t16 = s16 & 15;
+      const int u = 4 * (s16 >> 4) + 2 * (t16 >> 3) + (t16 & 1), qi = (t16 >> 1) & 3;
+      uint8_t* pl = planes + u * kPlaneStride + qi * 16 + 8 * half;
+      *reinterpret_cast<uint2*>(pl) = make_uint2(b1[0], b1[1]);
+      *reinterpret_cast<uint2*>(pl + 64) = make_uint2(b2[0], b2[1]);
+      *reinterpret_cast<uint2*>(pl + 128) = make_uint2(b3[0], b3[1]);
+      if (half == 0) {
+        xscale[4 * u + qi] = mx > 0.f ? mx / 127.0f : 1.0f;
+        xsum[4 * u + qi] = sm;
+      }
+    }
+  }
+  __syncthreads();
+
+  if (producer) {
+    for (int it = first; it < iters && prod_ok; ++it) produce(it);
+    for (int s = 0; s < a.stages; ++s)
+      if (issued & (1u << s))
+        mbar_wait(full0 + 8 * s, (parity_bits >> s) & 1u, a.wait_limit_ns, &g_gemv_error);
+  } else if (warp < compute_warps) {
+    // ------------------------------------------------------------ compute --
+    const int team = warp / a.team_warps, wt = warp - team * a.team_warps;
+    const int u = wt * 32 + lane;
+    const bool active = u < U;
+    const int sb = u >> 2, hh = (u >> 1) & 1, lq = u & 1;
+    XSplit16 xs[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (active) {
+        const uint8_t* pu = planes + u * kPlaneStride + 16 * i;
+        const uint4 v1 = lds128(pu), v2 = lds128(pu + 64), v3 = lds128(pu + 128);
+        xs[i].p1[0] = v1.x; xs[i].p1[1] = v1.y; xs[i].p1[2] = v1.z; xs[i].p1[3] = v1.w;
+        xs[i].p2[0] = v2.x; xs[i].p2[1] = v2.y; xs[i].p2[2] = v2.z; xs[i].p2[3] = v2.w;
+        xs[i].p3[0] = v3.x; xs[i].p3[1] = v3.y; xs[i].p3[2] = v3.z; xs[i].p3[3] = v3.w;
+        xs[i].scale = xscale[4 * u + i];
+        xs[i].sum = xsum[4 * u + i];
+      } else {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) xs[i].p1[w] = xs[i].p2[w] = xs[i].p3[w] = 0;
+        xs[i].scale = 1.f;
+        xs[i].sum = 0.f;
+      }
+    }
+    const int off = sb * kQ6KBytes;
+    bool ok = true;
+    for (int it0 = 0; it0 < iters && ok; it0 += SPB) {
+      float pa[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) pa[i] = 0.f;
+#pragma unroll
+      for (int qq = 0; qq < SPB; ++qq) {
+        const int it = it0 + qq;
+        if (it < iters && ok) {
+          const int s = it % a.stages;
+          const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * s, ph, a.wait_limit_ns, &g_gemv_error));
+          if (ok) {
+            const int nr = min(rps, rows - it * rps);
+            const uint8_t* stage = ring + s * stage_bytes + (size_t)team * RPT * rowbytes;
+#pragma unroll
+            for (int j = 0; j < RPT; ++j)
+              if (active && team * RPT + j < nr)
+                pa[qq * RPT + j] = q6_unit_dot(stage + j * rowbytes + off, hh, lq, xs);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * s);
+          }
+        }
+      }
+      const float tot = reduce8(pa, lane);
+      const int slot = (lane >> 2) & 7;
+      const int it = it0 + slot / RPT;
+      if ((lane & 3) == 0 && it < iters) {
+        const int rr = team * RPT + slot % RPT;
+        if (rr < min(rps, rows - it * rps)) atomicAdd(&acc[it * rps + rr], tot);
+      }
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < rows; i += blockDim.x) a.y[r0 + i] = acc[i];
+}
+
 // ---------------------------------------------------------------- launch --
 
 // Resident CTAs per SM for a kernel at a dynamic shared-memory size; the
@@ -791,6 +1061,8 @@ rq_status run_q4k(const uint8_t* w, const float* x, float* y, int N, int K,
     smem_set = smem;
   }
   const int grid = persistent_grid(kern, smem, (N + R - 1) / R);
+  // launched without programmatic serialization: measured on GB300, this
+  // small persistent grid launched early slows its neighbours down
   kern<<<grid, kThreads, smem, st>>>(w, x, y, N, K);
   return launch_status();
 }
@@ -808,6 +1080,8 @@ rq_status run_q6k(const uint8_t* w, const float* x, float* y, int N, int K,
     smem_set = smem;
   }
   const int grid = persistent_grid(kern, smem, (N + R - 1) / R);
+  // launched without programmatic serialization: measured on GB300, this
+  // small persistent grid launched early slows its neighbours down
   kern<<<grid, kThreads, smem, st>>>(w, x, y, N, K);
   return launch_status();
 }
@@ -835,6 +1109,7 @@ rq_status run_q4k_m1(const uint8_t* w, const float* x, float* y, int N, int K,
   a.y = y;
   a.N = N;
   a.K = K;
+  a.row_align = 1;
   a.team_warps = (U + 31) / 32;
   a.teams = a.team_warps >= warps_per_cta ? 1 : warps_per_cta / a.team_warps;
   a.rows_per_stage = rpt * a.teams;
@@ -869,8 +1144,70 @@ rq_status run_q4k_m1(const uint8_t* w, const float* x, float* y, int N, int K,
       return RQ_ERR_CUDA;
     set = smem;
   }
-  kern<<<grid, threads, smem, st>>>(a);
-  return launch_status();
+  return launch_kernel(kern, grid, threads, smem, st, a);
+}
+
+// One-token Q6_K launch: as for Q4_K, plus the row alignment of the
+// bulk copies (rows are 16-byte aligned in groups of 16 / gcd(rowbytes, 16)).
+rq_status run_q6k_m1(const uint8_t* w, const float* x, float* y, int N, int K,
+                     cudaStream_t st) {
+  if ((reinterpret_cast<uintptr_t>(w) & 15) != 0) return RQ_ERR_SHAPE;
+  auto knob = [](const char* name, int dflt, int lo, int hi) {
+    const char* e = std::getenv(name);
+    const int v = e ? std::atoi(e) : dflt;
+    return v < lo ? lo : (v > hi ? hi : v);
+  };
+  const int warps_per_cta = knob("RQ_GEMV_WARPS", 16, 1, 16);
+  int rpt = knob("RQ_GEMV_RPT", 4, 2, 8);
+  rpt = rpt >= 8 ? 8 : (rpt >= 4 ? 4 : 2);
+  const int ring_kb = knob("RQ_GEMV_RING_KB", 150, 16, 200);
+  const int max_stages = knob("RQ_GEMV_STAGES", 8, 2, 16);
+  const int nsb = K / kQK, U = nsb * 4, nsub16 = K / 16;
+  const int rowbytes = nsb * kQ6KBytes;
+  int g = 1;
+  while (g < 16 && rowbytes % (2 * g) == 0) g *= 2;  // gcd(rowbytes, 16)
+  const int ra = 16 / g;
+  M1Args a;
+  a.W = w;
+  a.x = x;
+  a.y = y;
+  a.N = N;
+  a.K = K;
+  a.row_align = ra;
+  a.team_warps = (U + 31) / 32;
+  a.teams = a.team_warps >= warps_per_cta ? 1 : warps_per_cta / a.team_warps;
+  a.rows_per_stage = rpt * a.teams;
+  if (a.rows_per_stage % ra != 0) return RQ_ERR_SHAPE;
+  const int stage_bytes = a.rows_per_stage * rowbytes;
+  const int sms = device_sm_count();
+  const int ngrp = (N + ra - 1) / ra;
+  const int grid = ngrp < sms ? ngrp : sms;
+  const int max_rows = (ngrp + grid - 1) / grid * ra;
+  const size_t fixed = (size_t)U * kPlaneStride + 8 * (size_t)nsub16 +
+                       16 * (size_t)max_stages + 4 * (size_t)max_rows;
+  const size_t limit = 227 * 1024;
+  if (fixed + 2 * (size_t)stage_bytes > limit) return RQ_ERR_SHAPE;
+  size_t ring = (size_t)ring_kb * 1024;
+  if (ring > limit - fixed) ring = limit - fixed;
+  int stages = (int)(ring / stage_bytes);
+  stages = stages > max_stages ? max_stages : (stages < 2 ? 2 : stages);
+  a.stages = stages;
+  a.ring_bytes = (uint32_t)(stages * stage_bytes);
+  a.wait_limit_ns = kWaitLimitNs;
+  const size_t smem = a.ring_bytes + (size_t)U * kPlaneStride + 8 * (size_t)nsub16 +
+                      16 * (size_t)stages + 4 * (size_t)max_rows;
+  const int threads = (a.teams * a.team_warps + 1) * 32;
+  auto kern = rpt == 8 ? q6k_gemv_m1_kernel<8>
+                       : (rpt == 4 ? q6k_gemv_m1_kernel<4> : q6k_gemv_m1_kernel<2>);
+  static size_t smem_set[3] = {48 * 1024, 48 * 1024, 48 * 1024};
+  size_t& set = smem_set[rpt == 8 ? 2 : (rpt == 4 ? 1 : 0)];
+  if (smem > set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return RQ_ERR_CUDA;
+    set = smem;
+  }
+  return launch_kernel(kern, grid, threads, smem, st, a);
 }
 
 }  // namespace
@@ -921,7 +1258,14 @@ rq_status launch_q4k_gemv(const uint8_t* w, const float* x, float* y, int M,
 rq_status launch_q6k_gemv(const uint8_t* w, const float* x, float* y, int M,
                           int N, int K, cudaStream_t st) {
   switch (M) {
-    case 1: return run_q6k<1, 2>(w, x, y, N, K, st);
+    case 1:
+      if (K <= 16 * 2048 && std::getenv("RQ_GEMV_Q6_GENERIC") == nullptr) {
+        // RQ_ERR_SHAPE: the one-token kernel does not take this shape or
+        // alignment and nothing was launched
+        const rq_status s1 = run_q6k_m1(w, x, y, N, K, st);
+        if (s1 != RQ_ERR_SHAPE) return s1;
+      }
+      return run_q6k<1, 2>(w, x, y, N, K, st);
     case 2: return run_q6k<2, 2>(w, x, y, N, K, st);
     case 3: return run_q6k<3, 1>(w, x, y, N, K, st);
     case 4: return run_q6k<4, 1>(w, x, y, N, K, st);

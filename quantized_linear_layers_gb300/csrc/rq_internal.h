@@ -16,6 +16,28 @@ inline rq_status launch_status() { return cuda_status(cudaGetLastError()); }
 
 int device_sm_count();
 
+// Programmatic dependent launch of the library's kernels (on unless the
+// environment sets RQ_PDL=0 when the library first launches).
+bool pdl_enabled();
+
+// Launch with programmatic stream serialization (when enabled), so that the
+// kernel can be scheduled while its predecessor in the stream finishes.
+template <typename... KArgs, typename... Args>
+rq_status launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                        cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cuda_status(cudaLaunchKernelEx(&cfg, kernel, args...));
+}
+
 // rq_quant.cu ---------------------------------------------------------------
 // Zero *absmax_bits on the stream, then reduce max|x| into it.
 rq_status launch_absmax(const float* x, int64_t n, uint32_t* absmax_bits,

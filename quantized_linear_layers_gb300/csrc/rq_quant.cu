@@ -41,6 +41,8 @@ __device__ __forceinline__ void block_max_to(uint32_t m, uint32_t* out) {
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads)
 absmax_kernel(const float* __restrict__ x, int64_t n, uint32_t* out) {
+  pdl_wait();
+  pdl_trigger();
   uint32_t m = 0;
   const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
   const int64_t nthreads = (int64_t)gridDim.x * kThreads;
@@ -73,6 +75,8 @@ __global__ void __launch_bounds__(kThreads)
 quant_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
              const uint32_t* __restrict__ absmax_bits, uint8_t* __restrict__ out,
              float* __restrict__ dequant_out) {
+  pdl_wait();
+  pdl_trigger();
   const float a = absmax_prime(*absmax_bits);
   const float s = __fdiv_rn(448.0f, a);
   if (dequant_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0)
@@ -143,6 +147,8 @@ act_quant_fused_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
   const int64_t cnt4 = len >> 2;  // float4s moved by the bulk copies
   const int tid = threadIdx.x;
 
+  pdl_wait();
+  pdl_trigger();
   if (tid == 0) {
     gen_s = ld_acquire_u32(state + 3);
     for (int p = 0; p < kFusedParts; ++p) mbar_init(smem_u32(&bars[p]), 1);
@@ -234,11 +240,8 @@ rq_status launch_absmax(const float* x, int64_t n, uint32_t* absmax_bits,
   if (n == 0) return RQ_OK;
   const bool vec = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
   const int grid = grid_for(vec ? (n + 3) / 4 : n);
-  if (vec)
-    absmax_kernel<true><<<grid, kThreads, 0, st>>>(x, n, absmax_bits);
-  else
-    absmax_kernel<false><<<grid, kThreads, 0, st>>>(x, n, absmax_bits);
-  return launch_status();
+  if (vec) return launch_kernel(absmax_kernel<true>, grid, kThreads, 0, st, x, n, absmax_bits);
+  return launch_kernel(absmax_kernel<false>, grid, kThreads, 0, st, x, n, absmax_bits);
 }
 
 rq_status launch_quant(const float* x, int64_t n, int64_t n_out,
@@ -248,12 +251,10 @@ rq_status launch_quant(const float* x, int64_t n, int64_t n_out,
                    (reinterpret_cast<uintptr_t>(out) & 3) == 0;
   const int grid = grid_for(vec ? (n_out + 3) / 4 : n_out);
   if (vec)
-    quant_kernel<true><<<grid, kThreads, 0, st>>>(x, n, n_out, absmax_bits, out,
-                                                  dequant_out);
-  else
-    quant_kernel<false><<<grid, kThreads, 0, st>>>(x, n, n_out, absmax_bits,
-                                                   out, dequant_out);
-  return launch_status();
+    return launch_kernel(quant_kernel<true>, grid, kThreads, 0, st, x, n, n_out, absmax_bits,
+                         out, dequant_out);
+  return launch_kernel(quant_kernel<false>, grid, kThreads, 0, st, x, n, n_out, absmax_bits, out,
+                       dequant_out);
 }
 
 bool act_quant_fused_fits(const float* x, int64_t n, const uint8_t* out) {
@@ -278,11 +279,20 @@ rq_status launch_act_quant_fused(const float* x, int64_t n, int64_t n_out,
   int64_t chunk = fused_chunk(n);
   const int grid = (int)((n + chunk - 1) / chunk);
   const size_t smem = (size_t)((chunk + 3) / 4) * 16;
-  void* args[] = {(void*)&x, (void*)&n, (void*)&n_out, (void*)&chunk, (void*)&out,
-                  (void*)&absmax_out, (void*)&dequant_out, (void*)&state};
-  const cudaError_t e = cudaLaunchCooperativeKernel((const void*)act_quant_fused_kernel,
-                                                    dim3(grid), dim3(kFusedThreads), args,
-                                                    smem, st);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kFusedThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, act_quant_fused_kernel, x, n, n_out, chunk,
+                                           out, absmax_out, dequant_out, state);
   if (e == cudaErrorCooperativeLaunchTooLarge) {
     cudaGetLastError();
     return RQ_ERR_SHAPE;

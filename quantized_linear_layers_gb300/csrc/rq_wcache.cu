@@ -86,6 +86,8 @@ __device__ __forceinline__ void block_max_to(uint32_t m, uint32_t* out) {
 
 __global__ void __launch_bounds__(kThreads)
 q4_absmax_kernel(const uint8_t* __restrict__ W, int64_t units, uint32_t* out) {
+  pdl_wait();
+  pdl_trigger();
   uint32_t m = 0;
   for (int64_t u = (int64_t)blockIdx.x * kThreads + threadIdx.x; u < units;
        u += (int64_t)gridDim.x * kThreads) {
@@ -102,6 +104,8 @@ __global__ void __launch_bounds__(kThreads)
 q4_encode_kernel(const uint8_t* __restrict__ W, int64_t units,
                  const uint32_t* __restrict__ absmax_bits, uint8_t* __restrict__ out,
                  float* __restrict__ dequant_out) {
+  pdl_wait();
+  pdl_trigger();
   const float a = absmax_prime(*absmax_bits);
   const float s = __fdiv_rn(448.0f, a);
   if (blockIdx.x == 0 && threadIdx.x == 0) *dequant_out = __fdiv_rn(a, 448.0f);
@@ -150,6 +154,8 @@ __device__ __forceinline__ float q6_d(const uint8_t* blk) {
 
 __global__ void __launch_bounds__(kThreads)
 q6_absmax_kernel(const uint8_t* __restrict__ W, int64_t units, uint32_t* out) {
+  pdl_wait();
+  pdl_trigger();
   uint32_t m = 0;
   for (int64_t u = (int64_t)blockIdx.x * kThreads + threadIdx.x; u < units;
        u += (int64_t)gridDim.x * kThreads) {
@@ -167,6 +173,8 @@ __global__ void __launch_bounds__(kThreads)
 q6_encode_kernel(const uint8_t* __restrict__ W, int64_t units,
                  const uint32_t* __restrict__ absmax_bits, uint8_t* __restrict__ out,
                  float* __restrict__ dequant_out) {
+  pdl_wait();
+  pdl_trigger();
   const float a = absmax_prime(*absmax_bits);
   const float s = __fdiv_rn(448.0f, a);
   if (blockIdx.x == 0 && threadIdx.x == 0) *dequant_out = __fdiv_rn(a, 448.0f);
@@ -201,14 +209,14 @@ rq_status launch_dequant_absmax(int qtype, const uint8_t* w, int N, int K,
   const int64_t blocks = (int64_t)N * (K / kQK);
   if (qtype == RQ_Q4K) {
     const int64_t units = blocks * 4;
-    q4_absmax_kernel<<<grid_for(units), kThreads, 0, st>>>(w, units, absmax_bits);
+    return launch_kernel(q4_absmax_kernel, grid_for(units), kThreads, 0, st, w, units,
+                         absmax_bits);
   } else if (qtype == RQ_Q6K) {
     const int64_t units = blocks * 8;
-    q6_absmax_kernel<<<grid_for(units), kThreads, 0, st>>>(w, units, absmax_bits);
-  } else {
-    return RQ_ERR_QTYPE;
+    return launch_kernel(q6_absmax_kernel, grid_for(units), kThreads, 0, st, w, units,
+                         absmax_bits);
   }
-  return launch_status();
+  return RQ_ERR_QTYPE;
 }
 
 rq_status launch_dequant_encode(int qtype, const uint8_t* w, int N, int K,
@@ -217,16 +225,14 @@ rq_status launch_dequant_encode(int qtype, const uint8_t* w, int N, int K,
   const int64_t blocks = (int64_t)N * (K / kQK);
   if (qtype == RQ_Q4K) {
     const int64_t units = blocks * 4;
-    q4_encode_kernel<<<grid_for(units), kThreads, 0, st>>>(w, units, absmax_bits,
-                                                          out, dequant_out);
+    return launch_kernel(q4_encode_kernel, grid_for(units), kThreads, 0, st, w, units,
+                         absmax_bits, out, dequant_out);
   } else if (qtype == RQ_Q6K) {
     const int64_t units = blocks * 8;
-    q6_encode_kernel<<<grid_for(units), kThreads, 0, st>>>(w, units, absmax_bits,
-                                                          out, dequant_out);
-  } else {
-    return RQ_ERR_QTYPE;
+    return launch_kernel(q6_encode_kernel, grid_for(units), kThreads, 0, st, w, units,
+                         absmax_bits, out, dequant_out);
   }
-  return launch_status();
+  return RQ_ERR_QTYPE;
 }
 
 }  // namespace rq

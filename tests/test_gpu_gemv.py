@@ -134,3 +134,32 @@ def test_tensor_core_and_generic_kernels_agree(rq, monkeypatch, M):
     monkeypatch.setenv("RQ_GEMV_NO_MMA", "1")
     got2 = gpu_gemv(rq, Q4K, W, x, N, K)
     assert gemv_ok(got2, ref, absdot)[0]
+
+
+@pytest.mark.parametrize("N,K", [(157, 768), (1001, 2560), (3001, 18944), (512, 3584)])
+def test_q6k_one_token_rows_and_alignment_groups(rq, N, K):
+    """One-token Q6_K kernel: 210-byte super-blocks make rows 16-byte
+    aligned only in groups of 2, 4 or 8; row blocks, stages and the last
+    partial stage (bytes past the final 16-byte boundary) all meet the bound."""
+    W = synthetic.q6k_matrix(600 + N, N, K)
+    x = synthetic.activation(601 + K, 1, K, outlier_frac=1e-3)
+    got = gpu_gemv(rq, Q6K, W, x, N, K)
+    ref, absdot = oracle.gemv(Q6K, W, x, N, K)
+    ok, worst = gemv_ok(got, ref, absdot)
+    assert ok, worst
+
+
+@pytest.mark.parametrize("M", [1, 3])
+def test_q6k_weight_only_4_byte_aligned(rq, M):
+    """A Q6_K weight at a 4-byte (not 16-byte) aligned address takes the
+    generic kernel and gives the same bound."""
+    N, K = 200, 1024
+    W = synthetic.q6k_matrix(9, N, K)
+    buf = torch.zeros(W.size + 16, dtype=torch.uint8, device="cuda")
+    buf[4:4 + W.size] = to_dev(W.ravel())
+    x = synthetic.activation(10, M, K)
+    y = empty((M, N), torch.float32)
+    rq.rq_q6k_gemv(buf[4:], to_dev(x), y, M, N, K)
+    torch.cuda.synchronize()
+    ref, absdot = oracle.gemv(Q6K, W, x, N, K)
+    assert gemv_ok(y.cpu().numpy(), ref, absdot)[0]
