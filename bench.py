@@ -7,14 +7,17 @@ One step = one pass of the whole hot path over the 28-layer decoder stack
     Q4_K / Q6_K GEMV), replayed from a CUDA graph captured once;
   * prefill pass: 28 x 7 rq_linear calls at M = 2048 tokens (routed to the
     FP8 path: weight-cache hit, activation absmax + E4M3 on a miss, reuse
-    across q/k/v and gate/up, tcgen05 FP8 GEMM), launched eagerly with the
-    library's kernel tracing on.
+    across q/k/v and gate/up, tcgen05 FP8 GEMM), launched eagerly.
 
 Headline `value`: FP8 prefill TFLOP/s at M = 2048 (2*M*N*K summed over the
 196 GEMMs / device time of the prefill pass, quantization included).  The
 GEMV HBM GB/s of the decode pass at M = 1 is reported in `gemv`.  `roofline`
 is for the dominant kernel (the FP8 GEMM): its algorithmic FLOPs / its
-traced device time.  `e2e` repeats the measurement through the public API
+device time from CUDA events around each GEMM launch, in K passes run right
+after the timed ones (events between kernels would slow the timed passes).
+`--sweep` prints the other configurations (GEMV at M = 1, 4, 8 over the
+decoder shapes; FP8 GEMM at M = 512; the prefill stack at M = 16 .. 4096).
+`e2e` repeats the measurement through the public API
 with host buffers (stack input copied in from pinned memory, last output
 copied back) each step.  `cpu_baseline` times the CPU oracle on a bounded
 sample.  `--impl reference` times the oracle alone as the reference arm.
@@ -257,7 +260,7 @@ def run_reference(args, world, rank):
 class Stack:
     """Device-resident 28-layer workload."""
 
-    def __init__(self, rq, torch, dev, seed=SEED):
+    def __init__(self, rq, torch, dev, seed=SEED, Ms=(M_DECODE, M_PREFILL)):
         self.rq, self.torch, self.dev = rq, torch, dev
         self.ctx = rq.Context()
         L = synthetic.N_LAYERS
@@ -270,17 +273,17 @@ class Stack:
             self.weights.append(row)
         # activations: one seeded set per kind, copied into per-layer buffers
         self.acts = {}
-        for M in (M_DECODE, M_PREFILL):
+        for M in Ms:
             base = {}
             for j, (kind, K) in enumerate(ACT_K.items()):
-                frac = 1e-3 if M == M_PREFILL else 0.0
+                frac = 1e-3 if M > 8 else 0.0
                 a = synthetic.activation(synthetic.substream(seed, 700 + 10 * M + j), M, K,
                                          outlier_frac=frac)
                 base[kind] = torch.from_numpy(a).to(dev)
             self.acts[M] = [{k: v.clone() for k, v in base.items()} for _ in range(L)]
         self.out = {M: {name: torch.empty(M, N, device=dev)
                         for name, _, N, _ in synthetic.LAYER_LINEARS}
-                    for M in (M_DECODE, M_PREFILL)}
+                    for M in Ms}
         torch.cuda.synchronize()
 
     def run_pass(self, M, stream=None, acts=None):
@@ -340,31 +343,60 @@ def run_gpu(args, world, rank, local):
     torch.cuda.synchronize()
     sampler.start()
     t_wall = time.perf_counter()
+    # The timed steps carry no per-kernel events: an event between two
+    # kernels keeps them from overlapping (programmatic dependent launch),
+    # which slowed the prefill pass by about 9% even with only the GEMMs
+    # traced.
     for _ in range(args.steps):
         torch.cuda.nvtx.range_push("timed_step")
         e0, e1, e2 = ev(), ev(), ev()
         e0.record(stream)
         graph.replay()
         e1.record(stream)
-        st.ctx.rq_ctx_trace_begin(1024)
         st.run_pass(M_PREFILL, stream)
         e2.record(stream)
-        tr = st.ctx.rq_ctx_trace_end()  # waits for the pass's events
         torch.cuda.nvtx.range_pop()
-        for k, (n, ms) in tr.items():
-            c = traced.setdefault(k, [0, 0.0])
-            c[0] += n
-            c[1] += ms
         dec_ms.append(e0.elapsed_time(e1))
         pre_ms.append(e1.elapsed_time(e2))
         step_ms.append(e0.elapsed_time(e2))
     torch.cuda.synchronize()
     wall_s = time.perf_counter() - t_wall
     dist_barrier(world)
-    clocks = sampler.stop()
     status = rq.rq_get_device_status()
     if status != 0:
         raise RuntimeError("device status %d in timed region" % status)
+
+    # Roofline of the GEMM: the same K prefill passes again, right after the
+    # timed steps (clocks still sampled), with CUDA events around each of
+    # the 196 GEMM launches on the launching stream.
+    st.ctx.rq_ctx_trace_kinds(["gemm"])
+    traced_pre_ms = []
+    for _ in range(args.steps):
+        e1, e2 = ev(), ev()
+        e1.record(stream)
+        st.ctx.rq_ctx_trace_begin(1024)
+        st.run_pass(M_PREFILL, stream)
+        e2.record(stream)
+        tr = st.ctx.rq_ctx_trace_end()  # waits for the pass's events
+        traced_pre_ms.append(e1.elapsed_time(e2))
+        for k, (n, ms) in tr.items():
+            c = traced.setdefault(k, [0, 0.0])
+            c[0] += n
+            c[1] += ms
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+
+    # per-kind breakdown of the prefill pass, from two fully traced passes
+    # (informational: tracing every kernel slows the pass)
+    st.ctx.rq_ctx_trace_kinds(list(st.ctx.TRACE_KINDS))
+    breakdown = {}
+    for _ in range(2):
+        st.ctx.rq_ctx_trace_begin(1024)
+        st.run_pass(M_PREFILL, stream)
+        for k, (n, ms) in st.ctx.rq_ctx_trace_end().items():
+            c = breakdown.setdefault(k, [0, 0.0])
+            c[0] += n
+            c[1] += ms / 2
 
     K = args.steps
     pre_s = dist_max(sum(pre_ms) / 1e3, world)
@@ -389,7 +421,7 @@ def run_gpu(args, world, rank, local):
         "data": "synthetic",
         "config": {
             "workload": "28-layer decoder linear stack: decode pass M=1 (GEMV, graph "
-                        "replay) + prefill pass M=2048 (FP8, eager, traced)",
+                        "replay) + prefill pass M=2048 (FP8, eager)",
             "hidden": synthetic.HIDDEN, "intermediate": synthetic.INTERMEDIATE,
             "kv_dim": synthetic.KV_DIM, "layers": synthetic.N_LAYERS,
             "M_decode": M_DECODE, "M_prefill": M_PREFILL, "gemm_threshold": 4,
@@ -409,9 +441,13 @@ def run_gpu(args, world, rank, local):
                                     "ratio 2)" % pk["source"],
                      "traffic": traffic,
                      "flops_per_launch_avg": flops / 196.0,
-                     "avg_launch_ms": gemm_trace_ms / gemm_calls if gemm_calls else None},
-        "trace_ms_per_step": {k: v[1] / K for k, v in traced.items()},
-        "gpu_launches": K * 196 + sum(c for c, _ in traced.values()),
+                     "avg_launch_ms": gemm_trace_ms / gemm_calls if gemm_calls else None,
+                     "source": "CUDA events around each GEMM launch in K prefill passes run "
+                               "right after the timed steps (%.3f ms per pass with the "
+                               "events, %.3f ms without)" % (sum(traced_pre_ms) / K,
+                                                             pre_s / K * 1e3)},
+        "kernel_ms_per_prefill_pass": {k: v[1] for k, v in breakdown.items()},
+        "gpu_launches": K * (196 + sum(c for c, _ in breakdown.values()) // 2),
         "clocks": clocks, "e2e": e2e, "setup_s": setup_s, "wall_s": wall_s,
         "act_cache": st.ctx.stats(),
     }
@@ -479,6 +515,101 @@ def run_e2e(args, st, torch, rq, dev, stream, world):
     return {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps,
             "note": "prefill FLOPs / (decode + prefill eager step with copies)"}
+
+
+def graph_time_ms(torch, dev, calls, reps=2):
+    """Device time per call of `calls` (a list of thunks), captured once in a
+    CUDA graph and replayed `reps` times after one warm replay."""
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        for c in calls[:3]:
+            c()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            for c in calls:
+                c()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (reps * len(calls))
+
+
+def run_sweep(args):
+    """The configurations other than the headline line, one JSON line each:
+    the decode GEMV over the decoder's shapes at M = 1, 4, 8 (graph replay,
+    weights rotated through >= 512 MB so that every launch reads HBM); the
+    FP8 GEMM at M = 512 on the four prefill shapes; the 28-layer prefill
+    stack through rq_linear at M = 16 .. 4096 (eager, untraced)."""
+    import torch
+    import quantized_linear_layers_gb300 as rq
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pk = peaks()
+    fp8_peak = 2.0 * pk["bf16_sustained"]
+
+    def out(d):
+        print(json.dumps(d), flush=True)
+
+    # decode GEMV sweep
+    for name, qt, N, K in [("q,o", synthetic.Q4K, 3584, 3584), ("k", synthetic.Q4K, 512, 3584),
+                           ("v", synthetic.Q6K, 512, 3584), ("gate,up", synthetic.Q4K, 18944, 3584),
+                           ("down", synthetic.Q4K, 3584, 18944)]:
+        W0 = torch.from_numpy(synthetic.weight_matrix(11, qt, N, K)).to(dev)
+        Ws = [W0] + [W0.clone() for _ in range(-(-(512 << 20) // W0.numel()) - 1)]
+        fn = rq.rq_q4k_gemv if qt == synthetic.Q4K else rq.rq_q6k_gemv
+        for M in (1, 4, 8):
+            x = torch.from_numpy(synthetic.activation(12 + M, M, K)).to(dev)
+            y = torch.empty(M, N, device=dev)
+            calls = [lambda W=W: fn(W, x, y, M, N, K) for W in Ws[:max(len(Ws), 20)]]
+            ms = graph_time_ms(torch, dev, calls)
+            nbytes = packed_bytes(qt, N, K) + 4 * M * (K + N)
+            out({"sweep": "gemv", "linear": name, "qtype": "Q4_K" if qt == synthetic.Q4K
+                 else "Q6_K", "M": M, "N": N, "K": K, "us": ms * 1e3,
+                 "GB/s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / pk["hbm_gbs"]})
+        del Ws, W0
+    # FP8 GEMM at M = 512
+    ctx = rq.Context()
+    M = 512
+    for N, K in [(3584, 3584), (512, 3584), (18944, 3584), (3584, 18944)]:
+        W = torch.from_numpy(synthetic.q4k_matrix(13, N, K)).to(dev)
+        wq, wd = ctx.rq_fp8_weight_cache(synthetic.Q4K, W, N, K)
+        x = torch.from_numpy(synthetic.activation(14, M, K, outlier_frac=1e-3)).to(dev)
+        xq, xd = ctx.rq_fp8_act_cache(x, M, K)
+        y = torch.empty(M, N, device=dev)
+        calls = [lambda: rq.rq_fp8_gemm(xq, xd, wq, wd, y, M, N, K)] * 20
+        ms = graph_time_ms(torch, dev, calls)
+        tf = 2.0 * M * N * K / ms / 1e9
+        out({"sweep": "fp8_gemm", "M": M, "N": N, "K": K, "us": ms * 1e3, "TFLOP/s": tf,
+             "frac_fp8_peak": tf / fp8_peak})
+    ctx.close()
+    # prefill stack at several M
+    Ms = (16, 128, 512, 2048, 4096)
+    st = Stack(rq, torch, dev, Ms=Ms)
+    for M in Ms:
+        st.run_pass(M)  # weight cache on the first pass
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 3
+        e0.record()
+        for _ in range(reps):
+            st.ctx.rq_act_cache_invalidate()
+            st.run_pass(M)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        out({"sweep": "prefill_stack", "M": M, "ms_per_pass": ms,
+             "TFLOP/s": stack_flops(M) / ms / 1e9,
+             "act_cache": st.ctx.stats()})
+    if rq.rq_get_device_status() != 0:
+        raise SystemExit(1)
 
 
 def run_case(args):
@@ -592,11 +723,15 @@ def main():
     ap.add_argument("--N", type=int, default=3584)
     ap.add_argument("--K", type=int, default=3584)
     ap.add_argument("--launches", type=int, default=3)
+    ap.add_argument("--sweep", action="store_true",
+                    help="print the GEMV, FP8 GEMM and prefill-stack sweeps instead")
     ap.add_argument("--graph", action="store_true",
                     help="single-kernel mode: time the launches as one CUDA graph replay")
     args = ap.parse_args()
     if args.case:
         return run_case(args)
+    if args.sweep:
+        return run_sweep(args)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup()

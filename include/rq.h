@@ -271,6 +271,14 @@ typedef enum {
  * RQ_ERR_ALLOC. */
 rq_status rq_ctx_trace_begin(rq_ctx *ctx, int capacity);
 
+/* Restrict tracing to the kinds whose bit (1 << kind) is set in `mask`
+ * (all kinds by default): the events of a traced kernel keep it from
+ * overlapping its neighbours (programmatic dependent launch), so a caller
+ * timing a whole pass traces only the kernels it needs.  Takes effect for
+ * kernels launched after the call.  Errors: RQ_ERR_NULL, RQ_ERR_SHAPE (mask
+ * 0 or with bits at or above RQ_TRACE_KINDS). */
+rq_status rq_ctx_trace_kinds(rq_ctx *ctx, unsigned int mask);
+
 /* Stop tracing, wait for the traced events, and return per kind the number
  * of kernels and their summed device time in milliseconds (arrays of
  * RQ_TRACE_KINDS host entries; either may be NULL).  Errors: RQ_ERR_NULL,

@@ -62,6 +62,7 @@ _SIGS = {
     "rq_act_cache_invalidate": ([_vp], _i32),
     "rq_ctx_trace_begin": ([_vp, _i32], _i32),
     "rq_ctx_trace_end": ([_vp, _vp, _vp], _i32),
+    "rq_ctx_trace_kinds": ([_vp, ctypes.c_uint], _i32),
     "rq_get_device_status": ([_vp], _i32),
     "rq_debug_wait_timeout": ([_i64, _vp], _i32),
 }
@@ -216,6 +217,13 @@ class Context:
 
     def rq_ctx_trace_begin(self, capacity):
         _check(_lib.rq_ctx_trace_begin(self._h, capacity), "rq_ctx_trace_begin")
+
+    def rq_ctx_trace_kinds(self, kinds):
+        """Trace only the named kinds (a subset of TRACE_KINDS)."""
+        mask = 0
+        for k in kinds:
+            mask |= 1 << self.TRACE_KINDS.index(k)
+        _check(_lib.rq_ctx_trace_kinds(self._h, mask), "rq_ctx_trace_kinds")
 
     def rq_ctx_trace_end(self):
         """-> {kind: (kernel count, summed device ms)}"""

@@ -79,6 +79,7 @@ struct rq_ctx {
   int device = 0;
   // kernel tracing
   bool trace_on = false;
+  unsigned int trace_mask = (1u << RQ_TRACE_KINDS) - 1u;  // kinds that are traced
   int trace_cap = 0, trace_used = 0;
   std::vector<TraceSlot> trace;
   int threshold = 4;
@@ -111,7 +112,8 @@ cudaError_t record(cudaEvent_t ev, cudaStream_t st) {
 class TraceScope {
  public:
   TraceScope(rq_ctx* ctx, int kind, cudaStream_t st) : st_(st) {
-    if (ctx != nullptr && ctx->trace_on && ctx->trace_used < ctx->trace_cap) {
+    if (ctx != nullptr && ctx->trace_on && ((ctx->trace_mask >> kind) & 1u) != 0 &&
+        ctx->trace_used < ctx->trace_cap) {
       slot_ = &ctx->trace[ctx->trace_used++];
       slot_->kind = kind;
       record(slot_->start, st_);
@@ -425,6 +427,13 @@ rq_status rq_ctx_trace_begin(rq_ctx* ctx, int capacity) {
   ctx->trace_cap = capacity;
   ctx->trace_used = 0;
   ctx->trace_on = true;
+  return RQ_OK;
+}
+
+rq_status rq_ctx_trace_kinds(rq_ctx* ctx, unsigned int mask) {
+  if (ctx == nullptr) return RQ_ERR_NULL;
+  if (mask == 0u || (mask >> RQ_TRACE_KINDS) != 0u) return RQ_ERR_SHAPE;
+  ctx->trace_mask = mask;
   return RQ_OK;
 }
 

@@ -441,16 +441,35 @@ __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
   return *reinterpret_cast<const uint4*>(p);
 }
 
-// Group coefficients from a header: (256 d sc_lo, 4096 d sc_hi, dmin m_lo,
-// dmin m_hi) for sub-blocks 2g, 2g+1.
+// Exact int -> float for |v| < 2^22 on the FP32 pipe (no conversion
+// instruction): v is added into the mantissa of 1.5 * 2^23.
+__device__ __forceinline__ float i2f_small(int v) {
+  return __int_as_float(v + 0x4B400000) - 12582912.0f;
+}
+
+// Byte b (0 or 1) of a 16-bit pair as a float (the byte goes into the
+// mantissa of 2^23).
+__device__ __forceinline__ float byte_to_float(uint32_t pair, int b) {
+  return __uint_as_float(__byte_perm(pair, 0x4B000000u, b ? 0x7441u : 0x7440u)) - 8388608.0f;
+}
+
+// dp4a with unsigned bytes in a and signed bytes in b.
+__device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Group coefficients from a header: (d sc_lo, d sc_hi / 16, dmin m_lo,
+// dmin m_hi) for sub-blocks 2g, 2g+1 (the high nibbles enter the dot
+// products as 16 q, hence the 1/16).
 __device__ __forceinline__ float4 q4_coeffs(const uint4& h, int sh, bool upper) {
   const uint32_t a16 = h.y >> sh, b16 = h.z >> sh, c16 = h.w >> sh;
   const uint32_t scp = upper ? ((c16 & 0x0F0Fu) | ((a16 >> 2) & 0x3030u)) : (a16 & 0x3F3Fu);
   const uint32_t mp = upper ? (((c16 >> 4) & 0x0F0Fu) | ((b16 >> 2) & 0x3030u)) : (b16 & 0x3F3Fu);
   const float2 dd = half_pair(h.x);
-  return make_float4((dd.x * 256.0f) * (float)(scp & 0xFFu),
-                     (dd.x * 4096.0f) * (float)((scp >> 8) & 0xFFu),
-                     dd.y * (float)(mp & 0xFFu), dd.y * (float)((mp >> 8) & 0xFFu));
+  return make_float4(dd.x * byte_to_float(scp, 0), (dd.x * 0.0625f) * byte_to_float(scp, 1),
+                     dd.y * byte_to_float(mp, 0), dd.y * byte_to_float(mp, 1));
 }
 
 // x of one 32-weight sub-block as three int8 planes: with s = max|x| / 127,
@@ -472,7 +491,8 @@ struct Dot3 {
 };
 
 __device__ __forceinline__ float dot3_value(const Dot3& d, float scale) {
-  const float v = fmaf((float)d.a3, 1.0f / 16384.0f, fmaf((float)d.a2, 1.0f / 128.0f, (float)d.a1));
+  const float v = fmaf(i2f_small(d.a3), 1.0f / 16384.0f,
+                       fmaf(i2f_small(d.a2), 1.0f / 128.0f, i2f_small(d.a1)));
   return v * scale;
 }
 
@@ -488,32 +508,31 @@ __device__ __forceinline__ float2 q4_group_dot2i(const uint8_t* r0, const uint8_
   Dot3 l0 = {0, 0, 0}, g0 = {0, 0, 0}, l1 = {0, 0, 0}, g1 = {0, 0, 0};
 #pragma unroll
   for (int w = 0; w < 8; ++w) {
-    const int lo0 = (int)(q0[w] & 0x0F0F0F0Fu), hi0 = (int)((q0[w] >> 4) & 0x0F0F0F0Fu);
-    const int lo1 = (int)(q1[w] & 0x0F0F0F0Fu), hi1 = (int)((q1[w] >> 4) & 0x0F0F0F0Fu);
+    // high nibbles stay in place: unsigned bytes 16 q against signed x
+    const int lo0 = (int)(q0[w] & 0x0F0F0F0Fu), lo1 = (int)(q1[w] & 0x0F0F0F0Fu);
+    const uint32_t hi0 = q0[w] & 0xF0F0F0F0u, hi1 = q1[w] & 0xF0F0F0F0u;
     l0.a1 = __dp4a(lo0, xl.p1[w], l0.a1);
     l1.a1 = __dp4a(lo1, xl.p1[w], l1.a1);
     l0.a2 = __dp4a(lo0, xl.p2[w], l0.a2);
     l1.a2 = __dp4a(lo1, xl.p2[w], l1.a2);
     l0.a3 = __dp4a(lo0, xl.p3[w], l0.a3);
     l1.a3 = __dp4a(lo1, xl.p3[w], l1.a3);
-    g0.a1 = __dp4a(hi0, xh.p1[w], g0.a1);
-    g1.a1 = __dp4a(hi1, xh.p1[w], g1.a1);
-    g0.a2 = __dp4a(hi0, xh.p2[w], g0.a2);
-    g1.a2 = __dp4a(hi1, xh.p2[w], g1.a2);
-    g0.a3 = __dp4a(hi0, xh.p3[w], g0.a3);
-    g1.a3 = __dp4a(hi1, xh.p3[w], g1.a3);
+    g0.a1 = dp4a_us(hi0, xh.p1[w], g0.a1);
+    g1.a1 = dp4a_us(hi1, xh.p1[w], g1.a1);
+    g0.a2 = dp4a_us(hi0, xh.p2[w], g0.a2);
+    g1.a2 = dp4a_us(hi1, xh.p2[w], g1.a2);
+    g0.a3 = dp4a_us(hi0, xh.p3[w], g0.a3);
+    g1.a3 = dp4a_us(hi1, xh.p3[w], g1.a3);
   }
-  // coefficients with the 2^p factors of the float path removed: (d sc_lo,
-  // d sc_hi, dmin m_lo, dmin m_hi)
   const float4 c0 = q4_coeffs(h0, sh, upper), c1 = q4_coeffs(h1, sh, upper);
   const float dl0 = dot3_value(l0, xl.scale), dh0 = dot3_value(g0, xh.scale);
   const float dl1 = dot3_value(l1, xl.scale), dh1 = dot3_value(g1, xh.scale);
-  float p0 = (c0.x * (1.0f / 256.0f)) * dl0;
-  p0 = fmaf(c0.y * (1.0f / 4096.0f), dh0, p0);
+  float p0 = c0.x * dl0;
+  p0 = fmaf(c0.y, dh0, p0);
   p0 = fmaf(-c0.z, xl.sum, p0);
   p0 = fmaf(-c0.w, xh.sum, p0);
-  float p1 = (c1.x * (1.0f / 256.0f)) * dl1;
-  p1 = fmaf(c1.y * (1.0f / 4096.0f), dh1, p1);
+  float p1 = c1.x * dl1;
+  p1 = fmaf(c1.y, dh1, p1);
   p1 = fmaf(-c1.z, xl.sum, p1);
   p1 = fmaf(-c1.w, xh.sum, p1);
   return make_float2(p0, p1);
@@ -834,7 +853,7 @@ __device__ __forceinline__ float q6_unit_dot(const uint8_t* blk, int hh, int lq,
   for (int i = 0; i < 4; ++i) {
     const uint32_t word = i < 2 ? sw0 : sw1;
     const int bsel = lq + 2 * (i & 1);
-    const float s8 = (float)(int)(int8_t)((word >> (8 * bsel)) & 0xFFu);
+    const float s8 = i2f_small((int)(word << (24 - 8 * bsel)) >> 24);  // signed byte
     r = fmaf(s8, dot3_value(t[i], xs[i].scale) - 32.0f * xs[i].sum, r);
   }
   return d * r;
@@ -1097,10 +1116,13 @@ rq_status run_q4k_m1(const uint8_t* w, const float* x, float* y, int N, int K,
     const int v = e ? std::atoi(e) : dflt;
     return v < lo ? lo : (v > hi ? hi : v);
   };
-  const int warps_per_cta = knob("RQ_GEMV_WARPS", 16, 1, 16);
-  int rpt = knob("RQ_GEMV_RPT", 4, 2, 8);
+  // defaults from launch-shape sweeps on GB300: few rows per SM favour
+  // smaller teams and stages; long rows favour a shallower ring
+  const bool few_rows = N <= 8 * device_sm_count();
+  const int warps_per_cta = knob("RQ_GEMV_WARPS", few_rows ? 8 : 16, 1, 16);
+  int rpt = knob("RQ_GEMV_RPT", few_rows ? 2 : 4, 2, 8);
   rpt = rpt >= 8 ? 8 : (rpt >= 4 ? 4 : 2);
-  const int ring_kb = knob("RQ_GEMV_RING_KB", 150, 16, 200);
+  const int ring_kb = knob("RQ_GEMV_RING_KB", K >= 8192 ? 100 : 150, 16, 200);
   const int max_stages = knob("RQ_GEMV_STAGES", 8, 2, 16);
   const int U = K / 64, nsub = K / 32;
   M1Args a;
@@ -1157,8 +1179,9 @@ rq_status run_q6k_m1(const uint8_t* w, const float* x, float* y, int N, int K,
     const int v = e ? std::atoi(e) : dflt;
     return v < lo ? lo : (v > hi ? hi : v);
   };
-  const int warps_per_cta = knob("RQ_GEMV_WARPS", 16, 1, 16);
-  int rpt = knob("RQ_GEMV_RPT", 4, 2, 8);
+  const bool few_rows = N <= 8 * device_sm_count();
+  const int warps_per_cta = knob("RQ_GEMV_WARPS", few_rows ? 8 : 16, 1, 16);
+  int rpt = knob("RQ_GEMV_RPT", few_rows ? 2 : 4, 2, 8);
   rpt = rpt >= 8 ? 8 : (rpt >= 4 ? 4 : 2);
   const int ring_kb = knob("RQ_GEMV_RING_KB", 150, 16, 200);
   const int max_stages = knob("RQ_GEMV_STAGES", 8, 2, 16);

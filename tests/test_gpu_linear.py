@@ -189,3 +189,29 @@ def test_wait_timeout_is_reported_and_cleared(rq):
     assert rq.rq_get_device_status() == 0
     check_gemm(y.cpu().numpy(), gemm_route_ref(Q4K, W, x, N, K))
     ctx.close()
+
+
+def test_trace_kinds_mask(rq):
+    """Tracing restricted to GEMMs records only the GEMM launch; an empty
+    mask is rejected; restoring all kinds traces the activation kernels."""
+    N, K, M = 256, 512, 64
+    W = synthetic.q4k_matrix(3, N, K)
+    Wd = to_dev(W)
+    xd = to_dev(synthetic.activation(4, M, K))
+    y = empty((M, N), torch.float32)
+    ctx = rq.Context()
+    ctx.rq_ctx_trace_kinds(["gemm"])
+    ctx.rq_ctx_trace_begin(16)
+    ctx.rq_linear(Q4K, Wd, xd, y, M, N, K)
+    tr = ctx.rq_ctx_trace_end()
+    assert tr["gemm"][0] == 1 and tr["gemm"][1] > 0
+    assert tr["wcache"][0] == tr["quant"][0] == tr["absmax"][0] == 0
+    with pytest.raises(rq.RqError):
+        ctx.rq_ctx_trace_kinds([])
+    ctx.rq_ctx_trace_kinds(list(ctx.TRACE_KINDS))
+    ctx.rq_act_cache_invalidate()
+    ctx.rq_ctx_trace_begin(16)
+    ctx.rq_linear(Q4K, Wd, xd, y, M, N, K)
+    tr = ctx.rq_ctx_trace_end()
+    assert tr["gemm"][0] == 1 and tr["quant"][0] == 1
+    ctx.close()
