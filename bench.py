@@ -347,6 +347,7 @@ def run_gpu(args, world, rank, local):
     # kernels keeps them from overlapping (programmatic dependent launch),
     # which slowed the prefill pass by about 9% even with only the GEMMs
     # traced.
+    events = []
     for _ in range(args.steps):
         torch.cuda.nvtx.range_push("timed_step")
         e0, e1, e2 = ev(), ev(), ev()
@@ -356,10 +357,12 @@ def run_gpu(args, world, rank, local):
         st.run_pass(M_PREFILL, stream)
         e2.record(stream)
         torch.cuda.nvtx.range_pop()
+        events.append((e0, e1, e2))
+    torch.cuda.synchronize()
+    for e0, e1, e2 in events:
         dec_ms.append(e0.elapsed_time(e1))
         pre_ms.append(e1.elapsed_time(e2))
         step_ms.append(e0.elapsed_time(e2))
-    torch.cuda.synchronize()
     wall_s = time.perf_counter() - t_wall
     dist_barrier(world)
     status = rq.rq_get_device_status()

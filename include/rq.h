@@ -200,9 +200,10 @@ rq_status rq_fp8_act_cache(rq_ctx *ctx, const float *x, int M, int K,
  *                   then the FP8 GEMM.  When x is 16-byte aligned and fits
  *                   the shared memory of one wave of CTAs (about 220 KB per
  *                   SM), absmax and quantization are one cooperative kernel
- *                   that reads x once (same bytes as the two-kernel form;
- *                   environment RQ_ONE_PASS_QUANT=0 at ctx creation turns it
- *                   off).
+ *                   that reads x once; otherwise two kernels, the second
+ *                   reading x backwards so that its first reads hit L2
+ *                   (same bytes either way; environment RQ_ONE_PASS_QUANT=0
+ *                   at ctx creation selects the two kernels always).
  * The activation cache ([gemm.rs], PMAT-084 reuse across Q/K/V and gate/up)
  * is keyed by (x, M, K, generation); rq_act_cache_invalidate bumps the
  * generation and must be called when x's contents change in place.
@@ -257,9 +258,10 @@ rq_status rq_act_cache_invalidate(rq_ctx *ctx);
  * stream is being captured).  Kinds: */
 typedef enum {
     RQ_TRACE_GEMV = 0,    /* Q4_K / Q6_K GEMV                         */
-    RQ_TRACE_ABSMAX = 1,  /* zeroing + absmax of the activation       */
-    RQ_TRACE_QUANT = 2,   /* activation E4M3 quantization (or the
-                             one-pass absmax + quantization kernel)   */
+    RQ_TRACE_ABSMAX = 1,  /* (not emitted by rq_linear, which traces the
+                             activation's absmax and encoding together
+                             as RQ_TRACE_QUANT)                       */
+    RQ_TRACE_QUANT = 2,   /* activation absmax + E4M3 quantization    */
     RQ_TRACE_GEMM = 3,    /* FP8 GEMM                                 */
     RQ_TRACE_WCACHE = 4,  /* FP8 weight-cache build (a miss)          */
     RQ_TRACE_KINDS = 5

@@ -91,6 +91,7 @@ struct rq_ctx {
   float* act_deq = nullptr;    // device float
   unsigned int* fused = nullptr;  // one-pass quantization state (4 device words)
   bool fused_ok = true;           // RQ_ONE_PASS_QUANT=0 keeps the two-kernel path
+  uint32_t* slots = nullptr;      // per-CTA partial maxima of the two-kernel path
   // activation cache key
   bool act_valid = false;
   const float* act_x = nullptr;
@@ -180,6 +181,13 @@ rq_status rq_ctx_create(rq_ctx** out) {
   }
   const char* one_pass = std::getenv("RQ_ONE_PASS_QUANT");
   if (one_pass != nullptr && std::atoi(one_pass) == 0) c->fused_ok = false;
+  void* sl = nullptr;
+  if (cudaMalloc(&sl, sizeof(uint32_t) * (size_t)act_quant_slots()) != cudaSuccess) {
+    cudaFree(p);
+    delete c;
+    return RQ_ERR_ALLOC;
+  }
+  c->slots = static_cast<uint32_t*>(sl);
   *out = c;
   return RQ_OK;
 }
@@ -193,6 +201,7 @@ void rq_ctx_destroy(rq_ctx* ctx) {
   for (auto& kv : ctx->weights) cudaFree(kv.second.fp8);
   if (ctx->act) cudaFree(ctx->act);
   if (ctx->absmax) cudaFree(ctx->absmax);
+  if (ctx->slots) cudaFree(ctx->slots);
   delete ctx;
 }
 
@@ -347,14 +356,10 @@ rq_status rq_fp8_act_cache(rq_ctx* ctx, const float* x, int M, int K,
       s = launch_act_quant_fused(x, n, (int64_t)need, ctx->act, ctx->absmax, ctx->act_deq,
                                  ctx->fused, st);
     } else {
-      {
-        TraceScope ts(ctx, RQ_TRACE_ABSMAX, st);
-        s = launch_absmax(x, n, ctx->absmax, st);
-      }
-      if (s == RQ_OK) {
-        TraceScope ts(ctx, RQ_TRACE_QUANT, st);
-        s = launch_quant(x, n, (int64_t)need, ctx->absmax, ctx->act, ctx->act_deq, st);
-      }
+      // two kernels: per-CTA maxima into slots, then the encoding
+      TraceScope ts(ctx, RQ_TRACE_QUANT, st);
+      s = launch_act_quant_two_pass(x, n, (int64_t)need, ctx->act, ctx->slots, ctx->absmax,
+                                    ctx->act_deq, st);
     }
     if (s != RQ_OK) {
       ctx->act_valid = false;

@@ -57,6 +57,13 @@ rq_status launch_act_quant_fused(const float* x, int64_t n, int64_t n_out,
                                  uint8_t* out, uint32_t* absmax_out,
                                  float* dequant_out, unsigned int* state,
                                  cudaStream_t st);
+// Two kernels, no zeroing: per-CTA partial maxima into `slots` (at least
+// act_quant_slots() words), then the encoding, which reduces the slots and
+// walks x backwards (its last-read part is still in L2).
+int act_quant_slots();
+rq_status launch_act_quant_two_pass(const float* x, int64_t n, int64_t n_out, uint8_t* out,
+                                    uint32_t* slots, uint32_t* absmax_out,
+                                    float* dequant_out, cudaStream_t st);
 // Read and clear the one-pass kernel's device error word (after a sync).
 rq_status read_and_clear_quant_error();
 

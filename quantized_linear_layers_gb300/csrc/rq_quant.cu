@@ -224,6 +224,112 @@ int64_t fused_chunk(int64_t n) {
   return c < kFusedMinChunk ? kFusedMinChunk : c;
 }
 
+// ------------------------------------------------- two-pass, slot variant --
+//
+// For the activation cache: absmax_slots_kernel writes each CTA's partial
+// maximum to its own slot (no zeroing and no atomics needed), and
+// quant_slots_kernel reduces the slots at its start and then encodes the
+// tensor walking it backwards, so that the part of x the first pass read
+// last (still in L2, 129 MB) is read first.  Same arithmetic as
+// absmax_kernel + quant_kernel, hence the same bytes.
+
+constexpr int kSlotUnroll = 4;  // float4 loads in flight per thread
+
+template <bool VEC>
+__global__ void __launch_bounds__(kThreads)
+absmax_slots_kernel(const float* __restrict__ x, int64_t n, uint32_t* __restrict__ slots) {
+  pdl_wait();
+  pdl_trigger();
+  uint32_t m = 0;
+  const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  const int64_t nthreads = (int64_t)gridDim.x * kThreads;
+  int64_t done = 0;
+  if (VEC) {
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    const int64_t n4 = n >> 2;
+    int64_t i = tid;
+    for (; i + (kSlotUnroll - 1) * nthreads < n4; i += kSlotUnroll * nthreads) {
+      float4 v[kSlotUnroll];
+#pragma unroll
+      for (int u = 0; u < kSlotUnroll; ++u) v[u] = __ldg(x4 + i + u * nthreads);
+#pragma unroll
+      for (int u = 0; u < kSlotUnroll; ++u) m = max4(m, v[u]);
+    }
+    for (; i < n4; i += nthreads) m = max4(m, __ldg(x4 + i));
+    done = n4 << 2;
+  }
+  for (int64_t i = done + tid; i < n; i += nthreads) m = max(m, abs_bits_skip_nan(__ldg(x + i)));
+  __shared__ uint32_t warp_max[kThreads / 32];
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) warp_max[warp] = m;
+  __syncthreads();
+  if (warp == 0) {
+    m = lane < kThreads / 32 ? warp_max[lane] : 0u;
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if (lane == 0) slots[blockIdx.x] = m;
+  }
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(kThreads)
+quant_slots_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
+                   const uint32_t* __restrict__ slots, int nslots, uint8_t* __restrict__ out,
+                   uint32_t* __restrict__ absmax_out, float* __restrict__ dequant_out) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ uint32_t warp_max[kThreads / 32];
+  __shared__ uint32_t absmax_s;
+  uint32_t m = 0;
+  for (int i = threadIdx.x; i < nslots; i += kThreads) m = max(m, slots[i]);
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) warp_max[warp] = m;
+  __syncthreads();
+  if (warp == 0) {
+    m = lane < kThreads / 32 ? warp_max[lane] : 0u;
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if (lane == 0) absmax_s = m;
+  }
+  __syncthreads();
+  const uint32_t bits = absmax_s;
+  const float a = absmax_prime(bits);
+  const float s = __fdiv_rn(448.0f, a);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    if (absmax_out != nullptr) *absmax_out = bits;
+    if (dequant_out != nullptr) *dequant_out = __fdiv_rn(a, 448.0f);
+  }
+  const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  const int64_t nthreads = (int64_t)gridDim.x * kThreads;
+  int64_t done = 0;
+  if (VEC) {
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    uint32_t* o4 = reinterpret_cast<uint32_t*>(out);
+    const int64_t n4 = n >> 2;
+    // rounds of kSlotUnroll * nthreads float4s, the last (partial) round
+    // first, then backwards
+    const int64_t per_round = kSlotUnroll * nthreads;
+    for (int64_t base = ((n4 - 1) / per_round) * per_round; base >= 0 && n4 > 0;
+         base -= per_round) {
+      float4 v[kSlotUnroll];
+#pragma unroll
+      for (int u = 0; u < kSlotUnroll; ++u) {
+        const int64_t i = base + u * nthreads + tid;
+        if (i < n4) v[u] = __ldg(x4 + i);
+      }
+#pragma unroll
+      for (int u = 0; u < kSlotUnroll; ++u) {
+        const int64_t i = base + u * nthreads + tid;
+        if (i < n4) o4[i] = pack4(v[u], s);
+      }
+    }
+    done = n4 << 2;
+  }
+  for (int64_t i = done + tid; i < n; i += nthreads)
+    out[i] = (uint8_t)e4m3_scaled(__ldg(x + i), s);
+  for (int64_t i = n + tid; i < n_out; i += nthreads) out[i] = 0;
+}
+
 int grid_for(int64_t work_items) {
   const int64_t per_wave = (int64_t)device_sm_count() * 4;  // 4 CTAs / SM
   int64_t blocks = (work_items + kThreads - 1) / kThreads;
@@ -255,6 +361,27 @@ rq_status launch_quant(const float* x, int64_t n, int64_t n_out,
                          out, dequant_out);
   return launch_kernel(quant_kernel<false>, grid, kThreads, 0, st, x, n, n_out, absmax_bits, out,
                        dequant_out);
+}
+
+int act_quant_slots() { return device_sm_count() * 4; }
+
+rq_status launch_act_quant_two_pass(const float* x, int64_t n, int64_t n_out, uint8_t* out,
+                                    uint32_t* slots, uint32_t* absmax_out,
+                                    float* dequant_out, cudaStream_t st) {
+  const bool vec = (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(out) & 3) == 0;
+  const int nslots = act_quant_slots();
+  int g1 = grid_for(vec ? (n + 3) / 4 : n);
+  if (g1 > nslots) g1 = nslots;
+  rq_status s = vec ? launch_kernel(absmax_slots_kernel<true>, g1, kThreads, 0, st, x, n, slots)
+                    : launch_kernel(absmax_slots_kernel<false>, g1, kThreads, 0, st, x, n, slots);
+  if (s != RQ_OK) return s;
+  const int g2 = grid_for(vec ? (n_out + 3) / 4 : n_out);
+  if (vec)
+    return launch_kernel(quant_slots_kernel<true>, g2, kThreads, 0, st, x, n, n_out,
+                         (const uint32_t*)slots, g1, out, absmax_out, dequant_out);
+  return launch_kernel(quant_slots_kernel<false>, g2, kThreads, 0, st, x, n, n_out,
+                       (const uint32_t*)slots, g1, out, absmax_out, dequant_out);
 }
 
 bool act_quant_fused_fits(const float* x, int64_t n, const uint8_t* out) {
