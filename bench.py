@@ -437,7 +437,9 @@ def run_gpu(args, world, rank, local):
                               "peak": pk["hbm_gbs"], "unit": "GB/s",
                               "frac": gemv_gbs / world / pk["hbm_gbs"],
                               "note": "decode pass time incl. launch gaps"}},
-        "roofline": {"bound": "tensor", "kernel": "fp8_gemm_kernel (tcgen05 kind::f8f6f4)",
+        "roofline": {"bound": "tensor",
+                     "kernel": "FP8 GEMM: fp8_gemm_kernel + fp8_gemm_pair_kernel "
+                               "(tcgen05 kind::f8f6f4), all 196 launches of the pass",
                      "achieved": gemm_achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                      "frac": (gemm_achieved / fp8_peak) if gemm_achieved else None,
                      "peak_source": "2 x bf16_tflops_sustained of %s (fp8/bf16 nominal "

@@ -120,6 +120,12 @@ rq_status rq_quant_e4m3(const float *x, int64_t n, const uint32_t *absmax_bits,
  *   x: f32 [M x K], 16-byte aligned.  y: f32 [M x N] (written, not added to).
  * fp32 accumulation; agrees with the fp64 reference within
  * 1e-4 * sum_k |x[m,k] * w(n,k)| per element.
+ * Ordering: the kernel may start streaming w before the kernel launched just
+ * before it on the stream has finished (programmatic dependent launch); it
+ * reads x and writes y only after that kernel has completed.  So w must not
+ * be written by the immediately preceding kernel on the stream (a copy or
+ * any earlier kernel is fine).  The same holds for rq_q6k_gemv and for the
+ * GEMV route of rq_linear.
  * Errors: RQ_ERR_NULL, RQ_ERR_SHAPE (M not in 1..8, N < 1, K < 256,
  * K % 256 != 0, misaligned w or x). */
 rq_status rq_q4k_gemv(const void *w, const float *x, float *y, int M, int N,
