@@ -549,6 +549,201 @@ fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
 }
 
 // A block that waits on an mbarrier nothing completes (timeout test hook).
+// ------------------------------------------------------ split-K variant --
+//
+// For shapes with too few 128 x BN output tiles to fill the SMs (small N,
+// or a few hundred tokens and below): a cluster of S CTAs shares one output
+// tile, CTA rank s accumulating K blocks [s*kb/S, (s+1)*kb/S) in its own
+// TMEM.  The epilogue writes the partial tile into the CTA's stage buffers
+// (idle once the last MMA has completed); after a cluster barrier each CTA
+// sums 1/S of the tile's token columns over the S partials through
+// distributed shared memory, in rank order, scales and stores y.  One tile
+// per cluster (not persistent), no atomics, no zeroing of y.
+
+struct SplitArgs {
+  const float* x_deq;
+  const float* w_deq;
+  float* y;
+  int M, N, K;
+  int bn, tiles_m, splits;
+  uint32_t tmem_cols;
+  uint64_t wait_limit_ns;
+};
+
+// 16 bytes at a shared::cluster address (ordered after the cluster barrier
+// by the barrier's own memory clobber; no clobber here, so that several
+// loads are in flight before the first is used).
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+constexpr int kMaxSplits = 8;
+
+__global__ void __launch_bounds__(kThreads, 1)
+fp8_gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                       const __grid_constant__ CUtensorMap tmap_x, const SplitArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;                                  // kStages x 16 KB
+  uint8_t* sB = smem + kStages * kABytes;              // kStages x 32 KB
+  float* part = reinterpret_cast<float*>(smem);        // [bn][128] after the mainloop
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBBytesMax);
+  // bars: full[kStages], empty[kStages], tfull[1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 1);
+  pdl_wait();
+  pdl_trigger();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
+  const uint32_t tfull = smem_u32(bars + 2 * kStages);
+  const int S = args.splits;
+  const uint32_t rank = cluster_rank();
+  const int t = (int)blockIdx.x / S;
+  const int tn = t / args.tiles_m, tm = t - tn * args.tiles_m;
+  const int bn = args.bn;
+  const int kblocks = args.K / kBK;
+  const int kb0 = (int)((int64_t)rank * kblocks / S);
+  const int kb1 = (int)((int64_t)(rank + 1) * kblocks / S);
+  const uint32_t stage_tx = (uint32_t)(kABytes + bn * kBK);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    mbar_init(tfull, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_x)) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(args.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, last_parity = 0;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, args.wait_limit_ns, &g_rq_device_error))
+          break;
+        const uint32_t fb = full0 + 8 * stage;
+        mbar_arrive_expect_tx(fb, stage_tx);
+        tma_load_2d(smem_u32(sA + stage * kABytes), &tmap_w, fb, kb * kBK, tn * kBM);
+        tma_load_2d(smem_u32(sB + stage * kBBytesMax), &tmap_x, fb, kb * kBK, tm * bn);
+        issued_mask |= 1u << stage;
+        last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == kStages) { stage = 0; phase ^= 1; }
+      }
+      for (int s = 0; s < kStages; ++s)
+        if (issued_mask & (1u << s))
+          mbar_wait(full0 + 8 * s, (last_parity >> s) & 1u, args.wait_limit_ns,
+                    &g_rq_device_error);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      const uint32_t idesc = instr_desc(kBM, bn);
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(full0 + 8 * stage, phase, args.wait_limit_ns, &g_rq_device_error)) break;
+        tc_fence_after();
+        const uint32_t a_addr = smem_u32(sA + stage * kABytes);
+        const uint32_t b_addr = smem_u32(sB + stage * kBBytesMax);
+#pragma unroll
+        for (int kk = 0; kk < kBK / 32; ++kk)
+          mma_f8(tmem_base, smem_desc(a_addr + 32 * kk), smem_desc(b_addr + 32 * kk), idesc,
+                 (kb != kb0 || kk != 0) ? 1u : 0u);
+        mma_commit(empty0 + 8 * stage);
+        if (++stage == kStages) { stage = 0; phase ^= 1; }
+      }
+      // completes when every MMA above has: the partial is in TMEM and no
+      // MMA reads the stage buffers any more
+      mma_commit(tfull);
+    }
+  } else {
+    // ------------------------------------ epilogue: partial tile to smem --
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const bool ready = mbar_wait(tfull, 0, args.wait_limit_ns, &g_rq_device_error);
+    if (__all_sync(0xFFFFFFFFu, ready)) {
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16);
+      for (int c = 0; c < bn; c += 16) {
+        uint32_t v[16];
+        tmem_ld16(taddr + (uint32_t)c, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) part[(c + j) * kBM + row] = __uint_as_float(v[j]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // every partial of the cluster is in shared memory
+
+  const float scale_x = *args.x_deq, scale_w = *args.w_deq;
+  uint32_t base[kMaxSplits];  // the partial's address in each CTA of the cluster
+#pragma unroll
+  for (int q = 0; q < kMaxSplits; ++q) {
+    base[q] = 0;
+    if (q < S)
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                   : "=r"(base[q])
+                   : "r"(smem_u32(part)), "r"((uint32_t)q));
+  }
+  // this CTA's share of the tile: token columns [c0, c1), 4 rows per item
+  const int c0 = (int)((int64_t)rank * bn / S), c1 = (int)((int64_t)(rank + 1) * bn / S);
+  const int items = (c1 - c0) * (kBM / 4);
+  for (int i = threadIdx.x; i < items; i += blockDim.x) {
+    const int c = c0 + i / (kBM / 4), r = (i % (kBM / 4)) * 4;
+    const uint32_t off = (uint32_t)((c * kBM + r) * 4);
+    float4 v[kMaxSplits];
+#pragma unroll
+    for (int q = 0; q < kMaxSplits; ++q)
+      if (q < S) v[q] = ld_cluster_f4(base[q] + off);
+    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < kMaxSplits; ++q)
+      if (q < S) {  // rank order
+        sum.x += v[q].x;
+        sum.y += v[q].y;
+        sum.z += v[q].z;
+        sum.w += v[q].w;
+      }
+    const int n = tn * kBM + r, m = tm * bn + c;
+    if (m < args.M) {
+      float* yr = args.y + (size_t)m * args.N;
+      const float o[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (n + e < args.N) yr[n + e] = (o[e] * scale_x) * scale_w;
+    }
+  }
+  cluster_sync();  // no CTA leaves while a peer may still read its memory
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(args.tmem_cols)
+                 : "memory");
+  }
+}
+
 __global__ void wait_timeout_kernel(uint64_t limit_ns) {
   __shared__ uint64_t bar;
   if (threadIdx.x == 0) {
@@ -681,11 +876,92 @@ bool use_pair_kernel(int N, int bn_pair) {
 
 }  // namespace
 
+// K splits for the split-K kernel (1: not used).  Used when the widest
+// tiles leave more than half of the SMs idle; each split keeps at least four
+// K blocks.  RQ_GEMM_SPLIT forces a split count (1 = never), for tuning.
+static int choose_splits(int m_pad, int N, int K, int sms, int* bn_out) {
+  const int bn = m_pad < kMaxBN ? m_pad : kMaxBN;
+  *bn_out = bn;
+  const int tiles = ((N + kBM - 1) / kBM) * ((m_pad + bn - 1) / bn);
+  const int kblocks = K / kBK;
+  int S = 1;
+  const char* env = std::getenv("RQ_GEMM_SPLIT");
+  if (env != nullptr) {
+    S = std::atoi(env);
+  } else if (2 * tiles <= sms) {
+    S = sms / tiles;
+    if (S > kblocks / 4) S = kblocks / 4;
+    if (S > kMaxSplits) S = kMaxSplits;
+    if (S >= 2) {
+      // Both kernels stream their operands at a rate set by the rows they
+      // load per K block (128 weight rows + the tile's tokens); the split
+      // kernel adds the exchange of a 128 x BN partial tile, worth about
+      // 2400 row-blocks at BN = 256 (fitted to GB300 timings).
+      const int rbn = choose_bn(m_pad, N, sms);
+      const long rtiles = (long)((N + kBM - 1) / kBM) * ((m_pad + rbn - 1) / rbn);
+      const long rounds = (rtiles + sms - 1) / sms;
+      const long reg_cost = rounds * (kBM + rbn) * kblocks;
+      const long split_cost = (long)(kBM + bn) * ((kblocks + S - 1) / S) + 2400L * bn / 256;
+      if (split_cost >= reg_cost) S = 1;
+    }
+  }
+  if (S > kMaxSplits) S = kMaxSplits;
+  if (S > kblocks) S = kblocks;
+  return S < 2 ? 1 : S;
+}
+
+static rq_status launch_fp8_gemm_splitk(const uint8_t* x_fp8, const float* x_deq,
+                                 const uint8_t* w_fp8, const float* w_deq, float* y, int M,
+                                 int N, int K, int bn, int S, cudaStream_t st) {
+  const int m_pad = (M + 15) / 16 * 16;
+  CUtensorMap tw, tx;
+  if (!make_map(&tw, w_fp8, N, K, kBM) || !make_map(&tx, x_fp8, m_pad, K, bn))
+    return RQ_ERR_CUDA;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(fp8_gemm_splitk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess)
+      return RQ_ERR_CUDA;
+    attr_done = true;
+  }
+  SplitArgs a;
+  a.x_deq = x_deq;
+  a.w_deq = w_deq;
+  a.y = y;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.bn = bn;
+  a.tiles_m = (m_pad + bn - 1) / bn;
+  a.splits = S;
+  a.tmem_cols = tmem_columns(bn / 2);
+  a.wait_limit_ns = kWaitLimitNs;
+  const int tiles = ((N + kBM - 1) / kBM) * a.tiles_m;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(tiles * S);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
+  return cuda_status(cudaLaunchKernelEx(&cfg, fp8_gemm_splitk_kernel, tw, tx, a));
+}
+
 rq_status launch_fp8_gemm(const uint8_t* x_fp8, const float* x_deq,
                           const uint8_t* w_fp8, const float* w_deq, float* y,
                           int M, int N, int K, cudaStream_t st) {
   const int m_pad = (M + 15) / 16 * 16;
   const int sms = device_sm_count();
+  int bn_split = 0;
+  const int S = choose_splits(m_pad, N, K, sms, &bn_split);
+  if (S > 1) return launch_fp8_gemm_splitk(x_fp8, x_deq, w_fp8, w_deq, y, M, N, K, bn_split, S, st);
   const int bn_pair = sms >= 2 ? choose_bn_pair(m_pad, N, resident_pairs(sms)) : 0;
   const bool pair = sms >= 2 && use_pair_kernel(N, bn_pair);
   const int bn = pair ? bn_pair : choose_bn(m_pad, N, sms);

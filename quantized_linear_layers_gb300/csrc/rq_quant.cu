@@ -235,9 +235,29 @@ int64_t fused_chunk(int64_t n) {
 
 constexpr int kSlotUnroll = 4;  // float4 loads in flight per thread
 
+// L2 eviction priorities as cache policies for the loads below.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ float4 ldg_f4_policy(const float4* p, uint64_t pol) {
+  float4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
+
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads)
-absmax_slots_kernel(const float* __restrict__ x, int64_t n, uint32_t* __restrict__ slots) {
+absmax_slots_kernel(const float* __restrict__ x, int64_t n, uint32_t* __restrict__ slots,
+                    int64_t keep_from4) {
   pdl_wait();
   pdl_trigger();
   uint32_t m = 0;
@@ -245,13 +265,17 @@ absmax_slots_kernel(const float* __restrict__ x, int64_t n, uint32_t* __restrict
   const int64_t nthreads = (int64_t)gridDim.x * kThreads;
   int64_t done = 0;
   if (VEC) {
+    // float4s from keep_from4 on are read with L2 priority evict_last: the
+    // encoder reads them again first
+    const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
     const float4* x4 = reinterpret_cast<const float4*>(x);
     const int64_t n4 = n >> 2;
     int64_t i = tid;
     for (; i + (kSlotUnroll - 1) * nthreads < n4; i += kSlotUnroll * nthreads) {
       float4 v[kSlotUnroll];
+      const uint64_t pol = i >= keep_from4 ? keep : stream;
 #pragma unroll
-      for (int u = 0; u < kSlotUnroll; ++u) v[u] = __ldg(x4 + i + u * nthreads);
+      for (int u = 0; u < kSlotUnroll; ++u) v[u] = ldg_f4_policy(x4 + i + u * nthreads, pol);
 #pragma unroll
       for (int u = 0; u < kSlotUnroll; ++u) m = max4(m, v[u]);
     }
@@ -309,13 +333,14 @@ quant_slots_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
     // rounds of kSlotUnroll * nthreads float4s, the last (partial) round
     // first, then backwards
     const int64_t per_round = kSlotUnroll * nthreads;
+    const uint64_t last_use = l2_policy_evict_first();
     for (int64_t base = ((n4 - 1) / per_round) * per_round; base >= 0 && n4 > 0;
          base -= per_round) {
       float4 v[kSlotUnroll];
 #pragma unroll
       for (int u = 0; u < kSlotUnroll; ++u) {
         const int64_t i = base + u * nthreads + tid;
-        if (i < n4) v[u] = __ldg(x4 + i);
+        if (i < n4) v[u] = ldg_f4_policy(x4 + i, last_use);
       }
 #pragma unroll
       for (int u = 0; u < kSlotUnroll; ++u) {
@@ -373,8 +398,14 @@ rq_status launch_act_quant_two_pass(const float* x, int64_t n, int64_t n_out, ui
   const int nslots = act_quant_slots();
   int g1 = grid_for(vec ? (n + 3) / 4 : n);
   if (g1 > nslots) g1 = nslots;
-  rq_status s = vec ? launch_kernel(absmax_slots_kernel<true>, g1, kThreads, 0, st, x, n, slots)
-                    : launch_kernel(absmax_slots_kernel<false>, g1, kThreads, 0, st, x, n, slots);
+  // the last ~80 MB of x stay in L2 (129 MB) for the encoder's first reads
+  const int64_t n4 = n / 4;
+  int64_t keep_from4 = n4 - (int64_t)(80ll << 20) / 16;
+  if (keep_from4 < 0) keep_from4 = 0;
+  rq_status s = vec ? launch_kernel(absmax_slots_kernel<true>, g1, kThreads, 0, st, x, n, slots,
+                                    keep_from4)
+                    : launch_kernel(absmax_slots_kernel<false>, g1, kThreads, 0, st, x, n, slots,
+                                    keep_from4);
   if (s != RQ_OK) return s;
   const int g2 = grid_for(vec ? (n_out + 3) / 4 : n_out);
   if (vec)

@@ -163,3 +163,32 @@ def test_single_and_pair_kernels(rq, monkeypatch, pair, M, N, K, bn):
     Wb = random_e4m3(N + 5 * K, (N, K))
     got = gpu_gemm(rq, Xb, 0.01, Wb, 0.02, M)
     check_full(got, oracle.fp8_gemm(Xb, 0.01, Wb, 0.02))
+
+
+@pytest.mark.parametrize("S", ["2", "3", "5", "8"])
+@pytest.mark.parametrize("M,N,K", [(300, 200, 4096), (5, 384, 2048), (2048, 512, 3584)])
+def test_split_k_cluster_kernel(rq, monkeypatch, S, M, N, K):
+    """The split-K kernel (a cluster of S CTAs per output tile, partials
+    summed through distributed shared memory) agrees with the oracle for
+    every split count, ragged M and N included."""
+    monkeypatch.setenv("RQ_GEMM_SPLIT", S)
+    Xb = random_e4m3(M + N + int(S), (M, K))
+    Wb = random_e4m3(N + K + int(S), (N, K))
+    got = gpu_gemm(rq, Xb, 0.01, Wb, 0.02, M)
+    check_full(got, oracle.fp8_gemm(Xb, 0.01, Wb, 0.02))
+
+
+def test_split_k_integer_sums_are_exact(rq, monkeypatch):
+    """Integer-valued codes: every partial and the rank-ordered sum of the
+    partials are exact integers, so the split result is exact."""
+    monkeypatch.setenv("RQ_GEMM_SPLIT", "4")
+    vals = np.arange(-8, 9)
+    code = {v: int(oracle.e4m3_encode(np.float32(v))) for v in vals}
+    M, N, K = 64, 384, 2048
+    rng = np.random.default_rng(5)
+    xv = rng.integers(-8, 9, (M, K))
+    wv = rng.integers(-8, 9, (N, K))
+    Xb = np.vectorize(code.get)(xv).astype(np.uint8)
+    Wb = np.vectorize(code.get)(wv).astype(np.uint8)
+    got = gpu_gemm(rq, Xb, 1.0, Wb, 1.0, M)
+    assert np.array_equal(got, (xv @ wv.T).astype(np.float32))
