@@ -548,7 +548,6 @@ fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
   }
 }
 
-// A block that waits on an mbarrier nothing completes (timeout test hook).
 // ------------------------------------------------------ split-K variant --
 //
 // For shapes with too few 128 x BN output tiles to fill the SMs (small N,
@@ -744,6 +743,7 @@ fp8_gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmap_w,
   }
 }
 
+// A block that waits on an mbarrier nothing completes (timeout test hook).
 __global__ void wait_timeout_kernel(uint64_t limit_ns) {
   __shared__ uint64_t bar;
   if (threadIdx.x == 0) {
