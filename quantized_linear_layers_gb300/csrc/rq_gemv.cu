@@ -435,6 +435,7 @@ struct M1Args {
   uint32_t ring_bytes;  // stages * rows_per_stage * rowbytes
   uint64_t wait_limit_ns;
   int row_align;        // Q6_K: rows per 16-byte-aligned group of rows
+  int M;                // tokens (the multi-token Q6_K kernel)
 };
 
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
@@ -1041,6 +1042,218 @@ __global__ void __launch_bounds__(544, 1) q6k_gemv_m1_kernel(const M1Args a) {
   for (int i = threadIdx.x; i < rows; i += blockDim.x) a.y[r0 + i] = acc[i];
 }
 
+// ------------------------------------------------- Q6_K, 2..8 tokens ------
+//
+// The one-token Q6_K kernel's ring, teams and unit ownership, with the x
+// planes of all M tokens in shared memory instead of registers.  Per row a
+// lane unpacks its 64 quants once, then for each token reads that token's
+// planes for its unit (conflict-free 16-byte loads) and takes the dp4a
+// products; the M per-token sums of a row are reduced across the warp at
+// once with the 8-slot transpose pattern (slot = token).
+
+__global__ void __launch_bounds__(544, 1) q6k_gemv_mt_kernel(const M1Args a) {
+  extern __shared__ __align__(128) uint8_t smem_q6t[];
+  const int M = a.M;
+  const int nsb = a.K >> 8, U = nsb * 4, nsub16 = a.K >> 4;
+  const int rowbytes = nsb * kQ6KBytes;
+  const int rps = a.rows_per_stage;
+  const uint32_t stage_bytes = (uint32_t)(rps * rowbytes);
+  uint8_t* ring = smem_q6t;
+  uint8_t* planes = ring + a.ring_bytes;                                    // M * U * 208
+  float* xscale = reinterpret_cast<float*>(planes + (size_t)M * U * kPlaneStride);  // M * nsub16
+  float* xsum = xscale + M * nsub16;                                         // M * nsub16
+  uint64_t* bars = reinterpret_cast<uint64_t*>(xsum + M * nsub16);
+  float* acc = reinterpret_cast<float*>(bars + 2 * a.stages);               // rows * M
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + a.stages);
+
+  const int compute_warps = a.teams * a.team_warps;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ra = a.row_align;
+  const int ngrp = (a.N + ra - 1) / ra;
+  const int r0 = min(a.N, (int)((int64_t)blockIdx.x * ngrp / gridDim.x) * ra);
+  const int r1 = min(a.N, (int)((int64_t)(blockIdx.x + 1) * ngrp / gridDim.x) * ra);
+  const int rows = r1 - r0;
+  const int iters = (rows + rps - 1) / rps;
+  const int first = iters < a.stages ? iters : a.stages;
+
+  for (int i = threadIdx.x; i < rows * M; i += blockDim.x) acc[i] = 0.f;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, compute_warps);
+    }
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  uint32_t issued = 0, parity_bits = 0;
+  bool prod_ok = true;
+  auto produce = [&](int it) {
+    const int s = it % a.stages;
+    const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
+    if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, a.wait_limit_ns, &g_gemv_error)) {
+      prod_ok = false;
+      return;
+    }
+    const int nr = min(rps, rows - it * rps);
+    const uint32_t bytes = (uint32_t)(nr * rowbytes);
+    const uint32_t bulk = bytes & ~15u;
+    const uint8_t* src = a.W + (size_t)(r0 + it * rps) * rowbytes;
+    uint8_t* dst = ring + s * stage_bytes;
+    for (uint32_t b = bulk; b < bytes; b += 2)
+      *reinterpret_cast<unsigned short*>(dst + b) = (unsigned short)ldg_nc_u16(src + b);
+    mbar_arrive_expect_tx(full0 + 8 * s, bulk);
+    if (bulk != 0) bulk_g2s(smem_u32(dst), src, bulk, full0 + 8 * s);
+    issued |= 1u << s;
+    parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
+  };
+  const bool producer = warp == compute_warps && lane == 0;
+  if (producer)
+    for (int it = 0; it < first && prod_ok; ++it) produce(it);
+  pdl_wait();  // x and y only after the previous launch has completed
+  pdl_trigger();
+
+  // x planes of every token: two lanes per 16-value sub-block
+  if (warp < compute_warps) {
+    const int half = lane & 1;
+    for (int idx = warp * 16 + (lane >> 1); idx < M * nsub16; idx += compute_warps * 16) {
+      const int m = idx / nsub16, s16 = idx - m * nsub16;
+      const float4* px =
+          reinterpret_cast<const float4*>(a.x + (size_t)m * a.K + 16 * s16 + 8 * half);
+      const float4 va = __ldg(px), vb = __ldg(px + 1);
+      const float v[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+      float mx = 0.f, sm = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        mx = fmaxf(mx, fabsf(v[i]));
+        sm += v[i];
+      }
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+      sm += __shfl_xor_sync(0xFFFFFFFFu, sm, 1);
+      const float inv = mx > 0.f ? 127.0f / mx : 0.0f;
+      uint32_t b1[2] = {0, 0}, b2[2] = {0, 0}, b3[2] = {0, 0};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float t = fminf(fmaxf(v[i] * inv, -127.0f), 127.0f);
+        int i1, i2, i3;
+        const float f1 = round_magic(t, i1);
+        const float u2 = (t - f1) * 128.0f;
+        const float f2 = round_magic(u2, i2);
+        round_magic((u2 - f2) * 128.0f, i3);
+        const int sh8 = 8 * (i & 3);
+        b1[i >> 2] |= ((uint32_t)i1 & 0xFFu) << sh8;
+        b2[i >> 2] |= ((uint32_t)i2 & 0xFFu) << sh8;
+        b3[i >> 2] |= ((uint32_t)i3 & 0xFFu) << sh8;
+      }
+      const int t16 = s16 & 15;
+      const int u = 4 * (s16 >> 4) + 2 * (t16 >> 3) + (t16 & 1), qi = (t16 >> 1) & 3;
+      uint8_t* pl = planes + ((size_t)m * U + u) * kPlaneStride + qi * 16 + 8 * half;
+      *reinterpret_cast<uint2*>(pl) = make_uint2(b1[0], b1[1]);
+      *reinterpret_cast<uint2*>(pl + 64) = make_uint2(b2[0], b2[1]);
+      *reinterpret_cast<uint2*>(pl + 128) = make_uint2(b3[0], b3[1]);
+      if (half == 0) {
+        xscale[m * nsub16 + 4 * u + qi] = mx > 0.f ? mx / 127.0f : 1.0f;
+        xsum[m * nsub16 + 4 * u + qi] = sm;
+      }
+    }
+  }
+  __syncthreads();
+
+  if (producer) {
+    for (int it = first; it < iters && prod_ok; ++it) produce(it);
+    for (int s = 0; s < a.stages; ++s)
+      if (issued & (1u << s))
+        mbar_wait(full0 + 8 * s, (parity_bits >> s) & 1u, a.wait_limit_ns, &g_gemv_error);
+  } else if (warp < compute_warps) {
+    const int team = warp / a.team_warps, wt = warp - team * a.team_warps;
+    const int rpt = rps / a.teams;
+    const int u = wt * 32 + lane;
+    const bool active = u < U;
+    const int sb = u >> 2, hh = (u >> 1) & 1, lq = u & 1;
+    const int off = sb * kQ6KBytes;
+    bool ok = true;
+    for (int it = 0; it < iters && ok; ++it) {
+      const int s = it % a.stages;
+      const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * s, ph, a.wait_limit_ns, &g_gemv_error));
+      if (!ok) break;
+      const int nr = min(rps, rows - it * rps);
+      const uint8_t* stage = ring + s * stage_bytes;
+      for (int j = 0; j < rpt; ++j) {
+        const int rr = team * rpt + j;
+        float pa[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) pa[m] = 0.f;
+        if (active && rr < nr) {
+          const uint8_t* blk = stage + (size_t)rr * rowbytes + off;
+          uint32_t qa[4], qb[4], qh[4], sc[4];
+          lds16u(blk + 64 * hh + 16 * lq, qa);
+          lds16u(blk + 64 * hh + 32 + 16 * lq, qb);
+          lds16u(blk + 128 + 32 * hh + 16 * lq, qh);
+          lds16u(blk + 192, sc);
+          const float d = __half2float(
+              __ushort_as_half(*reinterpret_cast<const unsigned short*>(blk + 208)));
+          int q[4][4];  // quarter i, word w
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const uint32_t h = qh[w];
+            q[0][w] = (int)((qa[w] & 0x0F0F0F0Fu) | ((h << 4) & 0x30303030u));
+            q[1][w] = (int)((qb[w] & 0x0F0F0F0Fu) | ((h << 2) & 0x30303030u));
+            q[2][w] = (int)(((qa[w] >> 4) & 0x0F0F0F0Fu) | (h & 0x30303030u));
+            q[3][w] = (int)(((qb[w] >> 4) & 0x0F0F0F0Fu) | ((h >> 2) & 0x30303030u));
+          }
+          const uint32_t sw0 = hh ? sc[2] : sc[0], sw1 = hh ? sc[3] : sc[1];
+          float s8[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t word = i < 2 ? sw0 : sw1;
+            const int bsel = lq + 2 * (i & 1);
+            s8[i] = d * i2f_small((int)(word << (24 - 8 * bsel)) >> 24);
+          }
+#pragma unroll
+          for (int m = 0; m < 8; ++m) {
+            if (m < M) {
+              const uint8_t* pu = planes + ((size_t)m * U + u) * kPlaneStride;
+              const float* xsc = xscale + m * nsub16 + 4 * u;
+              const float* xsm = xsum + m * nsub16 + 4 * u;
+              float r = 0.f;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const uint4 v1 = lds128(pu + 16 * i), v2 = lds128(pu + 64 + 16 * i);
+                const uint4 v3 = lds128(pu + 128 + 16 * i);
+                const int p1[4] = {(int)v1.x, (int)v1.y, (int)v1.z, (int)v1.w};
+                const int p2[4] = {(int)v2.x, (int)v2.y, (int)v2.z, (int)v2.w};
+                const int p3[4] = {(int)v3.x, (int)v3.y, (int)v3.z, (int)v3.w};
+                Dot3 t = {0, 0, 0};
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                  t.a1 = __dp4a(q[i][w], p1[w], t.a1);
+                  t.a2 = __dp4a(q[i][w], p2[w], t.a2);
+                  t.a3 = __dp4a(q[i][w], p3[w], t.a3);
+                }
+                r = fmaf(s8[i], dot3_value(t, xsc[i]) - 32.0f * xsm[i], r);
+              }
+              pa[m] = r;
+            }
+          }
+        }
+        // slot (lane >> 2) & 7 of the warp's 8 token sums
+        const float tot = reduce8(pa, lane);
+        const int slot = (lane >> 2) & 7;
+        if ((lane & 3) == 0 && slot < M && rr < nr)
+          atomicAdd(&acc[(it * rps + rr) * M + slot], tot);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < rows * M; i += blockDim.x) {
+    const int row = i / M, m = i - row * M;
+    a.y[(size_t)m * a.N + r0 + row] = acc[i];
+  }
+}
+
 // ---------------------------------------------------------------- launch --
 
 // Resident CTAs per SM for a kernel at a dynamic shared-memory size; the
@@ -1132,6 +1345,7 @@ rq_status run_q4k_m1(const uint8_t* w, const float* x, float* y, int N, int K,
   a.N = N;
   a.K = K;
   a.row_align = 1;
+  a.M = 1;
   a.team_warps = (U + 31) / 32;
   a.teams = a.team_warps >= warps_per_cta ? 1 : warps_per_cta / a.team_warps;
   a.rows_per_stage = rpt * a.teams;
@@ -1171,7 +1385,7 @@ rq_status run_q4k_m1(const uint8_t* w, const float* x, float* y, int N, int K,
 
 // One-token Q6_K launch: as for Q4_K, plus the row alignment of the
 // bulk copies (rows are 16-byte aligned in groups of 16 / gcd(rowbytes, 16)).
-rq_status run_q6k_m1(const uint8_t* w, const float* x, float* y, int N, int K,
+rq_status run_q6k_m1(const uint8_t* w, const float* x, float* y, int M, int N, int K,
                      cudaStream_t st) {
   if ((reinterpret_cast<uintptr_t>(w) & 15) != 0) return RQ_ERR_SHAPE;
   auto knob = [](const char* name, int dflt, int lo, int hi) {
@@ -1197,6 +1411,7 @@ rq_status run_q6k_m1(const uint8_t* w, const float* x, float* y, int N, int K,
   a.N = N;
   a.K = K;
   a.row_align = ra;
+  a.M = M;
   a.team_warps = (U + 31) / 32;
   a.teams = a.team_warps >= warps_per_cta ? 1 : warps_per_cta / a.team_warps;
   a.rows_per_stage = rpt * a.teams;
@@ -1206,8 +1421,8 @@ rq_status run_q6k_m1(const uint8_t* w, const float* x, float* y, int N, int K,
   const int ngrp = (N + ra - 1) / ra;
   const int grid = ngrp < sms ? ngrp : sms;
   const int max_rows = (ngrp + grid - 1) / grid * ra;
-  const size_t fixed = (size_t)U * kPlaneStride + 8 * (size_t)nsub16 +
-                       16 * (size_t)max_stages + 4 * (size_t)max_rows;
+  const size_t fixed = (size_t)M * U * kPlaneStride + 8 * (size_t)M * nsub16 +
+                       16 * (size_t)max_stages + 4 * (size_t)M * max_rows;
   const size_t limit = 227 * 1024;
   if (fixed + 2 * (size_t)stage_bytes > limit) return RQ_ERR_SHAPE;
   size_t ring = (size_t)ring_kb * 1024;
@@ -1217,13 +1432,14 @@ rq_status run_q6k_m1(const uint8_t* w, const float* x, float* y, int N, int K,
   a.stages = stages;
   a.ring_bytes = (uint32_t)(stages * stage_bytes);
   a.wait_limit_ns = kWaitLimitNs;
-  const size_t smem = a.ring_bytes + (size_t)U * kPlaneStride + 8 * (size_t)nsub16 +
-                      16 * (size_t)stages + 4 * (size_t)max_rows;
+  const size_t smem = a.ring_bytes + (size_t)M * U * kPlaneStride + 8 * (size_t)M * nsub16 +
+                      16 * (size_t)stages + 4 * (size_t)M * max_rows;
   const int threads = (a.teams * a.team_warps + 1) * 32;
-  auto kern = rpt == 8 ? q6k_gemv_m1_kernel<8>
-                       : (rpt == 4 ? q6k_gemv_m1_kernel<4> : q6k_gemv_m1_kernel<2>);
-  static size_t smem_set[3] = {48 * 1024, 48 * 1024, 48 * 1024};
-  size_t& set = smem_set[rpt == 8 ? 2 : (rpt == 4 ? 1 : 0)];
+  auto kern = M > 1 ? q6k_gemv_mt_kernel
+                    : (rpt == 8 ? q6k_gemv_m1_kernel<8>
+                                : (rpt == 4 ? q6k_gemv_m1_kernel<4> : q6k_gemv_m1_kernel<2>));
+  static size_t smem_set[4] = {48 * 1024, 48 * 1024, 48 * 1024, 48 * 1024};
+  size_t& set = smem_set[M > 1 ? 3 : (rpt == 8 ? 2 : (rpt == 4 ? 1 : 0))];
   if (smem > set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
@@ -1285,10 +1501,20 @@ rq_status launch_q6k_gemv(const uint8_t* w, const float* x, float* y, int M,
       if (K <= 16 * 2048 && std::getenv("RQ_GEMV_Q6_GENERIC") == nullptr) {
         // RQ_ERR_SHAPE: the one-token kernel does not take this shape or
         // alignment and nothing was launched
-        const rq_status s1 = run_q6k_m1(w, x, y, N, K, st);
+        const rq_status s1 = run_q6k_m1(w, x, y, 1, N, K, st);
         if (s1 != RQ_ERR_SHAPE) return s1;
       }
       return run_q6k<1, 2>(w, x, y, N, K, st);
+    default:
+      break;
+  }
+  if (M >= 2 && M <= 8 && K <= 16 * 2048 && std::getenv("RQ_GEMV_Q6_GENERIC") == nullptr) {
+    // the multi-token variant (x planes of all tokens in shared memory);
+    // RQ_ERR_SHAPE: they do not fit and nothing was launched
+    const rq_status s2 = run_q6k_m1(w, x, y, M, N, K, st);
+    if (s2 != RQ_ERR_SHAPE) return s2;
+  }
+  switch (M) {
     case 2: return run_q6k<2, 2>(w, x, y, N, K, st);
     case 3: return run_q6k<3, 1>(w, x, y, N, K, st);
     case 4: return run_q6k<4, 1>(w, x, y, N, K, st);
