@@ -3,14 +3,16 @@
 One step = one pass of the whole hot path over the 28-layer decoder stack
 (hidden 3584, intermediate 18944, k/v 512; q,k,o,gate,up,down Q4_K, v Q6_K):
 
-  * decode pass: 28 x 7 rq_linear calls at M = 1 token (routed to the
-    Q4_K / Q6_K GEMV), replayed from a CUDA graph captured once;
-  * prefill pass: 28 x 7 rq_linear calls at M = 2048 tokens (routed to the
-    FP8 path: weight-cache hit, activation absmax + E4M3 on a miss, reuse
-    across q/k/v and gate/up, tcgen05 FP8 GEMM), launched eagerly.
+  * decode pass: the 28 x 7 linears at M = 1 token as 4 calls per layer
+    (rq_linear_group for q/k/v and gate/up, which share their input;
+    rq_linear for o and down), routed to the Q4_K / Q6_K GEMV, replayed
+    from a CUDA graph captured once;
+  * prefill pass: the same calls at M = 2048 tokens (FP8 path: weight-cache
+    hit, activation absmax + E4M3 once per shared input, one tcgen05 FP8
+    GEMM per call), launched eagerly.
 
 Headline `value`: FP8 prefill TFLOP/s at M = 2048 (2*M*N*K summed over the
-196 GEMMs / device time of the prefill pass, quantization included).  The
+28 x 7 linears / device time of the prefill pass, quantization included).  The
 GEMV HBM GB/s of the decode pass at M = 1 is reported in `gemv`.  `roofline`
 is for the dominant kernel (the FP8 GEMM): its algorithmic FLOPs / its
 device time from CUDA events around each GEMM launch, in K passes run right
@@ -46,6 +48,8 @@ M_DECODE = 1
 M_PREFILL = 2048
 # per layer: which activation feeds each linear
 SOURCE = {"q": "x", "k": "x", "v": "x", "o": "a", "gate": "h", "up": "h", "down": "g"}
+# linears that share an input are one rq_linear_group call
+GROUPS = (("q", "k", "v"), ("o",), ("gate", "up"), ("down",))
 ACT_K = {"x": synthetic.HIDDEN, "a": synthetic.HIDDEN, "h": synthetic.HIDDEN,
          "g": synthetic.INTERMEDIATE}
 
@@ -291,8 +295,28 @@ class Stack:
         ctx = self.ctx
         for layer in range(synthetic.N_LAYERS):
             a = acts[layer]
-            for name, qt, N, K, W in self.weights[layer]:
-                ctx.rq_linear(qt, W, a[SOURCE[name]], self.out[M][name], M, N, K, stream)
+            lin = {name: (qt, N, K, W) for name, qt, N, K, W in self.weights[layer]}
+            for grp in GROUPS:
+                x = a[SOURCE[grp[0]]]
+                K = lin[grp[0]][2]
+                if len(grp) == 1:
+                    qt, N, _, W = lin[grp[0]]
+                    ctx.rq_linear(qt, W, x, self.out[M][grp[0]], M, N, K, stream)
+                else:
+                    ctx.rq_linear_group([lin[n][0] for n in grp], [lin[n][3] for n in grp], x,
+                                        [self.out[M][n] for n in grp], [lin[n][1] for n in grp],
+                                        M, K, stream)
+
+    @staticmethod
+    def decode_launches_per_pass():
+        """GEMV launches of the one-token pass: a group's Q4_K members are
+        one launch, its other members one each."""
+        per_layer = 0
+        qtypes = {name: qt for name, qt, _, _ in synthetic.LAYER_LINEARS}
+        for grp in GROUPS:
+            q4 = sum(1 for n in grp if qtypes[n] == synthetic.Q4K)
+            per_layer += (1 if q4 >= 2 else q4) + (len(grp) - q4)
+        return per_layer * synthetic.N_LAYERS
 
 
 def run_gpu(args, world, rank, local):
@@ -317,7 +341,7 @@ def run_gpu(args, world, rank, local):
     if status != 0:
         raise RuntimeError("device status %d after warm-up" % status)
 
-    # capture the decode pass (launch-bound: 196 short kernels) in a graph
+    # capture the decode pass (launch-bound: 140 short kernels) in a graph
     graph = torch.cuda.CUDAGraph()
     cap_stream = torch.cuda.Stream(dev)
     cap_stream.wait_stream(stream)
@@ -371,7 +395,7 @@ def run_gpu(args, world, rank, local):
 
     # Roofline of the GEMM: the same K prefill passes again, right after the
     # timed steps (clocks still sampled), with CUDA events around each of
-    # the 196 GEMM launches on the launching stream.
+    # the GEMM launches (4 per layer) on the launching stream.
     st.ctx.rq_ctx_trace_kinds(["gemm"])
     traced_pre_ms = []
     for _ in range(args.steps):
@@ -423,8 +447,9 @@ def run_gpu(args, world, rank, local):
         "dtype": "e4m3 x e4m3 -> f32 (prefill); f32 x q4k/q6k -> f32 (decode)",
         "data": "synthetic",
         "config": {
-            "workload": "28-layer decoder linear stack: decode pass M=1 (GEMV, graph "
-                        "replay) + prefill pass M=2048 (FP8, eager)",
+            "workload": "28-layer decoder linear stack (7 linears per layer; q/k/v and "
+                        "gate/up as grouped calls): decode pass M=1 (GEMV, graph replay) "
+                        "+ prefill pass M=2048 (FP8, eager)",
             "hidden": synthetic.HIDDEN, "intermediate": synthetic.INTERMEDIATE,
             "kv_dim": synthetic.KV_DIM, "layers": synthetic.N_LAYERS,
             "M_decode": M_DECODE, "M_prefill": M_PREFILL, "gemm_threshold": 4,
@@ -439,20 +464,21 @@ def run_gpu(args, world, rank, local):
                               "note": "decode pass time incl. launch gaps"}},
         "roofline": {"bound": "tensor",
                      "kernel": "FP8 GEMM: fp8_gemm_kernel + fp8_gemm_pair_kernel "
-                               "(tcgen05 kind::f8f6f4), all 196 launches of the pass",
+                               "(tcgen05 kind::f8f6f4), all GEMM launches of the pass",
                      "achieved": gemm_achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                      "frac": (gemm_achieved / fp8_peak) if gemm_achieved else None,
                      "peak_source": "2 x bf16_tflops_sustained of %s (fp8/bf16 nominal "
                                     "ratio 2)" % pk["source"],
                      "traffic": traffic,
-                     "flops_per_launch_avg": flops / 196.0,
+                     "flops_per_launch_avg": flops / max(1, gemm_calls // K),
                      "avg_launch_ms": gemm_trace_ms / gemm_calls if gemm_calls else None,
                      "source": "CUDA events around each GEMM launch in K prefill passes run "
                                "right after the timed steps (%.3f ms per pass with the "
                                "events, %.3f ms without)" % (sum(traced_pre_ms) / K,
                                                              pre_s / K * 1e3)},
         "kernel_ms_per_prefill_pass": {k: v[1] for k, v in breakdown.items()},
-        "gpu_launches": K * (196 + sum(c for c, _ in breakdown.values()) // 2),
+        "gpu_launches": K * (Stack.decode_launches_per_pass() +
+                             sum(c for c, _ in breakdown.values()) // 2),
         "clocks": clocks, "e2e": e2e, "setup_s": setup_s, "wall_s": wall_s,
         "act_cache": st.ctx.stats(),
     }

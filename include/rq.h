@@ -217,6 +217,28 @@ rq_status rq_fp8_act_cache(rq_ctx *ctx, const float *x, int M, int K,
 rq_status rq_linear(rq_ctx *ctx, rq_qtype qtype, const void *w, const float *x,
                     float *y, int M, int N, int K, rq_stream_t stream);
 
+/* Linear layers that share one input ([gemm.rs], PMAT-084: Q, K and V read
+ * the same activation, and so do gate and up):
+ *   y_i = x . W_i^T   for i < count,  W_i: N_i rows of qtypes[i] super-blocks.
+ * Routes like rq_linear.  On the FP8 route the activation is quantized once
+ * (activation cache) and the group is one GEMM launch over the members'
+ * FP8 weights, cached once per group contiguously by rows (member i keeps
+ * its own per-tensor scale; its bytes equal rq_fp8_weight_cache's).  On
+ * the GEMV route a single token's Q4_K members are one launch (one pass of
+ * x), the others are launched one by one.  Results are those of count
+ * rq_linear calls within the same tolerances.
+ *   count: 1 .. RQ_MAX_GROUP.  qtypes, w, y, N: host arrays of count
+ *   entries (w[i], y[i] device pointers as for rq_linear).  All members
+ *   share x (f32 [M x K], 16-byte aligned), M and K.
+ * The group's FP8 weights are owned by ctx (keyed by the members' pointers,
+ * types and shapes) and freed by rq_ctx_destroy.
+ * Errors: RQ_ERR_NULL, RQ_ERR_QTYPE, RQ_ERR_SHAPE (count out of range, or
+ * as rq_linear), RQ_ERR_ALLOC, RQ_ERR_CUDA. */
+#define RQ_MAX_GROUP 4
+rq_status rq_linear_group(rq_ctx *ctx, int count, const rq_qtype *qtypes,
+                          const void *const *w, const float *x, float *const *y,
+                          const int *N, int M, int K, rq_stream_t stream);
+
 /* FP8 linear layer that allocates nothing.  The source pages have no
  * counterpart to this entry point.
  *

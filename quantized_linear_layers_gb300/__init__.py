@@ -58,6 +58,7 @@ _SIGS = {
     "rq_fp8_act_cache": ([_vp, _vp, _i32, _i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                           _vp], _i32),
     "rq_linear": ([_vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _vp], _i32),
+    "rq_linear_group": ([_vp, _i32, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp], _i32),
     "rq_fp8_linear_noalloc": ([_vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp], _i32),
     "rq_act_cache_invalidate": ([_vp], _i32),
     "rq_ctx_trace_begin": ([_vp, _i32], _i32),
@@ -208,6 +209,16 @@ class Context:
                                      ctypes.byref(xd), _stream(stream)),
                "rq_fp8_act_cache")
         return xq.value, xd.value
+
+    def rq_linear_group(self, qtypes, ws, x, ys, Ns, M, K, stream=None):
+        """Linears sharing x: ys[i] = x . ws[i]^T, one call."""
+        n = len(qtypes)
+        qt = (_i32 * n)(*qtypes)
+        wp = (_vp * n)(*[_ptr(w) for w in ws])
+        yp = (_vp * n)(*[_ptr(y) for y in ys])
+        nn = (_i32 * n)(*Ns)
+        _check(_lib.rq_linear_group(self._h, n, qt, wp, _ptr(x), yp, nn, M, K,
+                                    _stream(stream)), "rq_linear_group")
 
     def rq_linear(self, qtype, w, x, y, M, N, K, stream=None):
         _check(_lib.rq_linear(self._h, qtype, _ptr(w), _ptr(x), _ptr(y), M, N, K,

@@ -62,6 +62,15 @@ struct WeightEntry {
   size_t bytes = 0;
 };
 
+// FP8 weights of a group of linears that share an input, concatenated by
+// rows: member i's rows start at starts[i]; its dequant scale is deq[i].
+struct GroupEntry {
+  uint8_t* fp8 = nullptr;
+  float* deq = nullptr;
+  int starts[RQ_MAX_GROUP + 1] = {0};
+  size_t bytes = 0;
+};
+
 rq_status check_quant_shape(int qtype, int N, int K) {
   if (qtype != RQ_Q4K && qtype != RQ_Q6K) return RQ_ERR_QTYPE;
   if (N < 1 || K < 256 || K % 256 != 0) return RQ_ERR_SHAPE;
@@ -84,6 +93,7 @@ struct rq_ctx {
   std::vector<TraceSlot> trace;
   int threshold = 4;
   std::map<WeightKey, WeightEntry> weights;
+  std::map<std::vector<WeightKey>, GroupEntry> groups;
   int64_t weight_bytes = 0;
   uint8_t* act = nullptr;  // activation E4M3 scratch [M_pad x K]
   size_t act_cap = 0;
@@ -199,6 +209,7 @@ void rq_ctx_destroy(rq_ctx* ctx) {
     if (t.stop) cudaEventDestroy(t.stop);
   }
   for (auto& kv : ctx->weights) cudaFree(kv.second.fp8);
+  for (auto& kv : ctx->groups) cudaFree(kv.second.fp8);
   if (ctx->act) cudaFree(ctx->act);
   if (ctx->absmax) cudaFree(ctx->absmax);
   if (ctx->slots) cudaFree(ctx->slots);
@@ -222,7 +233,7 @@ rq_status rq_ctx_get_stats(const rq_ctx* ctx, int64_t* act_hits_host,
   if (ctx == nullptr) return RQ_ERR_NULL;
   if (act_hits_host) *act_hits_host = ctx->hits;
   if (act_misses_host) *act_misses_host = ctx->misses;
-  if (weights_host) *weights_host = (int64_t)ctx->weights.size();
+  if (weights_host) *weights_host = (int64_t)(ctx->weights.size() + ctx->groups.size());
   if (weight_bytes_host) *weight_bytes_host = ctx->weight_bytes;
   return RQ_OK;
 }
@@ -415,6 +426,103 @@ rq_status rq_linear(rq_ctx* ctx, rq_qtype qtype, const void* w, const float* x, 
   if (s != RQ_OK) return s;
   TraceScope ts(ctx, RQ_TRACE_GEMM, st);
   return launch_fp8_gemm(xq, xdeq, wq, wdeq, y, M, N, K, st);
+}
+
+rq_status rq_linear_group(rq_ctx* ctx, int count, const rq_qtype* qtypes, const void* const* w,
+                          const float* x, float* const* y, const int* N, int M, int K,
+                          rq_stream_t stream) {
+  if (ctx == nullptr || qtypes == nullptr || w == nullptr || x == nullptr || y == nullptr ||
+      N == nullptr)
+    return RQ_ERR_NULL;
+  if (count < 1 || count > RQ_MAX_GROUP || M < 1) return RQ_ERR_SHAPE;
+  for (int i = 0; i < count; ++i) {
+    if (w[i] == nullptr || y[i] == nullptr) return RQ_ERR_NULL;
+    rq_status s = check_quant_shape(qtypes[i], N[i], K);
+    if (s != RQ_OK) return s;
+    if (!aligned(w[i], qtypes[i] == RQ_Q4K ? 16 : 4) || !aligned(y[i], 4)) return RQ_ERR_SHAPE;
+  }
+  if (!aligned(x, 16)) return RQ_ERR_SHAPE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (count == 1) return rq_linear(ctx, qtypes[0], w[0], x, y[0], M, N[0], K, stream);
+
+  if (M < ctx->threshold) {
+    // GEMV route: one launch for a single token's Q4_K members
+    int starts[RQ_MAX_GROUP + 1];
+    const uint8_t* ws[RQ_MAX_GROUP];
+    float* ys[RQ_MAX_GROUP];
+    int n4 = 0;
+    starts[0] = 0;
+    if (M == 1) {
+      for (int i = 0; i < count; ++i)
+        if (qtypes[i] == RQ_Q4K) {
+          ws[n4] = static_cast<const uint8_t*>(w[i]);
+          ys[n4] = y[i];
+          starts[n4 + 1] = starts[n4] + N[i];
+          ++n4;
+        }
+    }
+    bool grouped = false;
+    if (n4 >= 2) {
+      TraceScope ts(ctx, RQ_TRACE_GEMV, st);
+      const rq_status s = launch_q4k_gemv_group(n4, starts, ws, ys, x, K, st);
+      if (s != RQ_OK && s != RQ_ERR_SHAPE) return s;
+      grouped = s == RQ_OK;
+    }
+    for (int i = 0; i < count; ++i) {
+      if (grouped && qtypes[i] == RQ_Q4K) continue;
+      const rq_status s = rq_linear(ctx, qtypes[i], w[i], x, y[i], M, N[i], K, stream);
+      if (s != RQ_OK) return s;
+    }
+    return RQ_OK;
+  }
+
+  // FP8 route: the group's weights, concatenated by rows, cached once
+  std::vector<WeightKey> key;
+  for (int i = 0; i < count; ++i) key.push_back(WeightKey{w[i], (int)qtypes[i], N[i], K});
+  auto it = ctx->groups.find(key);
+  if (it == ctx->groups.end()) {
+    GroupEntry e;
+    e.starts[0] = 0;
+    for (int i = 0; i < count; ++i) e.starts[i + 1] = e.starts[i] + N[i];
+    for (int i = count; i < RQ_MAX_GROUP; ++i) e.starts[i + 1] = e.starts[count];
+    const size_t body = (size_t)e.starts[count] * (size_t)K;
+    const size_t bytes = (body + 255) / 256 * 256 + 256;
+    void* p = nullptr;
+    if (cudaMalloc(&p, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      return RQ_ERR_ALLOC;
+    }
+    e.fp8 = static_cast<uint8_t*>(p);
+    e.deq = reinterpret_cast<float*>(e.fp8 + (body + 255) / 256 * 256);
+    e.bytes = bytes;
+    rq_status s = RQ_OK;
+    {
+      TraceScope ts(ctx, RQ_TRACE_WCACHE, st);
+      for (int i = 0; i < count && s == RQ_OK; ++i) {
+        const uint8_t* wb = static_cast<const uint8_t*>(w[i]);
+        s = cuda_status(cudaMemsetAsync(ctx->absmax, 0, sizeof(uint32_t), st));
+        if (s == RQ_OK) s = launch_dequant_absmax(qtypes[i], wb, N[i], K, ctx->absmax, st);
+        if (s == RQ_OK)
+          s = launch_dequant_encode(qtypes[i], wb, N[i], K, ctx->absmax,
+                                    e.fp8 + (size_t)e.starts[i] * K, e.deq + i, st);
+      }
+    }
+    if (s != RQ_OK) {
+      cudaFree(p);
+      return s;
+    }
+    it = ctx->groups.emplace(key, e).first;
+    ctx->weight_bytes += (int64_t)bytes;
+  }
+  const uint8_t* xq = nullptr;
+  const float* xdeq = nullptr;
+  rq_status s = rq_fp8_act_cache(ctx, x, M, K, &xq, &xdeq, stream);
+  if (s != RQ_OK) return s;
+  const float* deqs[RQ_MAX_GROUP];
+  for (int i = 0; i < count; ++i) deqs[i] = it->second.deq + i;
+  TraceScope ts(ctx, RQ_TRACE_GEMM, st);
+  return launch_fp8_gemm_group(xq, xdeq, it->second.fp8, count, it->second.starts, y, deqs, M,
+                               K, st);
 }
 
 rq_status rq_ctx_trace_begin(rq_ctx* ctx, int capacity) {

@@ -40,6 +40,7 @@ constexpr int kBM = 128;               // weight rows per tile (MMA M)
 constexpr int kBK = 128;               // K bytes per stage = one swizzle row
 constexpr int kStages = 4;
 constexpr int kMaxBN = 256;
+constexpr int kMaxSegs = RQ_MAX_GROUP;  // members of a grouped launch
 constexpr int kThreads = 192;
 constexpr int kABytes = kBM * kBK;           // 16 KB
 constexpr int kBBytesMax = kMaxBN * kBK;     // 32 KB
@@ -117,10 +118,27 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
 
 // ------------------------------------------------------------- kernel ----
 
+// Output rows [start[i], start[i+1]) of the (concatenated) weight belong to
+// member i of a group of linear layers that share the input: its own output
+// y[i] ([M x (start[i+1] - start[i])], row-major) and its own weight scale.
+// A single GEMM is one segment.
+struct OutSegs {
+  int count;
+  int start[kMaxSegs + 1];
+  float* y[kMaxSegs];
+  const float* w_deq[kMaxSegs];
+};
+
+// Segment of output row n (a short scan: at most kMaxSegs segments).
+__device__ __forceinline__ int seg_of(const OutSegs& o, int n) {
+  int i = 0;
+  while (i + 1 < o.count && n >= o.start[i + 1]) ++i;
+  return i;
+}
+
 struct GemmArgs {
   const float* x_deq;
-  const float* w_deq;
-  float* y;
+  OutSegs out;
   int M, N, K;
   int bn;          // tokens per tile: multiple of 16, <= 256
   int tiles_n;     // ceil(N / 128)
@@ -249,7 +267,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
   } else {
     // --------------------------------------------------------- epilogue --
     const int quad = warp & 3;  // TMEM lanes 32*quad .. +31
-    const float scale_x = *args.x_deq, scale_w = *args.w_deq;
+    const float scale_x = *args.x_deq;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
@@ -262,6 +280,10 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
       tc_fence_after();
       const int n = tn * kBM + quad * 32 + lane;
       const int m0 = tm * bn;
+      const int sg = seg_of(args.out, n);
+      const int ns = args.out.start[sg + 1] - args.out.start[sg];
+      float* yr = args.out.y[sg] + (n - args.out.start[sg]);
+      const float scale_w = n < args.N ? *args.out.w_deq[sg] : 0.f;
       const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * bn);
       for (int c = 0; c < bn; c += 16) {
         uint32_t v[16];
@@ -270,8 +292,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int m = m0 + c + j;
-            if (m < args.M)
-              args.y[(size_t)m * args.N + n] = (__uint_as_float(v[j]) * scale_x) * scale_w;
+            if (m < args.M) yr[(size_t)m * ns] = (__uint_as_float(v[j]) * scale_x) * scale_w;
           }
         }
       }
@@ -500,7 +521,7 @@ fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
   } else {
     // --------------------------------------------------- epilogue (both)
     const int quad = warp & 3;
-    const float scale_x = *args.x_deq, scale_w = *args.w_deq;
+    const float scale_x = *args.x_deq;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = pair; t < ntiles; t += npairs) {
@@ -511,6 +532,10 @@ fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
       tc_fence_after();
       const int n = tn * 256 + (int)rank * kBM + quad * 32 + lane;
       const int m0 = tm * bn;
+      const int sg = seg_of(args.out, n);
+      const int ns = args.out.start[sg + 1] - args.out.start[sg];
+      float* yr = args.out.y[sg] + (n - args.out.start[sg]);
+      const float scale_w = n < args.N ? *args.out.w_deq[sg] : 0.f;
       const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * bn);
       for (int c = 0; c < bn; c += 16) {
         uint32_t v[16];
@@ -519,8 +544,7 @@ fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int m = m0 + c + j;
-            if (m < args.M)
-              args.y[(size_t)m * args.N + n] = (__uint_as_float(v[j]) * scale_x) * scale_w;
+            if (m < args.M) yr[(size_t)m * ns] = (__uint_as_float(v[j]) * scale_x) * scale_w;
           }
         }
       }
@@ -561,8 +585,7 @@ fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
 
 struct SplitArgs {
   const float* x_deq;
-  const float* w_deq;
-  float* y;
+  OutSegs out;
   int M, N, K;
   int bn, tiles_m, splits;
   uint32_t tmem_cols;
@@ -696,7 +719,7 @@ fp8_gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmap_w,
   __syncthreads();
   cluster_sync();  // every partial of the cluster is in shared memory
 
-  const float scale_x = *args.x_deq, scale_w = *args.w_deq;
+  const float scale_x = *args.x_deq;
   uint32_t base[kMaxSplits];  // the partial's address in each CTA of the cluster
 #pragma unroll
   for (int q = 0; q < kMaxSplits; ++q) {
@@ -727,11 +750,17 @@ fp8_gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmap_w,
       }
     const int n = tn * kBM + r, m = tm * bn + c;
     if (m < args.M) {
-      float* yr = args.y + (size_t)m * args.N;
       const float o[4] = {sum.x, sum.y, sum.z, sum.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (n + e < args.N) yr[n + e] = (o[e] * scale_x) * scale_w;
+      for (int e = 0; e < 4; ++e) {
+        const int ne = n + e;
+        if (ne < args.N) {
+          const int sg = seg_of(args.out, ne);
+          const int ns = args.out.start[sg + 1] - args.out.start[sg];
+          args.out.y[sg][(size_t)m * ns + (ne - args.out.start[sg])] =
+              (o[e] * scale_x) * *args.out.w_deq[sg];
+        }
+      }
     }
   }
   cluster_sync();  // no CTA leaves while a peer may still read its memory
@@ -911,8 +940,8 @@ static int choose_splits(int m_pad, int N, int K, int sms, int* bn_out) {
 }
 
 static rq_status launch_fp8_gemm_splitk(const uint8_t* x_fp8, const float* x_deq,
-                                 const uint8_t* w_fp8, const float* w_deq, float* y, int M,
-                                 int N, int K, int bn, int S, cudaStream_t st) {
+                                        const uint8_t* w_fp8, const OutSegs& out, int M, int N,
+                                        int K, int bn, int S, cudaStream_t st) {
   const int m_pad = (M + 15) / 16 * 16;
   CUtensorMap tw, tx;
   if (!make_map(&tw, w_fp8, N, K, kBM) || !make_map(&tx, x_fp8, m_pad, K, bn))
@@ -926,8 +955,7 @@ static rq_status launch_fp8_gemm_splitk(const uint8_t* x_fp8, const float* x_deq
   }
   SplitArgs a;
   a.x_deq = x_deq;
-  a.w_deq = w_deq;
-  a.y = y;
+  a.out = out;
   a.M = M;
   a.N = N;
   a.K = K;
@@ -954,14 +982,29 @@ static rq_status launch_fp8_gemm_splitk(const uint8_t* x_fp8, const float* x_deq
   return cuda_status(cudaLaunchKernelEx(&cfg, fp8_gemm_splitk_kernel, tw, tx, a));
 }
 
-rq_status launch_fp8_gemm(const uint8_t* x_fp8, const float* x_deq,
-                          const uint8_t* w_fp8, const float* w_deq, float* y,
-                          int M, int N, int K, cudaStream_t st) {
+rq_status launch_fp8_gemm_group(const uint8_t* x_fp8, const float* x_deq,
+                                const uint8_t* w_fp8, int count, const int* starts,
+                                float* const* ys, const float* const* w_deqs, int M, int K,
+                                cudaStream_t st) {
+  if (count < 1 || count > kMaxSegs) return RQ_ERR_SHAPE;
+  OutSegs out;
+  out.count = count;
+  for (int i = 0; i <= count; ++i) out.start[i] = starts[i];
+  for (int i = 0; i < count; ++i) {
+    out.y[i] = ys[i];
+    out.w_deq[i] = w_deqs[i];
+  }
+  for (int i = count; i < kMaxSegs; ++i) {
+    out.start[i + 1] = starts[count];
+    out.y[i] = nullptr;
+    out.w_deq[i] = nullptr;
+  }
+  const int N = starts[count];
   const int m_pad = (M + 15) / 16 * 16;
   const int sms = device_sm_count();
   int bn_split = 0;
   const int S = choose_splits(m_pad, N, K, sms, &bn_split);
-  if (S > 1) return launch_fp8_gemm_splitk(x_fp8, x_deq, w_fp8, w_deq, y, M, N, K, bn_split, S, st);
+  if (S > 1) return launch_fp8_gemm_splitk(x_fp8, x_deq, w_fp8, out, M, N, K, bn_split, S, st);
   const int bn_pair = sms >= 2 ? choose_bn_pair(m_pad, N, resident_pairs(sms)) : 0;
   const bool pair = sms >= 2 && use_pair_kernel(N, bn_pair);
   const int bn = pair ? bn_pair : choose_bn(m_pad, N, sms);
@@ -970,8 +1013,7 @@ rq_status launch_fp8_gemm(const uint8_t* x_fp8, const float* x_deq,
     return RQ_ERR_CUDA;
   GemmArgs a;
   a.x_deq = x_deq;
-  a.w_deq = w_deq;
-  a.y = y;
+  a.out = out;
   a.M = M;
   a.N = N;
   a.K = K;
@@ -1004,6 +1046,13 @@ rq_status launch_fp8_gemm(const uint8_t* x_fp8, const float* x_deq,
   }
   const int grid = tiles < sms ? tiles : sms;
   return launch_kernel(fp8_gemm_kernel, grid, kThreads, kSmemBytes, st, tw, tx, a);
+}
+
+rq_status launch_fp8_gemm(const uint8_t* x_fp8, const float* x_deq,
+                          const uint8_t* w_fp8, const float* w_deq, float* y,
+                          int M, int N, int K, cudaStream_t st) {
+  const int starts[2] = {0, N};
+  return launch_fp8_gemm_group(x_fp8, x_deq, w_fp8, 1, starts, &y, &w_deq, M, K, st);
 }
 
 rq_status read_and_clear_device_error(cudaStream_t st) {

@@ -436,7 +436,20 @@ struct M1Args {
   uint64_t wait_limit_ns;
   int row_align;        // Q6_K: rows per 16-byte-aligned group of rows
   int M;                // tokens (the multi-token Q6_K kernel)
+  // One-token Q4_K: the rows are the concatenation of nseg weights that
+  // share x (rows [seg_start[i], seg_start[i+1]) are rows of seg_w[i] and
+  // go to seg_y[i]); a single weight is one segment.
+  int nseg;
+  int seg_start[RQ_MAX_GROUP + 1];
+  const uint8_t* seg_w[RQ_MAX_GROUP];
+  float* seg_y[RQ_MAX_GROUP];
 };
+
+__device__ __forceinline__ int m1_seg(const M1Args& a, int row) {
+  int i = 0;
+  while (i + 1 < a.nseg && row >= a.seg_start[i + 1]) ++i;
+  return i;
+}
 
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
   return *reinterpret_cast<const uint4*>(p);
@@ -632,8 +645,16 @@ __global__ void __launch_bounds__(544, 1) q4k_gemv_m1_kernel(const M1Args a) {
     const int nr = min(rps, rows - it * rps);
     const uint32_t bytes = (uint32_t)(nr * rowbytes);
     mbar_arrive_expect_tx(full0 + 8 * s, bytes);
-    bulk_g2s(smem_u32(ring + s * stage_bytes), a.W + (size_t)(r0 + it * rps) * rowbytes, bytes,
-             full0 + 8 * s);
+    // one copy per segment the stage's rows fall in
+    for (int v = r0 + it * rps, done = 0; done < nr;) {
+      const int sg = m1_seg(a, v);
+      const int take = min(nr - done, a.seg_start[sg + 1] - v);
+      bulk_g2s(smem_u32(ring + s * stage_bytes + (size_t)done * rowbytes),
+               a.seg_w[sg] + (size_t)(v - a.seg_start[sg]) * rowbytes,
+               (uint32_t)(take * rowbytes), full0 + 8 * s);
+      v += take;
+      done += take;
+    }
     issued |= 1u << s;
     parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
   };
@@ -777,7 +798,10 @@ __global__ void __launch_bounds__(544, 1) q4k_gemv_m1_kernel(const M1Args a) {
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < rows; i += blockDim.x) a.y[r0 + i] = acc[i];
+  for (int i = threadIdx.x; i < rows; i += blockDim.x) {
+    const int sg = m1_seg(a, r0 + i);
+    a.seg_y[sg][r0 + i - a.seg_start[sg]] = acc[i];
+  }
 }
 
 // ------------------------------------------------- Q6_K, one token ---------
@@ -1322,8 +1346,9 @@ rq_status run_q6k(const uint8_t* w, const float* x, float* y, int N, int K,
 // per CTA, one CTA per SM, shared memory split between the x planes and a
 // ring of weight stages.  The RQ_GEMV_* environment variables override the
 // launch shape for tuning runs.
-rq_status run_q4k_m1(const uint8_t* w, const float* x, float* y, int N, int K,
-                     cudaStream_t st) {
+rq_status run_q4k_m1(int nseg, const int* starts, const uint8_t* const* ws, float* const* ys,
+                     const float* x, int K, cudaStream_t st) {
+  const int N = starts[nseg];
   auto knob = [](const char* name, int dflt, int lo, int hi) {
     const char* e = std::getenv(name);
     const int v = e ? std::atoi(e) : dflt;
@@ -1339,11 +1364,17 @@ rq_status run_q4k_m1(const uint8_t* w, const float* x, float* y, int N, int K,
   const int max_stages = knob("RQ_GEMV_STAGES", 8, 2, 16);
   const int U = K / 64, nsub = K / 32;
   M1Args a;
-  a.W = w;
+  a.W = ws[0];
   a.x = x;
-  a.y = y;
+  a.y = ys[0];
   a.N = N;
   a.K = K;
+  a.nseg = nseg;
+  for (int i = 0; i <= RQ_MAX_GROUP; ++i) a.seg_start[i] = starts[i <= nseg ? i : nseg];
+  for (int i = 0; i < RQ_MAX_GROUP; ++i) {
+    a.seg_w[i] = i < nseg ? ws[i] : nullptr;
+    a.seg_y[i] = i < nseg ? ys[i] : nullptr;
+  }
   a.row_align = 1;
   a.M = 1;
   a.team_warps = (U + 31) / 32;
@@ -1412,6 +1443,13 @@ rq_status run_q6k_m1(const uint8_t* w, const float* x, float* y, int M, int N, i
   a.K = K;
   a.row_align = ra;
   a.M = M;
+  a.nseg = 1;
+  a.seg_start[0] = 0;
+  for (int i = 1; i <= RQ_MAX_GROUP; ++i) a.seg_start[i] = N;
+  for (int i = 0; i < RQ_MAX_GROUP; ++i) {
+    a.seg_w[i] = w;
+    a.seg_y[i] = y;
+  }
   a.team_warps = (U + 31) / 32;
   a.teams = a.team_warps >= warps_per_cta ? 1 : warps_per_cta / a.team_warps;
   a.rows_per_stage = rpt * a.teams;
@@ -1469,7 +1507,8 @@ rq_status launch_q4k_gemv(const uint8_t* w, const float* x, float* y, int M,
       if (K <= 16 * 2048) {
         // RQ_ERR_SHAPE here means the launch shape does not fit shared
         // memory; nothing was launched, so the generic kernel takes it
-        const rq_status s1 = run_q4k_m1(w, x, y, N, K, st);
+        const int starts[2] = {0, N};
+        const rq_status s1 = run_q4k_m1(1, starts, &w, &y, x, K, st);
         if (s1 != RQ_ERR_SHAPE) return s1;
       }
       return run_q4k<1, 2>(w, x, y, N, K, st);
@@ -1492,6 +1531,12 @@ rq_status launch_q4k_gemv(const uint8_t* w, const float* x, float* y, int M,
     case 8: return run_q4k<8, 1>(w, x, y, N, K, st);
     default: return RQ_ERR_SHAPE;
   }
+}
+
+rq_status launch_q4k_gemv_group(int count, const int* starts, const uint8_t* const* ws,
+                                float* const* ys, const float* x, int K, cudaStream_t st) {
+  if (count < 1 || count > RQ_MAX_GROUP || K > 16 * 2048) return RQ_ERR_SHAPE;
+  return run_q4k_m1(count, starts, ws, ys, x, K, st);
 }
 
 rq_status launch_q6k_gemv(const uint8_t* w, const float* x, float* y, int M,

@@ -72,6 +72,11 @@ rq_status launch_q4k_gemv(const uint8_t* w, const float* x, float* y, int M,
                           int N, int K, cudaStream_t st);
 rq_status launch_q6k_gemv(const uint8_t* w, const float* x, float* y, int M,
                           int N, int K, cudaStream_t st);
+// One-token Q4_K GEMV over the rows of several weights that share x
+// (member i: rows [starts[i], starts[i+1]) of ws[i] into ys[i]); one launch.
+// RQ_ERR_SHAPE (nothing launched) when the shape does not fit the kernel.
+rq_status launch_q4k_gemv_group(int count, const int* starts, const uint8_t* const* ws,
+                                float* const* ys, const float* x, int K, cudaStream_t st);
 // Read and clear the GEMV kernels' device error word (after a sync).
 rq_status read_and_clear_gemv_error();
 
@@ -96,6 +101,13 @@ rq_status launch_dequant_encode(int qtype, const uint8_t* w, int N, int K,
 rq_status launch_fp8_gemm(const uint8_t* x_fp8, const float* x_deq,
                           const uint8_t* w_fp8, const float* w_deq, float* y,
                           int M, int N, int K, cudaStream_t st);
+// One GEMM over weights concatenated by rows: member i owns rows
+// [starts[i], starts[i+1]), its scale w_deqs[i] and its output ys[i]
+// ([M x (starts[i+1] - starts[i])]).  count <= RQ_MAX_GROUP.
+rq_status launch_fp8_gemm_group(const uint8_t* x_fp8, const float* x_deq,
+                                const uint8_t* w_fp8, int count, const int* starts,
+                                float* const* ys, const float* const* w_deqs, int M, int K,
+                                cudaStream_t st);
 rq_status read_and_clear_device_error(cudaStream_t st);
 rq_status launch_debug_wait_timeout(int64_t limit_ns, cudaStream_t st);
 

@@ -80,6 +80,7 @@ def test_null_pointers_rejected_before_launch(rq):
     assert lib.rq_ctx_set_gemm_threshold(NULL, 4) == 1
     assert lib.rq_ctx_get_gemm_threshold(NULL) == -1
     assert lib.rq_ctx_trace_kinds(NULL, 1) == 1
+    assert lib.rq_linear_group(NULL, 2, fake, fake, fake, fake, fake, 1, 256, NULL) == 1
     lib.rq_ctx_destroy(NULL)  # no-op
 
 

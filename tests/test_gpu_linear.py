@@ -214,3 +214,60 @@ def test_trace_kinds_mask(rq):
     tr = ctx.rq_ctx_trace_end()
     assert tr["gemm"][0] == 1 and tr["quant"][0] == 1
     ctx.close()
+
+
+@pytest.mark.parametrize("M", [1, 2, 64, 300])
+def test_linear_group_matches_separate_linears(rq, M):
+    """rq_linear_group over members that share x (ragged N, both formats,
+    rows straddling 128-row tiles and GEMV stages) gives each member what
+    the oracle gives for it, on the GEMV (M < 4) and FP8 routes."""
+    K = 1024
+    members = [(Q4K, 200), (Q4K, 77), (Q6K, 130)]
+    Ws = [synthetic.weight_matrix(300 + i, qt, N, K) for i, (qt, N) in enumerate(members)]
+    Wd = [to_dev(W) for W in Ws]
+    x = synthetic.activation(310 + M, M, K, outlier_frac=1e-3)
+    xd = to_dev(x)
+    ys = [empty((M, N), torch.float32) for _, N in members]
+    ctx = rq.Context()
+    ctx.rq_linear_group([qt for qt, _ in members], Wd, xd, ys, [N for _, N in members], M, K)
+    torch.cuda.synchronize()
+    assert rq.rq_get_device_status() == 0
+    for (qt, N), W, y in zip(members, Ws, ys):
+        got = y.cpu().numpy()
+        if oracle.route_is_gemm(M, 4):
+            check_gemm(got, gemm_route_ref(qt, W, x, N, K))
+        else:
+            ref, absdot = oracle.gemv(qt, W, x, N, K)
+            assert gemv_ok(got, ref, absdot)[0]
+    st = ctx.stats()
+    if oracle.route_is_gemm(M, 4):
+        assert st["weights"] == 1 and st["act_misses"] == 1
+        # a second call hits both caches
+        ctx.rq_linear_group([qt for qt, _ in members], Wd, xd, ys, [N for _, N in members], M, K)
+        assert ctx.stats()["act_hits"] == 1 and ctx.stats()["weights"] == 1
+    ctx.close()
+
+
+def test_linear_group_decoder_shapes_one_token(rq):
+    """q + k (Q4_K, 3584 + 512 rows) and gate + up (2 x 18944) of the
+    decoder as one-token groups, sampled rows against the oracle."""
+    K = 3584
+    for seed, Ns in ((1, (3584, 512)), (2, (18944, 18944))):
+        Ws = [synthetic.q4k_matrix(400 + seed * 10 + i, N, K) for i, N in enumerate(Ns)]
+        x = synthetic.activation(420 + seed, 1, K)
+        ys = [empty((1, N), torch.float32) for N in Ns]
+        ctx = rq.Context()
+        ctx.rq_linear_group([Q4K] * len(Ns), [to_dev(W) for W in Ws], to_dev(x), ys, list(Ns), 1, K)
+        torch.cuda.synchronize()
+        for W, y, N in zip(Ws, ys, Ns):
+            rows = np.array([0, 1, N // 2, N - 2, N - 1])
+            ref, absdot = oracle.gemv_rows(Q4K, W, x, N, K, rows)
+            assert gemv_ok(y.cpu().numpy()[:, rows], ref, absdot)[0]
+        ctx.close()
+
+
+def test_linear_group_rejects_bad_counts(rq):
+    ctx = rq.Context()
+    with pytest.raises(rq.RqError):
+        ctx.rq_linear_group([], [], empty((1, 256), torch.float32), [], [], 1, 256)
+    ctx.close()
