@@ -720,6 +720,10 @@ fp8_gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmap_w,
   cluster_sync();  // every partial of the cluster is in shared memory
 
   const float scale_x = *args.x_deq;
+  float seg_scale[kMaxSegs];  // x scale times each member's weight scale
+#pragma unroll
+  for (int i = 0; i < kMaxSegs; ++i)
+    seg_scale[i] = i < args.out.count ? scale_x * *args.out.w_deq[i] : 0.f;
   uint32_t base[kMaxSplits];  // the partial's address in each CTA of the cluster
 #pragma unroll
   for (int q = 0; q < kMaxSplits; ++q) {
@@ -729,12 +733,30 @@ fp8_gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmap_w,
                    : "=r"(base[q])
                    : "r"(smem_u32(part)), "r"((uint32_t)q));
   }
-  // this CTA's share of the tile: token columns [c0, c1), 4 rows per item
+  // this CTA's share of the tile: token columns [c0, c1).  Thread t keeps
+  // rows 4*(t % 32) .. +3 (blockDim is a multiple of 32), so the members,
+  // output pointers and scales of its rows are found once.
   const int c0 = (int)((int64_t)rank * bn / S), c1 = (int)((int64_t)(rank + 1) * bn / S);
-  const int items = (c1 - c0) * (kBM / 4);
-  for (int i = threadIdx.x; i < items; i += blockDim.x) {
-    const int c = c0 + i / (kBM / 4), r = (i % (kBM / 4)) * 4;
-    const uint32_t off = (uint32_t)((c * kBM + r) * 4);
+  const int r = (threadIdx.x & 31) * 4;
+  const int n = tn * kBM + r;
+  float* yrow[4];
+  int ystride[4];
+  float rscale[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int ne = n + e;
+    const int sg = seg_of(args.out, ne < args.N ? ne : args.N - 1);
+    ystride[e] = args.out.start[sg + 1] - args.out.start[sg];
+    yrow[e] = ne < args.N ? args.out.y[sg] + (ne - args.out.start[sg]) : nullptr;
+    float sc = seg_scale[0];
+#pragma unroll
+    for (int i = 1; i < kMaxSegs; ++i)
+      if (sg == i) sc = seg_scale[i];
+    rscale[e] = sc;
+  }
+  const uint32_t roff = (uint32_t)(r * 4);
+  for (int c = c0 + (int)(threadIdx.x >> 5); c < c1; c += (int)(blockDim.x >> 5)) {
+    const uint32_t off = (uint32_t)(c * kBM * 4) + roff;
     float4 v[kMaxSplits];
 #pragma unroll
     for (int q = 0; q < kMaxSplits; ++q)
@@ -748,19 +770,12 @@ fp8_gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmap_w,
         sum.z += v[q].z;
         sum.w += v[q].w;
       }
-    const int n = tn * kBM + r, m = tm * bn + c;
+    const int m = tm * bn + c;
     if (m < args.M) {
       const float o[4] = {sum.x, sum.y, sum.z, sum.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int ne = n + e;
-        if (ne < args.N) {
-          const int sg = seg_of(args.out, ne);
-          const int ns = args.out.start[sg + 1] - args.out.start[sg];
-          args.out.y[sg][(size_t)m * ns + (ne - args.out.start[sg])] =
-              (o[e] * scale_x) * *args.out.w_deq[sg];
-        }
-      }
+      for (int e = 0; e < 4; ++e)
+        if (yrow[e] != nullptr) yrow[e][(size_t)m * ystride[e]] = o[e] * rscale[e];
     }
   }
   cluster_sync();  // no CTA leaves while a peer may still read its memory
@@ -823,11 +838,13 @@ uint32_t tmem_columns(int bn) {
 }
 
 // Tokens per tile.  Every CTA is resident at once (one per SM), so a launch
-// takes ceil(tiles / SMs) rounds and a round costs about the time of one tile,
-// which grows with BN plus a fixed part (pipeline fill, epilogue tail).
-// Candidates are multiples of 16 up to 256; the cheapest estimate wins, ties
-// going to the wider tile.  RQ_GEMM_BN (a multiple of 16, 16..256) forces a
-// width, for tuning measurements.
+// takes ceil(tiles / SMs) rounds.  The kernels stream their operands from L2
+// at a rate that caps them (about 100 GB/s per SM on GB300), so a round
+// costs about the operand rows a CTA loads per K block: 128 weight rows plus
+// the tile's BN tokens (BN/2 in the pair kernel).  Candidates are multiples
+// of 16 up to 256; the cheapest estimate wins, ties going to the wider tile.
+// RQ_GEMM_BN (a multiple of 16, 16..256) forces a width, for tuning
+// measurements.
 int choose_bn(int m_pad, int N, int sms) {
   const char* env = std::getenv("RQ_GEMM_BN");
   const int v = env ? std::atoi(env) : 0;
@@ -840,13 +857,23 @@ int choose_bn(int m_pad, int N, int sms) {
   for (int bn = kMaxBN; bn >= 64; bn -= 16) {
     const long tiles = tiles_n * ((m_pad + bn - 1) / bn);
     const long rounds = (tiles + sms - 1) / sms;
-    const long cost = rounds * (bn + 48);
+    const long cost = rounds * (kBM + bn);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best = bn;
     }
   }
   return best;
+}
+
+// Cost estimates of the two kernels in the units above.
+int pair_cost(int m_pad, int N, int pairs, int bn) {
+  const long tiles = (long)((N + 255) / 256) * ((m_pad + bn - 1) / bn);
+  return (int)(((tiles + pairs - 1) / pairs) * (kBM + bn / 2));
+}
+int single_cost(int m_pad, int N, int sms, int bn) {
+  const long tiles = (long)((N + kBM - 1) / kBM) * ((m_pad + bn - 1) / bn);
+  return (int)(((tiles + sms - 1) / sms) * (kBM + bn));
 }
 
 // Tokens per tile for the pair kernel: multiples of 32 (each CTA holds half),
@@ -863,7 +890,7 @@ int choose_bn_pair(int m_pad, int N, int pairs) {
   for (int bn = kMaxBN; bn >= 64; bn -= 32) {
     const long tiles = tiles_n * ((m_pad + bn - 1) / bn);
     const long rounds = (tiles + pairs - 1) / pairs;
-    const long cost = rounds * (bn + 48);
+    const long cost = rounds * (kBM + bn / 2);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best = bn;
@@ -892,15 +919,15 @@ int resident_pairs(int sms) {
   return cached;
 }
 
-// The pair kernel wins when its 256-row tiles come in wide token tiles
-// (BN >= 224); where N is small the 256-row tiles quantize badly and the
-// one-CTA kernel with narrower tiles is faster (measured on GB300).
-// RQ_GEMM_PAIR=0 / 1 forces the one-CTA / pair kernel.
-bool use_pair_kernel(int N, int bn_pair) {
+// The pair kernel halves the token rows each CTA loads, so it wins unless
+// its 256-row tiles leave more of the last round idle; the two are compared
+// with the same cost estimate.  RQ_GEMM_PAIR=0 / 1 forces the one-CTA / pair
+// kernel.
+bool use_pair_kernel(int m_pad, int N, int sms, int pairs, int bn_pair, int bn_single) {
   if (N <= kBM) return false;
   const char* env = std::getenv("RQ_GEMM_PAIR");
   if (env != nullptr) return std::atoi(env) != 0;
-  return bn_pair >= 224;
+  return pair_cost(m_pad, N, pairs, bn_pair) < single_cost(m_pad, N, sms, bn_single);
 }
 
 }  // namespace
@@ -1005,9 +1032,11 @@ rq_status launch_fp8_gemm_group(const uint8_t* x_fp8, const float* x_deq,
   int bn_split = 0;
   const int S = choose_splits(m_pad, N, K, sms, &bn_split);
   if (S > 1) return launch_fp8_gemm_splitk(x_fp8, x_deq, w_fp8, out, M, N, K, bn_split, S, st);
-  const int bn_pair = sms >= 2 ? choose_bn_pair(m_pad, N, resident_pairs(sms)) : 0;
-  const bool pair = sms >= 2 && use_pair_kernel(N, bn_pair);
-  const int bn = pair ? bn_pair : choose_bn(m_pad, N, sms);
+  const int pairs = sms >= 2 ? resident_pairs(sms) : 0;
+  const int bn_pair = sms >= 2 ? choose_bn_pair(m_pad, N, pairs) : 0;
+  const int bn_single = choose_bn(m_pad, N, sms);
+  const bool pair = sms >= 2 && use_pair_kernel(m_pad, N, sms, pairs, bn_pair, bn_single);
+  const int bn = pair ? bn_pair : bn_single;
   CUtensorMap tw, tx;
   if (!make_map(&tw, w_fp8, N, K, kBM) || !make_map(&tx, x_fp8, m_pad, K, pair ? bn / 2 : bn))
     return RQ_ERR_CUDA;
