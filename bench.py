@@ -310,12 +310,18 @@ class Stack:
     @staticmethod
     def decode_launches_per_pass():
         """GEMV launches of the one-token pass: a group's Q4_K members are
-        one launch, its other members one each."""
+        one launch, joined by its Q6_K member when it has exactly one (unless
+        RQ_GEMV_NO_DUAL is set); its other members one each."""
         per_layer = 0
         qtypes = {name: qt for name, qt, _, _ in synthetic.LAYER_LINEARS}
+        dual = os.environ.get("RQ_GEMV_NO_DUAL") is None
         for grp in GROUPS:
             q4 = sum(1 for n in grp if qtypes[n] == synthetic.Q4K)
-            per_layer += (1 if q4 >= 2 else q4) + (len(grp) - q4)
+            q6 = len(grp) - q4
+            if len(grp) >= 2 and dual and q4 >= 1 and q6 == 1:
+                per_layer += 1
+            else:
+                per_layer += (1 if q4 >= 2 else q4) + q6
         return per_layer * synthetic.N_LAYERS
 
 
@@ -341,7 +347,7 @@ def run_gpu(args, world, rank, local):
     if status != 0:
         raise RuntimeError("device status %d after warm-up" % status)
 
-    # capture the decode pass (launch-bound: 140 short kernels) in a graph
+    # capture the decode pass (launch-bound: short kernels) in a graph
     graph = torch.cuda.CUDAGraph()
     cap_stream = torch.cuda.Stream(dev)
     cap_stream.wait_stream(stream)

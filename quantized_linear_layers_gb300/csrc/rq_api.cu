@@ -461,8 +461,23 @@ rq_status rq_linear_group(rq_ctx* ctx, int count, const rq_qtype* qtypes, const 
           ++n4;
         }
     }
-    bool grouped = false;
-    if (n4 >= 2) {
+    // ... and, with exactly one Q6_K member, that member in the same launch
+    int i6 = -1, n6 = 0;
+    for (int i = 0; i < count; ++i)
+      if (qtypes[i] == RQ_Q6K) {
+        i6 = i;
+        ++n6;
+      }
+    bool grouped = false, dual = false;
+    if (M == 1 && n4 >= 1 && n6 == 1 && std::getenv("RQ_GEMV_NO_DUAL") == nullptr) {
+      TraceScope ts(ctx, RQ_TRACE_GEMV, st);
+      const rq_status s = launch_gemv_m1_dual(n4, starts, ws, ys,
+                                              static_cast<const uint8_t*>(w[i6]), y[i6], N[i6],
+                                              x, K, st);
+      if (s != RQ_OK && s != RQ_ERR_SHAPE) return s;
+      grouped = dual = s == RQ_OK;
+    }
+    if (!grouped && n4 >= 2) {
       TraceScope ts(ctx, RQ_TRACE_GEMV, st);
       const rq_status s = launch_q4k_gemv_group(n4, starts, ws, ys, x, K, st);
       if (s != RQ_OK && s != RQ_ERR_SHAPE) return s;
@@ -470,6 +485,7 @@ rq_status rq_linear_group(rq_ctx* ctx, int count, const rq_qtype* qtypes, const 
     }
     for (int i = 0; i < count; ++i) {
       if (grouped && qtypes[i] == RQ_Q4K) continue;
+      if (dual && i == i6) continue;
       const rq_status s = rq_linear(ctx, qtypes[i], w[i], x, y[i], M, N[i], K, stream);
       if (s != RQ_OK) return s;
     }

@@ -597,7 +597,7 @@ __device__ __forceinline__ float reduce8(float (&v)[8], int lane) {
 constexpr int kPlaneStride = 208;
 
 template <int RPT>
-__global__ void __launch_bounds__(544, 1) q4k_gemv_m1_kernel(const M1Args a) {
+__device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, const int nblk) {
   static_assert(RPT == 2 || RPT == 4 || RPT == 8, "rows per team per stage");
   constexpr int SPB = 8 / RPT;  // stages per 8-row reduction batch
   extern __shared__ __align__(128) uint8_t smem_m1[];
@@ -616,8 +616,8 @@ __global__ void __launch_bounds__(544, 1) q4k_gemv_m1_kernel(const M1Args a) {
 
   const int compute_warps = a.teams * a.team_warps;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r0 = (int)((int64_t)blockIdx.x * a.N / gridDim.x);
-  const int r1 = (int)((int64_t)(blockIdx.x + 1) * a.N / gridDim.x);
+  const int r0 = (int)((int64_t)bid * a.N / nblk);
+  const int r1 = (int)((int64_t)(bid + 1) * a.N / nblk);
   const int rows = r1 - r0;
   const int iters = (rows + rps - 1) / rps;
   const int first = iters < a.stages ? iters : a.stages;
@@ -804,6 +804,11 @@ __global__ void __launch_bounds__(544, 1) q4k_gemv_m1_kernel(const M1Args a) {
   }
 }
 
+template <int RPT>
+__global__ void __launch_bounds__(544, 1) q4k_gemv_m1_kernel(const M1Args a) {
+  q4k_m1_body<RPT>(a, blockIdx.x, gridDim.x);
+}
+
 // ------------------------------------------------- Q6_K, one token ---------
 //
 // Same structure as the one-token Q4_K kernel (bulk-copy ring of row stages,
@@ -888,7 +893,7 @@ __device__ __forceinline__ float q6_unit_dot(const uint8_t* blk, int hh, int lq,
 // (0..2), quarter i (0..3), byte j (0..15) at p*64 + i*16 + j.
 
 template <int RPT>
-__global__ void __launch_bounds__(544, 1) q6k_gemv_m1_kernel(const M1Args a) {
+__device__ __forceinline__ void q6k_m1_body(const M1Args& a, const int bid, const int nblk) {
   static_assert(RPT == 2 || RPT == 4 || RPT == 8, "rows per team per stage");
   constexpr int SPB = 8 / RPT;
   extern __shared__ __align__(128) uint8_t smem_q6[];
@@ -908,8 +913,8 @@ __global__ void __launch_bounds__(544, 1) q6k_gemv_m1_kernel(const M1Args a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ra = a.row_align;
   const int ngrp = (a.N + ra - 1) / ra;
-  const int r0 = min(a.N, (int)((int64_t)blockIdx.x * ngrp / gridDim.x) * ra);
-  const int r1 = min(a.N, (int)((int64_t)(blockIdx.x + 1) * ngrp / gridDim.x) * ra);
+  const int r0 = min(a.N, (int)((int64_t)bid * ngrp / nblk) * ra);
+  const int r1 = min(a.N, (int)((int64_t)(bid + 1) * ngrp / nblk) * ra);
   const int rows = r1 - r0;
   const int iters = (rows + rps - 1) / rps;
   const int first = iters < a.stages ? iters : a.stages;
@@ -1064,6 +1069,24 @@ __global__ void __launch_bounds__(544, 1) q6k_gemv_m1_kernel(const M1Args a) {
   }
   __syncthreads();
   for (int i = threadIdx.x; i < rows; i += blockDim.x) a.y[r0 + i] = acc[i];
+}
+
+template <int RPT>
+__global__ void __launch_bounds__(544, 1) q6k_gemv_m1_kernel(const M1Args a) {
+  q6k_m1_body<RPT>(a, blockIdx.x, gridDim.x);
+}
+
+// One launch for a token's Q4_K members and one Q6_K member that share x
+// (the decoder's q, k and v): CTAs [0, g4) run the Q4_K body over its
+// members' rows, the others the Q6_K body, each with its own arguments and
+// its own layout of the (shared) dynamic shared memory.
+template <int R4, int R6>
+__global__ void __launch_bounds__(544, 1) gemv_m1_dual_kernel(const M1Args a4, const M1Args a6,
+                                                              int g4) {
+  if ((int)blockIdx.x < g4)
+    q4k_m1_body<R4>(a4, blockIdx.x, g4);
+  else
+    q6k_m1_body<R6>(a6, blockIdx.x - g4, gridDim.x - g4);
 }
 
 // ------------------------------------------------- Q6_K, 2..8 tokens ------
@@ -1342,28 +1365,53 @@ rq_status run_q6k(const uint8_t* w, const float* x, float* y, int N, int K,
   return launch_status();
 }
 
-// One-token Q4_K launch: team_warps = ceil(K/64/32), up to 16 compute warps
-// per CTA, one CTA per SM, shared memory split between the x planes and a
-// ring of weight stages.  The RQ_GEMV_* environment variables override the
-// launch shape for tuning runs.
-rq_status run_q4k_m1(int nseg, const int* starts, const uint8_t* const* ws, float* const* ys,
-                     const float* x, int K, cudaStream_t st) {
-  const int N = starts[nseg];
-  auto knob = [](const char* name, int dflt, int lo, int hi) {
-    const char* e = std::getenv(name);
-    const int v = e ? std::atoi(e) : dflt;
-    return v < lo ? lo : (v > hi ? hi : v);
-  };
-  // defaults from launch-shape sweeps on GB300: few rows per SM favour
-  // smaller teams and stages; long rows favour a shallower ring
-  const bool few_rows = N <= 8 * device_sm_count();
-  const int warps_per_cta = knob("RQ_GEMV_WARPS", few_rows ? 8 : 16, 1, 16);
-  int rpt = knob("RQ_GEMV_RPT", few_rows ? 2 : 4, 2, 8);
-  rpt = rpt >= 8 ? 8 : (rpt >= 4 ? 4 : 2);
-  const int ring_kb = knob("RQ_GEMV_RING_KB", K >= 8192 ? 100 : 150, 16, 200);
-  const int max_stages = knob("RQ_GEMV_STAGES", 8, 2, 16);
-  const int U = K / 64, nsub = K / 32;
+// Launch shape of a one-token kernel: its arguments, dynamic shared memory,
+// threads, grid and rows per team per stage.
+struct M1Plan {
   M1Args a;
+  size_t smem;
+  int threads;
+  int grid;
+  int rpt;
+};
+
+int m1_knob(const char* name, int dflt, int lo, int hi) {
+  const char* e = std::getenv(name);
+  const int v = e ? std::atoi(e) : dflt;
+  return v < lo ? lo : (v > hi ? hi : v);
+}
+
+template <typename Kern>
+rq_status m1_allow_smem(Kern kern, size_t smem, size_t& set) {
+  if (smem <= set) return RQ_OK;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return RQ_ERR_CUDA;
+  set = smem;
+  return RQ_OK;
+}
+
+// One-token Q4_K shape: team_warps = ceil(K/64/32), up to 16 compute warps
+// per CTA, one CTA per SM (or `grid` CTAs when positive), shared memory split
+// between the x planes and a ring of weight stages.  The RQ_GEMV_*
+// environment variables override the shape for tuning runs.
+rq_status plan_q4k_m1(int nseg, const int* starts, const uint8_t* const* ws, float* const* ys,
+                      const float* x, int K, int grid, M1Plan* p) {
+  const int N = starts[nseg];
+  const int sms = device_sm_count();
+  if (grid <= 0) grid = N < sms ? N : sms;
+  if (grid > N) grid = N;
+  const int max_rows = (N + grid - 1) / grid;
+  // defaults from launch-shape sweeps on GB300: few rows per CTA favour
+  // smaller teams and stages; long rows favour a shallower ring
+  const bool few_rows = max_rows <= 8;
+  const int warps_per_cta = m1_knob("RQ_GEMV_WARPS", few_rows ? 8 : 16, 1, 16);
+  int rpt = m1_knob("RQ_GEMV_RPT", few_rows ? 2 : 4, 2, 8);
+  rpt = rpt >= 8 ? 8 : (rpt >= 4 ? 4 : 2);
+  const int ring_kb = m1_knob("RQ_GEMV_RING_KB", K >= 8192 ? 100 : 150, 16, 200);
+  const int max_stages = m1_knob("RQ_GEMV_STAGES", 8, 2, 16);
+  const int U = K / 64, nsub = K / 32;
+  M1Args& a = p->a;
   a.W = ws[0];
   a.x = x;
   a.y = ys[0];
@@ -1382,9 +1430,6 @@ rq_status run_q4k_m1(int nseg, const int* starts, const uint8_t* const* ws, floa
   a.rows_per_stage = rpt * a.teams;
   const int rowbytes = (K / kQK) * kQ4KBytes;
   const int stage_bytes = a.rows_per_stage * rowbytes;
-  const int sms = device_sm_count();
-  const int grid = N < sms ? N : sms;
-  const int max_rows = (N + grid - 1) / grid;
   const size_t nsub2 = (size_t)((nsub + 1) & ~1);
   const size_t fixed = (size_t)U * kPlaneStride + 8 * nsub2 +
                        16 * (size_t)max_stages + 4 * (size_t)max_rows;
@@ -1397,45 +1442,50 @@ rq_status run_q4k_m1(int nseg, const int* starts, const uint8_t* const* ws, floa
   a.stages = stages;
   a.ring_bytes = (uint32_t)(stages * stage_bytes);
   a.wait_limit_ns = kWaitLimitNs;
-  const size_t smem = a.ring_bytes + (size_t)U * kPlaneStride + 8 * nsub2 +
-                      16 * (size_t)stages +
-                      4 * (size_t)max_rows;
-  const int threads = (a.teams * a.team_warps + 1) * 32;
-  auto kern = rpt == 8 ? q4k_gemv_m1_kernel<8>
-                       : (rpt == 4 ? q4k_gemv_m1_kernel<4> : q4k_gemv_m1_kernel<2>);
-  static size_t smem_set[3] = {48 * 1024, 48 * 1024, 48 * 1024};
-  size_t& set = smem_set[rpt == 8 ? 2 : (rpt == 4 ? 1 : 0)];
-  if (smem > set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-      return RQ_ERR_CUDA;
-    set = smem;
-  }
-  return launch_kernel(kern, grid, threads, smem, st, a);
+  p->smem = a.ring_bytes + (size_t)U * kPlaneStride + 8 * nsub2 + 16 * (size_t)stages +
+            4 * (size_t)max_rows;
+  p->threads = (a.teams * a.team_warps + 1) * 32;
+  p->grid = grid;
+  p->rpt = rpt;
+  return RQ_OK;
 }
 
-// One-token Q6_K launch: as for Q4_K, plus the row alignment of the
-// bulk copies (rows are 16-byte aligned in groups of 16 / gcd(rowbytes, 16)).
-rq_status run_q6k_m1(const uint8_t* w, const float* x, float* y, int M, int N, int K,
-                     cudaStream_t st) {
+rq_status run_q4k_m1(int nseg, const int* starts, const uint8_t* const* ws, float* const* ys,
+                     const float* x, int K, cudaStream_t st) {
+  M1Plan p;
+  const rq_status s = plan_q4k_m1(nseg, starts, ws, ys, x, K, 0, &p);
+  if (s != RQ_OK) return s;
+  auto kern = p.rpt == 8 ? q4k_gemv_m1_kernel<8>
+                         : (p.rpt == 4 ? q4k_gemv_m1_kernel<4> : q4k_gemv_m1_kernel<2>);
+  static size_t smem_set[3] = {48 * 1024, 48 * 1024, 48 * 1024};
+  const rq_status sa = m1_allow_smem(kern, p.smem, smem_set[p.rpt == 8 ? 2 : (p.rpt == 4 ? 1 : 0)]);
+  if (sa != RQ_OK) return sa;
+  return launch_kernel(kern, p.grid, p.threads, p.smem, st, p.a);
+}
+
+// One-token (M = 1) or multi-token (M = 2..8) Q6_K shape: as for Q4_K, plus
+// the row alignment of the bulk copies (rows are 16-byte aligned in groups of
+// 16 / gcd(rowbytes, 16)); `grid` CTAs when positive.
+rq_status plan_q6k_m1(const uint8_t* w, const float* x, float* y, int M, int N, int K, int grid,
+                      M1Plan* p) {
   if ((reinterpret_cast<uintptr_t>(w) & 15) != 0) return RQ_ERR_SHAPE;
-  auto knob = [](const char* name, int dflt, int lo, int hi) {
-    const char* e = std::getenv(name);
-    const int v = e ? std::atoi(e) : dflt;
-    return v < lo ? lo : (v > hi ? hi : v);
-  };
-  const bool few_rows = N <= 8 * device_sm_count();
-  const int warps_per_cta = knob("RQ_GEMV_WARPS", few_rows ? 8 : 16, 1, 16);
-  int rpt = knob("RQ_GEMV_RPT", few_rows ? 2 : 4, 2, 8);
-  rpt = rpt >= 8 ? 8 : (rpt >= 4 ? 4 : 2);
-  const int ring_kb = knob("RQ_GEMV_RING_KB", 150, 16, 200);
-  const int max_stages = knob("RQ_GEMV_STAGES", 8, 2, 16);
   const int nsb = K / kQK, U = nsb * 4, nsub16 = K / 16;
   const int rowbytes = nsb * kQ6KBytes;
   int g = 1;
   while (g < 16 && rowbytes % (2 * g) == 0) g *= 2;  // gcd(rowbytes, 16)
   const int ra = 16 / g;
-  M1Args a;
+  const int sms = device_sm_count();
+  const int ngrp = (N + ra - 1) / ra;
+  if (grid <= 0) grid = ngrp < sms ? ngrp : sms;
+  if (grid > ngrp) grid = ngrp;
+  const int max_rows = (ngrp + grid - 1) / grid * ra;
+  const bool few_rows = max_rows <= 8;
+  const int warps_per_cta = m1_knob("RQ_GEMV_WARPS", few_rows ? 8 : 16, 1, 16);
+  int rpt = m1_knob("RQ_GEMV_RPT", few_rows ? 2 : 4, 2, 8);
+  rpt = rpt >= 8 ? 8 : (rpt >= 4 ? 4 : 2);
+  const int ring_kb = m1_knob("RQ_GEMV_RING_KB", 150, 16, 200);
+  const int max_stages = m1_knob("RQ_GEMV_STAGES", 8, 2, 16);
+  M1Args& a = p->a;
   a.W = w;
   a.x = x;
   a.y = y;
@@ -1455,10 +1505,6 @@ rq_status run_q6k_m1(const uint8_t* w, const float* x, float* y, int M, int N, i
   a.rows_per_stage = rpt * a.teams;
   if (a.rows_per_stage % ra != 0) return RQ_ERR_SHAPE;
   const int stage_bytes = a.rows_per_stage * rowbytes;
-  const int sms = device_sm_count();
-  const int ngrp = (N + ra - 1) / ra;
-  const int grid = ngrp < sms ? ngrp : sms;
-  const int max_rows = (ngrp + grid - 1) / grid * ra;
   const size_t fixed = (size_t)M * U * kPlaneStride + 8 * (size_t)M * nsub16 +
                        16 * (size_t)max_stages + 4 * (size_t)M * max_rows;
   const size_t limit = 227 * 1024;
@@ -1470,21 +1516,27 @@ rq_status run_q6k_m1(const uint8_t* w, const float* x, float* y, int M, int N, i
   a.stages = stages;
   a.ring_bytes = (uint32_t)(stages * stage_bytes);
   a.wait_limit_ns = kWaitLimitNs;
-  const size_t smem = a.ring_bytes + (size_t)M * U * kPlaneStride + 8 * (size_t)M * nsub16 +
-                      16 * (size_t)stages + 4 * (size_t)M * max_rows;
-  const int threads = (a.teams * a.team_warps + 1) * 32;
+  p->smem = a.ring_bytes + (size_t)M * U * kPlaneStride + 8 * (size_t)M * nsub16 +
+            16 * (size_t)stages + 4 * (size_t)M * max_rows;
+  p->threads = (a.teams * a.team_warps + 1) * 32;
+  p->grid = grid;
+  p->rpt = rpt;
+  return RQ_OK;
+}
+
+rq_status run_q6k_m1(const uint8_t* w, const float* x, float* y, int M, int N, int K,
+                     cudaStream_t st) {
+  M1Plan p;
+  const rq_status s = plan_q6k_m1(w, x, y, M, N, K, 0, &p);
+  if (s != RQ_OK) return s;
   auto kern = M > 1 ? q6k_gemv_mt_kernel
-                    : (rpt == 8 ? q6k_gemv_m1_kernel<8>
-                                : (rpt == 4 ? q6k_gemv_m1_kernel<4> : q6k_gemv_m1_kernel<2>));
+                    : (p.rpt == 8 ? q6k_gemv_m1_kernel<8>
+                                  : (p.rpt == 4 ? q6k_gemv_m1_kernel<4> : q6k_gemv_m1_kernel<2>));
   static size_t smem_set[4] = {48 * 1024, 48 * 1024, 48 * 1024, 48 * 1024};
-  size_t& set = smem_set[M > 1 ? 3 : (rpt == 8 ? 2 : (rpt == 4 ? 1 : 0))];
-  if (smem > set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-      return RQ_ERR_CUDA;
-    set = smem;
-  }
-  return launch_kernel(kern, grid, threads, smem, st, a);
+  const rq_status sa =
+      m1_allow_smem(kern, p.smem, smem_set[M > 1 ? 3 : (p.rpt == 8 ? 2 : (p.rpt == 4 ? 1 : 0))]);
+  if (sa != RQ_OK) return sa;
+  return launch_kernel(kern, p.grid, p.threads, p.smem, st, p.a);
 }
 
 }  // namespace
@@ -1537,6 +1589,32 @@ rq_status launch_q4k_gemv_group(int count, const int* starts, const uint8_t* con
                                 float* const* ys, const float* x, int K, cudaStream_t st) {
   if (count < 1 || count > RQ_MAX_GROUP || K > 16 * 2048) return RQ_ERR_SHAPE;
   return run_q4k_m1(count, starts, ws, ys, x, K, st);
+}
+
+rq_status launch_gemv_m1_dual(int count, const int* starts, const uint8_t* const* ws,
+                              float* const* ys, const uint8_t* w6, float* y6, int n6,
+                              const float* x, int K, cudaStream_t st) {
+  if (count < 1 || count > RQ_MAX_GROUP || K > 16 * 2048 || n6 < 1) return RQ_ERR_SHAPE;
+  const int sms = device_sm_count();
+  // CTAs in proportion to the work: a Q6_K weight costs about 1.5 times the
+  // instructions of a Q4_K weight in these kernels
+  const double c4 = (double)starts[count], c6 = 1.5 * n6;
+  int g6 = (int)(sms * c6 / (c4 + c6) + 0.5);
+  g6 = m1_knob("RQ_GEMV_DUAL_G6", g6, 1, sms - 1);
+  M1Plan p4, p6;
+  rq_status s = plan_q4k_m1(count, starts, ws, ys, x, K, sms - g6, &p4);
+  if (s != RQ_OK) return s;
+  s = plan_q6k_m1(w6, x, y6, 1, n6, K, g6, &p6);
+  if (s != RQ_OK) return s;
+  if ((p4.rpt != 2 && p4.rpt != 4) || (p6.rpt != 2 && p6.rpt != 4)) return RQ_ERR_SHAPE;
+  auto kern = p4.rpt == 4 ? (p6.rpt == 4 ? gemv_m1_dual_kernel<4, 4> : gemv_m1_dual_kernel<4, 2>)
+                          : (p6.rpt == 4 ? gemv_m1_dual_kernel<2, 4> : gemv_m1_dual_kernel<2, 2>);
+  const size_t smem = p4.smem > p6.smem ? p4.smem : p6.smem;
+  const int threads = p4.threads > p6.threads ? p4.threads : p6.threads;
+  static size_t smem_set[4] = {48 * 1024, 48 * 1024, 48 * 1024, 48 * 1024};
+  s = m1_allow_smem(kern, smem, smem_set[(p4.rpt == 4 ? 2 : 0) + (p6.rpt == 4 ? 1 : 0)]);
+  if (s != RQ_OK) return s;
+  return launch_kernel(kern, p4.grid + p6.grid, threads, smem, st, p4.a, p6.a, p4.grid);
 }
 
 rq_status launch_q6k_gemv(const uint8_t* w, const float* x, float* y, int M,

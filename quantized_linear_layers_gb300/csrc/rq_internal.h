@@ -77,6 +77,12 @@ rq_status launch_q6k_gemv(const uint8_t* w, const float* x, float* y, int M,
 // RQ_ERR_SHAPE (nothing launched) when the shape does not fit the kernel.
 rq_status launch_q4k_gemv_group(int count, const int* starts, const uint8_t* const* ws,
                                 float* const* ys, const float* x, int K, cudaStream_t st);
+// One launch for the one-token GEMVs of Q4_K members (as above) and one Q6_K
+// weight w6 ([n6 x K], into y6) that share x.  RQ_ERR_SHAPE (nothing
+// launched) when the shapes do not fit the kernel.
+rq_status launch_gemv_m1_dual(int count, const int* starts, const uint8_t* const* ws,
+                              float* const* ys, const uint8_t* w6, float* y6, int n6,
+                              const float* x, int K, cudaStream_t st);
 // Read and clear the GEMV kernels' device error word (after a sync).
 rq_status read_and_clear_gemv_error();
 

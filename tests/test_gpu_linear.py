@@ -266,6 +266,52 @@ def test_linear_group_decoder_shapes_one_token(rq):
         ctx.close()
 
 
+@pytest.mark.parametrize("g6", [None, "1", "40", "151"])
+def test_linear_group_mixed_formats_one_launch(rq, monkeypatch, g6):
+    """One token through q + k (Q4_K) and v (Q6_K) of the decoder: one
+    GEMV launch whose CTAs split between the two formats (the split forced
+    to its extremes too); every member's sampled rows against the oracle."""
+    if g6 is not None:
+        monkeypatch.setenv("RQ_GEMV_DUAL_G6", g6)
+    K = 3584
+    members = [(Q4K, 3584), (Q4K, 512), (Q6K, 512)]
+    Ws = [synthetic.weight_matrix(430 + i, qt, N, K) for i, (qt, N) in enumerate(members)]
+    x = synthetic.activation(440, 1, K)
+    ys = [empty((1, N), torch.float32) for _, N in members]
+    ctx = rq.Context()
+    ctx.rq_ctx_trace_kinds(list(ctx.TRACE_KINDS))
+    ctx.rq_ctx_trace_begin(16)
+    ctx.rq_linear_group([qt for qt, _ in members], [to_dev(W) for W in Ws], to_dev(x), ys,
+                        [N for _, N in members], 1, K)
+    tr = ctx.rq_ctx_trace_end()
+    assert tr["gemv"][0] == 1
+    assert rq.rq_get_device_status() == 0
+    for (qt, N), W, y in zip(members, Ws, ys):
+        rows = np.array([0, 1, 2, 3, N // 2 - 1, N // 2, N - 3, N - 2, N - 1])
+        ref, absdot = oracle.gemv_rows(qt, W, x, N, K, rows)
+        assert gemv_ok(y.cpu().numpy()[:, rows], ref, absdot)[0], (qt, N)
+    ctx.close()
+
+
+@pytest.mark.parametrize("K,N4,N6", [(256, 3, 5), (768, 1, 1), (1280, 333, 97)])
+def test_linear_group_mixed_formats_ragged(rq, K, N4, N6):
+    """A Q4_K and a Q6_K member sharing one token: row counts below and
+    off the Q6_K row alignment, every row against the oracle."""
+    members = [(Q6K, N6), (Q4K, N4)]
+    Ws = [synthetic.weight_matrix(450 + i, qt, N, K) for i, (qt, N) in enumerate(members)]
+    x = synthetic.activation(460, 1, K, outlier_frac=1e-3)
+    ys = [empty((1, N), torch.float32) for _, N in members]
+    ctx = rq.Context()
+    ctx.rq_linear_group([qt for qt, _ in members], [to_dev(W) for W in Ws], to_dev(x), ys,
+                        [N for _, N in members], 1, K)
+    torch.cuda.synchronize()
+    assert rq.rq_get_device_status() == 0
+    for (qt, N), W, y in zip(members, Ws, ys):
+        ref, absdot = oracle.gemv(qt, W, x, N, K)
+        assert gemv_ok(y.cpu().numpy(), ref, absdot)[0], (qt, N)
+    ctx.close()
+
+
 def test_linear_group_rejects_bad_counts(rq):
     ctx = rq.Context()
     with pytest.raises(rq.RqError):
