@@ -579,12 +579,41 @@ def graph_time_ms(torch, dev, calls, reps=2):
     return e0.elapsed_time(e1) / (reps * len(calls))
 
 
+def pass_graph_ms(torch, dev, st, M, reps=5):
+    """One pass of the stack at M tokens captured in a CUDA graph (after an
+    eager pass that fills the weight caches); mean replay time in ms."""
+    stream = torch.cuda.current_stream(dev)
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        st.ctx.rq_act_cache_invalidate()
+        st.run_pass(M, cap)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=cap):
+            st.ctx.rq_act_cache_invalidate()
+            st.run_pass(M, cap)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
 def run_sweep(args):
     """The configurations other than the headline line, one JSON line each:
     the decode GEMV over the decoder's shapes at M = 1, 4, 8 (graph replay,
     weights rotated through >= 512 MB so that every launch reads HBM); the
-    FP8 GEMM at M = 512 on the four prefill shapes; the 28-layer prefill
-    stack through rq_linear at M = 16 .. 4096 (eager, untraced)."""
+    FP8 GEMM at M = 512 on the four prefill shapes; the stack at 2 .. 16
+    tokens through the GEMV route and through the FP8 route (graph replay),
+    which locates the crossover of the two; the 28-layer prefill stack at
+    M = 16 .. 4096 (eager, untraced)."""
     import torch
     import quantized_linear_layers_gb300 as rq
     dev = torch.device("cuda", 0)
@@ -595,8 +624,9 @@ def run_sweep(args):
     def out(d):
         print(json.dumps(d), flush=True)
 
+    parts = set(args.sweep_parts.split(","))
     # decode GEMV sweep
-    for name, qt, N, K in [("q,o", synthetic.Q4K, 3584, 3584), ("k", synthetic.Q4K, 512, 3584),
+    for name, qt, N, K in [] if "gemv" not in parts else [("q,o", synthetic.Q4K, 3584, 3584), ("k", synthetic.Q4K, 512, 3584),
                            ("v", synthetic.Q6K, 512, 3584), ("gate,up", synthetic.Q4K, 18944, 3584),
                            ("down", synthetic.Q4K, 3584, 18944)]:
         W0 = torch.from_numpy(synthetic.weight_matrix(11, qt, N, K)).to(dev)
@@ -615,7 +645,8 @@ def run_sweep(args):
     # FP8 GEMM at M = 512
     ctx = rq.Context()
     M = 512
-    for N, K in [(3584, 3584), (512, 3584), (18944, 3584), (3584, 18944)]:
+    for N, K in [] if "gemm" not in parts else [(3584, 3584), (512, 3584), (18944, 3584),
+                                                (3584, 18944)]:
         W = torch.from_numpy(synthetic.q4k_matrix(13, N, K)).to(dev)
         wq, wd = ctx.rq_fp8_weight_cache(synthetic.Q4K, W, N, K)
         x = torch.from_numpy(synthetic.activation(14, M, K, outlier_frac=1e-3)).to(dev)
@@ -627,6 +658,26 @@ def run_sweep(args):
         out({"sweep": "fp8_gemm", "M": M, "N": N, "K": K, "us": ms * 1e3, "TFLOP/s": tf,
              "frac_fp8_peak": tf / fp8_peak})
     ctx.close()
+    # route crossover: the stack at a few tokens through the GEMV route
+    # (threshold above M; chunks of 8 tokens) and through the FP8 route
+    # (threshold 1), each pass graph-replayed
+    if "route" in parts:
+        Ms = (2, 3, 4, 6, 8, 12, 16)
+        st = Stack(rq, torch, dev, Ms=Ms)
+        for M in Ms:
+            row = {}
+            for route, th in (("gemv", M + 1), ("fp8", 1)):
+                st.ctx.set_gemm_threshold(th)
+                row[route] = pass_graph_ms(torch, dev, st, M)
+            out({"sweep": "route", "M": M, "gemv_ms": row["gemv"], "fp8_ms": row["fp8"],
+                 "faster": min(row, key=row.get)})
+        st.ctx.close()
+        del st
+        torch.cuda.empty_cache()
+    if "stack" not in parts:
+        if rq.rq_get_device_status() != 0:
+            raise SystemExit(1)
+        return
     # prefill stack at several M
     Ms = (16, 128, 512, 2048, 4096)
     st = Stack(rq, torch, dev, Ms=Ms)
@@ -760,6 +811,8 @@ def main():
     ap.add_argument("--N", type=int, default=3584)
     ap.add_argument("--K", type=int, default=3584)
     ap.add_argument("--launches", type=int, default=3)
+    ap.add_argument("--sweep-parts", default="gemv,gemm,route,stack",
+                    help="comma-separated parts of --sweep: gemv, gemm, route, stack")
     ap.add_argument("--sweep", action="store_true",
                     help="print the GEMV, FP8 GEMM and prefill-stack sweeps instead")
     ap.add_argument("--graph", action="store_true",
