@@ -613,7 +613,7 @@ def run_sweep(args):
     FP8 GEMM at M = 512 on the four prefill shapes; the stack at 2 .. 16
     tokens through the GEMV route and through the FP8 route (graph replay),
     which locates the crossover of the two; the 28-layer prefill stack at
-    M = 16 .. 4096 (eager, untraced)."""
+    M = 16 .. 4096 (eager, untraced; and one pass captured in a CUDA graph)."""
     import torch
     import quantized_linear_layers_gb300 as rq
     dev = torch.device("cuda", 0)
@@ -693,9 +693,12 @@ def run_sweep(args):
         e1.record()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / reps
+        stats = st.ctx.stats()
+        gms = pass_graph_ms(torch, dev, st, M)
         out({"sweep": "prefill_stack", "M": M, "ms_per_pass": ms,
              "TFLOP/s": stack_flops(M) / ms / 1e9,
-             "act_cache": st.ctx.stats()})
+             "graph_ms_per_pass": gms, "graph_TFLOP/s": stack_flops(M) / gms / 1e9,
+             "act_cache": stats})
     if rq.rq_get_device_status() != 0:
         raise SystemExit(1)
 

@@ -38,14 +38,13 @@ namespace {
 
 constexpr int kBM = 128;               // weight rows per tile (MMA M)
 constexpr int kBK = 128;               // K bytes per stage = one swizzle row
-constexpr int kStages = 4;
+constexpr int kStages = 4;             // default ring depth, one-CTA and split-K kernels
+constexpr int kMaxStages = 16;
 constexpr int kMaxBN = 256;
 constexpr int kMaxSegs = RQ_MAX_GROUP;  // members of a grouped launch
 constexpr int kThreads = 192;
 constexpr int kABytes = kBM * kBK;           // 16 KB
-constexpr int kBBytesMax = kMaxBN * kBK;     // 32 KB
-constexpr int kSmemBytes = kStages * (kABytes + kBBytesMax) + 1024 /*barriers*/ +
-                           1024 /*alignment slack*/;
+constexpr int kSmemLimit = 227 * 1024;  // dynamic shared memory a CTA may opt into
 
 // --------------------------------------------------------- PTX wrappers --
 
@@ -143,6 +142,7 @@ struct GemmArgs {
   int bn;          // tokens per tile: multiple of 16, <= 256
   int tiles_n;     // ceil(N / 128)
   int tiles_m;     // ceil(M_pad / bn)
+  int stages;      // stages of the shared-memory ring
   uint32_t tmem_cols;
   uint64_t wait_limit_ns;
 };
@@ -153,28 +153,30 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;                                  // kStages x 16 KB
-  uint8_t* sB = smem + kStages * kABytes;              // kStages x 32 KB
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBBytesMax);
-  // bars: full[kStages], empty[kStages], tfull[2], tempty[2], done[1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  const int nst = args.stages;                         // stages of the ring
+  const uint32_t b_stride = (uint32_t)args.bn * kBK;   // token tile bytes per stage
+  uint8_t* sA = smem;                                  // nst x 16 KB
+  uint8_t* sB = smem + nst * kABytes;                  // nst x BN x 128 B
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + nst * b_stride);
+  // bars: full[nst], empty[nst], tfull[2], tempty[2], done[1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * nst + 5);
   // nothing global is read before the previous launch has completed: the
   // weight operand may have been written by the launch just before
   pdl_wait();
   pdl_trigger();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
-  const uint32_t tfull0 = smem_u32(bars + 2 * kStages);
-  const uint32_t tempty0 = smem_u32(bars + 2 * kStages + 2);
-  const uint32_t done_bar = smem_u32(bars + 2 * kStages + 4);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + nst);
+  const uint32_t tfull0 = smem_u32(bars + 2 * nst);
+  const uint32_t tempty0 = smem_u32(bars + 2 * nst + 2);
+  const uint32_t done_bar = smem_u32(bars + 2 * nst + 4);
   const int bn = args.bn;
   const int kblocks = args.K / kBK;
   const int ntiles = args.tiles_n * args.tiles_m;
   const uint32_t stage_tx = (uint32_t)(kABytes + bn * kBK);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < nst; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
@@ -216,14 +218,14 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
           const uint32_t fb = full0 + 8 * stage;
           mbar_arrive_expect_tx(fb, stage_tx);
           tma_load_2d(smem_u32(sA + stage * kABytes), &tmap_w, fb, kb * kBK, tn * kBM);
-          tma_load_2d(smem_u32(sB + stage * kBBytesMax), &tmap_x, fb, kb * kBK, tm * bn);
+          tma_load_2d(smem_u32(sB + stage * b_stride), &tmap_x, fb, kb * kBK, tm * bn);
           issued_mask |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
+          if (++stage == nst) { stage = 0; phase ^= 1; }
         }
       }
       // Drain: every issued copy has landed before the CTA can exit.
-      for (int s = 0; s < kStages; ++s)
+      for (int s = 0; s < nst; ++s)
         if (issued_mask & (1u << s))
           mbar_wait(full0 + 8 * s, (last_parity >> s) & 1u, args.wait_limit_ns,
                     &g_rq_device_error);
@@ -248,13 +250,13 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
           }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(sA + stage * kABytes);
-          const uint32_t b_addr = smem_u32(sB + stage * kBBytesMax);
+          const uint32_t b_addr = smem_u32(sB + stage * b_stride);
 #pragma unroll
           for (int kk = 0; kk < kBK / 32; ++kk)
             mma_f8(d_tmem, smem_desc(a_addr + 32 * kk), smem_desc(b_addr + 32 * kk), idesc,
                    (kb | kk) != 0);
           mma_commit(empty0 + 8 * stage);  // frees the stage when these MMAs finish
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
+          if (++stage == nst) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
         mma_commit(tfull0 + 8 * acc);  // accumulator ready for the epilogue
@@ -327,7 +329,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
 // the leader's "tmem empty" barriers.  Each CTA's TMEM holds its 128 rows of
 // the accumulator.  All waits are bounded as in the 1-CTA kernel.
 
-constexpr int kStages2 = 6;
+constexpr int kStages2 = 6;  // default ring depth, pair kernel
 constexpr int kBHalfMax = kMaxBN / 2 * kBK;  // 16 KB: this CTA's half of B
 constexpr int kSmemBytes2 = kStages2 * (kABytes + kBHalfMax) + 1024 + 1024;
 
@@ -402,21 +404,23 @@ fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;                            // kStages2 x 16 KB
-  uint8_t* sB = smem + kStages2 * kABytes;       // kStages2 x 16 KB (half the token tile)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages2 * kBHalfMax);
-  // bars: full[kStages2], empty[kStages2], tfull[2], tempty[2], done[1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages2 + 5);
+  const int nst = args.stages;
+  const uint32_t b_stride = (uint32_t)(args.bn / 2) * kBK;  // this CTA's half of the token tile
+  uint8_t* sA = smem;                            // nst x 16 KB
+  uint8_t* sB = smem + nst * kABytes;            // nst x BN/2 x 128 B
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + nst * b_stride);
+  // bars: full[nst], empty[nst], tfull[2], tempty[2], done[1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * nst + 5);
   pdl_wait();
   pdl_trigger();
 
   const uint32_t rank = cluster_rank();
   const bool leader = rank == 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages2);
-  const uint32_t tfull0 = smem_u32(bars + 2 * kStages2);
-  const uint32_t tempty0 = smem_u32(bars + 2 * kStages2 + 2);
-  const uint32_t done_bar = smem_u32(bars + 2 * kStages2 + 4);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + nst);
+  const uint32_t tfull0 = smem_u32(bars + 2 * nst);
+  const uint32_t tempty0 = smem_u32(bars + 2 * nst + 2);
+  const uint32_t done_bar = smem_u32(bars + 2 * nst + 4);
   const int bn = args.bn, half = bn / 2;
   const int kblocks = args.K / kBK;
   const int ntiles = args.tiles_n * args.tiles_m;  // tiles_n counts 256-row tiles
@@ -424,7 +428,7 @@ fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
   const uint32_t stage_tx = (uint32_t)(kABytes + half * kBK);  // bytes per CTA per stage
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages2; ++s) {
+    for (int s = 0; s < nst; ++s) {
       mbar_init(full0 + 8 * s, 1);   // the leader's expect_tx for both CTAs' bytes
       mbar_init(empty0 + 8 * s, 1);  // the leader's commit
     }
@@ -470,16 +474,16 @@ fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
           const uint32_t lead_full = peer_addr(full0 + 8 * stage, 0);
           if (leader) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * stage_tx);
           tma_load_2d_pair(smem_u32(sA + stage * kABytes), &tmap_w, lead_full, kb * kBK, wrow);
-          tma_load_2d_pair(smem_u32(sB + stage * kBHalfMax), &tmap_x, lead_full, kb * kBK, trow);
-          if (++stage == kStages2) { stage = 0; phase ^= 1; }
+          tma_load_2d_pair(smem_u32(sB + stage * b_stride), &tmap_x, lead_full, kb * kBK, trow);
+          if (++stage == nst) { stage = 0; phase ^= 1; }
         }
       }
       // Drain: this CTA's last copies have landed once the leader's MMAs
       // that consume them have freed the stages (seen on our own "empty").
-      for (int i = 0; i < kStages2 && ok; ++i) {
+      for (int i = 0; i < nst && ok; ++i) {
         if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, args.wait_limit_ns, &g_rq_device_error))
           break;
-        if (++stage == kStages2) { stage = 0; phase ^= 1; }
+        if (++stage == nst) { stage = 0; phase ^= 1; }
       }
     }
   } else if (warp == 1) {
@@ -503,13 +507,13 @@ fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
           }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(sA + stage * kABytes);
-          const uint32_t b_addr = smem_u32(sB + stage * kBHalfMax);
+          const uint32_t b_addr = smem_u32(sB + stage * b_stride);
 #pragma unroll
           for (int kk = 0; kk < kBK / 32; ++kk)
             mma_f8_pair(d_tmem, smem_desc(a_addr + 32 * kk), smem_desc(b_addr + 32 * kk), idesc,
                         (kb | kk) != 0);
           mma_commit_pair(empty0 + 8 * stage);
-          if (++stage == kStages2) { stage = 0; phase ^= 1; }
+          if (++stage == nst) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
         mma_commit_pair(tfull0 + 8 * acc);
@@ -588,6 +592,7 @@ struct SplitArgs {
   OutSegs out;
   int M, N, K;
   int bn, tiles_m, splits;
+  int stages;  // stages of the shared-memory ring (their bytes also hold the partial tile)
   uint32_t tmem_cols;
   uint64_t wait_limit_ns;
 };
@@ -611,18 +616,20 @@ fp8_gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmap_w,
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;                                  // kStages x 16 KB
-  uint8_t* sB = smem + kStages * kABytes;              // kStages x 32 KB
+  const int nst = args.stages;
+  const uint32_t b_stride = (uint32_t)args.bn * kBK;
+  uint8_t* sA = smem;                                  // nst x 16 KB
+  uint8_t* sB = smem + nst * kABytes;                  // nst x BN x 128 B
   float* part = reinterpret_cast<float*>(smem);        // [bn][128] after the mainloop
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBBytesMax);
-  // bars: full[kStages], empty[kStages], tfull[1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 1);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + nst * b_stride);
+  // bars: full[nst], empty[nst], tfull[1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * nst + 1);
   pdl_wait();
   pdl_trigger();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
-  const uint32_t tfull = smem_u32(bars + 2 * kStages);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + nst);
+  const uint32_t tfull = smem_u32(bars + 2 * nst);
   const int S = args.splits;
   const uint32_t rank = cluster_rank();
   const int t = (int)blockIdx.x / S;
@@ -634,7 +641,7 @@ fp8_gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmap_w,
   const uint32_t stage_tx = (uint32_t)(kABytes + bn * kBK);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < nst; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
@@ -667,12 +674,12 @@ fp8_gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmap_w,
         const uint32_t fb = full0 + 8 * stage;
         mbar_arrive_expect_tx(fb, stage_tx);
         tma_load_2d(smem_u32(sA + stage * kABytes), &tmap_w, fb, kb * kBK, tn * kBM);
-        tma_load_2d(smem_u32(sB + stage * kBBytesMax), &tmap_x, fb, kb * kBK, tm * bn);
+        tma_load_2d(smem_u32(sB + stage * b_stride), &tmap_x, fb, kb * kBK, tm * bn);
         issued_mask |= 1u << stage;
         last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
+        if (++stage == nst) { stage = 0; phase ^= 1; }
       }
-      for (int s = 0; s < kStages; ++s)
+      for (int s = 0; s < nst; ++s)
         if (issued_mask & (1u << s))
           mbar_wait(full0 + 8 * s, (last_parity >> s) & 1u, args.wait_limit_ns,
                     &g_rq_device_error);
@@ -687,13 +694,13 @@ fp8_gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmap_w,
         if (!mbar_wait(full0 + 8 * stage, phase, args.wait_limit_ns, &g_rq_device_error)) break;
         tc_fence_after();
         const uint32_t a_addr = smem_u32(sA + stage * kABytes);
-        const uint32_t b_addr = smem_u32(sB + stage * kBBytesMax);
+        const uint32_t b_addr = smem_u32(sB + stage * b_stride);
 #pragma unroll
         for (int kk = 0; kk < kBK / 32; ++kk)
           mma_f8(tmem_base, smem_desc(a_addr + 32 * kk), smem_desc(b_addr + 32 * kk), idesc,
                  (kb != kb0 || kk != 0) ? 1u : 0u);
         mma_commit(empty0 + 8 * stage);
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
+        if (++stage == nst) { stage = 0; phase ^= 1; }
       }
       // completes when every MMA above has: the partial is in TMEM and no
       // MMA reads the stage buffers any more
@@ -837,6 +844,25 @@ uint32_t tmem_columns(int bn) {
   return c;
 }
 
+// Ring depth for a token tile of b_stride bytes per stage: `dflt`, or
+// RQ_GEMM_STAGES (tuning runs), within what fits next to the barriers and
+// the alignment slack; at least min_bytes of stage buffers (the split-K
+// kernel keeps its partial tile there).
+int gemm_stages(int b_stride, int dflt, int min_bytes) {
+  const char* env = std::getenv("RQ_GEMM_STAGES");
+  int s = env ? std::atoi(env) : dflt;
+  const int per = kABytes + b_stride;
+  const int fit = (kSmemLimit - 2048) / per;
+  while (s * per < min_bytes) ++s;
+  if (s > fit) s = fit;
+  if (s > kMaxStages) s = kMaxStages;
+  return s < 2 ? 2 : s;
+}
+
+size_t gemm_smem_bytes(int stages, int b_stride) {
+  return 1024 /*alignment slack*/ + (size_t)stages * (kABytes + b_stride) + 1024 /*barriers*/;
+}
+
 // Tokens per tile.  Every CTA is resident at once (one per SM), so a launch
 // takes ceil(tiles / SMs) rounds.  The kernels stream their operands from L2
 // at a rate that caps them (about 100 GB/s per SM on GB300), so a round
@@ -909,7 +935,7 @@ int resident_pairs(int sms) {
     cfg.dynamicSmemBytes = kSmemBytes2;
     int n = 0;
     cudaFuncSetAttribute(fp8_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         kSmemBytes2);
+                         kSmemLimit);
     if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_pair_kernel, &cfg) != cudaSuccess || n < 1) {
       cudaGetLastError();
       n = 1;
@@ -976,11 +1002,12 @@ static rq_status launch_fp8_gemm_splitk(const uint8_t* x_fp8, const float* x_deq
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(fp8_gemm_splitk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess)
+                             kSmemLimit) != cudaSuccess)
       return RQ_ERR_CUDA;
     attr_done = true;
   }
   SplitArgs a;
+  a.stages = gemm_stages(bn * kBK, kStages, bn * kBM * 4);
   a.x_deq = x_deq;
   a.out = out;
   a.M = M;
@@ -1002,7 +1029,7 @@ static rq_status launch_fp8_gemm_splitk(const uint8_t* x_fp8, const float* x_deq
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(tiles * S);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = gemm_smem_bytes(a.stages, bn * kBK);
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_enabled() ? 2 : 1;
@@ -1056,25 +1083,30 @@ rq_status launch_fp8_gemm_group(const uint8_t* x_fp8, const float* x_deq,
     static bool attr2 = false;
     if (!attr2) {
       if (cudaFuncSetAttribute(fp8_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSmemBytes2) != cudaSuccess)
+                               kSmemLimit) != cudaSuccess)
         return RQ_ERR_CUDA;
       attr2 = true;
     }
+    const int b_stride = bn / 2 * kBK;
+    a.stages = gemm_stages(b_stride, kStages2, 0);
     // A persistent grid must be resident at once: not every SM can be
     // paired inside its GPC, so the grid is the number of pairs that fit.
     const int max_pairs = resident_pairs(sms);
     const int grid = 2 * (tiles < max_pairs ? tiles : max_pairs);
-    return launch_kernel(fp8_gemm_pair_kernel, grid, kThreads, kSmemBytes2, st, tw, tx, a);
+    return launch_kernel(fp8_gemm_pair_kernel, grid, kThreads,
+                         gemm_smem_bytes(a.stages, b_stride), st, tw, tx, a);
   }
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(fp8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess)
+                             kSmemLimit) != cudaSuccess)
       return RQ_ERR_CUDA;
     attr_done = true;
   }
+  a.stages = gemm_stages(bn * kBK, kStages, 0);
   const int grid = tiles < sms ? tiles : sms;
-  return launch_kernel(fp8_gemm_kernel, grid, kThreads, kSmemBytes, st, tw, tx, a);
+  return launch_kernel(fp8_gemm_kernel, grid, kThreads, gemm_smem_bytes(a.stages, bn * kBK), st,
+                       tw, tx, a);
 }
 
 rq_status launch_fp8_gemm(const uint8_t* x_fp8, const float* x_deq,
