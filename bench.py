@@ -745,7 +745,11 @@ def run_case(args):
     elif args.case == "gemm":
         ctx = rq.Context()
         W = torch.from_numpy(synthetic.q4k_matrix(4, N, K)).to(dev)
-        wq, wd = ctx.rq_fp8_weight_cache(synthetic.Q4K, W, N, K)
+        # FP8 caches of copies of the weight (at least 512 MB in all), so
+        # that successive launches read their weight from HBM, not L2
+        Wsrc = [W] + [W.clone() for _ in range(-(-(512 << 20) // (N * K)) - 1)]
+        caches = [ctx.rq_fp8_weight_cache(synthetic.Q4K, Wc, N, K) for Wc in Wsrc]
+        wit = iter(range(1 << 62))
         x = torch.from_numpy(synthetic.activation(5, M, K, outlier_frac=1e-3)).to(dev)
         m_pad = (M + 15) // 16 * 16
         bits = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -754,7 +758,9 @@ def run_case(args):
         rq.rq_absmax(x, M * K, bits)
         rq.rq_quant_e4m3(x, M * K, bits, xq, xd)
         y = torch.empty(M, N, device=dev)
-        call = lambda: rq.rq_fp8_gemm(xq, xd, wq, wd, y, M, N, K)  # noqa: E731
+        def call():
+            wq, wd = caches[next(wit) % len(caches)]
+            rq.rq_fp8_gemm(xq, xd, wq, wd, y, M, N, K)
     else:
         raise SystemExit("unknown case " + args.case)
     for _ in range(3):
@@ -768,6 +774,9 @@ def run_case(args):
         cs = torch.cuda.Stream(dev)
         cs.wait_stream(torch.cuda.current_stream(dev))
         with torch.cuda.stream(cs):
+            for _ in range(3):  # warm the capture stream too
+                call()
+            torch.cuda.synchronize()
             with torch.cuda.graph(g, stream=cs):
                 for _ in range(args.launches):
                     call()

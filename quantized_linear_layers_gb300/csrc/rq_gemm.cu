@@ -25,6 +25,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstdio>
 #include <cstdlib>
 
 #include "rq_device.cuh"
@@ -1027,6 +1028,9 @@ static rq_status launch_fp8_gemm_splitk(const uint8_t* x_fp8, const float* x_deq
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
+  if (std::getenv("RQ_GEMM_LOG") != nullptr)
+    std::fprintf(stderr, "rq_gemm: split-k M=%d N=%d K=%d bn=%d tiles=%d splits=%d stages=%d\n",
+                 M, N, K, bn, tiles, S, a.stages);
   cfg.gridDim = dim3(tiles * S);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = gemm_smem_bytes(a.stages, bn * kBK);
@@ -1093,6 +1097,9 @@ rq_status launch_fp8_gemm_group(const uint8_t* x_fp8, const float* x_deq,
     // paired inside its GPC, so the grid is the number of pairs that fit.
     const int max_pairs = resident_pairs(sms);
     const int grid = 2 * (tiles < max_pairs ? tiles : max_pairs);
+    if (std::getenv("RQ_GEMM_LOG") != nullptr)
+      std::fprintf(stderr, "rq_gemm: pair M=%d N=%d K=%d bn=%d tiles=%d grid=%d stages=%d\n", M,
+                   N, K, bn, tiles, grid, a.stages);
     return launch_kernel(fp8_gemm_pair_kernel, grid, kThreads,
                          gemm_smem_bytes(a.stages, b_stride), st, tw, tx, a);
   }
@@ -1105,6 +1112,9 @@ rq_status launch_fp8_gemm_group(const uint8_t* x_fp8, const float* x_deq,
   }
   a.stages = gemm_stages(bn * kBK, kStages, 0);
   const int grid = tiles < sms ? tiles : sms;
+  if (std::getenv("RQ_GEMM_LOG") != nullptr)
+    std::fprintf(stderr, "rq_gemm: single M=%d N=%d K=%d bn=%d tiles=%d grid=%d stages=%d\n", M,
+                 N, K, bn, tiles, grid, a.stages);
   return launch_kernel(fp8_gemm_kernel, grid, kThreads, gemm_smem_bytes(a.stages, bn * kBK), st,
                        tw, tx, a);
 }
