@@ -192,4 +192,3 @@ def test_split_k_integer_sums_are_exact(rq, monkeypatch):
     Wb = np.vectorize(code.get)(wv).astype(np.uint8)
     got = gpu_gemm(rq, Xb, 1.0, Wb, 1.0, M)
     assert np.array_equal(got, (xv @ wv.T).astype(np.float32))
-
