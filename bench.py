@@ -662,7 +662,7 @@ def run_sweep(args):
     # (threshold above M; chunks of 8 tokens) and through the FP8 route
     # (threshold 1), each pass graph-replayed
     if "route" in parts:
-        Ms = (2, 3, 4, 6, 8, 12, 16)
+        Ms = (2, 3, 4, 5, 6, 8, 12, 16)
         st = Stack(rq, torch, dev, Ms=Ms)
         for M in Ms:
             row = {}

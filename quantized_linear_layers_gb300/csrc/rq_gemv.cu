@@ -436,6 +436,10 @@ struct M1Args {
   uint64_t wait_limit_ns;
   int row_align;        // Q6_K: rows per 16-byte-aligned group of rows
   int M;                // tokens (the multi-token Q6_K kernel)
+  // One-token Q4_K: 2 = clusters of two CTAs share a block of rows, CTA
+  // rank h taking super-blocks [h*nsb/2, (h+1)*nsb/2) of each row (rank 0
+  // adds rank 1's partial sums and writes y); 1 = one CTA per row block.
+  int ksplit;
   // One-token Q4_K: the rows are the concatenation of nseg weights that
   // share x (rows [seg_start[i], seg_start[i+1]) are rows of seg_w[i] and
   // go to seg_y[i]); a single weight is one segment.
@@ -449,6 +453,29 @@ __device__ __forceinline__ int m1_seg(const M1Args& a, int row) {
   int i = 0;
   while (i + 1 < a.nseg && row >= a.seg_start[i + 1]) ++i;
   return i;
+}
+
+__device__ __forceinline__ uint32_t m1_cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void m1_cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+// A float in the shared memory of CTA `rank` of the cluster, at the offset
+// of `local` in this CTA.
+__device__ __forceinline__ float m1_ld_peer(const float* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(remote)
+               : "r"(smem_u32(local)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
@@ -601,8 +628,13 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
   static_assert(RPT == 2 || RPT == 4 || RPT == 8, "rows per team per stage");
   constexpr int SPB = 8 / RPT;  // stages per 8-row reduction batch
   extern __shared__ __align__(128) uint8_t smem_m1[];
-  const int nsb = a.K >> 8, U = nsb * 4, nsub = a.K >> 5;
-  const int rowbytes = nsb * kQ4KBytes;
+  // this CTA's share of each row: super-blocks [h*nsb, (h+1)*nsb) of a
+  // row of ksplit*nsb
+  const int h = a.ksplit == 2 ? (int)m1_cluster_rank() : 0;
+  const int nsb = (a.K >> 8) / a.ksplit, U = nsb * 4, nsub = nsb * 8;
+  const int rowbytes = nsb * kQ4KBytes;            // bytes of a row this CTA reads
+  const int rowstride = rowbytes * a.ksplit;       // bytes of a whole row
+  const float* xh = a.x + (size_t)h * nsb * 256;
   const int rps = a.rows_per_stage;  // teams * RPT
   const uint32_t stage_bytes = (uint32_t)(rps * rowbytes);
   uint8_t* ring = smem_m1;
@@ -616,8 +648,9 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
 
   const int compute_warps = a.teams * a.team_warps;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r0 = (int)((int64_t)bid * a.N / nblk);
-  const int r1 = (int)((int64_t)(bid + 1) * a.N / nblk);
+  const int cb = bid / a.ksplit, ncb = nblk / a.ksplit;  // row block of the cluster
+  const int r0 = (int)((int64_t)cb * a.N / ncb);
+  const int r1 = (int)((int64_t)(cb + 1) * a.N / ncb);
   const int rows = r1 - r0;
   const int iters = (rows + rps - 1) / rps;
   const int first = iters < a.stages ? iters : a.stages;
@@ -645,12 +678,13 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
     const int nr = min(rps, rows - it * rps);
     const uint32_t bytes = (uint32_t)(nr * rowbytes);
     mbar_arrive_expect_tx(full0 + 8 * s, bytes);
-    // one copy per segment the stage's rows fall in
+    // one copy per segment the stage's rows fall in (per row when the rows
+    // are split between the CTAs of a cluster)
     for (int v = r0 + it * rps, done = 0; done < nr;) {
       const int sg = m1_seg(a, v);
-      const int take = min(nr - done, a.seg_start[sg + 1] - v);
+      const int take = a.ksplit == 1 ? min(nr - done, a.seg_start[sg + 1] - v) : 1;
       bulk_g2s(smem_u32(ring + s * stage_bytes + (size_t)done * rowbytes),
-               a.seg_w[sg] + (size_t)(v - a.seg_start[sg]) * rowbytes,
+               a.seg_w[sg] + (size_t)(v - a.seg_start[sg]) * rowstride + (size_t)h * rowbytes,
                (uint32_t)(take * rowbytes), full0 + 8 * s);
       v += take;
       done += take;
@@ -673,7 +707,7 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
   if (warp < compute_warps) {
     const int q = lane & 3;
     for (int sb32 = warp * 8 + (lane >> 2); sb32 < nsub; sb32 += compute_warps * 8) {
-      const float4* px = reinterpret_cast<const float4*>(a.x + 32 * sb32 + 8 * q);
+      const float4* px = reinterpret_cast<const float4*>(xh + 32 * sb32 + 8 * q);
       const float4 va = __ldg(px), vb = __ldg(px + 1);
       const float v[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
       float mx = 0.f, sm = 0.f;
@@ -798,6 +832,16 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
     }
   }
   __syncthreads();
+  if (a.ksplit == 2) {
+    m1_cluster_sync();  // both halves of every row are in their CTAs' acc
+    if (h == 0)
+      for (int i = threadIdx.x; i < rows; i += blockDim.x) {
+        const int sg = m1_seg(a, r0 + i);
+        a.seg_y[sg][r0 + i - a.seg_start[sg]] = acc[i] + m1_ld_peer(acc + i, 1);
+      }
+    m1_cluster_sync();  // rank 1's shared memory stays until rank 0 has read it
+    return;
+  }
   for (int i = threadIdx.x; i < rows; i += blockDim.x) {
     const int sg = m1_seg(a, r0 + i);
     a.seg_y[sg][r0 + i - a.seg_start[sg]] = acc[i];
@@ -1396,21 +1440,30 @@ rq_status m1_allow_smem(Kern kern, size_t smem, size_t& set) {
 // between the x planes and a ring of weight stages.  The RQ_GEMV_*
 // environment variables override the shape for tuning runs.
 rq_status plan_q4k_m1(int nseg, const int* starts, const uint8_t* const* ws, float* const* ys,
-                      const float* x, int K, int grid, M1Plan* p) {
+                      const float* x, int K, int grid, bool allow_ksplit, M1Plan* p) {
   const int N = starts[nseg];
   const int sms = device_sm_count();
-  if (grid <= 0) grid = N < sms ? N : sms;
-  if (grid > N) grid = N;
-  const int max_rows = (N + grid - 1) / grid;
+  // rows longer than 8 warps' worth of 64-weight groups are split between
+  // the two CTAs of a cluster (more warps per SM for the long rows of a
+  // down projection); RQ_GEMV_KSPLIT=0 / 1 forces it off / on (on needs an
+  // even number of super-blocks per row)
+  const int nsb_full = K / kQK;
+  int ksplit = ((nsb_full * 4 + 31) / 32 > 8) ? 2 : 1;
+  if (const char* e = std::getenv("RQ_GEMV_KSPLIT")) ksplit = std::atoi(e) != 0 ? 2 : 1;
+  if (!allow_ksplit || nsb_full % 2 != 0 || sms < 2) ksplit = 1;
+  if (grid <= 0) grid = ksplit * (N < sms / ksplit ? N : sms / ksplit);
+  if (grid > ksplit * N) grid = ksplit * N;
+  const int max_rows = (N + grid / ksplit - 1) / (grid / ksplit);
   // defaults from launch-shape sweeps on GB300: few rows per CTA favour
   // smaller teams and stages; long rows favour a shallower ring
   const bool few_rows = max_rows <= 8;
   const int warps_per_cta = m1_knob("RQ_GEMV_WARPS", few_rows ? 8 : 16, 1, 16);
   int rpt = m1_knob("RQ_GEMV_RPT", few_rows ? 2 : 4, 2, 8);
   rpt = rpt >= 8 ? 8 : (rpt >= 4 ? 4 : 2);
-  const int ring_kb = m1_knob("RQ_GEMV_RING_KB", K >= 8192 ? 100 : 150, 16, 200);
+  const int Kc = K / ksplit;  // the part of a row one CTA reads
+  const int ring_kb = m1_knob("RQ_GEMV_RING_KB", Kc >= 8192 ? 100 : 150, 16, 200);
   const int max_stages = m1_knob("RQ_GEMV_STAGES", 8, 2, 16);
-  const int U = K / 64, nsub = K / 32;
+  const int U = Kc / 64, nsub = Kc / 32;
   M1Args& a = p->a;
   a.W = ws[0];
   a.x = x;
@@ -1425,10 +1478,12 @@ rq_status plan_q4k_m1(int nseg, const int* starts, const uint8_t* const* ws, flo
   }
   a.row_align = 1;
   a.M = 1;
+  a.ksplit = ksplit;
   a.team_warps = (U + 31) / 32;
+  if (a.team_warps > 16) return RQ_ERR_SHAPE;
   a.teams = a.team_warps >= warps_per_cta ? 1 : warps_per_cta / a.team_warps;
   a.rows_per_stage = rpt * a.teams;
-  const int rowbytes = (K / kQK) * kQ4KBytes;
+  const int rowbytes = (Kc / kQK) * kQ4KBytes;
   const int stage_bytes = a.rows_per_stage * rowbytes;
   const size_t nsub2 = (size_t)((nsub + 1) & ~1);
   const size_t fixed = (size_t)U * kPlaneStride + 8 * nsub2 +
@@ -1453,14 +1508,29 @@ rq_status plan_q4k_m1(int nseg, const int* starts, const uint8_t* const* ws, flo
 rq_status run_q4k_m1(int nseg, const int* starts, const uint8_t* const* ws, float* const* ys,
                      const float* x, int K, cudaStream_t st) {
   M1Plan p;
-  const rq_status s = plan_q4k_m1(nseg, starts, ws, ys, x, K, 0, &p);
+  const rq_status s = plan_q4k_m1(nseg, starts, ws, ys, x, K, 0, true, &p);
   if (s != RQ_OK) return s;
   auto kern = p.rpt == 8 ? q4k_gemv_m1_kernel<8>
                          : (p.rpt == 4 ? q4k_gemv_m1_kernel<4> : q4k_gemv_m1_kernel<2>);
   static size_t smem_set[3] = {48 * 1024, 48 * 1024, 48 * 1024};
   const rq_status sa = m1_allow_smem(kern, p.smem, smem_set[p.rpt == 8 ? 2 : (p.rpt == 4 ? 1 : 0)]);
   if (sa != RQ_OK) return sa;
-  return launch_kernel(kern, p.grid, p.threads, p.smem, st, p.a);
+  if (p.a.ksplit == 1) return launch_kernel(kern, p.grid, p.threads, p.smem, st, p.a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(p.threads);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, p.a));
 }
 
 // One-token (M = 1) or multi-token (M = 2..8) Q6_K shape: as for Q4_K, plus
@@ -1493,6 +1563,7 @@ rq_status plan_q6k_m1(const uint8_t* w, const float* x, float* y, int M, int N, 
   a.K = K;
   a.row_align = ra;
   a.M = M;
+  a.ksplit = 1;
   a.nseg = 1;
   a.seg_start[0] = 0;
   for (int i = 1; i <= RQ_MAX_GROUP; ++i) a.seg_start[i] = N;
@@ -1556,9 +1627,10 @@ rq_status launch_q4k_gemv(const uint8_t* w, const float* x, float* y, int M,
     case 1:
       // the one-token kernel keeps 64 x values per lane in registers; its
       // team of ceil(K/2048) warps plus the producer warp fit 544 threads
-      if (K <= 16 * 2048) {
-        // RQ_ERR_SHAPE here means the launch shape does not fit shared
-        // memory; nothing was launched, so the generic kernel takes it
+      if (K <= 32 * 2048) {
+        // RQ_ERR_SHAPE here means the launch shape does not fit the kernel
+        // or its shared memory; nothing was launched, so the generic
+        // kernel takes it
         const int starts[2] = {0, N};
         const rq_status s1 = run_q4k_m1(1, starts, &w, &y, x, K, st);
         if (s1 != RQ_ERR_SHAPE) return s1;
@@ -1587,7 +1659,7 @@ rq_status launch_q4k_gemv(const uint8_t* w, const float* x, float* y, int M,
 
 rq_status launch_q4k_gemv_group(int count, const int* starts, const uint8_t* const* ws,
                                 float* const* ys, const float* x, int K, cudaStream_t st) {
-  if (count < 1 || count > RQ_MAX_GROUP || K > 16 * 2048) return RQ_ERR_SHAPE;
+  if (count < 1 || count > RQ_MAX_GROUP || K > 32 * 2048) return RQ_ERR_SHAPE;
   return run_q4k_m1(count, starts, ws, ys, x, K, st);
 }
 
@@ -1602,7 +1674,7 @@ rq_status launch_gemv_m1_dual(int count, const int* starts, const uint8_t* const
   int g6 = (int)(sms * c6 / (c4 + c6) + 0.5);
   g6 = m1_knob("RQ_GEMV_DUAL_G6", g6, 1, sms - 1);
   M1Plan p4, p6;
-  rq_status s = plan_q4k_m1(count, starts, ws, ys, x, K, sms - g6, &p4);
+  rq_status s = plan_q4k_m1(count, starts, ws, ys, x, K, sms - g6, false, &p4);
   if (s != RQ_OK) return s;
   s = plan_q6k_m1(w6, x, y6, 1, n6, K, g6, &p6);
   if (s != RQ_OK) return s;

@@ -163,3 +163,19 @@ def test_q6k_weight_only_4_byte_aligned(rq, M):
     torch.cuda.synchronize()
     ref, absdot = oracle.gemv(Q6K, W, x, N, K)
     assert gemv_ok(y.cpu().numpy(), ref, absdot)[0]
+
+
+@pytest.mark.parametrize("force", ["", "1", "0"])
+@pytest.mark.parametrize("N,K", [(1, 512), (67, 768), (300, 8704), (151, 18944), (37, 40960)])
+def test_one_token_q4k_rows_split_between_two_ctas(rq, monkeypatch, force, N, K):
+    """One token, rows whose super-blocks are split between the two CTAs of
+    a cluster (automatic for rows longer than 8 warps' worth, forced on or
+    off otherwise; K = 40960 needs it): every output against the oracle."""
+    if force:
+        monkeypatch.setenv("RQ_GEMV_KSPLIT", force)
+    W = synthetic.q4k_matrix(2000 + N + K, N, K)
+    x = synthetic.activation(2001 + K, 1, K, outlier_frac=1e-3)
+    got = gpu_gemv(rq, Q4K, W, x, N, K)
+    ref, absdot = oracle.gemv(Q4K, W, x, N, K)
+    ok, worst = gemv_ok(got, ref, absdot)
+    assert ok, "worst error / bound = %.3g" % worst
