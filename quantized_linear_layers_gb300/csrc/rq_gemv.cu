@@ -501,17 +501,6 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
   return d;
 }
 
-// Group coefficients from a header: (d sc_lo, d sc_hi / 16, dmin m_lo,
-// dmin m_hi) for sub-blocks 2g, 2g+1 (the high nibbles enter the dot
-// products as 16 q, hence the 1/16).
-__device__ __forceinline__ float4 q4_coeffs(const uint4& h, int sh, bool upper) {
-  const uint32_t a16 = h.y >> sh, b16 = h.z >> sh, c16 = h.w >> sh;
-  const uint32_t scp = upper ? ((c16 & 0x0F0Fu) | ((a16 >> 2) & 0x3030u)) : (a16 & 0x3F3Fu);
-  const uint32_t mp = upper ? (((c16 >> 4) & 0x0F0Fu) | ((b16 >> 2) & 0x3030u)) : (b16 & 0x3F3Fu);
-  const float2 dd = half_pair(h.x);
-  return make_float4(dd.x * byte_to_float(scp, 0), (dd.x * 0.0625f) * byte_to_float(scp, 1),
-                     dd.y * byte_to_float(mp, 0), dd.y * byte_to_float(mp, 1));
-}
 
 // x of one 32-weight sub-block as three int8 planes: with s = max|x| / 127,
 // x = s * (x1 + x2 / 128 + x3 / 16384) + e, |e| <= max|x| / (127 * 32768).
@@ -535,6 +524,33 @@ __device__ __forceinline__ float dot3_value(const Dot3& d, float scale) {
   const float v = fmaf(i2f_small(d.a3), 1.0f / 16384.0f,
                        fmaf(i2f_small(d.a2), 1.0f / 128.0f, i2f_small(d.a1)));
   return v * scale;
+}
+
+// The same for the one-token Q4_K kernel, with the plane products combined
+// in 32-bit integers first and rounded to fp32 once (relative error 2^-24):
+// 2^14 (x1 + x2/2^7 + x3/2^14) for the low nibbles (exact: |a1| <= 32*127*15,
+// so the sum stays below 2^30); the high nibbles enter in place as 16 q, so
+// every product is a multiple of 16 and 2^14 (x1 + ...) / 16 = a1*2^10 +
+// a2*2^3 + a3/2^4 is exact too.  Both are 2^14 times the plane sum; the
+// 2^-14 rides in the row coefficients (q4_coeffs).
+__device__ __forceinline__ float dot3_lo_int(const Dot3& d, float scale) {
+  return __int2float_rn(d.a1 * 16384 + d.a2 * 128 + d.a3) * scale;
+}
+__device__ __forceinline__ float dot3_hi_int(const Dot3& d, float scale) {
+  return __int2float_rn(d.a1 * 1024 + d.a2 * 8 + (d.a3 >> 4)) * scale;
+}
+
+// Group coefficients from a header for sub-blocks 2g, 2g+1, with the 2^-14
+// of dot3_lo_int / dot3_hi_int: (d sc_lo 2^-14, d sc_hi 2^-14, dmin m_lo,
+// dmin m_hi); no underflow (d >= 2^-24 and sc >= 1 when it is non-zero).
+__device__ __forceinline__ float4 q4_coeffs(const uint4& h, int sh, bool upper) {
+  const uint32_t a16 = h.y >> sh, b16 = h.z >> sh, c16 = h.w >> sh;
+  const uint32_t scp = upper ? ((c16 & 0x0F0Fu) | ((a16 >> 2) & 0x3030u)) : (a16 & 0x3F3Fu);
+  const uint32_t mp = upper ? (((c16 >> 4) & 0x0F0Fu) | ((b16 >> 2) & 0x3030u)) : (b16 & 0x3F3Fu);
+  const float2 dd = half_pair(h.x);
+  const float d14 = dd.x * (1.0f / 16384.0f);
+  return make_float4(d14 * byte_to_float(scp, 0), d14 * byte_to_float(scp, 1),
+                     dd.y * byte_to_float(mp, 0), dd.y * byte_to_float(mp, 1));
 }
 
 // Two rows' 64-weight dot products (integer path), interleaved.
@@ -566,8 +582,8 @@ __device__ __forceinline__ float2 q4_group_dot2i(const uint8_t* r0, const uint8_
     g1.a3 = dp4a_us(hi1, xh.p3[w], g1.a3);
   }
   const float4 c0 = q4_coeffs(h0, sh, upper), c1 = q4_coeffs(h1, sh, upper);
-  const float dl0 = dot3_value(l0, xl.scale), dh0 = dot3_value(g0, xh.scale);
-  const float dl1 = dot3_value(l1, xl.scale), dh1 = dot3_value(g1, xh.scale);
+  const float dl0 = dot3_lo_int(l0, xl.scale), dh0 = dot3_hi_int(g0, xh.scale);
+  const float dl1 = dot3_lo_int(l1, xl.scale), dh1 = dot3_hi_int(g1, xh.scale);
   float p0 = c0.x * dl0;
   p0 = fmaf(c0.y, dh0, p0);
   p0 = fmaf(-c0.z, xl.sum, p0);
