@@ -489,13 +489,13 @@ def run_gpu(args, world, rank, local):
         "act_cache": st.ctx.stats(),
     }
     if rank == 0 and not args.no_cpu_baseline and world == 1:
-        f, s = OracleSample(args.ref_rows).run()
+        f, s = OracleSample(args.cpu_rows).run()
         nb, sg = oracle_gemv_sample()
         line["cpu_baseline"] = {
             "value": f / s / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
             "sample": "%d token rows of the M=2048 prefill through the 7 linears of "
                       "layer 0 (quant + exact FP8 dot products); GEMV: one layer at "
-                      "M=1 in fp64" % args.ref_rows,
+                      "M=1 in fp64" % args.cpu_rows,
             "seconds": s, "gemv_gbs": nb / sg / 1e9, "gemv_seconds": sg}
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -812,7 +812,10 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--ref-rows", type=int, default=16)
+    ap.add_argument("--ref-rows", type=int, default=16,
+                    help="token rows per step of the reference arm's oracle sample")
+    ap.add_argument("--cpu-rows", type=int, default=64,
+                    help="token rows of the cpu_baseline oracle sample (about 10 s)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the end-to-end leg (profiling runs only)")
