@@ -59,7 +59,7 @@ rq_status launch_act_quant_fused(const float* x, int64_t n, int64_t n_out,
                                  cudaStream_t st);
 // Two kernels, no zeroing: per-CTA partial maxima into `slots` (at least
 // act_quant_slots() words), then the encoding, which reduces the slots and
-// walks x backwards (its last-read part is still in L2).
+// walks x backwards (what the first pass read last may still be in L2).
 int act_quant_slots();
 rq_status launch_act_quant_two_pass(const float* x, int64_t n, int64_t n_out, uint8_t* out,
                                     uint32_t* slots, uint32_t* absmax_out,

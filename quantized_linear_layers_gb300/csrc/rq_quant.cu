@@ -6,6 +6,8 @@
 // F32_TO_E4M3_DEVICE_SCALED_PTX (scale read from device memory, thread 0
 // writes absmax/448).  Both are HBM-bound streaming kernels: 16-byte loads,
 // grid sized to a multiple of the SM count, grid-stride loops.
+#include <cstdlib>
+
 #include "rq_device.cuh"
 #include "rq_internal.h"
 
@@ -229,18 +231,13 @@ int64_t fused_chunk(int64_t n) {
 // For the activation cache: absmax_slots_kernel writes each CTA's partial
 // maximum to its own slot (no zeroing and no atomics needed), and
 // quant_slots_kernel reduces the slots at its start and then encodes the
-// tensor walking it backwards, so that the part of x the first pass read
-// last (still in L2, 129 MB) is read first.  Same arithmetic as
-// absmax_kernel + quant_kernel, hence the same bytes.
+// tensor walking it backwards, so that whatever of x the first pass left in
+// L2 (what it read last) is read first.  Same arithmetic as absmax_kernel +
+// quant_kernel, hence the same bytes.
 
 constexpr int kSlotUnroll = 4;  // float4 loads in flight per thread
 
 // L2 eviction priorities as cache policies for the loads below.
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -256,8 +253,7 @@ __device__ __forceinline__ float4 ldg_f4_policy(const float4* p, uint64_t pol) {
 
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads)
-absmax_slots_kernel(const float* __restrict__ x, int64_t n, uint32_t* __restrict__ slots,
-                    int64_t keep_from4) {
+absmax_slots_kernel(const float* __restrict__ x, int64_t n, uint32_t* __restrict__ slots) {
   pdl_wait();
   pdl_trigger();
   uint32_t m = 0;
@@ -265,15 +261,15 @@ absmax_slots_kernel(const float* __restrict__ x, int64_t n, uint32_t* __restrict
   const int64_t nthreads = (int64_t)gridDim.x * kThreads;
   int64_t done = 0;
   if (VEC) {
-    // float4s from keep_from4 on are read with L2 priority evict_last: the
-    // encoder reads them again first
-    const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
+    // streamed with L2 priority evict_first (measured on GB300: asking L2
+    // to keep the tail of x for the encoder with evict_last made the pair
+    // of kernels slower, 55.4 -> 57.1 us at 2048 x 18944)
+    const uint64_t pol = l2_policy_evict_first();
     const float4* x4 = reinterpret_cast<const float4*>(x);
     const int64_t n4 = n >> 2;
     int64_t i = tid;
     for (; i + (kSlotUnroll - 1) * nthreads < n4; i += kSlotUnroll * nthreads) {
       float4 v[kSlotUnroll];
-      const uint64_t pol = i >= keep_from4 ? keep : stream;
 #pragma unroll
       for (int u = 0; u < kSlotUnroll; ++u) v[u] = ldg_f4_policy(x4 + i + u * nthreads, pol);
 #pragma unroll
@@ -398,14 +394,8 @@ rq_status launch_act_quant_two_pass(const float* x, int64_t n, int64_t n_out, ui
   const int nslots = act_quant_slots();
   int g1 = grid_for(vec ? (n + 3) / 4 : n);
   if (g1 > nslots) g1 = nslots;
-  // the last ~80 MB of x stay in L2 (129 MB) for the encoder's first reads
-  const int64_t n4 = n / 4;
-  int64_t keep_from4 = n4 - (int64_t)(80ll << 20) / 16;
-  if (keep_from4 < 0) keep_from4 = 0;
-  rq_status s = vec ? launch_kernel(absmax_slots_kernel<true>, g1, kThreads, 0, st, x, n, slots,
-                                    keep_from4)
-                    : launch_kernel(absmax_slots_kernel<false>, g1, kThreads, 0, st, x, n, slots,
-                                    keep_from4);
+  rq_status s = vec ? launch_kernel(absmax_slots_kernel<true>, g1, kThreads, 0, st, x, n, slots)
+                    : launch_kernel(absmax_slots_kernel<false>, g1, kThreads, 0, st, x, n, slots);
   if (s != RQ_OK) return s;
   const int g2 = grid_for(vec ? (n_out + 3) / 4 : n_out);
   if (vec)
