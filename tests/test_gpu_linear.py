@@ -134,7 +134,7 @@ def oracle_act_bytes(x, M, K):
 
 @pytest.mark.parametrize("one_pass", ["1", "0"])
 @pytest.mark.parametrize("M,K", [(2048, 3584), (611, 1024), (37, 3584), (5, 256),
-                                 (16, 128), (3, 4101), (2048, 18944)])
+                                 (16, 128), (3, 4101), (2048, 18944), (1001, 18947)])
 def test_activation_cache_bytes_bit_exact(rq, monkeypatch, one_pass, M, K):
     """The FP8 activation (one-pass kernel or absmax + quant kernels) is the
     oracle's bytes, pad rows zero, over three successive misses with
