@@ -501,6 +501,19 @@ def run_gpu(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def gemm_code_sha256(path):
+    """SHA-256 of a CUDA source with its comments and blank space removed, so
+    that the record of a kernel's DRAM traffic survives comment edits but
+    not code changes."""
+    import re
+    with open(path) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    text = " ".join(text.split())
+    return hashlib.sha256(text.encode()).hexdigest()
+
+
 def gemm_traffic_per_launch():
     """DRAM bytes per GEMM launch (stack average) from the committed ncu
     summary, if it was taken on the current kernel source (else None)."""
@@ -514,9 +527,7 @@ def gemm_traffic_per_launch():
             if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 rec[k.strip()] = v.strip()
-    with open(src, "rb") as f:
-        h = hashlib.sha256(f.read()).hexdigest()
-    if rec.get("kernel_source_sha256") != h:
+    if rec.get("kernel_code_sha256") != gemm_code_sha256(src):
         return None
     return int(rec["traffic_bytes_per_launch"])
 

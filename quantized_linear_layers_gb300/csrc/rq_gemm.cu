@@ -11,7 +11,8 @@
 //
 // Roles (192 threads, one CTA per SM, persistent over output tiles):
 //   warp 0      TMA producer: 128 x 128 B tiles of W and BN x 128 B tiles of
-//               X (SWIZZLE_128B) into a 4-stage shared-memory ring;
+//               X (SWIZZLE_128B) into a shared-memory ring (4 stages by
+//               default; RQ_GEMM_STAGES sets another depth for tuning);
 //   warp 1      allocates TMEM, and one thread issues tcgen05.mma
 //               (kind::f8f6f4, E4M3 x E4M3 -> f32, M = 128, N = BN, K = 32)
 //               into one of two TMEM accumulators (2 x BN columns);
@@ -332,6 +333,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
 
 constexpr int kStages2 = 6;  // default ring depth, pair kernel
 constexpr int kBHalfMax = kMaxBN / 2 * kBK;  // 16 KB: this CTA's half of B
+// the most shared memory the pair kernel takes by default (occupancy query)
 constexpr int kSmemBytes2 = kStages2 * (kABytes + kBHalfMax) + 1024 + 1024;
 
 __device__ __forceinline__ uint32_t cluster_rank() {
