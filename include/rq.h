@@ -224,10 +224,10 @@ rq_status rq_linear(rq_ctx *ctx, rq_qtype qtype, const void *w, const float *x,
  * (activation cache) and the group is one GEMM launch over the members'
  * FP8 weights, cached once per group contiguously by rows (member i keeps
  * its own per-tensor scale; its bytes equal rq_fp8_weight_cache's).  On
- * the GEMV route a single token's Q4_K members are one launch (one pass of
- * x), joined in that launch by the group's Q6_K member when it has exactly
- * one (the CTAs split between the two formats); other members are launched
- * one by one.  Results are those of count rq_linear calls within the same
+ * the GEMV route the Q4_K members are one launch (one pass of x) for up to
+ * 8 tokens; for a single token the group's Q6_K member joins that launch
+ * when it has exactly one (the CTAs split between the two formats); other
+ * members are launched one by one.  Results are those of count rq_linear calls within the same
  * tolerances.
  *   count: 1 .. RQ_MAX_GROUP.  qtypes, w, y, N: host arrays of count
  *   entries (w[i], y[i] device pointers as for rq_linear).  All members

@@ -446,17 +446,18 @@ rq_status rq_linear_group(rq_ctx* ctx, int count, const rq_qtype* qtypes, const 
   if (count == 1) return rq_linear(ctx, qtypes[0], w[0], x, y[0], M, N[0], K, stream);
 
   if (M < ctx->threshold) {
-    // GEMV route: one launch for a single token's Q4_K members
-    int starts[RQ_MAX_GROUP + 1];
+    // GEMV route: one launch for the Q4_K members of up to 8 tokens
+    int starts[RQ_MAX_GROUP + 1], ns[RQ_MAX_GROUP];
     const uint8_t* ws[RQ_MAX_GROUP];
     float* ys[RQ_MAX_GROUP];
     int n4 = 0;
     starts[0] = 0;
-    if (M == 1) {
+    if (M <= 8) {
       for (int i = 0; i < count; ++i)
         if (qtypes[i] == RQ_Q4K) {
           ws[n4] = static_cast<const uint8_t*>(w[i]);
           ys[n4] = y[i];
+          ns[n4] = N[i];
           starts[n4 + 1] = starts[n4] + N[i];
           ++n4;
         }
@@ -477,9 +478,17 @@ rq_status rq_linear_group(rq_ctx* ctx, int count, const rq_qtype* qtypes, const 
       if (s != RQ_OK && s != RQ_ERR_SHAPE) return s;
       grouped = dual = s == RQ_OK;
     }
-    if (!grouped && n4 >= 2) {
+    if (!grouped && n4 >= 2 && M == 1) {
       TraceScope ts(ctx, RQ_TRACE_GEMV, st);
       const rq_status s = launch_q4k_gemv_group(n4, starts, ws, ys, x, K, st);
+      if (s != RQ_OK && s != RQ_ERR_SHAPE) return s;
+      grouped = s == RQ_OK;
+    }
+    if (!grouped && n4 >= 2 && M >= 2 && std::getenv("RQ_GEMV_NO_MMA") == nullptr) {
+      // RQ_ERR_SHAPE: the shape does not fit the tensor-core kernel and
+      // nothing was launched (the members then run one by one)
+      TraceScope ts(ctx, RQ_TRACE_GEMV, st);
+      const rq_status s = launch_q4k_gemv_mma_group(n4, ws, ns, ys, x, M, K, st);
       if (s != RQ_OK && s != RQ_ERR_SHAPE) return s;
       grouped = s == RQ_OK;
     }

@@ -66,19 +66,45 @@ constexpr int kMaxSlice = 15;   // super-blocks per K-slice (compute warps); wit
 constexpr int kMaxKs = 8;       // K-slices per cluster
 constexpr int kTok = 8;         // MMA N: tokens (M <= 8, padded with zeros)
 
+// The weights of one launch: `nseg` members that share x, member i owning
+// tiles [tile_start[i], tile_start[i+1]) of the launch's 16-row tiles (its
+// N_i rows, padded to whole tiles) and writing y_i [M x N_i].
 struct FtArgs {
   const float* x;
-  float* y;
-  int M, N, K;
+  int M, K;
+  int nseg;
+  int tile_start[RQ_MAX_GROUP + 1];
+  int seg_n[RQ_MAX_GROUP];
+  float* seg_y[RQ_MAX_GROUP];
   int nsb;         // super-blocks per row (K / 256)
   int S;           // super-blocks per K-slice = compute warps per CTA
-  int tiles;       // 16-row tiles, ceil(N / 16)
+  int tiles;       // 16-row tiles of all members
   int clusters;
   int stages;
   int max_tiles;   // most tiles any cluster owns (accumulator rows / 16)
   int perm;        // 1: spread a half-warp's four rows over distinct banks
   uint64_t wait_limit_ns;
 };
+
+// One 3-D tensor map per member (box: 16 rows x S super-blocks x 144 B).
+struct FtMaps {
+  CUtensorMap m[RQ_MAX_GROUP];
+};
+
+__device__ __forceinline__ int ft_seg(const FtArgs& a, int tile) {
+  int i = 0;
+  while (i + 1 < a.nseg && tile >= a.tile_start[i + 1]) ++i;
+  return i;
+}
+
+// Output element (token m, row `row` of the launch's tile rows): its member's
+// y and row, or nullptr for a padding row past the member's N.
+__device__ __forceinline__ float* ft_out(const FtArgs& a, int m, int row) {
+  const int t = row / kTileRows;
+  const int sg = ft_seg(a, t);
+  const int r = (t - a.tile_start[sg]) * kTileRows + row % kTileRows;
+  return r < a.seg_n[sg] ? a.seg_y[sg] + (size_t)m * a.seg_n[sg] + r : nullptr;
+}
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int c0, int c1, int c2) {
@@ -185,7 +211,7 @@ __device__ __forceinline__ uint32_t q4_min_pair(const uint4& h, int g) {
 // and the hi and lo halves take one MMA each.
 template <bool PACK>
 __global__ void __launch_bounds__((kMaxSlice + 1) * 32, 1)
-q4k_gemv_ft_kernel(const __grid_constant__ CUtensorMap tmap, const FtArgs a) {
+q4k_gemv_ft_kernel(const __grid_constant__ FtMaps maps, const __grid_constant__ FtArgs a) {
   extern __shared__ __align__(128) uint8_t smem_ft[];
   const int S = a.S;
   const uint32_t stage_bytes = (uint32_t)(kTileRows * S * kQ4KBytes);
@@ -220,11 +246,15 @@ q4k_gemv_ft_kernel(const __grid_constant__ CUtensorMap tmap, const FtArgs a) {
   uint32_t issued = 0, parity_bits = 0;
   const bool producer = warp == S && lane == 0;
   const int first = ntiles < a.stages ? ntiles : a.stages;
+  auto load_tile = [&](int it, int s) {
+    const int t = t0 + it, sg = ft_seg(a, t);
+    tma_load_3d(smem_u32(ring + (size_t)s * stage_bytes), &maps.m[sg], full0 + 8 * s, 0, sb0,
+                (t - a.tile_start[sg]) * kTileRows);
+  };
   if (producer) {
     for (int it = 0; it < first; ++it) {
       mbar_arrive_expect_tx(full0 + 8 * it, stage_bytes);
-      tma_load_3d(smem_u32(ring + (size_t)it * stage_bytes), &tmap, full0 + 8 * it, 0, sb0,
-                  (t0 + it) * kTileRows);
+      load_tile(it, it);
       issued |= 1u << it;
     }
   }
@@ -237,8 +267,7 @@ q4k_gemv_ft_kernel(const __grid_constant__ CUtensorMap tmap, const FtArgs a) {
         const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
         if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, a.wait_limit_ns, &g_ft_error)) break;
         mbar_arrive_expect_tx(full0 + 8 * s, stage_bytes);
-        tma_load_3d(smem_u32(ring + (size_t)s * stage_bytes), &tmap, full0 + 8 * s, 0, sb0,
-                    (t0 + it) * kTileRows);
+        load_tile(it, s);
         issued |= 1u << s;
         parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
       }
@@ -414,11 +443,12 @@ q4k_gemv_ft_kernel(const __grid_constant__ CUtensorMap tmap, const FtArgs a) {
   __syncthreads();
 
   const int r0 = t0 * kTileRows;
-  const int rows = min(t1 * kTileRows, a.N) - r0;
+  const int rows = (t1 - t0) * kTileRows;
   if (ks == 1) {
     for (int i = threadIdx.x; i < rows * a.M; i += blockDim.x) {
       const int m = i / rows, row = i % rows;
-      a.y[(size_t)m * a.N + r0 + row] = acc[row * kTok + m];
+      float* out = ft_out(a, m, r0 + row);
+      if (out != nullptr) *out = acc[row * kTok + m];
     }
     return;
   }
@@ -431,7 +461,8 @@ q4k_gemv_ft_kernel(const __grid_constant__ CUtensorMap tmap, const FtArgs a) {
     const float* p = acc + row * kTok + m;
     float v = 0.f;
     for (int r = 0; r < ks; ++r) v += ld_cluster_f32(p, (uint32_t)r);
-    a.y[(size_t)m * a.N + r0 + row] = v;
+    float* out = ft_out(a, m, r0 + row);
+    if (out != nullptr) *out = v;
   }
   cluster_sync();  // no CTA leaves while a peer may still read its memory
 }
@@ -513,12 +544,16 @@ int resident_clusters(int ks, int threads, size_t smem) {
 
 }  // namespace
 
-rq_status launch_q4k_gemv_mma(const uint8_t* w, const float* x, float* y, int M, int N, int K,
-                              cudaStream_t st) {
-  if (M < 2 || M > kTok) return RQ_ERR_SHAPE;
+rq_status launch_q4k_gemv_mma_group(int count, const uint8_t* const* ws, const int* Ns,
+                                    float* const* ys, const float* x, int M, int K,
+                                    cudaStream_t st) {
+  if (M < 2 || M > kTok || count < 1 || count > RQ_MAX_GROUP) return RQ_ERR_SHAPE;
   const int nsb = K / kQK;
   const int sms = device_sm_count();
-  const int tiles = (N + kTileRows - 1) / kTileRows;
+  int tile_start[RQ_MAX_GROUP + 1];
+  tile_start[0] = 0;
+  for (int i = 0; i < count; ++i) tile_start[i + 1] = tile_start[i] + (Ns[i] + kTileRows - 1) / kTileRows;
+  const int tiles = tile_start[count];
   const int ks_min = (nsb + kMaxSlice - 1) / kMaxSlice;
   if (ks_min > kMaxKs) return RQ_ERR_SHAPE;
   int ks = ks_min;
@@ -565,15 +600,24 @@ rq_status launch_q4k_gemv_mma(const uint8_t* w, const float* x, float* y, int M,
   }
   if (stages < 2 || clusters < 1) return RQ_ERR_SHAPE;
   const size_t smem = ft_smem(S, stages, max_tiles);
-  const CUtensorMap* map = weight_map(w, N, K, S);
-  if (map == nullptr) return RQ_ERR_CUDA;
+  FtMaps maps;
+  for (int i = 0; i < RQ_MAX_GROUP; ++i) {
+    const int j = i < count ? i : 0;
+    const CUtensorMap* map = weight_map(ws[j], Ns[j], K, S);
+    if (map == nullptr) return RQ_ERR_CUDA;
+    maps.m[i] = *map;
+  }
 
   FtArgs a;
   a.x = x;
-  a.y = y;
   a.M = M;
-  a.N = N;
   a.K = K;
+  a.nseg = count;
+  for (int i = 0; i <= RQ_MAX_GROUP; ++i) a.tile_start[i] = tile_start[i <= count ? i : count];
+  for (int i = 0; i < RQ_MAX_GROUP; ++i) {
+    a.seg_n[i] = i < count ? Ns[i] : 0;
+    a.seg_y[i] = i < count ? ys[i] : nullptr;
+  }
   a.nsb = nsb;
   a.S = S;
   a.tiles = tiles;
@@ -598,8 +642,13 @@ rq_status launch_q4k_gemv_mma(const uint8_t* w, const float* x, float* y, int M,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_enabled() ? 2 : 1;
-  if (M <= 4) return cuda_status(cudaLaunchKernelEx(&cfg, q4k_gemv_ft_kernel<true>, *map, a));
-  return cuda_status(cudaLaunchKernelEx(&cfg, q4k_gemv_ft_kernel<false>, *map, a));
+  if (M <= 4) return cuda_status(cudaLaunchKernelEx(&cfg, q4k_gemv_ft_kernel<true>, maps, a));
+  return cuda_status(cudaLaunchKernelEx(&cfg, q4k_gemv_ft_kernel<false>, maps, a));
+}
+
+rq_status launch_q4k_gemv_mma(const uint8_t* w, const float* x, float* y, int M, int N, int K,
+                              cudaStream_t st) {
+  return launch_q4k_gemv_mma_group(1, &w, &N, &y, x, M, K, st);
 }
 
 rq_status read_and_clear_gemv_mma_error() {

@@ -91,6 +91,11 @@ rq_status read_and_clear_gemv_error();
 // launched) when the shape does not fit the kernel.
 rq_status launch_q4k_gemv_mma(const uint8_t* w, const float* x, float* y, int M, int N, int K,
                               cudaStream_t st);
+// The same for several Q4_K weights that share x (member i: ws[i] with Ns[i]
+// rows into ys[i] [M x Ns[i]]) in one launch.
+rq_status launch_q4k_gemv_mma_group(int count, const uint8_t* const* ws, const int* Ns,
+                                    float* const* ys, const float* x, int M, int K,
+                                    cudaStream_t st);
 rq_status read_and_clear_gemv_mma_error();
 
 // rq_wcache.cu --------------------------------------------------------------

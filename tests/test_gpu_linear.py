@@ -216,7 +216,7 @@ def test_trace_kinds_mask(rq):
     ctx.close()
 
 
-@pytest.mark.parametrize("M", [1, 2, 64, 300])
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 8, 64, 300])
 def test_linear_group_matches_separate_linears(rq, M):
     """rq_linear_group over members that share x (ragged N, both formats,
     rows straddling 128-row tiles and GEMV stages) gives each member what
@@ -309,6 +309,30 @@ def test_linear_group_mixed_formats_ragged(rq, K, N4, N6):
     for (qt, N), W, y in zip(members, Ws, ys):
         ref, absdot = oracle.gemv(qt, W, x, N, K)
         assert gemv_ok(y.cpu().numpy(), ref, absdot)[0], (qt, N)
+    ctx.close()
+
+
+@pytest.mark.parametrize("M", [4, 8])
+def test_linear_group_decoder_shapes_few_tokens(rq, monkeypatch, M):
+    """q + k and gate + up of the decoder at a few tokens (GEMV route, the
+    threshold raised above M): each group's Q4_K members in one tensor-core
+    launch; sampled rows of every member against the oracle."""
+    K = 3584
+    ctx = rq.Context(gemm_threshold=9)
+    for seed, Ns in ((3, (3584, 512)), (4, (18944, 18944))):
+        Ws = [synthetic.q4k_matrix(460 + seed * 10 + i, N, K) for i, N in enumerate(Ns)]
+        x = synthetic.activation(480 + seed + M, M, K)
+        ys = [empty((M, N), torch.float32) for N in Ns]
+        ctx.rq_ctx_trace_kinds(list(ctx.TRACE_KINDS))
+        ctx.rq_ctx_trace_begin(16)
+        ctx.rq_linear_group([Q4K] * len(Ns), [to_dev(W) for W in Ws], to_dev(x), ys, list(Ns),
+                            M, K)
+        assert ctx.rq_ctx_trace_end()["gemv"][0] == 1
+        assert rq.rq_get_device_status() == 0
+        for W, y, N in zip(Ws, ys, Ns):
+            rows = np.array([0, 1, 15, 16, N // 2, N - 17, N - 16, N - 1])
+            ref, absdot = oracle.gemv_rows(Q4K, W, x, N, K, rows)
+            assert gemv_ok(y.cpu().numpy()[:, rows], ref, absdot)[0], (N, M)
     ctx.close()
 
 
