@@ -1565,7 +1565,8 @@ rq_status plan_q6k_m1(const uint8_t* w, const float* x, float* y, int M, int N, 
   if (grid <= 0) grid = ngrp < sms ? ngrp : sms;
   if (grid > ngrp) grid = ngrp;
   const int max_rows = (ngrp + grid - 1) / grid * ra;
-  const bool few_rows = max_rows <= 8;
+  // (a few-token launch keeps 16 warps: its x prologue scales with M)
+  const bool few_rows = max_rows <= 8 && M == 1;
   const int warps_per_cta = m1_knob("RQ_GEMV_WARPS", few_rows ? 8 : 16, 1, 16);
   int rpt = m1_knob("RQ_GEMV_RPT", few_rows ? 2 : 4, 2, 8);
   rpt = rpt >= 8 ? 8 : (rpt >= 4 ? 4 : 2);
