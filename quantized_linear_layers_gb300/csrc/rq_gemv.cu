@@ -19,6 +19,7 @@
 //    exactly; sum x*(0.5 + q*2^-p) - 0.5*sum x = 2^-p * sum x*q, so each
 //    weight costs one PRMT and one FFMA, and the 2^p is folded into d*sc.
 //  * fp32 accumulation, one warp-shuffle reduction per row.
+#include <cstdio>
 #include <cstdlib>
 #include <map>
 #include <utility>
@@ -1387,6 +1388,13 @@ int persistent_grid(KernelT kernel, size_t smem, int ngroups) {
   return want < cap ? (want < 1 ? 1 : want) : cap;
 }
 
+// RQ_GEMV_LOG: one line per GEMV launch on stderr naming the kernel chosen
+// (tuning runs and the tests that pin the choice for the decoder shapes).
+void gemv_log(const char* kernel, int M, int N, int K, int grid) {
+  if (std::getenv("RQ_GEMV_LOG") != nullptr)
+    std::fprintf(stderr, "rq_gemv: %s M=%d N=%d K=%d grid=%d\n", kernel, M, N, K, grid);
+}
+
 template <int M, int R>
 rq_status run_q4k(const uint8_t* w, const float* x, float* y, int N, int K,
                   cudaStream_t st) {
@@ -1402,6 +1410,7 @@ rq_status run_q4k(const uint8_t* w, const float* x, float* y, int N, int K,
   const int grid = persistent_grid(kern, smem, (N + R - 1) / R);
   // launched without programmatic serialization: measured on GB300, this
   // small persistent grid launched early slows its neighbours down
+  gemv_log("q4k_generic", M, N, K, grid);
   kern<<<grid, kThreads, smem, st>>>(w, x, y, N, K);
   return launch_status();
 }
@@ -1421,6 +1430,7 @@ rq_status run_q6k(const uint8_t* w, const float* x, float* y, int N, int K,
   const int grid = persistent_grid(kern, smem, (N + R - 1) / R);
   // launched without programmatic serialization: measured on GB300, this
   // small persistent grid launched early slows its neighbours down
+  gemv_log("q6k_generic", M, N, K, grid);
   kern<<<grid, kThreads, smem, st>>>(w, x, y, N, K);
   return launch_status();
 }
@@ -1531,6 +1541,7 @@ rq_status run_q4k_m1(int nseg, const int* starts, const uint8_t* const* ws, floa
   static size_t smem_set[3] = {48 * 1024, 48 * 1024, 48 * 1024};
   const rq_status sa = m1_allow_smem(kern, p.smem, smem_set[p.rpt == 8 ? 2 : (p.rpt == 4 ? 1 : 0)]);
   if (sa != RQ_OK) return sa;
+  gemv_log(p.a.ksplit == 1 ? "q4k_m1" : "q4k_m1_ksplit", 1, p.a.N, K, p.grid);
   if (p.a.ksplit == 1) return launch_kernel(kern, p.grid, p.threads, p.smem, st, p.a);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
@@ -1566,8 +1577,8 @@ rq_status plan_q6k_m1(const uint8_t* w, const float* x, float* y, int M, int N, 
   if (grid > ngrp) grid = ngrp;
   const int max_rows = (ngrp + grid - 1) / grid * ra;
   // (a few-token launch keeps 16 warps: its x prologue scales with M)
-  const bool few_rows = max_rows <= 8 && M == 1;
-  const int warps_per_cta = m1_knob("RQ_GEMV_WARPS", few_rows ? 8 : 16, 1, 16);
+  const bool few_rows = max_rows <= 8;
+  const int warps_per_cta = m1_knob("RQ_GEMV_WARPS", few_rows && M == 1 ? 8 : 16, 1, 16);
   int rpt = m1_knob("RQ_GEMV_RPT", few_rows ? 2 : 4, 2, 8);
   rpt = rpt >= 8 ? 8 : (rpt >= 4 ? 4 : 2);
   const int ring_kb = m1_knob("RQ_GEMV_RING_KB", 150, 16, 200);
@@ -1624,6 +1635,7 @@ rq_status run_q6k_m1(const uint8_t* w, const float* x, float* y, int M, int N, i
   const rq_status sa =
       m1_allow_smem(kern, p.smem, smem_set[M > 1 ? 3 : (p.rpt == 8 ? 2 : (p.rpt == 4 ? 1 : 0))]);
   if (sa != RQ_OK) return sa;
+  gemv_log(M > 1 ? "q6k_mt" : "q6k_m1", M, N, K, p.grid);
   return launch_kernel(kern, p.grid, p.threads, p.smem, st, p.a);
 }
 
@@ -1703,6 +1715,7 @@ rq_status launch_gemv_m1_dual(int count, const int* starts, const uint8_t* const
   static size_t smem_set[4] = {48 * 1024, 48 * 1024, 48 * 1024, 48 * 1024};
   s = m1_allow_smem(kern, smem, smem_set[(p4.rpt == 4 ? 2 : 0) + (p6.rpt == 4 ? 1 : 0)]);
   if (s != RQ_OK) return s;
+  gemv_log("dual_q4k_q6k_m1", 1, starts[count] + n6, K, p4.grid + p6.grid);
   return launch_kernel(kern, p4.grid + p6.grid, threads, smem, st, p4.a, p6.a, p4.grid);
 }
 

@@ -48,6 +48,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
+#include <cstdio>
 #include <cstdlib>
 #include <map>
 #include <tuple>
@@ -642,6 +643,9 @@ rq_status launch_q4k_gemv_mma_group(int count, const uint8_t* const* ws, const i
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_enabled() ? 2 : 1;
+  if (std::getenv("RQ_GEMV_LOG") != nullptr)
+    std::fprintf(stderr, "rq_gemv: q4k_ft M=%d N=%d K=%d grid=%d\n", M, tiles * kTileRows, K,
+                 clusters * ks);
   if (M <= 4) return cuda_status(cudaLaunchKernelEx(&cfg, q4k_gemv_ft_kernel<true>, maps, a));
   return cuda_status(cudaLaunchKernelEx(&cfg, q4k_gemv_ft_kernel<false>, maps, a));
 }

@@ -179,3 +179,21 @@ def test_one_token_q4k_rows_split_between_two_ctas(rq, monkeypatch, force, N, K)
     ref, absdot = oracle.gemv(Q4K, W, x, N, K)
     ok, worst = gemv_ok(got, ref, absdot)
     assert ok, "worst error / bound = %.3g" % worst
+
+
+@pytest.mark.parametrize("qtype,N,K,M,kernel", [
+    (Q4K, 3584, 3584, 1, "q4k_m1"), (Q4K, 18944, 3584, 1, "q4k_m1"),
+    (Q4K, 3584, 18944, 1, "q4k_m1_ksplit"), (Q6K, 512, 3584, 1, "q6k_m1"),
+    (Q4K, 3584, 3584, 4, "q4k_ft"), (Q4K, 3584, 18944, 8, "q4k_ft"),
+    (Q6K, 512, 3584, 4, "q6k_mt"), (Q6K, 512, 3584, 8, "q6k_mt")])
+def test_decoder_shapes_take_their_kernels(rq, monkeypatch, capfd, qtype, N, K, M, kernel):
+    """The decoder's shapes run on the kernels the measurements are for (a
+    shape that does not fit them falls back to the generic kernel, which
+    is correct but slow, so a silent fallback is a regression)."""
+    monkeypatch.setenv("RQ_GEMV_LOG", "1")
+    W = synthetic.weight_matrix(3000 + N + K, qtype, N, K)
+    x = synthetic.activation(3001 + M, M, K)
+    capfd.readouterr()
+    gpu_gemv(rq, qtype, W, x, N, K)
+    lines = [l for l in capfd.readouterr().err.splitlines() if l.startswith("rq_gemv:")]
+    assert len(lines) == 1 and lines[0].split()[1] == kernel, lines

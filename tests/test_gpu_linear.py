@@ -336,6 +336,26 @@ def test_linear_group_decoder_shapes_few_tokens(rq, monkeypatch, M):
     ctx.close()
 
 
+@pytest.mark.parametrize("M,kernels", [(1, ["dual_q4k_q6k_m1"]), (4, ["q4k_ft", "q6k_mt"])])
+def test_decoder_qkv_group_launches(rq, monkeypatch, capfd, M, kernels):
+    """q/k/v of the decoder as one group call: one launch for a token (the
+    Q4_K and Q6_K members share it), the grouped tensor-core launch plus the
+    Q6_K member's own at a few tokens."""
+    monkeypatch.setenv("RQ_GEMV_LOG", "1")
+    K = 3584
+    members = [(Q4K, 3584), (Q4K, 512), (Q6K, 512)]
+    Ws = [to_dev(synthetic.weight_matrix(3100 + i, qt, N, K)) for i, (qt, N) in enumerate(members)]
+    x = to_dev(synthetic.activation(3110 + M, M, K))
+    ys = [empty((M, N), torch.float32) for _, N in members]
+    ctx = rq.Context(gemm_threshold=9)
+    capfd.readouterr()
+    ctx.rq_linear_group([qt for qt, _ in members], Ws, x, ys, [N for _, N in members], M, K)
+    torch.cuda.synchronize()
+    got = [l.split()[1] for l in capfd.readouterr().err.splitlines() if l.startswith("rq_gemv:")]
+    assert got == kernels
+    ctx.close()
+
+
 def test_linear_group_rejects_bad_counts(rq):
     ctx = rq.Context()
     with pytest.raises(rq.RqError):
