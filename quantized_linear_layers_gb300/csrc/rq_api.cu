@@ -82,6 +82,7 @@ rq_status check_quant_shape(int qtype, int N, int K) {
 struct TraceSlot {
   cudaEvent_t start = nullptr, stop = nullptr;
   int kind = 0;
+  int kernels = 1;  // kernels launched between the two events
 };
 
 struct rq_ctx {
@@ -127,8 +128,13 @@ class TraceScope {
         ctx->trace_used < ctx->trace_cap) {
       slot_ = &ctx->trace[ctx->trace_used++];
       slot_->kind = kind;
+      slot_->kernels = 1;
       record(slot_->start, st_);
     }
+  }
+  // the scope launches n kernels (default 1)
+  void kernels(int n) {
+    if (slot_ != nullptr) slot_->kernels = n;
   }
   ~TraceScope() {
     if (slot_ != nullptr) record(slot_->stop, st_);
@@ -362,13 +368,19 @@ rq_status rq_fp8_act_cache(rq_ctx* ctx, const float* x, int M, int K,
       ctx->act_cap = need;
     }
     const int64_t n = (int64_t)M * K;
+    s = RQ_ERR_SHAPE;
     if (ctx->fused_ok && act_quant_fused_fits(x, n, ctx->act)) {
       TraceScope ts(ctx, RQ_TRACE_QUANT, st);
       s = launch_act_quant_fused(x, n, (int64_t)need, ctx->act, ctx->absmax, ctx->act_deq,
                                  ctx->fused, st);
-    } else {
+      if (s == RQ_ERR_SHAPE) ts.kernels(0);
+    }
+    // RQ_ERR_SHAPE from the one-pass launcher: its wave did not fit the GPU
+    // and nothing was launched
+    if (s == RQ_ERR_SHAPE) {
       // two kernels: per-CTA maxima into slots, then the encoding
       TraceScope ts(ctx, RQ_TRACE_QUANT, st);
+      ts.kernels(2);
       s = launch_act_quant_two_pass(x, n, (int64_t)need, ctx->act, ctx->slots, ctx->absmax,
                                     ctx->act_deq, st);
     }
@@ -416,6 +428,7 @@ rq_status rq_linear(rq_ctx* ctx, rq_qtype qtype, const void* w, const float* x, 
   {
     const bool miss = ctx->weights.find(WeightKey{w, (int)qtype, N, K}) == ctx->weights.end();
     TraceScope ts(miss ? ctx : nullptr, RQ_TRACE_WCACHE, st);
+    ts.kernels(2);  // decode + absmax, decode + encode
     s = rq_fp8_weight_cache(ctx, qtype, w, N, K, &wq, &wdeq, stream);
   }
   if (s != RQ_OK) return s;
@@ -523,6 +536,7 @@ rq_status rq_linear_group(rq_ctx* ctx, int count, const rq_qtype* qtypes, const 
     rq_status s = RQ_OK;
     {
       TraceScope ts(ctx, RQ_TRACE_WCACHE, st);
+      ts.kernels(2 * count);
       for (int i = 0; i < count && s == RQ_OK; ++i) {
         const uint8_t* wb = static_cast<const uint8_t*>(w[i]);
         s = cuda_status(cudaMemsetAsync(ctx->absmax, 0, sizeof(uint32_t), st));
@@ -588,7 +602,7 @@ rq_status rq_ctx_trace_end(rq_ctx* ctx, int64_t* counts_host, double* ms_host) {
       s = RQ_ERR_CUDA;
       continue;
     }
-    counts[t.kind] += 1;
+    counts[t.kind] += t.kernels;
     ms[t.kind] += e;
   }
   ctx->trace_on = false;
