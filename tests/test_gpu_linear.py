@@ -362,6 +362,33 @@ def test_decoder_qkv_group_launches(rq, monkeypatch, capfd, M, kernels):
     ctx.close()
 
 
+@pytest.mark.parametrize("M", [1, 3, 40])
+def test_linear_group_of_four_members(rq, M):
+    """RQ_MAX_GROUP members (Q4_K and Q6_K mixed, one of them twice): each
+    member's output against the oracle on the route M takes."""
+    K = 768
+    members = [(Q4K, 48), (Q6K, 33), (Q4K, 130), (Q4K, 48)]
+    Ws = [synthetic.weight_matrix(3200 + i, qt, N, K) for i, (qt, N) in enumerate(members[:3])]
+    Ws.append(Ws[0])
+    Wd = [to_dev(W) for W in Ws[:3]]
+    Wd.append(Wd[0])
+    x = synthetic.activation(3210 + M, M, K, outlier_frac=1e-3)
+    ys = [empty((M, N), torch.float32) for _, N in members]
+    ctx = rq.Context()
+    ctx.rq_linear_group([qt for qt, _ in members], Wd, to_dev(x), ys, [N for _, N in members],
+                        M, K)
+    torch.cuda.synchronize()
+    assert rq.rq_get_device_status() == 0
+    for (qt, N), W, y in zip(members, Ws, ys):
+        got = y.cpu().numpy()
+        if oracle.route_is_gemm(M, 4):
+            check_gemm(got, gemm_route_ref(qt, W, x, N, K))
+        else:
+            ref, absdot = oracle.gemv(qt, W, x, N, K)
+            assert gemv_ok(got, ref, absdot)[0]
+    ctx.close()
+
+
 def test_linear_group_rejects_bad_counts(rq):
     ctx = rq.Context()
     with pytest.raises(rq.RqError):
