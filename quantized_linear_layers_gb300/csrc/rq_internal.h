@@ -48,10 +48,12 @@ rq_status launch_quant(const float* x, int64_t n, int64_t n_out,
                        const uint32_t* absmax_bits, uint8_t* out,
                        float* dequant_out, cudaStream_t st);
 
-// One-pass absmax + encode (one cooperative wave, tensor staged in shared
-// memory).  Needs x 16-byte and out 4-byte aligned and n small enough for
-// one wave; `state` is 4 device words, zero before the first launch and
-// used by one stream at a time.  absmax_out / dequant_out may be null.
+// Absmax + encode in one cooperative wave (each CTA's chunk staged in shared
+// memory as far as it fits, the rest, at most 64 MB in all, read twice).
+// Needs x 16-byte and out 4-byte aligned; RQ_ERR_SHAPE (nothing launched) if
+// the wave does not fit the GPU.  `state` is 4 device words, zero before the
+// first launch and used by one stream at a time.  absmax_out / dequant_out
+// may be null.
 bool act_quant_fused_fits(const float* x, int64_t n, const uint8_t* out);
 rq_status launch_act_quant_fused(const float* x, int64_t n, int64_t n_out,
                                  uint8_t* out, uint32_t* absmax_out,

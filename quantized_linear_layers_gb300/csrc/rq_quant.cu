@@ -6,6 +6,7 @@
 // F32_TO_E4M3_DEVICE_SCALED_PTX (scale read from device memory, thread 0
 // writes absmax/448).  Both are HBM-bound streaming kernels: 16-byte loads,
 // grid sized to a multiple of the SM count, grid-stride loops.
+#include <algorithm>
 #include <cstdlib>
 
 #include "rq_device.cuh"
@@ -109,11 +110,17 @@ quant_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
 
 // ------------------------------------------------------ one-pass variant --
 //
-// When the whole activation fits in the shared memory of one wave of CTAs
-// (one CTA per SM), it is read from HBM once: each CTA bulk-copies its chunk
-// into shared memory, reduces its max, all CTAs meet at a grid barrier that
-// publishes the tensor max, and each CTA encodes its chunk from shared memory.
-// Same arithmetic as absmax_kernel + quant_kernel, so the bytes are identical.
+// One wave of CTAs (one per SM), each owning a chunk of x.  A CTA keeps the
+// last `stash4` float4s of its chunk in shared memory (bulk copies) and
+// streams the rest, the head, through registers while the copies land,
+// reducing the max of both; all CTAs meet at a grid barrier that publishes
+// the tensor max; each CTA then encodes the head, read again newest lines
+// first (they are the likeliest to be in L2), and the stash from shared
+// memory.  When the chunks fit in shared memory (the activations of 2048
+// tokens x 3584) x is read from HBM once; the launcher takes this kernel
+// only while the heads are small enough to stay in L2 between the passes.
+// Same arithmetic as absmax_kernel + quant_kernel, so the bytes are
+// identical.
 //
 // state[0..1]: absmax words, used alternately by consecutive launches (the
 //              one for launch g is zero when it starts);
@@ -136,7 +143,7 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned int* p) {
 
 __global__ void __launch_bounds__(kFusedThreads, 1)
 act_quant_fused_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
-                       int64_t chunk, uint8_t* __restrict__ out,
+                       int64_t chunk, int64_t stash4, uint8_t* __restrict__ out,
                        uint32_t* __restrict__ absmax_out, float* __restrict__ dequant_out,
                        unsigned int* state) {
   extern __shared__ __align__(128) float4 stash[];
@@ -146,7 +153,10 @@ act_quant_fused_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
 
   const int64_t begin = (int64_t)blockIdx.x * chunk;
   const int64_t len = min(chunk, n - begin);
-  const int64_t cnt4 = len >> 2;  // float4s moved by the bulk copies
+  const int64_t cnt4 = len >> 2;               // whole float4s of the chunk
+  const int64_t s4 = min(cnt4, stash4);        // the last s4 of them: shared memory
+  const int64_t h4 = cnt4 - s4;                // the head: streamed twice
+  const float4* xb4 = reinterpret_cast<const float4*>(x + begin);
   const int tid = threadIdx.x;
 
   pdl_wait();
@@ -156,18 +166,27 @@ act_quant_fused_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
     for (int p = 0; p < kFusedParts; ++p) mbar_init(smem_u32(&bars[p]), 1);
     mbar_fence_init();
     for (int p = 0; p < kFusedParts; ++p) {
-      const int64_t lo = cnt4 * p / kFusedParts, hi = cnt4 * (p + 1) / kFusedParts;
+      const int64_t lo = s4 * p / kFusedParts, hi = s4 * (p + 1) / kFusedParts;
       const uint32_t bytes = (uint32_t)((hi - lo) * 16);
       mbar_arrive_expect_tx(smem_u32(&bars[p]), bytes);
-      if (bytes != 0) bulk_g2s(smem_u32(stash + lo), x + begin + 4 * lo, bytes, smem_u32(&bars[p]));
+      if (bytes != 0) bulk_g2s(smem_u32(stash + lo), xb4 + h4 + lo, bytes, smem_u32(&bars[p]));
     }
   }
   __syncthreads();
 
   uint32_t m = 0;
+  {
+    int64_t i = tid;
+    for (; i + 3 * kFusedThreads < h4; i += 4 * kFusedThreads) {
+      const float4 v0 = __ldg(xb4 + i), v1 = __ldg(xb4 + i + kFusedThreads);
+      const float4 v2 = __ldg(xb4 + i + 2 * kFusedThreads), v3 = __ldg(xb4 + i + 3 * kFusedThreads);
+      m = max4(max4(max4(max4(m, v0), v1), v2), v3);
+    }
+    for (; i < h4; i += kFusedThreads) m = max4(m, __ldg(xb4 + i));
+  }
   for (int p = 0; p < kFusedParts; ++p) {
     mbar_wait(smem_u32(&bars[p]), 0, kWaitLimitNs, &g_quant_error);
-    const int64_t lo = cnt4 * p / kFusedParts, hi = cnt4 * (p + 1) / kFusedParts;
+    const int64_t lo = s4 * p / kFusedParts, hi = s4 * (p + 1) / kFusedParts;
     for (int64_t i = lo + tid; i < hi; i += kFusedThreads) m = max4(m, stash[i]);
   }
   for (int64_t i = (cnt4 << 2) + tid; i < len; i += kFusedThreads)
@@ -211,7 +230,8 @@ act_quant_fused_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
     if (dequant_out != nullptr) *dequant_out = __fdiv_rn(a, 448.0f);
   }
   uint32_t* o4 = reinterpret_cast<uint32_t*>(out + begin);
-  for (int64_t i = tid; i < cnt4; i += kFusedThreads) o4[i] = pack4(stash[i], s);
+  for (int64_t i = h4 - 1 - tid; i >= 0; i -= kFusedThreads) o4[i] = pack4(__ldg(xb4 + i), s);
+  for (int64_t i = tid; i < s4; i += kFusedThreads) o4[h4 + i] = pack4(stash[i], s);
   for (int64_t i = (cnt4 << 2) + tid; i < len; i += kFusedThreads)
     out[begin + i] = (uint8_t)e4m3_scaled(__ldg(x + begin + i), s);
   const int64_t stride = (int64_t)gridDim.x * kFusedThreads;
@@ -405,10 +425,24 @@ rq_status launch_act_quant_two_pass(const float* x, int64_t n, int64_t n_out, ui
                        (const uint32_t*)slots, g1, out, absmax_out, dequant_out);
 }
 
+// Heads (the parts of the chunks beyond shared memory) up to this many bytes
+// in all: measured on GB300, the one kernel beats the two while its heads
+// stay in L2 between its passes (512 x 18944: 16.3 against 18.9 us) and
+// loses once they do not (2048 x 18944, 121 MB of heads: 62 against 55 us).
+constexpr int64_t kFusedHeadMax = 64ll << 20;
+
+int64_t fused_stash4(int64_t chunk) {
+  return std::min<int64_t>(chunk / 4, kFusedSmemMax / 16);
+}
+
 bool act_quant_fused_fits(const float* x, int64_t n, const uint8_t* out) {
-  return n > 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
-         (reinterpret_cast<uintptr_t>(out) & 3) == 0 &&
-         fused_chunk(n) * 4 <= kFusedSmemMax;
+  if (n <= 0 || (reinterpret_cast<uintptr_t>(x) & 15) != 0 ||
+      (reinterpret_cast<uintptr_t>(out) & 3) != 0)
+    return false;
+  const int64_t chunk = fused_chunk(n);
+  const int64_t grid = (n + chunk - 1) / chunk;
+  const int64_t head_bytes = 4 * n - 16 * grid * fused_stash4(chunk);
+  return head_bytes <= kFusedHeadMax;
 }
 
 rq_status launch_act_quant_fused(const float* x, int64_t n, int64_t n_out,
@@ -426,7 +460,8 @@ rq_status launch_act_quant_fused(const float* x, int64_t n, int64_t n_out,
   }
   int64_t chunk = fused_chunk(n);
   const int grid = (int)((n + chunk - 1) / chunk);
-  const size_t smem = (size_t)((chunk + 3) / 4) * 16;
+  const int64_t stash4 = fused_stash4(chunk);
+  const size_t smem = (size_t)stash4 * 16;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kFusedThreads);
@@ -440,7 +475,7 @@ rq_status launch_act_quant_fused(const float* x, int64_t n, int64_t n_out,
   cfg.attrs = attr;
   cfg.numAttrs = pdl_enabled() ? 2 : 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, act_quant_fused_kernel, x, n, n_out, chunk,
-                                           out, absmax_out, dequant_out, state);
+                                           stash4, out, absmax_out, dequant_out, state);
   if (e == cudaErrorCooperativeLaunchTooLarge) {
     cudaGetLastError();
     return RQ_ERR_SHAPE;
