@@ -45,6 +45,9 @@ constexpr int kMaxStages = 16;
 constexpr int kMaxBN = 256;
 constexpr int kMaxSegs = RQ_MAX_GROUP;  // members of a grouped launch
 constexpr int kThreads = 192;
+// pair kernel: producer, MMA issuer and 8 epilogue warps (two per TMEM lane
+// quarter, each storing half of the tile's token columns)
+constexpr int kThreadsPair = 320;
 constexpr int kABytes = kBM * kBK;           // 16 KB
 constexpr int kSmemLimit = 227 * 1024;  // dynamic shared memory a CTA may opt into
 
@@ -401,7 +404,7 @@ __device__ __forceinline__ void mma_commit_pair_local(uint32_t bar) {
       : "memory");
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPair, 1)
 fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
                      const __grid_constant__ CUtensorMap tmap_x, const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
@@ -437,7 +440,7 @@ fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull0 + 8 * b, 1);
-      mbar_init(tempty0 + 8 * b, 8);  // 4 epilogue warps x 2 CTAs (leader's is used)
+      mbar_init(tempty0 + 8 * b, 16);  // 8 epilogue warps x 2 CTAs (leader's is used)
     }
     mbar_init(done_bar, 1);
     mbar_fence_init();
@@ -527,7 +530,9 @@ fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
     }
   } else {
     // --------------------------------------------------- epilogue (both)
-    const int quad = warp & 3;
+    const int quad = warp & 3;                       // TMEM lanes 32*quad .. +31
+    const int c_lo = ((warp - 2) >> 2) * (bn >> 1);  // this warp's half of the columns
+    const int c_hi = c_lo + (bn >> 1);
     const float scale_x = *args.x_deq;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -544,7 +549,7 @@ fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
       float* yr = args.out.y[sg] + (n - args.out.start[sg]);
       const float scale_w = n < args.N ? *args.out.w_deq[sg] : 0.f;
       const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * bn);
-      for (int c = 0; c < bn; c += 16) {
+      for (int c = c_lo; c < c_hi; c += 16) {
         uint32_t v[16];
         tmem_ld16(taddr + (uint32_t)c, v);
         if (n < args.N) {
@@ -934,7 +939,7 @@ int resident_pairs(int sms) {
   if (cached == 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (sms / 2));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kThreadsPair);
     cfg.dynamicSmemBytes = kSmemBytes2;
     int n = 0;
     cudaFuncSetAttribute(fp8_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1102,7 +1107,7 @@ rq_status launch_fp8_gemm_group(const uint8_t* x_fp8, const float* x_deq,
     if (std::getenv("RQ_GEMM_LOG") != nullptr)
       std::fprintf(stderr, "rq_gemm: pair M=%d N=%d K=%d bn=%d tiles=%d grid=%d stages=%d\n", M,
                    N, K, bn, tiles, grid, a.stages);
-    return launch_kernel(fp8_gemm_pair_kernel, grid, kThreads,
+    return launch_kernel(fp8_gemm_pair_kernel, grid, kThreadsPair,
                          gemm_smem_bytes(a.stages, b_stride), st, tw, tx, a);
   }
   static bool attr_done = false;
