@@ -1162,8 +1162,14 @@ __global__ void __launch_bounds__(544, 1) gemv_m1_dual_kernel(const M1Args a4, c
 __global__ void __launch_bounds__(544, 1) q6k_gemv_mt_kernel(const M1Args a) {
   extern __shared__ __align__(128) uint8_t smem_q6t[];
   const int M = a.M;
-  const int nsb = a.K >> 8, U = nsb * 4, nsub16 = a.K >> 4;
-  const int rowbytes = nsb * kQ6KBytes;
+  // with ksplit CTAs per cluster, CTA rank h computes super-blocks
+  // [h*nsb, (h+1)*nsb) of every row (whole rows are staged; rank 0 adds the
+  // others' sums through distributed shared memory)
+  const int ks = a.ksplit;
+  const int h = ks > 1 ? (int)m1_cluster_rank() : 0;
+  const int nsb = (a.K >> 8) / ks, U = nsb * 4, nsub16 = nsb * 16;
+  const int sb0 = h * nsb;
+  const int rowbytes = (a.K >> 8) * kQ6KBytes;
   const int rps = a.rows_per_stage;
   const uint32_t stage_bytes = (uint32_t)(rps * rowbytes);
   uint8_t* ring = smem_q6t;
@@ -1178,8 +1184,9 @@ __global__ void __launch_bounds__(544, 1) q6k_gemv_mt_kernel(const M1Args a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ra = a.row_align;
   const int ngrp = (a.N + ra - 1) / ra;
-  const int r0 = min(a.N, (int)((int64_t)blockIdx.x * ngrp / gridDim.x) * ra);
-  const int r1 = min(a.N, (int)((int64_t)(blockIdx.x + 1) * ngrp / gridDim.x) * ra);
+  const int cb = (int)blockIdx.x / ks, ncb = (int)gridDim.x / ks;  // row block of the cluster
+  const int r0 = min(a.N, (int)((int64_t)cb * ngrp / ncb) * ra);
+  const int r1 = min(a.N, (int)((int64_t)(cb + 1) * ngrp / ncb) * ra);
   const int rows = r1 - r0;
   const int iters = (rows + rps - 1) / rps;
   const int first = iters < a.stages ? iters : a.stages;
@@ -1227,7 +1234,7 @@ __global__ void __launch_bounds__(544, 1) q6k_gemv_mt_kernel(const M1Args a) {
     for (int idx = warp * 16 + (lane >> 1); idx < M * nsub16; idx += compute_warps * 16) {
       const int m = idx / nsub16, s16 = idx - m * nsub16;
       const float4* px =
-          reinterpret_cast<const float4*>(a.x + (size_t)m * a.K + 16 * s16 + 8 * half);
+          reinterpret_cast<const float4*>(a.x + (size_t)m * a.K + 256 * sb0 + 16 * s16 + 8 * half);
       const float4 va = __ldg(px), vb = __ldg(px + 1);
       const float v[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
       float mx = 0.f, sm = 0.f;
@@ -1278,7 +1285,7 @@ __global__ void __launch_bounds__(544, 1) q6k_gemv_mt_kernel(const M1Args a) {
     const int u = wt * 32 + lane;
     const bool active = u < U;
     const int sb = u >> 2, hh = (u >> 1) & 1, lq = u & 1;
-    const int off = sb * kQ6KBytes;
+    const int off = (sb0 + sb) * kQ6KBytes;
     bool ok = true;
     for (int it = 0; it < iters && ok; ++it) {
       const int s = it % a.stages;
@@ -1356,10 +1363,15 @@ __global__ void __launch_bounds__(544, 1) q6k_gemv_mt_kernel(const M1Args a) {
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < rows * M; i += blockDim.x) {
-    const int row = i / M, m = i - row * M;
-    a.y[(size_t)m * a.N + r0 + row] = acc[i];
-  }
+  if (ks > 1) m1_cluster_sync();  // every rank's sums are in its acc
+  if (h == 0)
+    for (int i = threadIdx.x; i < rows * M; i += blockDim.x) {
+      const int row = i / M, m = i - row * M;
+      float v = acc[i];
+      for (int r = 1; r < ks; ++r) v += m1_ld_peer(acc + i, (uint32_t)r);
+      a.y[(size_t)m * a.N + r0 + row] = v;
+    }
+  if (ks > 1) m1_cluster_sync();  // no CTA leaves while rank 0 may read its memory
 }
 
 // ---------------------------------------------------------------- launch --
@@ -1566,21 +1578,33 @@ rq_status run_q4k_m1(int nseg, const int* starts, const uint8_t* const* ws, floa
 rq_status plan_q6k_m1(const uint8_t* w, const float* x, float* y, int M, int N, int K, int grid,
                       M1Plan* p) {
   if ((reinterpret_cast<uintptr_t>(w) & 15) != 0) return RQ_ERR_SHAPE;
-  const int nsb = K / kQK, U = nsb * 4, nsub16 = K / 16;
+  const int nsb = K / kQK;
   const int rowbytes = nsb * kQ6KBytes;
   int g = 1;
   while (g < 16 && rowbytes % (2 * g) == 0) g *= 2;  // gcd(rowbytes, 16)
   const int ra = 16 / g;
   const int sms = device_sm_count();
   const int ngrp = (N + ra - 1) / ra;
-  if (grid <= 0) grid = ngrp < sms ? ngrp : sms;
-  if (grid > ngrp) grid = ngrp;
-  const int max_rows = (ngrp + grid - 1) / grid * ra;
+  // launches of 6..8 tokens with fewer row groups than SMs split each row's
+  // super-blocks between the two CTAs of a cluster (each CTA builds the x
+  // planes of its half only; measured on the 512 x 3584 shape: 10.6 -> 9.9 us
+  // at 8 tokens, no gain at 4, a loss at 2); RQ_GEMV_Q6_KSPLIT=0 / 1 forces
+  // it off / on for 2..8 tokens
+  int ks = (M >= 6 && ngrp < sms) ? 2 : 1;
+  if (const char* e = std::getenv("RQ_GEMV_Q6_KSPLIT")) ks = std::atoi(e) != 0 ? 2 : 1;
+  if (M == 1 || nsb % 2 != 0 || sms < 2) ks = 1;
+  const int U = nsb / ks * 4, nsub16 = nsb / ks * 16;
+  if (grid <= 0) grid = ks * (ngrp < sms / ks ? ngrp : sms / ks);
+  if (grid > ks * ngrp) grid = ks * ngrp;
+  const int max_rows = (ngrp + grid / ks - 1) / (grid / ks) * ra;
   // (a few-token launch keeps 16 warps: its x prologue scales with M)
   const bool few_rows = max_rows <= 8;
   const int warps_per_cta = m1_knob("RQ_GEMV_WARPS", few_rows && M == 1 ? 8 : 16, 1, 16);
   int rpt = m1_knob("RQ_GEMV_RPT", few_rows ? 2 : 4, 2, 8);
   rpt = rpt >= 8 ? 8 : (rpt >= 4 ? 4 : 2);
+  // split rows: one row per team per stage, so that all warps (which build
+  // the x planes) fit next to a ring of whole rows
+  if (ks > 1) rpt = 1;
   const int ring_kb = m1_knob("RQ_GEMV_RING_KB", 150, 16, 200);
   const int max_stages = m1_knob("RQ_GEMV_STAGES", 8, 2, 16);
   M1Args& a = p->a;
@@ -1591,7 +1615,7 @@ rq_status plan_q6k_m1(const uint8_t* w, const float* x, float* y, int M, int N, 
   a.K = K;
   a.row_align = ra;
   a.M = M;
-  a.ksplit = 1;
+  a.ksplit = ks;
   a.nseg = 1;
   a.seg_start[0] = 0;
   for (int i = 1; i <= RQ_MAX_GROUP; ++i) a.seg_start[i] = N;
@@ -1635,8 +1659,23 @@ rq_status run_q6k_m1(const uint8_t* w, const float* x, float* y, int M, int N, i
   const rq_status sa =
       m1_allow_smem(kern, p.smem, smem_set[M > 1 ? 3 : (p.rpt == 8 ? 2 : (p.rpt == 4 ? 1 : 0))]);
   if (sa != RQ_OK) return sa;
-  gemv_log(M > 1 ? "q6k_mt" : "q6k_m1", M, N, K, p.grid);
-  return launch_kernel(kern, p.grid, p.threads, p.smem, st, p.a);
+  gemv_log(M > 1 ? (p.a.ksplit > 1 ? "q6k_mt_ksplit" : "q6k_mt") : "q6k_m1", M, N, K, p.grid);
+  if (p.a.ksplit == 1) return launch_kernel(kern, p.grid, p.threads, p.smem, st, p.a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(p.threads);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.a.ksplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, p.a));
 }
 
 }  // namespace

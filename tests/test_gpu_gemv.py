@@ -185,7 +185,7 @@ def test_one_token_q4k_rows_split_between_two_ctas(rq, monkeypatch, force, N, K)
     (Q4K, 3584, 3584, 1, "q4k_m1"), (Q4K, 18944, 3584, 1, "q4k_m1"),
     (Q4K, 3584, 18944, 1, "q4k_m1_ksplit"), (Q6K, 512, 3584, 1, "q6k_m1"),
     (Q4K, 3584, 3584, 4, "q4k_ft"), (Q4K, 3584, 18944, 8, "q4k_ft"),
-    (Q6K, 512, 3584, 4, "q6k_mt"), (Q6K, 512, 3584, 8, "q6k_mt")])
+    (Q6K, 512, 3584, 4, "q6k_mt"), (Q6K, 512, 3584, 8, "q6k_mt_ksplit")])
 def test_decoder_shapes_take_their_kernels(rq, monkeypatch, capfd, qtype, N, K, M, kernel):
     """The decoder's shapes run on the kernels the measurements are for (a
     shape that does not fit them falls back to the generic kernel, which
@@ -197,3 +197,20 @@ def test_decoder_shapes_take_their_kernels(rq, monkeypatch, capfd, qtype, N, K, 
     gpu_gemv(rq, qtype, W, x, N, K)
     lines = [l for l in capfd.readouterr().err.splitlines() if l.startswith("rq_gemv:")]
     assert len(lines) == 1 and lines[0].split()[1] == kernel, lines
+
+
+@pytest.mark.parametrize("force", ["", "1", "0"])
+@pytest.mark.parametrize("M", [2, 5, 8])
+@pytest.mark.parametrize("N,K", [(1, 512), (37, 1024), (512, 3584), (1001, 2048), (300, 18944)])
+def test_few_token_q6k_rows_split_between_two_ctas(rq, monkeypatch, force, M, N, K):
+    """A few tokens on Q6_K with each row's super-blocks split between the
+    two CTAs of a cluster (automatic when there are fewer row groups than
+    SMs, forced on or off otherwise): every output against the oracle."""
+    if force:
+        monkeypatch.setenv("RQ_GEMV_Q6_KSPLIT", force)
+    W = synthetic.q6k_matrix(3300 + N + K, N, K)
+    x = synthetic.activation(3301 + M + K, M, K, outlier_frac=1e-3)
+    got = gpu_gemv(rq, Q6K, W, x, N, K)
+    ref, absdot = oracle.gemv(Q6K, W, x, N, K)
+    ok, worst = gemv_ok(got, ref, absdot)
+    assert ok, "worst error / bound = %.3g" % worst

@@ -345,7 +345,8 @@ def test_linear_group_decoder_shapes_few_tokens(rq, monkeypatch, M):
     ctx.close()
 
 
-@pytest.mark.parametrize("M,kernels", [(1, ["dual_q4k_q6k_m1"]), (4, ["q4k_ft", "q6k_mt"])])
+@pytest.mark.parametrize("M,kernels", [(1, ["dual_q4k_q6k_m1"]), (4, ["q4k_ft", "q6k_mt"]),
+                                       (8, ["q4k_ft", "q6k_mt_ksplit"])])
 def test_decoder_qkv_group_launches(rq, monkeypatch, capfd, M, kernels):
     """q/k/v of the decoder as one group call: one launch for a token (the
     Q4_K and Q6_K members share it), the grouped tensor-core launch plus the
