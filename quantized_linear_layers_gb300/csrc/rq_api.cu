@@ -425,8 +425,8 @@ rq_status rq_linear(rq_ctx* ctx, rq_qtype qtype, const void* w, const float* x, 
 
   const uint8_t* wq = nullptr;
   const float* wdeq = nullptr;
+  const bool miss = ctx->weights.find(WeightKey{w, (int)qtype, N, K}) == ctx->weights.end();
   {
-    const bool miss = ctx->weights.find(WeightKey{w, (int)qtype, N, K}) == ctx->weights.end();
     TraceScope ts(miss ? ctx : nullptr, RQ_TRACE_WCACHE, st);
     ts.kernels(2);  // decode + absmax, decode + encode
     s = rq_fp8_weight_cache(ctx, qtype, w, N, K, &wq, &wdeq, stream);
@@ -438,7 +438,9 @@ rq_status rq_linear(rq_ctx* ctx, rq_qtype qtype, const void* w, const float* x, 
   s = rq_fp8_act_cache(ctx, x, M, K, &xq, &xdeq, stream);
   if (s != RQ_OK) return s;
   TraceScope ts(ctx, RQ_TRACE_GEMM, st);
-  return launch_fp8_gemm(xq, xdeq, wq, wdeq, y, M, N, K, st);
+  // a cached weight built by an earlier call was complete before the launch
+  // preceding this GEMM began, so its first tiles may load early
+  return launch_fp8_gemm(xq, xdeq, wq, wdeq, y, M, N, K, st, !miss);
 }
 
 rq_status rq_linear_group(rq_ctx* ctx, int count, const rq_qtype* qtypes, const void* const* w,
@@ -518,7 +520,8 @@ rq_status rq_linear_group(rq_ctx* ctx, int count, const rq_qtype* qtypes, const 
   std::vector<WeightKey> key;
   for (int i = 0; i < count; ++i) key.push_back(WeightKey{w[i], (int)qtypes[i], N[i], K});
   auto it = ctx->groups.find(key);
-  if (it == ctx->groups.end()) {
+  const bool hit = it != ctx->groups.end();
+  if (!hit) {
     GroupEntry e;
     e.starts[0] = 0;
     for (int i = 0; i < count; ++i) e.starts[i + 1] = e.starts[i] + N[i];
@@ -560,8 +563,9 @@ rq_status rq_linear_group(rq_ctx* ctx, int count, const rq_qtype* qtypes, const 
   const float* deqs[RQ_MAX_GROUP];
   for (int i = 0; i < count; ++i) deqs[i] = it->second.deq + i;
   TraceScope ts(ctx, RQ_TRACE_GEMM, st);
+  // a group cache built by an earlier call may be loaded early (as in rq_linear)
   return launch_fp8_gemm_group(xq, xdeq, it->second.fp8, count, it->second.starts, y, deqs, M,
-                               K, st);
+                               K, st, hit);
 }
 
 rq_status rq_ctx_trace_begin(rq_ctx* ctx, int capacity) {

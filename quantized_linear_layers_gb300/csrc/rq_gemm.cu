@@ -148,6 +148,7 @@ struct GemmArgs {
   int tiles_n;     // ceil(N / 128)
   int tiles_m;     // ceil(M_pad / bn)
   int stages;      // stages of the shared-memory ring
+  int w_early;     // 1: the weight was written before the previous launch began
   uint32_t tmem_cols;
   uint64_t wait_limit_ns;
 };
@@ -165,11 +166,6 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + nst * b_stride);
   // bars: full[nst], empty[nst], tfull[2], tempty[2], done[1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * nst + 5);
-  // nothing global is read before the previous launch has completed: the
-  // weight operand may have been written by the launch just before
-  pdl_wait();
-  pdl_trigger();
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + nst);
   const uint32_t tfull0 = smem_u32(bars + 2 * nst);
@@ -205,24 +201,47 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Nothing another launch may write is read before the previous launch has
+  // completed, except, with w_early, the weight tiles of the first stages.
+  const bool producer = warp == 0 && lane == 0;
+  if (!producer) {
+    pdl_wait();
+    pdl_trigger();
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0) {
-      int stage = 0;
+      int early = 0;  // leading stages whose weight tile went out before the wait
+      if (args.w_early) {
+        for (int t = blockIdx.x; t < ntiles && early < nst; t += gridDim.x) {
+          const int tn = t / args.tiles_m;
+          for (int kb = 0; kb < kblocks && early < nst; ++kb, ++early) {
+            const uint32_t fb = full0 + 8 * early;
+            mbar_arrive_expect_tx(fb, stage_tx);
+            tma_load_2d(smem_u32(sA + early * kABytes), &tmap_w, fb, kb * kBK, tn * kBM);
+          }
+        }
+      }
+      pdl_wait();
+      pdl_trigger();
+      int stage = 0, unit = 0;
       uint32_t phase = 0;
       uint32_t issued_mask = 0, last_parity = 0;  // per stage: issued, parity
       bool ok = true;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
         const int tn = t / args.tiles_m, tm = t - tn * args.tiles_m;
-        for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, args.wait_limit_ns, &g_rq_device_error)) {
-            ok = false;
-            break;
-          }
+        for (int kb = 0; kb < kblocks; ++kb, ++unit) {
           const uint32_t fb = full0 + 8 * stage;
-          mbar_arrive_expect_tx(fb, stage_tx);
-          tma_load_2d(smem_u32(sA + stage * kABytes), &tmap_w, fb, kb * kBK, tn * kBM);
+          if (unit >= early) {
+            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, args.wait_limit_ns,
+                           &g_rq_device_error)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(fb, stage_tx);
+            tma_load_2d(smem_u32(sA + stage * kABytes), &tmap_w, fb, kb * kBK, tn * kBM);
+          }
           tma_load_2d(smem_u32(sB + stage * b_stride), &tmap_x, fb, kb * kBK, tm * bn);
           issued_mask |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -417,8 +436,6 @@ fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + nst * b_stride);
   // bars: full[nst], empty[nst], tfull[2], tempty[2], done[1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * nst + 5);
-  pdl_wait();
-  pdl_trigger();
 
   const uint32_t rank = cluster_rank();
   const bool leader = rank == 0;
@@ -459,27 +476,50 @@ fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
   cluster_sync();  // both CTAs' barriers are initialised before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Nothing another launch may write is read before the previous launch has
+  // completed, except, with w_early, the weight tiles of the first stages.
+  const bool producer = warp == 0 && lane == 0;
+  if (!producer) {
+    pdl_wait();
+    pdl_trigger();
+  }
 
   if (warp == 0) {
     // ---------------------------------------------- TMA producer (both CTAs)
     if (lane == 0) {
-      int stage = 0;
+      int early = 0;  // leading stages whose weight tile went out before the wait
+      if (args.w_early) {
+        for (int t = pair; t < ntiles && early < nst; t += npairs) {
+          const int wrow = t / args.tiles_m * 256 + (int)rank * kBM;
+          for (int kb = 0; kb < kblocks && early < nst; ++kb, ++early) {
+            // the leader arms its barrier for both CTAs' bytes; the peer's
+            // copies may land first (the transaction count may run negative)
+            if (leader) mbar_arrive_expect_tx(full0 + 8 * early, 2 * stage_tx);
+            tma_load_2d_pair(smem_u32(sA + early * kABytes), &tmap_w,
+                             peer_addr(full0 + 8 * early, 0), kb * kBK, wrow);
+          }
+        }
+      }
+      pdl_wait();
+      pdl_trigger();
+      int stage = 0, unit = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int t = pair; t < ntiles && ok; t += npairs) {
         const int tn = t / args.tiles_m, tm = t - tn * args.tiles_m;
         const int wrow = tn * 256 + (int)rank * kBM;
         const int trow = tm * bn + (int)rank * half;
-        for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, args.wait_limit_ns, &g_rq_device_error)) {
-            ok = false;
-            break;
-          }
-          // the leader arms its barrier for both CTAs' bytes; the peer's
-          // copies may land first (the transaction count may run negative)
+        for (int kb = 0; kb < kblocks; ++kb, ++unit) {
           const uint32_t lead_full = peer_addr(full0 + 8 * stage, 0);
-          if (leader) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * stage_tx);
-          tma_load_2d_pair(smem_u32(sA + stage * kABytes), &tmap_w, lead_full, kb * kBK, wrow);
+          if (unit >= early) {
+            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, args.wait_limit_ns,
+                           &g_rq_device_error)) {
+              ok = false;
+              break;
+            }
+            if (leader) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * stage_tx);
+            tma_load_2d_pair(smem_u32(sA + stage * kABytes), &tmap_w, lead_full, kb * kBK, wrow);
+          }
           tma_load_2d_pair(smem_u32(sB + stage * b_stride), &tmap_x, lead_full, kb * kBK, trow);
           if (++stage == nst) { stage = 0; phase ^= 1; }
         }
@@ -601,6 +641,7 @@ struct SplitArgs {
   int M, N, K;
   int bn, tiles_m, splits;
   int stages;  // stages of the shared-memory ring (their bytes also hold the partial tile)
+  int w_early;  // 1: the weight was written before the previous launch began
   uint32_t tmem_cols;
   uint64_t wait_limit_ns;
 };
@@ -632,8 +673,6 @@ fp8_gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmap_w,
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + nst * b_stride);
   // bars: full[nst], empty[nst], tfull[1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * nst + 1);
-  pdl_wait();
-  pdl_trigger();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + nst);
@@ -669,19 +708,36 @@ fp8_gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmap_w,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Nothing another launch may write is read before the previous launch has
+  // completed, except, with w_early, the weight tiles of the first stages.
+  const bool producer = warp == 0 && lane == 0;
+  if (!producer) {
+    pdl_wait();
+    pdl_trigger();
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0) {
+      const int early = args.w_early ? min(nst, kb1 - kb0) : 0;
+      for (int i = 0; i < early; ++i) {
+        mbar_arrive_expect_tx(full0 + 8 * i, stage_tx);
+        tma_load_2d(smem_u32(sA + i * kABytes), &tmap_w, full0 + 8 * i, (kb0 + i) * kBK,
+                    tn * kBM);
+      }
+      pdl_wait();
+      pdl_trigger();
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued_mask = 0, last_parity = 0;
       for (int kb = kb0; kb < kb1; ++kb) {
-        if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, args.wait_limit_ns, &g_rq_device_error))
-          break;
         const uint32_t fb = full0 + 8 * stage;
-        mbar_arrive_expect_tx(fb, stage_tx);
-        tma_load_2d(smem_u32(sA + stage * kABytes), &tmap_w, fb, kb * kBK, tn * kBM);
+        if (kb - kb0 >= early) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, args.wait_limit_ns, &g_rq_device_error))
+            break;
+          mbar_arrive_expect_tx(fb, stage_tx);
+          tma_load_2d(smem_u32(sA + stage * kABytes), &tmap_w, fb, kb * kBK, tn * kBM);
+        }
         tma_load_2d(smem_u32(sB + stage * b_stride), &tmap_x, fb, kb * kBK, tm * bn);
         issued_mask |= 1u << stage;
         last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -1002,7 +1058,7 @@ static int choose_splits(int m_pad, int N, int K, int sms, int* bn_out) {
 
 static rq_status launch_fp8_gemm_splitk(const uint8_t* x_fp8, const float* x_deq,
                                         const uint8_t* w_fp8, const OutSegs& out, int M, int N,
-                                        int K, int bn, int S, cudaStream_t st) {
+                                        int K, int bn, int S, bool w_early, cudaStream_t st) {
   const int m_pad = (M + 15) / 16 * 16;
   CUtensorMap tw, tx;
   if (!make_map(&tw, w_fp8, N, K, kBM) || !make_map(&tx, x_fp8, m_pad, K, bn))
@@ -1016,6 +1072,7 @@ static rq_status launch_fp8_gemm_splitk(const uint8_t* x_fp8, const float* x_deq
   }
   SplitArgs a;
   a.stages = gemm_stages(bn * kBK, kStages, bn * kBM * 4);
+  a.w_early = w_early ? 1 : 0;
   a.x_deq = x_deq;
   a.out = out;
   a.M = M;
@@ -1050,7 +1107,7 @@ static rq_status launch_fp8_gemm_splitk(const uint8_t* x_fp8, const float* x_deq
 rq_status launch_fp8_gemm_group(const uint8_t* x_fp8, const float* x_deq,
                                 const uint8_t* w_fp8, int count, const int* starts,
                                 float* const* ys, const float* const* w_deqs, int M, int K,
-                                cudaStream_t st) {
+                                cudaStream_t st, bool w_early) {
   if (count < 1 || count > kMaxSegs) return RQ_ERR_SHAPE;
   OutSegs out;
   out.count = count;
@@ -1069,7 +1126,8 @@ rq_status launch_fp8_gemm_group(const uint8_t* x_fp8, const float* x_deq,
   const int sms = device_sm_count();
   int bn_split = 0;
   const int S = choose_splits(m_pad, N, K, sms, &bn_split);
-  if (S > 1) return launch_fp8_gemm_splitk(x_fp8, x_deq, w_fp8, out, M, N, K, bn_split, S, st);
+  if (S > 1)
+    return launch_fp8_gemm_splitk(x_fp8, x_deq, w_fp8, out, M, N, K, bn_split, S, w_early, st);
   const int pairs = sms >= 2 ? resident_pairs(sms) : 0;
   const int bn_pair = sms >= 2 ? choose_bn_pair(m_pad, N, pairs) : 0;
   const int bn_single = choose_bn(m_pad, N, sms);
@@ -1089,6 +1147,7 @@ rq_status launch_fp8_gemm_group(const uint8_t* x_fp8, const float* x_deq,
   a.tiles_m = (m_pad + bn - 1) / bn;
   a.tmem_cols = tmem_columns(bn);
   a.wait_limit_ns = kWaitLimitNs;
+  a.w_early = w_early ? 1 : 0;
   const int tiles = a.tiles_n * a.tiles_m;
   if (pair) {
     static bool attr2 = false;
@@ -1128,9 +1187,9 @@ rq_status launch_fp8_gemm_group(const uint8_t* x_fp8, const float* x_deq,
 
 rq_status launch_fp8_gemm(const uint8_t* x_fp8, const float* x_deq,
                           const uint8_t* w_fp8, const float* w_deq, float* y,
-                          int M, int N, int K, cudaStream_t st) {
+                          int M, int N, int K, cudaStream_t st, bool w_early) {
   const int starts[2] = {0, N};
-  return launch_fp8_gemm_group(x_fp8, x_deq, w_fp8, 1, starts, &y, &w_deq, M, K, st);
+  return launch_fp8_gemm_group(x_fp8, x_deq, w_fp8, 1, starts, &y, &w_deq, M, K, st, w_early);
 }
 
 rq_status read_and_clear_device_error(cudaStream_t st) {

@@ -111,16 +111,19 @@ rq_status launch_dequant_encode(int qtype, const uint8_t* w, int N, int K,
                                 float* dequant_out, cudaStream_t st);
 
 // rq_gemm.cu ----------------------------------------------------------------
+// w_early: the weight was written before the launch preceding this one began
+// (a cached weight built by an earlier call); the kernel may then start
+// loading its first weight tiles before that launch has completed.
 rq_status launch_fp8_gemm(const uint8_t* x_fp8, const float* x_deq,
                           const uint8_t* w_fp8, const float* w_deq, float* y,
-                          int M, int N, int K, cudaStream_t st);
+                          int M, int N, int K, cudaStream_t st, bool w_early = false);
 // One GEMM over weights concatenated by rows: member i owns rows
 // [starts[i], starts[i+1]), its scale w_deqs[i] and its output ys[i]
 // ([M x (starts[i+1] - starts[i])]).  count <= RQ_MAX_GROUP.
 rq_status launch_fp8_gemm_group(const uint8_t* x_fp8, const float* x_deq,
                                 const uint8_t* w_fp8, int count, const int* starts,
                                 float* const* ys, const float* const* w_deqs, int M, int K,
-                                cudaStream_t st);
+                                cudaStream_t st, bool w_early = false);
 rq_status read_and_clear_device_error(cudaStream_t st);
 rq_status launch_debug_wait_timeout(int64_t limit_ns, cudaStream_t st);
 

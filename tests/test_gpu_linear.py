@@ -393,6 +393,34 @@ def test_linear_group_of_four_members(rq, M):
     ctx.close()
 
 
+@pytest.mark.parametrize("M,N,K", [(16, 3584, 3584), (300, 640, 1024), (2048, 3584, 3584),
+                                   (1000, 4608, 2048)])
+def test_cached_weight_calls_match_the_oracle(rq, M, N, K):
+    """Calls after the first find the FP8 weight in the cache, and the GEMM
+    then starts loading its first weight tiles before the launch before it
+    has completed; every call, with a new activation each time, against the
+    oracle (split-K, one-CTA and CTA-pair shapes)."""
+    W = synthetic.q4k_matrix(3400 + N + K, N, K)
+    Wd = to_dev(W)
+    wb, wd = oracle.fp8_weight_cache(Q4K, W, N, K)
+    ctx = rq.Context()
+    for call in range(3):
+        x = synthetic.activation(3410 + call + M, M, K, outlier_frac=1e-3)
+        y = empty((M, N), torch.float32)
+        ctx.rq_act_cache_invalidate()
+        ctx.rq_linear(Q4K, Wd, to_dev(x), y, M, N, K)
+        torch.cuda.synchronize()
+        assert rq.rq_get_device_status() == 0
+        xb, xd = oracle.quant_e4m3(x, oracle.absmax_bits(x))
+        got = y.cpu().numpy()
+        for m in sorted({0, 1, M // 2, M - 1}):
+            ref = oracle.fp8_gemm_pairs(xb, xd, wb, wd, np.full(N, m), np.arange(N))
+            ok, worst = gemm_ok(got[m], ref, np.sqrt(np.mean(ref ** 2)))
+            assert ok, (call, m, worst)
+    assert ctx.stats()["weights"] == 1
+    ctx.close()
+
+
 def test_linear_group_rejects_bad_counts(rq):
     ctx = rq.Context()
     with pytest.raises(rq.RqError):
