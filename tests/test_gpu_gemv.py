@@ -166,7 +166,8 @@ def test_q6k_weight_only_4_byte_aligned(rq, M):
 
 
 @pytest.mark.parametrize("force", ["", "1", "0"])
-@pytest.mark.parametrize("N,K", [(1, 512), (67, 768), (300, 8704), (151, 18944), (37, 40960)])
+@pytest.mark.parametrize("N,K", [(1, 512), (67, 768), (300, 8704), (151, 18944), (37, 40960),
+                                 (3, 65536)])
 def test_one_token_q4k_rows_split_between_two_ctas(rq, monkeypatch, force, N, K):
     """One token, rows whose super-blocks are split between the two CTAs of
     a cluster (automatic for rows longer than 8 warps' worth, forced on or
