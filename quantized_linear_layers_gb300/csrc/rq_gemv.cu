@@ -723,9 +723,23 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
   // stores of each plane's bytes.
   if (warp < compute_warps) {
     const int q = lane & 3;
-    for (int sb32 = warp * 8 + (lane >> 2); sb32 < nsub; sb32 += compute_warps * 8) {
+    // the next iteration's x is loaded before this one is converted, so the
+    // loads of consecutive iterations overlap
+    const int step32 = compute_warps * 8;
+    float4 na = make_float4(0.f, 0.f, 0.f, 0.f), nb = na;
+    int sb32 = warp * 8 + (lane >> 2);
+    if (sb32 < nsub) {
       const float4* px = reinterpret_cast<const float4*>(xh + 32 * sb32 + 8 * q);
-      const float4 va = __ldg(px), vb = __ldg(px + 1);
+      na = __ldg(px);
+      nb = __ldg(px + 1);
+    }
+    for (; sb32 < nsub; sb32 += step32) {
+      const float4 va = na, vb = nb;
+      if (sb32 + step32 < nsub) {
+        const float4* px = reinterpret_cast<const float4*>(xh + 32 * (sb32 + step32) + 8 * q);
+        na = __ldg(px);
+        nb = __ldg(px + 1);
+      }
       const float v[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
       float mx = 0.f, sm = 0.f;
 #pragma unroll
