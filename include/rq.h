@@ -205,7 +205,7 @@ rq_status rq_fp8_act_cache(rq_ctx *ctx, const float *x, int M, int K,
  *                   x into the ctx's [M_pad x K] scratch (pad rows zeroed),
  *                   then the FP8 GEMM.  When x is 16-byte aligned and
  *                   what does not fit the shared memory of one wave of CTAs
- *                   (about 220 KB per SM) is at most 64 MB, absmax and
+ *                   (about 220 KB per SM) is at most 16 MB, absmax and
  *                   quantization are one cooperative kernel (x read once
  *                   when it fits, otherwise only the rest read twice);
  *                   otherwise two kernels, the second reading x backwards

@@ -1109,6 +1109,8 @@ rq_status launch_fp8_gemm_group(const uint8_t* x_fp8, const float* x_deq,
                                 float* const* ys, const float* const* w_deqs, int M, int K,
                                 cudaStream_t st, bool w_early) {
   if (count < 1 || count > kMaxSegs) return RQ_ERR_SHAPE;
+  // RQ_GEMM_EARLY=0: no weight loads before the wait (A/B measurements)
+  if (const char* e = std::getenv("RQ_GEMM_EARLY")) w_early = w_early && std::atoi(e) != 0;
   OutSegs out;
   out.count = count;
   for (int i = 0; i <= count; ++i) out.start[i] = starts[i];

@@ -49,7 +49,7 @@ rq_status launch_quant(const float* x, int64_t n, int64_t n_out,
                        float* dequant_out, cudaStream_t st);
 
 // Absmax + encode in one cooperative wave (each CTA's chunk staged in shared
-// memory as far as it fits, the rest, at most 64 MB in all, read twice).
+// memory as far as it fits, the rest, at most 16 MB in all, read twice).
 // Needs x 16-byte and out 4-byte aligned; RQ_ERR_SHAPE (nothing launched) if
 // the wave does not fit the GPU.  `state` is 4 device words, zero before the
 // first launch and used by one stream at a time.  absmax_out / dequant_out

@@ -427,9 +427,12 @@ rq_status launch_act_quant_two_pass(const float* x, int64_t n, int64_t n_out, ui
 
 // Heads (the parts of the chunks beyond shared memory) up to this many bytes
 // in all: measured on GB300, the one kernel beats the two while its heads
-// stay in L2 between its passes (512 x 18944: 16.3 against 18.9 us) and
-// loses once they do not (2048 x 18944, 121 MB of heads: 62 against 55 us).
-constexpr int64_t kFusedHeadMax = 64ll << 20;
+// stay in L2 between its passes (512 x 18944, 5 MB of heads: 16.3 against
+// 18.9 us alone, and the 28-layer stack at 512 tokens 1 % faster) and loses
+// once they do not (2048 x 18944, 121 MB: 62 against 55 us); with 25 MB of
+// heads (4096 x 3584) it wins alone (22 against 25 us) but the stack at 4096
+// tokens, whose weights share L2, is 3-5 % slower than with two kernels.
+constexpr int64_t kFusedHeadMax = 16ll << 20;
 
 int64_t fused_stash4(int64_t chunk) {
   return std::min<int64_t>(chunk / 4, kFusedSmemMax / 16);
