@@ -203,9 +203,10 @@ rq_status rq_fp8_act_cache(rq_ctx *ctx, const float *x, int M, int K,
  *   M >= threshold: FP8 weight cache (a hit after the first call), then, on
  *                   an activation-cache miss, absmax + E4M3 quantization of
  *                   x into the ctx's [M_pad x K] scratch (pad rows zeroed),
- *                   then the FP8 GEMM.  When x is 16-byte aligned and
- *                   what does not fit the shared memory of one wave of CTAs
- *                   (about 220 KB per SM) is at most 16 MB, absmax and
+ *                   then the FP8 GEMM.  When x is 16-byte aligned, has at
+ *                   least 2^20 elements and what does not fit the shared
+ *                   memory of one wave of CTAs (about 220 KB per SM) is at
+ *                   most 16 MB, absmax and
  *                   quantization are one cooperative kernel (x read once
  *                   when it fits, otherwise only the rest read twice);
  *                   otherwise two kernels, the second reading x backwards

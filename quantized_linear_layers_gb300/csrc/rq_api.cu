@@ -102,6 +102,7 @@ struct rq_ctx {
   float* act_deq = nullptr;    // device float
   unsigned int* fused = nullptr;  // one-pass quantization state (4 device words)
   bool fused_ok = true;           // RQ_ONE_PASS_QUANT=0 keeps the two-kernel path
+  int64_t fused_min = 1 << 20;    // fewer elements: two kernels (RQ_ONE_PASS_MIN)
   uint32_t* slots = nullptr;      // per-CTA partial maxima of the two-kernel path
   // activation cache key
   bool act_valid = false;
@@ -197,6 +198,11 @@ rq_status rq_ctx_create(rq_ctx** out) {
   }
   const char* one_pass = std::getenv("RQ_ONE_PASS_QUANT");
   if (one_pass != nullptr && std::atoi(one_pass) == 0) c->fused_ok = false;
+  // a small activation goes through the two plain kernels: measured on
+  // GB300, the cooperative one-pass launch costs more than it saves there
+  // (the 28-layer stack at 16 tokens: 2.32 ms per pass one-pass, 2.10 ms
+  // with two kernels)
+  if (const char* e = std::getenv("RQ_ONE_PASS_MIN")) c->fused_min = std::atoll(e);
   void* sl = nullptr;
   if (cudaMalloc(&sl, sizeof(uint32_t) * (size_t)act_quant_slots()) != cudaSuccess) {
     cudaFree(p);
@@ -369,7 +375,7 @@ rq_status rq_fp8_act_cache(rq_ctx* ctx, const float* x, int M, int K,
     }
     const int64_t n = (int64_t)M * K;
     s = RQ_ERR_SHAPE;
-    if (ctx->fused_ok && act_quant_fused_fits(x, n, ctx->act)) {
+    if (ctx->fused_ok && n >= ctx->fused_min && act_quant_fused_fits(x, n, ctx->act)) {
       TraceScope ts(ctx, RQ_TRACE_QUANT, st);
       s = launch_act_quant_fused(x, n, (int64_t)need, ctx->act, ctx->absmax, ctx->act_deq,
                                  ctx->fused, st);

@@ -156,15 +156,15 @@ def test_activation_cache_bytes_bit_exact(rq, monkeypatch, one_pass, M, K):
         want, wd = oracle_act_bytes(xs, M, K)
         assert gd == wd
         assert np.array_equal(got, want), np.flatnonzero(got != want)[:8]
-        # absmax and encoding are traced together as QUANT: one kernel while
-        # what does not fit one wave of shared memory (220 KB per SM) is at
-        # most 16 MB, else two
+        # absmax and encoding are traced together as QUANT: one kernel from
+        # 2^20 elements on while what does not fit one wave of shared memory
+        # (220 KB per SM) is at most 16 MB, else two
         n = M * K
         sms = torch.cuda.get_device_properties(0).multi_processor_count
         chunk = max(4096, ((n + sms - 1) // sms + 3) & ~3)
         grid = (n + chunk - 1) // chunk
         head = 4 * n - 16 * grid * min(chunk // 4, 220 * 1024 // 16)
-        kernels = 1 if one_pass == "1" and head <= 16 << 20 else 2
+        kernels = 1 if one_pass == "1" and n >= 1 << 20 and head <= 16 << 20 else 2
         assert tr["absmax"][0] == 0 and tr["quant"][0] == kernels
     # a hit returns the same bytes without launching anything
     ctx.rq_ctx_trace_begin(8)
