@@ -132,7 +132,7 @@ def oracle_act_bytes(x, M, K):
     return want, od
 
 
-@pytest.mark.parametrize("one_pass", ["1", "0"])
+@pytest.mark.parametrize("one_pass", ["1", "0", "default"])
 @pytest.mark.parametrize("M,K", [(2048, 3584), (611, 1024), (37, 3584), (5, 256),
                                  (16, 128), (3, 4101), (2048, 18944), (1001, 18947),
                                  (512, 18944), (509, 18947)])
@@ -140,7 +140,12 @@ def test_activation_cache_bytes_bit_exact(rq, monkeypatch, one_pass, M, K):
     """The FP8 activation (one-pass kernel or absmax + quant kernels) is the
     oracle's bytes, pad rows zero, over three successive misses with
     different maxima (the one-pass kernel alternates its absmax words)."""
-    monkeypatch.setenv("RQ_ONE_PASS_QUANT", one_pass)
+    # "1": the one-pass kernel wherever it may run (no minimum size); "0":
+    # the two kernels; "default": the library's own choice
+    if one_pass != "default":
+        monkeypatch.setenv("RQ_ONE_PASS_QUANT", one_pass)
+    if one_pass == "1":
+        monkeypatch.setenv("RQ_ONE_PASS_MIN", "0")
     ctx = rq.Context()
     x = synthetic.activation(5000 + M + K, M, K, outlier_frac=1e-3)
     x.ravel()[min(4, x.size - 1)] = np.nan
@@ -164,7 +169,8 @@ def test_activation_cache_bytes_bit_exact(rq, monkeypatch, one_pass, M, K):
         chunk = max(4096, ((n + sms - 1) // sms + 3) & ~3)
         grid = (n + chunk - 1) // chunk
         head = 4 * n - 16 * grid * min(chunk // 4, 220 * 1024 // 16)
-        kernels = 1 if one_pass == "1" and n >= 1 << 20 and head <= 16 << 20 else 2
+        least = {"1": 0, "0": None, "default": 1 << 20}[one_pass]
+        kernels = 1 if least is not None and n >= least and head <= 16 << 20 else 2
         assert tr["absmax"][0] == 0 and tr["quant"][0] == kernels
     # a hit returns the same bytes without launching anything
     ctx.rq_ctx_trace_begin(8)
@@ -221,7 +227,8 @@ def test_trace_kinds_mask(rq):
     ctx.rq_ctx_trace_begin(16)
     ctx.rq_linear(Q4K, Wd, xd, y, M, N, K)
     tr = ctx.rq_ctx_trace_end()
-    assert tr["gemm"][0] == 1 and tr["quant"][0] == 1
+    # 64 x 512 elements: below the one-pass kernel's minimum, so two kernels
+    assert tr["gemm"][0] == 1 and tr["quant"][0] == 2
     ctx.close()
 
 
