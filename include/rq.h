@@ -203,15 +203,17 @@ rq_status rq_fp8_act_cache(rq_ctx *ctx, const float *x, int M, int K,
  *   M >= threshold: FP8 weight cache (a hit after the first call), then, on
  *                   an activation-cache miss, absmax + E4M3 quantization of
  *                   x into the ctx's [M_pad x K] scratch (pad rows zeroed),
- *                   then the FP8 GEMM.  When x is 16-byte aligned, has at
- *                   least 2^20 elements and what does not fit the shared
+ *                   then the FP8 GEMM.  Up to 2^17 elements, absmax and
+ *                   quantization are one launch of one thread-block
+ *                   cluster (x read twice, the second time from L2); from
+ *                   2^20 elements on, while what does not fit the shared
  *                   memory of one wave of CTAs (about 220 KB per SM) is at
- *                   most 16 MB, absmax and
- *                   quantization are one cooperative kernel (x read once
- *                   when it fits, otherwise only the rest read twice);
- *                   otherwise two kernels, the second reading x backwards
- *                   (same bytes either way; environment RQ_ONE_PASS_QUANT=0
- *                   at ctx creation selects the two kernels always).
+ *                   most 16 MB, one cooperative kernel (x read once when it
+ *                   fits, otherwise only the rest read twice); otherwise
+ *                   two kernels, the second reading x backwards (the same
+ *                   bytes every way; at ctx creation the environment
+ *                   variables RQ_CLUSTER_QUANT_MAX (elements, 0 = never)
+ *                   and RQ_ONE_PASS_QUANT=0 turn the first two off).
  * The activation cache ([gemm.rs], PMAT-084 reuse across Q/K/V and gate/up)
  * is keyed by (x, M, K, generation); rq_act_cache_invalidate bumps the
  * generation and must be called when x's contents change in place.

@@ -103,6 +103,10 @@ struct rq_ctx {
   unsigned int* fused = nullptr;  // one-pass quantization state (4 device words)
   bool fused_ok = true;           // RQ_ONE_PASS_QUANT=0 keeps the two-kernel path
   int64_t fused_min = 1 << 20;    // fewer elements: two kernels (RQ_ONE_PASS_MIN)
+  // at most this many elements: one cluster, one launch (RQ_CLUSTER_QUANT_MAX;
+  // measured on GB300, the 16-SM cluster beats the two grid-wide kernels on
+  // the 57 K elements of 16 tokens x 3584 and loses from ~230 K on)
+  int64_t cluster_max = 1 << 17;
   uint32_t* slots = nullptr;      // per-CTA partial maxima of the two-kernel path
   // activation cache key
   bool act_valid = false;
@@ -203,6 +207,7 @@ rq_status rq_ctx_create(rq_ctx** out) {
   // (the 28-layer stack at 16 tokens: 2.32 ms per pass one-pass, 2.10 ms
   // with two kernels)
   if (const char* e = std::getenv("RQ_ONE_PASS_MIN")) c->fused_min = std::atoll(e);
+  if (const char* e = std::getenv("RQ_CLUSTER_QUANT_MAX")) c->cluster_max = std::atoll(e);
   void* sl = nullptr;
   if (cudaMalloc(&sl, sizeof(uint32_t) * (size_t)act_quant_slots()) != cudaSuccess) {
     cudaFree(p);
@@ -375,14 +380,19 @@ rq_status rq_fp8_act_cache(rq_ctx* ctx, const float* x, int M, int K,
     }
     const int64_t n = (int64_t)M * K;
     s = RQ_ERR_SHAPE;
-    if (ctx->fused_ok && n >= ctx->fused_min && act_quant_fused_fits(x, n, ctx->act)) {
+    if (n <= ctx->cluster_max) {
+      // a few tokens: one cluster reads x twice (the second time from L2)
+      TraceScope ts(ctx, RQ_TRACE_QUANT, st);
+      s = launch_act_quant_cluster(x, n, (int64_t)need, ctx->act, ctx->absmax, ctx->act_deq, st);
+      if (s == RQ_ERR_SHAPE) ts.kernels(0);
+    } else if (ctx->fused_ok && n >= ctx->fused_min && act_quant_fused_fits(x, n, ctx->act)) {
       TraceScope ts(ctx, RQ_TRACE_QUANT, st);
       s = launch_act_quant_fused(x, n, (int64_t)need, ctx->act, ctx->absmax, ctx->act_deq,
                                  ctx->fused, st);
       if (s == RQ_ERR_SHAPE) ts.kernels(0);
     }
-    // RQ_ERR_SHAPE from the one-pass launcher: its wave did not fit the GPU
-    // and nothing was launched
+    // RQ_ERR_SHAPE from the one-cluster or one-pass launcher: nothing was
+    // launched
     if (s == RQ_ERR_SHAPE) {
       // two kernels: per-CTA maxima into slots, then the encoding
       TraceScope ts(ctx, RQ_TRACE_QUANT, st);

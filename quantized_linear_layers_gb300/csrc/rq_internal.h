@@ -66,6 +66,13 @@ int act_quant_slots();
 rq_status launch_act_quant_two_pass(const float* x, int64_t n, int64_t n_out, uint8_t* out,
                                     uint32_t* slots, uint32_t* absmax_out,
                                     float* dequant_out, cudaStream_t st);
+// Absmax + encode in one launch of one thread-block cluster (x read twice,
+// the second time from L2): for small activations.  Needs x 16-byte and out
+// 4-byte aligned (else RQ_ERR_SHAPE, nothing launched); absmax_out /
+// dequant_out may be null.
+rq_status launch_act_quant_cluster(const float* x, int64_t n, int64_t n_out, uint8_t* out,
+                                   uint32_t* absmax_out, float* dequant_out,
+                                   cudaStream_t st);
 // Read and clear the one-pass kernel's device error word (after a sync).
 rq_status read_and_clear_quant_error();
 

@@ -371,6 +371,115 @@ quant_slots_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
   for (int64_t i = n + tid; i < n_out; i += nthreads) out[i] = 0;
 }
 
+// ------------------------------------------------- one-cluster variant --
+//
+// Small activations (the inputs of a few tokens) in one launch: a single
+// thread-block cluster streams x for the max, exchanges the CTAs' maxima
+// through distributed shared memory behind the cluster barrier, and reads x
+// again, now from L2, to encode it.  No grid barrier and no second launch;
+// the same arithmetic as absmax_kernel + quant_kernel, hence the same bytes.
+
+constexpr int kClusterThreads = 1024;
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+// A word in the shared memory of CTA `rank` of the cluster, at the offset of
+// `local` in this CTA.
+__device__ __forceinline__ uint32_t ld_peer_u32(const uint32_t* local, uint32_t rank) {
+  uint32_t remote, v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(remote)
+               : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+// x 16-byte and out 4-byte aligned (the launcher checks).
+__global__ void __launch_bounds__(kClusterThreads, 1)
+act_quant_cluster_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
+                         uint8_t* __restrict__ out, uint32_t* __restrict__ absmax_out,
+                         float* __restrict__ dequant_out) {
+  __shared__ uint32_t warp_max[kClusterThreads / 32];
+  __shared__ uint32_t cta_max, all_max;
+  pdl_wait();
+  pdl_trigger();
+  const uint32_t rank = cluster_ctarank(), ncta = cluster_nctarank();
+  const int64_t tid = (int64_t)rank * kClusterThreads + threadIdx.x;
+  const int64_t nthreads = (int64_t)ncta * kClusterThreads;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const float4* x4 = reinterpret_cast<const float4*>(x);
+  const int64_t n4 = n >> 2;
+
+  // pass 1: this CTA's max, from HBM (or from L2 when x was just written)
+  uint32_t m = 0;
+  {
+    int64_t i = tid;
+    for (; i + 3 * nthreads < n4; i += 4 * nthreads) {
+      const float4 a = __ldg(x4 + i), b = __ldg(x4 + i + nthreads);
+      const float4 c = __ldg(x4 + i + 2 * nthreads), d = __ldg(x4 + i + 3 * nthreads);
+      m = max4(max4(m, a), b);
+      m = max4(max4(m, c), d);
+    }
+    for (; i < n4; i += nthreads) m = max4(m, __ldg(x4 + i));
+    for (int64_t j = (n4 << 2) + tid; j < n; j += nthreads)
+      m = max(m, abs_bits_skip_nan(__ldg(x + j)));
+  }
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  if (lane == 0) warp_max[warp] = m;
+  __syncthreads();
+  if (warp == 0) {
+    m = warp_max[lane];
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if (lane == 0) cta_max = m;
+  }
+  // every CTA's maximum is in its shared memory
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  if (warp == 0) {
+    m = (uint32_t)lane < ncta ? ld_peer_u32(&cta_max, (uint32_t)lane) : 0u;
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if (lane == 0) all_max = m;
+  }
+  // this CTA has read its peers' maxima; it waits at the end of the kernel
+  // until every CTA has, so that no shared memory is read after it is gone
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  __syncthreads();
+
+  // pass 2: encode with the tensor's scale; x is read again from L2
+  const uint32_t bits = all_max;
+  const float a = absmax_prime(bits);
+  const float s = __fdiv_rn(448.0f, a);
+  if (rank == 0 && threadIdx.x == 0) {
+    if (absmax_out != nullptr) *absmax_out = bits;
+    if (dequant_out != nullptr) *dequant_out = __fdiv_rn(a, 448.0f);
+  }
+  {
+    uint32_t* o4 = reinterpret_cast<uint32_t*>(out);
+    int64_t i = tid;
+    for (; i + 3 * nthreads < n4; i += 4 * nthreads) {
+      const float4 v0 = __ldg(x4 + i), v1 = __ldg(x4 + i + nthreads);
+      const float4 v2 = __ldg(x4 + i + 2 * nthreads), v3 = __ldg(x4 + i + 3 * nthreads);
+      o4[i] = pack4(v0, s);
+      o4[i + nthreads] = pack4(v1, s);
+      o4[i + 2 * nthreads] = pack4(v2, s);
+      o4[i + 3 * nthreads] = pack4(v3, s);
+    }
+    for (; i < n4; i += nthreads) o4[i] = pack4(__ldg(x4 + i), s);
+    for (int64_t j = (n4 << 2) + tid; j < n; j += nthreads)
+      out[j] = (uint8_t)e4m3_scaled(__ldg(x + j), s);
+    for (int64_t j = n + tid; j < n_out; j += nthreads) out[j] = 0;
+  }
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
 int grid_for(int64_t work_items) {
   const int64_t per_wave = (int64_t)device_sm_count() * 4;  // 4 CTAs / SM
   int64_t blocks = (work_items + kThreads - 1) / kThreads;
@@ -423,6 +532,57 @@ rq_status launch_act_quant_two_pass(const float* x, int64_t n, int64_t n_out, ui
                          (const uint32_t*)slots, g1, out, absmax_out, dequant_out);
   return launch_kernel(quant_slots_kernel<false>, g2, kThreads, 0, st, x, n, n_out,
                        (const uint32_t*)slots, g1, out, absmax_out, dequant_out);
+}
+
+// CTAs of the one-cluster kernel: 16 (a size beyond the portable 8) where
+// the GPU schedules such a cluster of these CTAs, else 8.
+int act_quant_cluster_ctas() {
+  static int ctas = 0;
+  if (ctas != 0) return ctas;
+  ctas = 8;
+  if (cudaFuncSetAttribute(act_quant_cluster_kernel,
+                           cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(16);
+    cfg.blockDim = dim3(kClusterThreads);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 16;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, act_quant_cluster_kernel, &cfg) ==
+            cudaSuccess &&
+        n >= 1)
+      ctas = 16;
+  }
+  cudaGetLastError();  // a refused attribute or query leaves no error behind
+  return ctas;
+}
+
+rq_status launch_act_quant_cluster(const float* x, int64_t n, int64_t n_out, uint8_t* out,
+                                   uint32_t* absmax_out, float* dequant_out,
+                                   cudaStream_t st) {
+  if ((reinterpret_cast<uintptr_t>(x) & 15) != 0 || (reinterpret_cast<uintptr_t>(out) & 3) != 0)
+    return RQ_ERR_SHAPE;
+  const int ctas = act_quant_cluster_ctas();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kClusterThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = ctas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
+  return cuda_status(cudaLaunchKernelEx(&cfg, act_quant_cluster_kernel, x, n, n_out, out,
+                                        absmax_out, dequant_out));
 }
 
 // Heads (the parts of the chunks beyond shared memory) up to this many bytes

@@ -132,20 +132,44 @@ def oracle_act_bytes(x, M, K):
     return want, od
 
 
-@pytest.mark.parametrize("one_pass", ["1", "0", "default"])
+def act_quant_kernels(mode, n):
+    """Kernels the activation cache launches for n elements: the one-cluster
+    kernel up to 2^17 elements; the one-pass kernel from 2^20 elements on
+    while what does not fit one wave of shared memory (220 KB per SM) is at
+    most 16 MB; else the two kernels."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    chunk = max(4096, ((n + sms - 1) // sms + 3) & ~3)
+    grid = (n + chunk - 1) // chunk
+    head = 4 * n - 16 * grid * min(chunk // 4, 220 * 1024 // 16)
+    if mode == "cluster" or (mode == "default" and n <= 1 << 17):
+        return 1
+    least = {"1": 0, "0": None, "default": 1 << 20}[mode]
+    return 1 if least is not None and n >= least and head <= 16 << 20 else 2
+
+
+def set_act_quant_mode(monkeypatch, mode):
+    """"cluster": the one-cluster kernel at every size; "1": the one-pass
+    kernel wherever it may run (no minimum size); "0": the two kernels;
+    "default": the library's own choice."""
+    if mode == "cluster":
+        monkeypatch.setenv("RQ_CLUSTER_QUANT_MAX", str(1 << 40))
+    elif mode != "default":
+        monkeypatch.setenv("RQ_CLUSTER_QUANT_MAX", "0")
+        monkeypatch.setenv("RQ_ONE_PASS_QUANT", mode)
+        if mode == "1":
+            monkeypatch.setenv("RQ_ONE_PASS_MIN", "0")
+
+
+@pytest.mark.parametrize("one_pass", ["cluster", "1", "0", "default"])
 @pytest.mark.parametrize("M,K", [(2048, 3584), (611, 1024), (37, 3584), (5, 256),
                                  (16, 128), (3, 4101), (2048, 18944), (1001, 18947),
-                                 (512, 18944), (509, 18947)])
+                                 (512, 18944), (509, 18947), (16, 18944), (128, 3584)])
 def test_activation_cache_bytes_bit_exact(rq, monkeypatch, one_pass, M, K):
-    """The FP8 activation (one-pass kernel or absmax + quant kernels) is the
-    oracle's bytes, pad rows zero, over three successive misses with
-    different maxima (the one-pass kernel alternates its absmax words)."""
-    # "1": the one-pass kernel wherever it may run (no minimum size); "0":
-    # the two kernels; "default": the library's own choice
-    if one_pass != "default":
-        monkeypatch.setenv("RQ_ONE_PASS_QUANT", one_pass)
-    if one_pass == "1":
-        monkeypatch.setenv("RQ_ONE_PASS_MIN", "0")
+    """The FP8 activation (one-cluster kernel, one-pass kernel or absmax +
+    quant kernels) is the oracle's bytes, pad rows zero, over three
+    successive misses with different maxima (the one-pass kernel alternates
+    its absmax words)."""
+    set_act_quant_mode(monkeypatch, one_pass)
     ctx = rq.Context()
     x = synthetic.activation(5000 + M + K, M, K, outlier_frac=1e-3)
     x.ravel()[min(4, x.size - 1)] = np.nan
@@ -161,22 +185,61 @@ def test_activation_cache_bytes_bit_exact(rq, monkeypatch, one_pass, M, K):
         want, wd = oracle_act_bytes(xs, M, K)
         assert gd == wd
         assert np.array_equal(got, want), np.flatnonzero(got != want)[:8]
-        # absmax and encoding are traced together as QUANT: one kernel from
-        # 2^20 elements on while what does not fit one wave of shared memory
-        # (220 KB per SM) is at most 16 MB, else two
-        n = M * K
-        sms = torch.cuda.get_device_properties(0).multi_processor_count
-        chunk = max(4096, ((n + sms - 1) // sms + 3) & ~3)
-        grid = (n + chunk - 1) // chunk
-        head = 4 * n - 16 * grid * min(chunk // 4, 220 * 1024 // 16)
-        least = {"1": 0, "0": None, "default": 1 << 20}[one_pass]
-        kernels = 1 if least is not None and n >= least and head <= 16 << 20 else 2
-        assert tr["absmax"][0] == 0 and tr["quant"][0] == kernels
+        # absmax and encoding are traced together as QUANT
+        assert tr["absmax"][0] == 0
+        assert tr["quant"][0] == act_quant_kernels(one_pass, M * K)
     # a hit returns the same bytes without launching anything
     ctx.rq_ctx_trace_begin(8)
     got2, _ = act_cache_bytes(ctx, xd, M, K)
     assert sum(c for c, _ in ctx.rq_ctx_trace_end().values()) == 0
     assert np.array_equal(got2, got)
+    ctx.close()
+
+
+@pytest.mark.parametrize("one_pass", ["cluster", "1", "0"])
+@pytest.mark.parametrize("M,K", [(16, 3584), (37, 4101), (300, 18944)])
+def test_activation_cache_infinite_max(rq, monkeypatch, one_pass, M, K):
+    """With -Inf in x the maximum is +Inf, so the scale is 0: every finite
+    value encodes to 0x00 and -Inf to 0xFE, in every kernel."""
+    set_act_quant_mode(monkeypatch, one_pass)
+    ctx = rq.Context()
+    x = synthetic.activation(6000 + M + K, M, K, outlier_frac=1e-3)
+    x.ravel()[x.size // 2] = -np.inf
+    x.ravel()[x.size // 3] = np.float32(1e-30)
+    ctx.rq_ctx_trace_begin(8)
+    got, gd = act_cache_bytes(ctx, to_dev(x), M, K)
+    tr = ctx.rq_ctx_trace_end()
+    assert rq.rq_get_device_status() == 0
+    want, wd = oracle_act_bytes(x, M, K)
+    assert gd == wd and np.isinf(gd)
+    assert np.array_equal(got, want), np.flatnonzero(got != want)[:8]
+    assert got[x.size // 2] == 0xFE and np.count_nonzero(got) == 1
+    assert tr["quant"][0] == act_quant_kernels(one_pass, M * K)
+    ctx.close()
+
+
+def test_activation_cache_rejects_unaligned_x(rq):
+    """The activation cache takes x on a 16-byte boundary only: RQ_ERR_SHAPE
+    before anything is launched."""
+    M, K = 16, 3584
+    ctx = rq.Context()
+    big = to_dev(np.zeros(M * K + 4, np.float32))
+    with pytest.raises(rq.RqError) as err:
+        ctx.rq_fp8_act_cache(big[1:], M, K)
+    assert err.value.status == 2  # RQ_ERR_SHAPE
+    ctx.close()
+
+
+@pytest.mark.parametrize("one_pass", ["cluster", "0"])
+def test_activation_cache_all_zero_input_each_kernel(rq, monkeypatch, one_pass):
+    """An all-zero x: absmax 0 is read as 1, so the scale is 1/448 and every
+    byte is 0x00, with both small-activation kernels."""
+    set_act_quant_mode(monkeypatch, one_pass)
+    M, K = 16, 3584
+    ctx = rq.Context()
+    xd = to_dev(np.zeros((M, K), np.float32))
+    got, gd = act_cache_bytes(ctx, xd, M, K)
+    assert not got.any() and gd == np.float32(1.0) / np.float32(448.0)
     ctx.close()
 
 
@@ -227,8 +290,8 @@ def test_trace_kinds_mask(rq):
     ctx.rq_ctx_trace_begin(16)
     ctx.rq_linear(Q4K, Wd, xd, y, M, N, K)
     tr = ctx.rq_ctx_trace_end()
-    # 64 x 512 elements: below the one-pass kernel's minimum, so two kernels
-    assert tr["gemm"][0] == 1 and tr["quant"][0] == 2
+    # 64 x 512 elements: one launch of the one-cluster kernel
+    assert tr["gemm"][0] == 1 and tr["quant"][0] == 1
     ctx.close()
 
 
