@@ -19,7 +19,8 @@ def rq():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    with open(HEADER) as f:
+        text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = re.findall(r"\b(rq_[a-z0-9_]+)\s*\(", text)
     return sorted(set(names))

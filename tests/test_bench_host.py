@@ -44,7 +44,8 @@ def test_traffic_record_is_guarded(tmp_path, monkeypatch):
     assert len(fields["kernel_code_sha256"]) == 64
     # a copy of the tree whose GEMM code differs reports no traffic
     (tmp_path / "profiles").mkdir()
-    (tmp_path / "profiles" / "fp8_gemm_traffic.txt").write_text(open(rec).read())
+    with open(rec) as f:
+        (tmp_path / "profiles" / "fp8_gemm_traffic.txt").write_text(f.read())
     src = tmp_path / "quantized_linear_layers_gb300" / "csrc"
     src.mkdir(parents=True)
     (src / "rq_gemm.cu").write_text("int changed;\n")

@@ -42,9 +42,11 @@ def test_scales_zero_absmax_uses_one(orc):
     q, d = orc.scales(f32_bits(448.0))
     assert q == np.float32(1.0) and d == np.float32(1.0)
     # correctly rounded fp32 division (numpy float32 division is IEEE RN)
+    # (448 / 2^-140 overflows to +Inf in fp32, as it does on the device)
     for a in [3.7, 1e-30, 12345.678, 2.0 ** -140]:
         q, d = orc.scales(f32_bits(a))
-        assert q == np.float32(448.0) / np.float32(a)
+        with np.errstate(over="ignore"):
+            assert q == np.float32(448.0) / np.float32(a)
         assert d == np.float32(a) / np.float32(448.0)
 
 
