@@ -226,6 +226,19 @@ def oracle_gemv_sample(seed=SEED):
     return nbytes, t_total
 
 
+def workload_config(world):
+    """The workload both arms report: the 28-layer stack's shapes and passes."""
+    return {
+        "workload": "28-layer decoder linear stack (7 linears per layer; q/k/v and "
+                    "gate/up as grouped calls): decode pass M=1 (GEMV, graph replay) "
+                    "+ prefill pass M=2048 (FP8, eager)",
+        "hidden": synthetic.HIDDEN, "intermediate": synthetic.INTERMEDIATE,
+        "kv_dim": synthetic.KV_DIM, "layers": synthetic.N_LAYERS,
+        "M_decode": M_DECODE, "M_prefill": M_PREFILL, "gemm_threshold": 4,
+        "parallelism": "replicas" if world > 1 else "single-gpu",
+        "l2": "inputs larger than L2 (no flush needed)"}
+
+
 def run_reference(args, world, rank):
     """Reference arm: the CPU oracle as it stands, on the host cores."""
     if rank != 0:
@@ -249,8 +262,7 @@ def run_reference(args, world, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "prefill linear stack sample (oracle)", "M": M_PREFILL,
-                   "layers_sampled": 1, "rows_sampled": rows},
+        "config": workload_config(world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1,
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -452,15 +464,7 @@ def run_gpu(args, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 x e4m3 -> f32 (prefill); f32 x q4k/q6k -> f32 (decode)",
         "data": "synthetic",
-        "config": {
-            "workload": "28-layer decoder linear stack (7 linears per layer; q/k/v and "
-                        "gate/up as grouped calls): decode pass M=1 (GEMV, graph replay) "
-                        "+ prefill pass M=2048 (FP8, eager)",
-            "hidden": synthetic.HIDDEN, "intermediate": synthetic.INTERMEDIATE,
-            "kv_dim": synthetic.KV_DIM, "layers": synthetic.N_LAYERS,
-            "M_decode": M_DECODE, "M_prefill": M_PREFILL, "gemm_threshold": 4,
-            "parallelism": "replicas" if world > 1 else "single-gpu",
-            "l2": "inputs larger than L2 (no flush needed)"},
+        "config": workload_config(world),
         "prefill_ms": pre_s / K * 1e3, "decode_ms": dec_s / K * 1e3,
         "gemv": {"value": gemv_gbs, "unit": "GB/s", "M": M_DECODE,
                  "bytes_per_pass": decode_bytes(M_DECODE),
