@@ -57,3 +57,11 @@ def test_reference_arm_under_torchrun_prints_one_line():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+    for key in ("metric", "unit", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data"):
+        assert key in d, key
+    # the same workload, metric and unit as the GPU arm's line
+    sys.path.insert(0, ROOT)
+    import bench
+    assert d["config"] == bench.workload_config(2)
+    assert d["metric"] == bench.METRIC and d["unit"] == "TFLOP/s" and d["higher_is_better"]
