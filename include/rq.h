@@ -20,9 +20,9 @@
  *  - Shapes: M = tokens (rows of x and y), N = output features (weight rows),
  *    K = input features.  Quantized weights need K % 256 == 0.
  *  - Not thread-safe per rq_ctx: one thread and one stream at a time per ctx.
- *  - One CUDA device per process (one process per GPU): launch settings
- *    (SM count, shared-memory and cluster-size opt-ins) are taken once, on
- *    the device current at the first call, and reused.
+ *  - One CUDA device per process (one process per GPU): a kernel's
+ *    shared-memory and cluster-size opt-ins are made once, on the device
+ *    current at its first launch, and reused.
  */
 #ifndef RQ_H
 #define RQ_H
