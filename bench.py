@@ -70,6 +70,49 @@ def stack_flops(M):
     return per_tok * M * synthetic.N_LAYERS
 
 
+def measure_fp8_peak(torch, dev):
+    """Dense FP8 throughput of this GPU in this run: torch._scaled_mm, E4M3 x
+    E4M3 -> bf16 at 8192^3, best of 10 single calls (burst) and calls back to
+    back for about 1.5 s (sustained).  -> dict, or None if unavailable."""
+    n = 8192
+    try:
+        a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn).t()  # column-major
+        one = torch.ones((), device=dev, dtype=torch.float32)
+
+        def f():
+            return torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+
+        for _ in range(3):
+            f()
+        torch.cuda.synchronize()
+        best = None
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            f()
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        calls = max(1, int(1500.0 / best))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(calls):
+            f()
+        e1.record()
+        torch.cuda.synchronize()
+        flop = 2.0 * n ** 3
+        res = {"burst": flop / best / 1e9, "sustained": flop * calls / e0.elapsed_time(e1) / 1e9,
+               "how": "torch._scaled_mm E4M3 x E4M3 -> bf16, 8192^3: best of 10 (burst), "
+                      "%d calls back to back (sustained)" % calls}
+        del a, b
+        torch.cuda.empty_cache()
+        return res
+    except Exception as e:  # an old torch without _scaled_mm on this GPU
+        return {"error": repr(e)[:200]}
+
+
 def packed_bytes(qtype, N, K):
     return N * (K // 256) * (144 if qtype == synthetic.Q4K else 210)
 
@@ -226,6 +269,82 @@ def oracle_gemv_sample(seed=SEED):
     return nbytes, t_total
 
 
+# All-core oracle sample: one process per host core (spawn, so that no
+# worker inherits a CUDA context), each running its own `rows` token rows of
+# the same prefill sample; a worker builds its weight cache once (untimed).
+_POOL_SAMPLE = None
+
+
+def _pool_init(rows, seed):
+    global _POOL_SAMPLE
+    _POOL_SAMPLE = OracleSample(rows, seed)
+
+
+def _pool_run(_):
+    return _POOL_SAMPLE.run()
+
+
+def oracle_all_cores(rows_per_core, seed=SEED):
+    """-> (flops, wall seconds, workers) of the prefill sample run on every
+    host core at once."""
+    import multiprocessing as mp
+    cores = os.cpu_count() or 1
+    with mp.get_context("spawn").Pool(cores, initializer=_pool_init,
+                                      initargs=(rows_per_core, seed)) as pool:
+        # warm-up (and wait for every worker's setup); a worker that cannot
+        # start makes the pool respawn it forever, hence the time limits
+        pool.map_async(_pool_run, range(cores), chunksize=1).get(timeout=600)
+        t0 = time.perf_counter()
+        res = pool.map_async(_pool_run, range(cores), chunksize=1).get(timeout=600)
+        wall = time.perf_counter() - t0
+    return sum(f for f, _ in res), wall, cores
+
+
+def oracle_config_numbers(sample, seed=SEED):
+    """One-core oracle figures per workload configuration (bounded samples):
+    C1 the 1 x 512 x 1024 Q4_K GEMV, C2 absmax + E4M3 of 512 x 3584, C3 one
+    decoder layer at M = 1 (x28 for the stack, extrapolated), C4 the FP8
+    GEMM on the four prefill shapes at M = 512 (8 sampled token rows)."""
+    import oracle
+    out = {}
+    W = synthetic.q4k_matrix(synthetic.substream(seed, 1), 512, 1024)
+    x = synthetic.activation(synthetic.substream(seed, 2), 1, 1024)
+    reps = 50
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.gemv(synthetic.Q4K, W, x, 512, 1024)
+    t = (time.perf_counter() - t0) / reps
+    out["C1_q4k_gemv_1x512x1024"] = {"ms": t * 1e3, "GB/s": (W.size + 4 * (1024 + 512)) / t / 1e9}
+    x = synthetic.activation(synthetic.substream(seed, 3), 512, 3584, outlier_frac=1e-3)
+    reps = 10
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.quant_e4m3(x, oracle.absmax_bits(x))
+    t = (time.perf_counter() - t0) / reps
+    out["C2_absmax_quant_512x3584"] = {"ms": t * 1e3, "GB/s": 5 * x.size / t / 1e9}
+    nb, sg = oracle_gemv_sample(seed)
+    out["C3_gemv_one_layer_M1"] = {"ms": sg * 1e3, "GB/s": nb / sg / 1e9,
+                                   "stack_ms_extrapolated_x28": 28 * sg * 1e3}
+    rows = 8
+    xq = synthetic.activation(synthetic.substream(seed, 4), rows, 3584, outlier_frac=1e-3)
+    xg = synthetic.activation(synthetic.substream(seed, 5), rows, 18944, outlier_frac=1e-3)
+    flops = 0
+    t0 = time.perf_counter()
+    for name, N, K, wb, wd in sample.wcache:
+        if name not in ("q", "k", "gate", "down"):
+            continue
+        x = xg if K == 18944 else xq
+        xb, xd = oracle.quant_e4m3(x, oracle.absmax_bits(x))
+        ms = np.repeat(np.arange(rows), N)
+        ns = np.tile(np.arange(N), rows)
+        oracle.fp8_gemm_pairs(xb, xd, wb, wd, ms, ns)
+        flops += 2 * rows * N * K
+    t = time.perf_counter() - t0
+    out["C4_fp8_gemm_M512_four_shapes"] = {"sampled_token_rows": rows, "s": t,
+                                           "GFLOP/s": flops / t / 1e9}
+    return out
+
+
 def workload_config(world):
     """The workload both arms report: the 28-layer stack's shapes and passes."""
     return {
@@ -240,30 +359,37 @@ def workload_config(world):
 
 
 def run_reference(args, world, rank):
-    """Reference arm: the CPU oracle as it stands, on the host cores."""
+    """Reference arm: the CPU oracle as it stands, on every host core (one
+    process per core, each running `--ref-rows` token rows per step)."""
     if rank != 0:
         return
+    import multiprocessing as mp
     rows = args.ref_rows
-    sample = OracleSample(rows)
-    for _ in range(args.warmup):
-        sample.run()
+    cores = os.cpu_count() or 1
     flops = 0
     secs = 0.0
-    for _ in range(args.steps):
-        f, s = sample.run()
-        flops += f
-        secs += s
+    with mp.get_context("spawn").Pool(cores, initializer=_pool_init,
+                                      initargs=(rows, SEED)) as pool:
+        # a worker that cannot start makes the pool respawn it forever, hence
+        # the time limits
+        for _ in range(args.warmup):
+            pool.map_async(_pool_run, range(cores), chunksize=1).get(timeout=600)
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            res = pool.map_async(_pool_run, range(cores), chunksize=1).get(timeout=600)
+            secs += time.perf_counter() - t0
+            flops += sum(f for f, _ in res)
     value = flops / secs / 1e12
-    desc = ("%d token rows of the M=2048 prefill through the 7 linears of one "
-              "layer (activation absmax + E4M3 + exact FP8 dot products) per step"
-              % rows)
+    desc = ("%d token rows of the M=2048 prefill through the 7 linears of one layer "
+            "(activation absmax + E4M3 + exact FP8 dot products) per step on each of %d "
+            "host cores (one process per core)" % (rows, cores))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(world),
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1,
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores,
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -337,6 +463,38 @@ class Stack:
         return per_layer * synthetic.N_LAYERS
 
 
+def decode_shape_rates(torch, dev, st, hbm_peak):
+    """Each call type of the decode pass timed on its own: one CUDA graph
+    of that call for all 28 layers (each layer's own weights, so every
+    launch reads HBM), replayed three times.  -> {call: figures}."""
+    res = {}
+    M = M_DECODE
+    ctx = st.ctx
+    for grp in GROUPS:
+        calls = []
+        nbytes = 0
+        for layer in range(synthetic.N_LAYERS):
+            a = st.acts[M][layer]
+            lin = {name: (qt, N, K, W) for name, qt, N, K, W in st.weights[layer]}
+            x = a[SOURCE[grp[0]]]
+            K = lin[grp[0]][2]
+            if len(grp) == 1:
+                qt, N, _, W = lin[grp[0]]
+                calls.append(lambda qt=qt, W=W, x=x, N=N, K=K, n=grp[0]:
+                             ctx.rq_linear(qt, W, x, st.out[M][n], M, N, K))
+            else:
+                calls.append(lambda x=x, K=K, lin=lin, grp=grp: ctx.rq_linear_group(
+                    [lin[n][0] for n in grp], [lin[n][3] for n in grp], x,
+                    [st.out[M][n] for n in grp], [lin[n][1] for n in grp], M, K))
+            nbytes += sum(packed_bytes(lin[n][0], lin[n][1], K) + 4 * M * lin[n][1]
+                          for n in grp) + 4 * M * K
+        ms = graph_time_ms(torch, dev, calls, reps=3)
+        gbs = nbytes / len(calls) / ms / 1e6
+        res["+".join(grp)] = {"us_per_launch": ms * 1e3, "MB_per_launch":
+                              nbytes / len(calls) / 1e6, "GB/s": gbs, "frac": gbs / hbm_peak}
+    return res
+
+
 def run_gpu(args, world, rank, local):
     import torch
     import quantized_linear_layers_gb300 as rq
@@ -345,6 +503,7 @@ def run_gpu(args, world, rank, local):
     torch.cuda.set_device(dev)
     pk = peaks()
     t_setup = time.perf_counter()
+    fp8 = measure_fp8_peak(torch, dev)
     st = Stack(rq, torch, dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -358,6 +517,7 @@ def run_gpu(args, world, rank, local):
     status = rq.rq_get_device_status()
     if status != 0:
         raise RuntimeError("device status %d after warm-up" % status)
+    rq.rq_gemv_exact_outputs()  # count the timed decode passes' exact-path outputs only
 
     # capture the decode pass (launch-bound: short kernels) in a graph
     graph = torch.cuda.CUDAGraph()
@@ -410,6 +570,7 @@ def run_gpu(args, world, rank, local):
     status = rq.rq_get_device_status()
     if status != 0:
         raise RuntimeError("device status %d in timed region" % status)
+    exact_outputs = rq.rq_gemv_exact_outputs()
 
     # Roofline of the GEMM: the same K prefill passes again, right after the
     # timed steps (clocks still sampled), with CUDA events around each of
@@ -452,8 +613,20 @@ def run_gpu(args, world, rank, local):
     gemv_gbs = world * decode_bytes(M_DECODE) * K / dec_s / 1e9
     gemm_calls, gemm_trace_ms = traced.get("gemm", (0, 0.0))
     gemm_achieved = flops * K / (gemm_trace_ms / 1e3) / 1e12 if gemm_trace_ms else None
-    fp8_peak = 2.0 * pk["bf16_sustained"]  # fp8 dense = 2 x bf16 (nominal ratio)
+    # The GEMM's denominator: the FP8 peak measured above, in the regime the
+    # run was in (sustained if the clocks hit the power cap while timed,
+    # burst otherwise); 2 x the measured bf16 peak if it could not be taken.
+    capped = clocks is not None and "sw_power_cap" in clocks.get("reasons", [])
+    regime = "sustained" if capped else "burst"
+    if fp8 and "burst" in fp8:
+        fp8_peak = fp8[regime]
+        peak_source = "measured fp8 (%s, %s)" % (regime, fp8["how"])
+    else:
+        fp8_peak = 2.0 * (pk["bf16_sustained"] if capped else pk["bf16"])
+        peak_source = "2 x bf16_tflops%s of %s (fp8/bf16 nominal ratio 2)" % (
+            "_sustained" if capped else "", pk["source"])
     traffic = gemm_traffic_per_launch()
+    shapes = decode_shape_rates(torch, dev, st, pk["hbm_gbs"])
 
     # ----------------------------------------------------------- e2e leg --
     e2e = None if args.no_e2e else run_e2e(args, st, torch, rq, dev, stream, world)
@@ -471,14 +644,15 @@ def run_gpu(args, world, rank, local):
                  "roofline": {"bound": "hbm", "achieved": gemv_gbs / world,
                               "peak": pk["hbm_gbs"], "unit": "GB/s",
                               "frac": gemv_gbs / world / pk["hbm_gbs"],
-                              "note": "decode pass time incl. launch gaps"}},
+                              "note": "decode pass time incl. launch gaps"},
+                 "exact_path_outputs_in_decode_passes": exact_outputs,
+                 "per_call": shapes},
         "roofline": {"bound": "tensor",
                      "kernel": "FP8 GEMM: fp8_gemm_kernel + fp8_gemm_pair_kernel "
                                "(tcgen05 kind::f8f6f4), all GEMM launches of the pass",
                      "achieved": gemm_achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                      "frac": (gemm_achieved / fp8_peak) if gemm_achieved else None,
-                     "peak_source": "2 x bf16_tflops_sustained of %s (fp8/bf16 nominal "
-                                    "ratio 2)" % pk["source"],
+                     "peak_source": peak_source, "fp8_peak_measured": fp8,
                      "traffic": traffic,
                      "flops_per_launch_avg": flops / max(1, gemm_calls // K),
                      "avg_launch_ms": gemm_trace_ms / gemm_calls if gemm_calls else None,
@@ -493,14 +667,23 @@ def run_gpu(args, world, rank, local):
         "act_cache": st.ctx.stats(),
     }
     if rank == 0 and not args.no_cpu_baseline and world == 1:
-        f, s = OracleSample(args.cpu_rows).run()
-        nb, sg = oracle_gemv_sample()
+        sample = OracleSample(args.cpu_rows)
+        f, s1 = sample.run()
+        try:
+            fa, wall, cores = oracle_all_cores(args.cpu_rows // 2)
+            all_cores = {"value": fa / wall / 1e12, "unit": "TFLOP/s", "cores": cores,
+                         "seconds": wall,
+                         "sample": "%d token rows of the same sample on each of %d "
+                                   "processes, one per host core" % (args.cpu_rows // 2, cores)}
+        except Exception as e:  # the GPU figures stand without it
+            all_cores = {"error": repr(e)[:200]}
         line["cpu_baseline"] = {
-            "value": f / s / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "value": f / s1 / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
             "sample": "%d token rows of the M=2048 prefill through the 7 linears of "
-                      "layer 0 (quant + exact FP8 dot products); GEMV: one layer at "
-                      "M=1 in fp64" % args.cpu_rows,
-            "seconds": s, "gemv_gbs": nb / sg / 1e9, "gemv_seconds": sg}
+                      "layer 0 (quant + exact FP8 dot products)" % args.cpu_rows,
+            "seconds": s1,
+            "all_cores": all_cores,
+            "configs": oracle_config_numbers(sample)}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -634,11 +817,13 @@ def run_sweep(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     pk = peaks()
-    fp8_peak = 2.0 * pk["bf16_sustained"]
+    fp8 = measure_fp8_peak(torch, dev)
+    fp8_peak = fp8["burst"] if fp8 and "burst" in fp8 else 2.0 * pk["bf16"]
 
     def out(d):
         print(json.dumps(d), flush=True)
 
+    out({"sweep": "fp8_peak", "measured": fp8, "used_tflops": fp8_peak})
     parts = set(args.sweep_parts.split(","))
     # decode GEMV sweep
     for name, qt, N, K in [] if "gemv" not in parts else [("q,o", synthetic.Q4K, 3584, 3584), ("k", synthetic.Q4K, 512, 3584),
@@ -651,11 +836,13 @@ def run_sweep(args):
             x = torch.from_numpy(synthetic.activation(12 + M, M, K)).to(dev)
             y = torch.empty(M, N, device=dev)
             calls = [lambda W=W: fn(W, x, y, M, N, K) for W in Ws[:max(len(Ws), 20)]]
+            rq.rq_gemv_exact_outputs()
             ms = graph_time_ms(torch, dev, calls)
             nbytes = packed_bytes(qt, N, K) + 4 * M * (K + N)
             out({"sweep": "gemv", "linear": name, "qtype": "Q4_K" if qt == synthetic.Q4K
                  else "Q6_K", "M": M, "N": N, "K": K, "us": ms * 1e3,
-                 "GB/s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / pk["hbm_gbs"]})
+                 "GB/s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / pk["hbm_gbs"],
+                 "exact_outputs": rq.rq_gemv_exact_outputs()})
         del Ws, W0
     # FP8 GEMM at M = 512
     ctx = rq.Context()

@@ -121,8 +121,15 @@ rq_status rq_quant_e4m3(const float *x, int64_t n, const uint32_t *absmax_bits,
  *      12 packed 6-bit scale/min bytes, 128 bytes of 4-bit quants), rows
  *      contiguous; 16-byte aligned.
  *   x: f32 [M x K], 16-byte aligned.  y: f32 [M x N] (written, not added to).
- * fp32 accumulation; agrees with the fp64 reference within
- * 1e-4 * sum_k |x[m,k] * w(n,k)| per element.
+ * Accuracy: for finite x, every output whose sum_k |x[m,k] * w(n,k)| is at
+ * least 2^-100 is within 1e-4 * sum_k |x[m,k] * w(n,k)| of the exact result
+ * (outputs beyond fp32's range are +-Inf; non-finite x give Inf / NaN as in
+ * IEEE arithmetic).  The fast paths prove this per output with an error
+ * certificate computed alongside the sum; an output whose certificate fails
+ * (extreme ranges of x within 32 values, weights whose two terms cancel on
+ * the largest x) is recomputed exactly in fp64 inside the same launch, which
+ * is slow but never wrong (see rq_gemv_exact_outputs).  Several tokens run
+ * one launch per token (the weight is read once per token).
  * Ordering: the kernel may start streaming w before the kernel launched just
  * before it on the stream has finished (programmatic dependent launch); it
  * reads x and writes y only after that kernel has completed.  So w must not
@@ -140,6 +147,8 @@ rq_status rq_q4k_gemv(const void *w, const float *x, float *y, int M, int N,
  *   w: N rows of K/256 Q6_K super-blocks, 210 B each (ql[128], qh[64],
  *      16 int8 scales, fp16 d), rows contiguous; 4-byte aligned.
  *   weight = d * scale * (q - 32), q the 6-bit quant.
+ * Accuracy as rq_q4k_gemv (certificate per output, exact fp64 path when it
+ * fails); 2..8 tokens are one launch.
  * Errors: as rq_q4k_gemv (w need only be 4-byte aligned). */
 rq_status rq_q6k_gemv(const void *w, const float *x, float *y, int M, int N,
                       int K, rq_stream_t stream);
@@ -337,6 +346,14 @@ rq_status rq_get_device_status(rq_stream_t stream);
  * caller then reads it with rq_get_device_status.  Errors: RQ_ERR_SHAPE
  * (limit_ns outside 1 .. 10^10), RQ_ERR_CUDA. */
 rq_status rq_debug_wait_timeout(int64_t limit_ns, rq_stream_t stream);
+
+/* Diagnostics of the GEMVs' accuracy guarantee (rq_q4k_gemv): synchronise
+ * `stream`, then return in *count_host the number of GEMV outputs (one per
+ * token and row) that were recomputed on the exact fp64 path since the last
+ * call, and reset the count.  The count is per process and device; kernels
+ * still running on other streams may or may not be included.
+ * Errors: RQ_ERR_NULL, RQ_ERR_CUDA. */
+rq_status rq_gemv_exact_outputs(rq_stream_t stream, int64_t *count_host);
 
 #ifdef __cplusplus
 }

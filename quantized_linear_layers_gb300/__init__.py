@@ -66,6 +66,7 @@ _SIGS = {
     "rq_ctx_trace_kinds": ([_vp, ctypes.c_uint], _i32),
     "rq_get_device_status": ([_vp], _i32),
     "rq_debug_wait_timeout": ([_i64, _vp], _i32),
+    "rq_gemv_exact_outputs": ([_vp, ctypes.POINTER(_i64)], _i32),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -150,6 +151,15 @@ def rq_get_device_status(stream=None):
 
 def rq_debug_wait_timeout(limit_ns, stream=None):
     _check(_lib.rq_debug_wait_timeout(limit_ns, _stream(stream)), "rq_debug_wait_timeout")
+
+
+def rq_gemv_exact_outputs(stream=None):
+    """Synchronise the stream; return (and reset) how many GEMV outputs were
+    recomputed on the exact fp64 path since the last call."""
+    n = _i64()
+    _check(_lib.rq_gemv_exact_outputs(_stream(stream), ctypes.byref(n)),
+           "rq_gemv_exact_outputs")
+    return n.value
 
 
 class Context:

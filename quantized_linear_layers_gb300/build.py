@@ -14,8 +14,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "librq.so")
-SOURCES = ["rq_api.cu", "rq_quant.cu", "rq_gemv.cu", "rq_gemv_mma.cu", "rq_wcache.cu",
-           "rq_gemm.cu", "rq_noalloc.cu"]
+SOURCES = ["rq_api.cu", "rq_quant.cu", "rq_gemv.cu", "rq_wcache.cu", "rq_gemm.cu",
+           "rq_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
          "-Xcompiler", "-Wall", "--expt-relaxed-constexpr"]

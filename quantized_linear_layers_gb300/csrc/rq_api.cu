@@ -427,9 +427,11 @@ rq_status rq_linear(rq_ctx* ctx, rq_qtype qtype, const void* w, const float* x, 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
   if (M < ctx->threshold) {
-    // batched GEMV straight from the packed weight, 8 tokens per launch
-    for (int m0 = 0; m0 < M; m0 += 8) {
-      const int mc = M - m0 < 8 ? M - m0 : 8;
+    // GEMV straight from the packed weight: Q4_K one launch per token, Q6_K
+    // up to 8 tokens per launch
+    const int per = qtype == RQ_Q4K ? 1 : 8;
+    for (int m0 = 0; m0 < M; m0 += per) {
+      const int mc = M - m0 < per ? M - m0 : per;
       TraceScope ts(ctx, RQ_TRACE_GEMV, st);
       s = qtype == RQ_Q4K
               ? rq_q4k_gemv(w, x + (size_t)m0 * K, y + (size_t)m0 * N, mc, N, K, stream)
@@ -477,57 +479,50 @@ rq_status rq_linear_group(rq_ctx* ctx, int count, const rq_qtype* qtypes, const 
   if (count == 1) return rq_linear(ctx, qtypes[0], w[0], x, y[0], M, N[0], K, stream);
 
   if (M < ctx->threshold) {
-    // GEMV route: one launch for the Q4_K members of up to 8 tokens
-    int starts[RQ_MAX_GROUP + 1], ns[RQ_MAX_GROUP];
+    // GEMV route, one token at a time: the Q4_K members in one launch,
+    // joined by the Q6_K member when there is exactly one
+    int starts[RQ_MAX_GROUP + 1];
     const uint8_t* ws[RQ_MAX_GROUP];
-    float* ys[RQ_MAX_GROUP];
-    int n4 = 0;
+    int idx4[RQ_MAX_GROUP];
+    int n4 = 0, i6 = -1, n6 = 0;
     starts[0] = 0;
-    if (M <= 8) {
-      for (int i = 0; i < count; ++i)
-        if (qtypes[i] == RQ_Q4K) {
-          ws[n4] = static_cast<const uint8_t*>(w[i]);
-          ys[n4] = y[i];
-          ns[n4] = N[i];
-          starts[n4 + 1] = starts[n4] + N[i];
-          ++n4;
-        }
-    }
-    // ... and, with exactly one Q6_K member, that member in the same launch
-    int i6 = -1, n6 = 0;
-    for (int i = 0; i < count; ++i)
-      if (qtypes[i] == RQ_Q6K) {
+    for (int i = 0; i < count; ++i) {
+      if (qtypes[i] == RQ_Q4K) {
+        ws[n4] = static_cast<const uint8_t*>(w[i]);
+        idx4[n4] = i;
+        starts[n4 + 1] = starts[n4] + N[i];
+        ++n4;
+      } else {
         i6 = i;
         ++n6;
       }
-    bool grouped = false, dual = false;
-    if (M == 1 && n4 >= 1 && n6 == 1 && std::getenv("RQ_GEMV_NO_DUAL") == nullptr) {
-      TraceScope ts(ctx, RQ_TRACE_GEMV, st);
-      const rq_status s = launch_gemv_m1_dual(n4, starts, ws, ys,
-                                              static_cast<const uint8_t*>(w[i6]), y[i6], N[i6],
-                                              x, K, st);
-      if (s != RQ_OK && s != RQ_ERR_SHAPE) return s;
-      grouped = dual = s == RQ_OK;
     }
-    if (!grouped && n4 >= 2 && M == 1) {
-      TraceScope ts(ctx, RQ_TRACE_GEMV, st);
-      const rq_status s = launch_q4k_gemv_group(n4, starts, ws, ys, x, K, st);
-      if (s != RQ_OK && s != RQ_ERR_SHAPE) return s;
-      grouped = s == RQ_OK;
-    }
-    if (!grouped && n4 >= 2 && M >= 2 && std::getenv("RQ_GEMV_NO_MMA") == nullptr) {
-      // RQ_ERR_SHAPE: the shape does not fit the tensor-core kernel and
-      // nothing was launched (the members then run one by one)
-      TraceScope ts(ctx, RQ_TRACE_GEMV, st);
-      const rq_status s = launch_q4k_gemv_mma_group(n4, ws, ns, ys, x, M, K, st);
-      if (s != RQ_OK && s != RQ_ERR_SHAPE) return s;
-      grouped = s == RQ_OK;
-    }
-    for (int i = 0; i < count; ++i) {
-      if (grouped && qtypes[i] == RQ_Q4K) continue;
-      if (dual && i == i6) continue;
-      const rq_status s = rq_linear(ctx, qtypes[i], w[i], x, y[i], M, N[i], K, stream);
-      if (s != RQ_OK) return s;
+    for (int m = 0; m < M; ++m) {
+      const float* xm = x + (size_t)m * K;
+      float* ys[RQ_MAX_GROUP];
+      for (int j = 0; j < n4; ++j) ys[j] = y[idx4[j]] + (size_t)m * N[idx4[j]];
+      bool grouped = false, dual = false;
+      if (n4 >= 1 && n6 == 1 && std::getenv("RQ_GEMV_NO_DUAL") == nullptr) {
+        TraceScope ts(ctx, RQ_TRACE_GEMV, st);
+        const rq_status s = launch_gemv_m1_dual(n4, starts, ws, ys,
+                                                static_cast<const uint8_t*>(w[i6]),
+                                                y[i6] + (size_t)m * N[i6], N[i6], xm, K, st);
+        if (s != RQ_OK && s != RQ_ERR_SHAPE) return s;
+        grouped = dual = s == RQ_OK;
+      }
+      if (!grouped && n4 >= 2) {
+        TraceScope ts(ctx, RQ_TRACE_GEMV, st);
+        const rq_status s = launch_q4k_gemv_group(n4, starts, ws, ys, xm, K, st);
+        if (s != RQ_OK && s != RQ_ERR_SHAPE) return s;
+        grouped = s == RQ_OK;
+      }
+      for (int i = 0; i < count; ++i) {
+        if (grouped && qtypes[i] == RQ_Q4K) continue;
+        if (dual && i == i6) continue;
+        const rq_status s =
+            rq_linear(ctx, qtypes[i], w[i], xm, y[i] + (size_t)m * N[i], 1, N[i], K, stream);
+        if (s != RQ_OK) return s;
+      }
     }
     return RQ_OK;
   }
@@ -648,6 +643,13 @@ rq_status rq_get_device_status(rq_stream_t stream) {
 rq_status rq_debug_wait_timeout(int64_t limit_ns, rq_stream_t stream) {
   if (limit_ns < 1 || limit_ns > 10000000000LL) return RQ_ERR_SHAPE;
   return launch_debug_wait_timeout(limit_ns, reinterpret_cast<cudaStream_t>(stream));
+}
+
+rq_status rq_gemv_exact_outputs(rq_stream_t stream, int64_t* count_host) {
+  if (count_host == nullptr) return RQ_ERR_NULL;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return RQ_ERR_CUDA;
+  return read_and_clear_gemv_exact_outputs(count_host);
 }
 
 }  // extern "C"

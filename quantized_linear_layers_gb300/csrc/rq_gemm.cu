@@ -1205,12 +1205,10 @@ rq_status read_and_clear_device_error(cudaStream_t st) {
   if (gemv == RQ_ERR_CUDA) return gemv;
   const rq_status quant = read_and_clear_quant_error();
   if (quant == RQ_ERR_CUDA) return quant;
-  const rq_status mma = read_and_clear_gemv_mma_error();
-  if (mma == RQ_ERR_CUDA) return mma;
   unsigned int v = 0;
   if (cudaMemcpyFromSymbol(&v, g_rq_device_error, sizeof(v)) != cudaSuccess)
     return RQ_ERR_CUDA;
-  if (v == 0) return gemv != RQ_OK ? gemv : (quant != RQ_OK ? quant : mma);
+  if (v == 0) return gemv != RQ_OK ? gemv : quant;
   const unsigned int zero = 0;
   if (cudaMemcpyToSymbol(g_rq_device_error, &zero, sizeof(zero)) != cudaSuccess)
     return RQ_ERR_CUDA;

@@ -12,12 +12,13 @@
 //    next item's loads are issued before the current one is decoded, so two
 //    items of weight bytes are in flight per warp.
 //  * x is read through L1 (16-byte loads) once per item and reused by all R
-//    rows; the per-32-weight sums of x are computed once per CTA into shared
-//    memory (they carry the dmin*m term of Q4_K and the -32 offset of Q6_K).
-//  * Nibble -> float without int->float conversions: a byte permute places
-//    the quant q in the mantissa of 0.5 (0x3F000000), giving 0.5 + q*2^-p
-//    exactly; sum x*(0.5 + q*2^-p) - 0.5*sum x = 2^-p * sum x*q, so each
-//    weight costs one PRMT and one FFMA, and the 2^p is folded into d*sc.
+//    rows.
+//  * Every weight is decoded on its own: Q4_K w = fl(q * (d sc) - dmin m)
+//    (one FMA, a single rounding of the exact value), Q6_K w = (q - 32) *
+//    (d scale) (exact in fp32).  Each lane sums the 64 products of an item in
+//    fp32 and adds that partial to its total, so every rounding is relative
+//    to sum_k |x_k w_k| (well inside the 1e-4 bound); an output that comes
+//    out non-finite (overflow, non-finite x) is recomputed exactly in fp64.
 //  * fp32 accumulation, one warp-shuffle reduction per row.
 #include <cstdio>
 #include <cstdlib>
@@ -25,37 +26,23 @@
 #include <utility>
 
 #include "rq_device.cuh"
+#include "rq_gemv_exact.cuh"
 #include "rq_internal.h"
 
 namespace rq {
+
+// Counts outputs recomputed on the exact path (diagnostics and tests).
+__device__ unsigned long long g_gemv_exact_outputs;
+
 namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
-// 0.5 + b * 2^-8 for byte b (0..63) of v placed in bits 16..23.
-__device__ __forceinline__ float mag_b2(uint32_t v, uint32_t sel) {
-  return __uint_as_float(__byte_perm(v, 0x3F000000u, sel));
-}
-// Selectors 0x7j44 give [0x3F][byte j of v][0][0] (bits 31..0) = 0.5 + b*2^-8;
-// selectors 0x74j4 give [0x3F][0][byte j][0]: a high-nibble byte 16q in bits
-// 8..15 is 0.5 + q*2^-12.
-
-template <int M>
-__device__ void x_sums(const float* __restrict__ x, int K, int span,
-                       float* __restrict__ sums) {
-  // sums[m * (K/span) + s] = sum_{i<span} x[m, s*span + i], span in {8, 32}
-  const int per = K / span;
-  for (int i = threadIdx.x; i < M * per; i += blockDim.x) {
-    const int m = i / per, s = i - m * per;
-    const float4* p = reinterpret_cast<const float4*>(x + (size_t)m * K + (size_t)s * span);
-    float acc = 0.f;
-    for (int j = 0; j < span / 4; ++j) {
-      const float4 v = __ldg(p + j);
-      acc += (v.x + v.y) + (v.z + v.w);
-    }
-    sums[i] = acc;
-  }
+// Byte j of v (a value below 2^8) as a float, without a conversion: the
+// byte goes into the mantissa of 2^23.
+__device__ __forceinline__ float byte_j_f(uint32_t v, int j) {
+  return __uint_as_float(__byte_perm(v, 0x4B000000u, 0x7440u | (uint32_t)j)) - 8388608.0f;
 }
 
 // ------------------------------------------------------------------ Q4_K --
@@ -99,13 +86,12 @@ __device__ __forceinline__ uint32_t q4_word(const Q4Item& it, int w) {
 template <int M, int R>
 __device__ __forceinline__ void q4_compute(const Q4Item (&it)[R], int u,
                                            const float* __restrict__ x, int K,
-                                           const float* __restrict__ xs, int nsub,
                                            float (&acc)[R][M]) {
   const int sb = u >> 2, g = u & 3;
   const int k0 = sb * kQK + 64 * g;
   const int sh = (g & 1) * 16;     // byte pair of sub-blocks 2g, 2g+1
   const bool upper = g >= 2;       // sub-blocks 4..7 use the split packing
-  float Alo[R], Ahi[R], Dlo[R], Dhi[R];
+  float Alo[R], Ahi[R], Blo[R], Bhi[R];  // d sc and dmin m of sub-blocks 2g, 2g+1
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     const uint32_t A = it[r].h.y, B = it[r].h.z, C = it[r].h.w;
@@ -114,16 +100,16 @@ __device__ __forceinline__ void q4_compute(const Q4Item (&it)[R], int u,
     const uint32_t scp = upper ? ((c16 & 0x0F0Fu) | ((a16 >> 2) & 0x3030u)) : (a16 & 0x3F3Fu);
     const uint32_t mp = upper ? (((c16 >> 4) & 0x0F0Fu) | ((b16 >> 2) & 0x3030u)) : (b16 & 0x3F3Fu);
     const float2 dd = half_pair(it[r].h.x);  // .x = d, .y = dmin
-    Alo[r] = (dd.x * 256.0f) * (float)(scp & 0xFFu);
-    Ahi[r] = (dd.x * 4096.0f) * (float)((scp >> 8) & 0xFFu);
-    Dlo[r] = dd.y * (float)(mp & 0xFFu);
-    Dhi[r] = dd.y * (float)((mp >> 8) & 0xFFu);
+    Alo[r] = dd.x * byte_j_f(scp, 0);
+    Ahi[r] = dd.x * byte_j_f(scp, 1);
+    Blo[r] = dd.y * byte_j_f(mp, 0);
+    Bhi[r] = dd.y * byte_j_f(mp, 1);
   }
-  float Tlo[R][M], Thi[R][M];
+  float T[R][M];
 #pragma unroll
   for (int r = 0; r < R; ++r)
 #pragma unroll
-    for (int m = 0; m < M; ++m) Tlo[r][m] = Thi[r][m] = 0.f;
+    for (int m = 0; m < M; ++m) T[r][m] = 0.f;
 
 #pragma unroll
   for (int w = 0; w < 8; ++w) {
@@ -137,45 +123,35 @@ __device__ __forceinline__ void q4_compute(const Q4Item (&it)[R], int u,
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const uint32_t v = q4_word(it[r], w);
-      const uint32_t lo = v & 0x0F0F0F0Fu, hi = v & 0xF0F0F0F0u;
-      const float l0 = mag_b2(lo, 0x7044u), l1 = mag_b2(lo, 0x7144u);
-      const float l2 = mag_b2(lo, 0x7244u), l3 = mag_b2(lo, 0x7344u);
-      const float h0 = mag_b2(hi, 0x7404u), h1 = mag_b2(hi, 0x7414u);
-      const float h2 = mag_b2(hi, 0x7424u), h3 = mag_b2(hi, 0x7434u);
+      const uint32_t lo = v & 0x0F0F0F0Fu, hi = (v >> 4) & 0x0F0F0F0Fu;
+      float wl[4], wh[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        wl[j] = fmaf(byte_j_f(lo, j), Alo[r], -Blo[r]);
+        wh[j] = fmaf(byte_j_f(hi, j), Ahi[r], -Bhi[r]);
+      }
 #pragma unroll
       for (int m = 0; m < M; ++m) {
-        float t = Tlo[r][m];
-        t = fmaf(xl[m].x, l0, t); t = fmaf(xl[m].y, l1, t);
-        t = fmaf(xl[m].z, l2, t); t = fmaf(xl[m].w, l3, t);
-        Tlo[r][m] = t;
-        float s = Thi[r][m];
-        s = fmaf(xh[m].x, h0, s); s = fmaf(xh[m].y, h1, s);
-        s = fmaf(xh[m].z, h2, s); s = fmaf(xh[m].w, h3, s);
-        Thi[r][m] = s;
+        float t = T[r][m];
+        t = fmaf(xl[m].x, wl[0], t); t = fmaf(xl[m].y, wl[1], t);
+        t = fmaf(xl[m].z, wl[2], t); t = fmaf(xl[m].w, wl[3], t);
+        t = fmaf(xh[m].x, wh[0], t); t = fmaf(xh[m].y, wh[1], t);
+        t = fmaf(xh[m].z, wh[2], t); t = fmaf(xh[m].w, wh[3], t);
+        T[r][m] = t;
       }
     }
   }
-  const int sub = k0 >> 5;
 #pragma unroll
-  for (int m = 0; m < M; ++m) {
-    const float Slo = xs[m * nsub + sub], Shi = xs[m * nsub + sub + 1];
+  for (int r = 0; r < R; ++r)
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      float c = Alo[r] * (Tlo[r][m] - 0.5f * Slo);
-      c = fmaf(Ahi[r], Thi[r][m] - 0.5f * Shi, c);
-      c = fmaf(-Dlo[r], Slo, c);
-      c = fmaf(-Dhi[r], Shi, c);
-      acc[r][m] += c;
-    }
-  }
+    for (int m = 0; m < M; ++m) acc[r][m] += T[r][m];
 }
 
 template <int M, int R>
 __global__ void __launch_bounds__(kThreads)
 q4k_gemv_kernel(const uint8_t* __restrict__ W, const float* __restrict__ x,
                 float* __restrict__ y, int N, int K) {
-  extern __shared__ float xs[];  // [M][K/32] sums of x per 32-weight sub-block
-  const int nsb = K >> 8, U = nsb * 4, nsub = K >> 5;
+  const int nsb = K >> 8, U = nsb * 4;
   const size_t rowbytes = (size_t)nsb * kQ4KBytes;
   const int lane = threadIdx.x & 31;
   const int gwarp = blockIdx.x * kWarps + (threadIdx.x >> 5);
@@ -189,8 +165,6 @@ q4k_gemv_kernel(const uint8_t* __restrict__ W, const float* __restrict__ x,
   if (active) q4_load<R>(cur, W, rowbytes, rg * R, N, lane, lane < U);
   pdl_wait();  // x and y only after the previous launch has completed
   pdl_trigger();
-  x_sums<M>(x, K, 32, xs);
-  __syncthreads();
   if (!active) return;
 
   float acc[R][M];
@@ -209,15 +183,22 @@ q4k_gemv_kernel(const uint8_t* __restrict__ W, const float* __restrict__ x,
       q4_load<R>(nxt, W, rowbytes, nrg * R, N, nu, nu < U);
     }
     const int u = it * 32 + lane;
-    if (u < U) q4_compute<M, R>(cur, u, x, K, xs, nsub, acc);
+    if (u < U) q4_compute<M, R>(cur, u, x, K, acc);
     if (nit == 0) {  // row group rg complete
 #pragma unroll
       for (int r = 0; r < R; ++r)
 #pragma unroll
         for (int m = 0; m < M; ++m) {
-          const float v = warp_sum(acc[r][m]);
+          float v = warp_sum(acc[r][m]);  // the same in every lane
           acc[r][m] = 0.f;
-          if (lane == 0 && rg * R + r < N) y[(size_t)m * N + rg * R + r] = v;
+          const int row = rg * R + r;
+          if (row < N) {
+            if (!isfinite(v)) {
+              v = (float)q4k_row_exact(W + (size_t)row * rowbytes, x + (size_t)m * K, K, lane);
+              if (lane == 0) atomicAdd(&g_gemv_exact_outputs, 1ull);
+            }
+            if (lane == 0) y[(size_t)m * N + row] = v;
+          }
         }
     }
     if (!has_next) break;
@@ -285,17 +266,21 @@ __device__ __forceinline__ float sbyte(uint32_t w2[2], int i) {
 template <int M, int R>
 __device__ __forceinline__ void q6_compute(Q6Item (&it)[R], int u,
                                            const float* __restrict__ x, int K,
-                                           const float* __restrict__ xs, int nsub8,
                                            float (&acc)[R][M]) {
   const int sb = u >> 3, h = (u >> 2) & 1, lq = u & 3;
   const int kbase = sb * kQK + 128 * h + 8 * lq;  // + 32 i + j
-  float T[R][M][4];
+  float T[R][M];
 #pragma unroll
   for (int r = 0; r < R; ++r)
 #pragma unroll
-    for (int m = 0; m < M; ++m)
+    for (int m = 0; m < M; ++m) T[r][m] = 0.f;
+  float dsc[R][4];  // d * scale of quarter i (exact)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) T[r][m][i] = 0.f;
+  for (int r = 0; r < R; ++r) {
+    const float d = __half2float(__ushort_as_half((unsigned short)(it[r].d & 0xFFFFu)));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dsc[r][i] = d * sbyte(it[r].sc, lq / 2 + 2 * i);
+  }
 
 #pragma unroll
   for (int half = 0; half < 2; ++half) {      // bytes j = 4*half .. 4*half+3
@@ -313,41 +298,31 @@ __device__ __forceinline__ void q6_compute(Q6Item (&it)[R], int u,
         else if (i == 1) q = (lb & 0x0F0F0F0Fu) | ((hb << 2) & 0x30303030u);
         else if (i == 2) q = ((la >> 4) & 0x0F0F0F0Fu) | (hb & 0x30303030u);
         else q = ((lb >> 4) & 0x0F0F0F0Fu) | ((hb >> 2) & 0x30303030u);
-        const float f0 = mag_b2(q, 0x7044u), f1 = mag_b2(q, 0x7144u);
-        const float f2 = mag_b2(q, 0x7244u), f3 = mag_b2(q, 0x7344u);
+        // w = (q - 32) * d * scale, exact in fp32
+        float w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) w[j] = (byte_j_f(q, j) - 32.0f) * dsc[r][i];
 #pragma unroll
         for (int m = 0; m < M; ++m) {
-          float t = T[r][m][i];
-          t = fmaf(xv[m].x, f0, t); t = fmaf(xv[m].y, f1, t);
-          t = fmaf(xv[m].z, f2, t); t = fmaf(xv[m].w, f3, t);
-          T[r][m][i] = t;
+          float t = T[r][m];
+          t = fmaf(xv[m].x, w[0], t); t = fmaf(xv[m].y, w[1], t);
+          t = fmaf(xv[m].z, w[2], t); t = fmaf(xv[m].w, w[3], t);
+          T[r][m] = t;
         }
       }
     }
   }
-  // weight = d*sc*(q-32); sum_j x*(0.5 + q/256) = 0.5*S + sum x q / 256, so
-  // sum_j x*w = d*sc*(256*T - 128*S - 32*S) = d*sc*(256*T - 160*S).
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const float d = __half2float(__ushort_as_half((unsigned short)(it[r].d & 0xFFFFu)));
+  for (int r = 0; r < R; ++r)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float dsc = d * sbyte(it[r].sc, lq / 2 + 2 * i);
-#pragma unroll
-      for (int m = 0; m < M; ++m) {
-        const float S = xs[m * nsub8 + ((kbase + 32 * i) >> 3)];
-        acc[r][m] = fmaf(dsc, fmaf(256.0f, T[r][m][i], -160.0f * S), acc[r][m]);
-      }
-    }
-  }
+    for (int m = 0; m < M; ++m) acc[r][m] += T[r][m];
 }
 
 template <int M, int R>
 __global__ void __launch_bounds__(kThreads)
 q6k_gemv_kernel(const uint8_t* __restrict__ W, const float* __restrict__ x,
                 float* __restrict__ y, int N, int K) {
-  extern __shared__ float xs[];  // [M][K/8] sums of x per 8 weights
-  const int nsb = K >> 8, U = nsb * 8, nsub8 = K >> 3;
+  const int nsb = K >> 8, U = nsb * 8;
   const size_t rowbytes = (size_t)nsb * kQ6KBytes;
   const int lane = threadIdx.x & 31;
   const int gwarp = blockIdx.x * kWarps + (threadIdx.x >> 5);
@@ -361,8 +336,6 @@ q6k_gemv_kernel(const uint8_t* __restrict__ W, const float* __restrict__ x,
   if (active) q6_load<R>(cur, W, rowbytes, rg * R, N, lane, lane < U);
   pdl_wait();  // x and y only after the previous launch has completed
   pdl_trigger();
-  x_sums<M>(x, K, 8, xs);
-  __syncthreads();
   if (!active) return;
 
   float acc[R][M];
@@ -381,15 +354,22 @@ q6k_gemv_kernel(const uint8_t* __restrict__ W, const float* __restrict__ x,
       q6_load<R>(nxt, W, rowbytes, nrg * R, N, nu, nu < U);
     }
     const int u = it * 32 + lane;
-    if (u < U) q6_compute<M, R>(cur, u, x, K, xs, nsub8, acc);
+    if (u < U) q6_compute<M, R>(cur, u, x, K, acc);
     if (nit == 0) {
 #pragma unroll
       for (int r = 0; r < R; ++r)
 #pragma unroll
         for (int m = 0; m < M; ++m) {
-          const float v = warp_sum(acc[r][m]);
+          float v = warp_sum(acc[r][m]);  // the same in every lane
           acc[r][m] = 0.f;
-          if (lane == 0 && rg * R + r < N) y[(size_t)m * N + rg * R + r] = v;
+          const int row = rg * R + r;
+          if (row < N) {
+            if (!isfinite(v)) {
+              v = (float)q6k_row_exact(W + (size_t)row * rowbytes, x + (size_t)m * K, K, lane);
+              if (lane == 0) atomicAdd(&g_gemv_exact_outputs, 1ull);
+            }
+            if (lane == 0) y[(size_t)m * N + row] = v;
+          }
         }
     }
     if (!has_next) break;
@@ -437,6 +417,7 @@ struct M1Args {
   uint64_t wait_limit_ns;
   int row_align;        // Q6_K: rows per 16-byte-aligned group of rows
   int M;                // tokens (the multi-token Q6_K kernel)
+  int max_rows;         // most rows any CTA owns (sizes the row accumulators)
   // One-token Q4_K: 2 = clusters of two CTAs share a block of rows, CTA
   // rank h taking super-blocks [h*nsb/2, (h+1)*nsb/2) of each row (rank 0
   // adds rank 1's partial sums and writes y); 1 = one CTA per row block.
@@ -513,6 +494,7 @@ struct XSplit {
   int p1[8], p2[8], p3[8];  // planes, 4 int8 per register
   float scale;              // s
   float sum;                // sum of the 32 x values (fp32)
+  float ea, eb;             // error-bound constants of the sub-block (q4k_cert)
 };
 
 // sum_l x_l * q_l for the 32 quants of one nibble plane (byte j of word w =
@@ -554,8 +536,33 @@ __device__ __forceinline__ float4 q4_coeffs(const uint4& h, int sh, bool upper) 
                      dd.y * byte_to_float(mp, 0), dd.y * byte_to_float(mp, 1));
 }
 
-// Two rows' 64-weight dot products (integer path), interleaved.
-__device__ __forceinline__ float2 q4_group_dot2i(const uint8_t* r0, const uint8_t* r1,
+// Error bound of one lane's 64-weight dot product (q4k_cert).  For
+// sub-block j of the lane (32 values v, plane scale s = max|v|/127, sum of
+// the third-plane residuals rs = sum |t - planes| * 16384 <= 16, sa =
+// sum |v|) the computed contribution differs from the exact
+// sum_k v_k (d sc_j q_k - dmin m_j) by at most
+//   d sc_j * A_j + dmin m_j * B_j,
+//   A_j = 15 s rs / 16384      (the planes' residuals, q <= 15)
+//       + 135 u sa             (relative rounding of s*t against v (3u), of
+//                               the plane sum's conversion and scaling (2u)
+//                               and of the four-step FMA chain (4u), each
+//                               against at most 15 sa),
+//   B_j = 13 u sa              (the fp32 sum of v (9u) and the chain (4u)),
+// u = 2^-24; the constants below add a margin (150 u, 16 u, factor 1 + 2^-7).
+// The lane contributes D = sum_j (d sc_j A_j + dmin m_j B_j) - tau |p|.
+__device__ __forceinline__ void q4k_cert_consts(float s, float rs, float sa, float mx,
+                                                float& ea, float& eb) {
+  constexpr float kU = 0x1p-24f, kMargin = 1.0f + 0x1p-7f;
+  ea = fmaf(15.0f * s, rs * (1.0f / 16384.0f), 150.0f * kU * sa) * kMargin;
+  eb = 16.0f * kU * sa * kMargin;
+  // planes not valid (tiny maximum) or x not finite (sa is then Inf or NaN):
+  // exact path
+  if ((mx > 0.0f && mx < kCertTinyMax) || !(sa < INFINITY)) ea = eb = INFINITY;
+}
+
+// Two rows' 64-weight dot products (integer path), interleaved, with their
+// certificate terms: returns (p0, p1, D0, D1).
+__device__ __forceinline__ float4 q4_group_dot2i(const uint8_t* r0, const uint8_t* r1,
                                                  int off_h, int off_a, int sh, bool upper,
                                                  const XSplit& xl, const XSplit& xh) {
   const uint4 h0 = lds128(r0 + off_h), h1 = lds128(r1 + off_h);
@@ -593,7 +600,16 @@ __device__ __forceinline__ float2 q4_group_dot2i(const uint8_t* r0, const uint8_
   p1 = fmaf(c1.y, dh1, p1);
   p1 = fmaf(-c1.z, xl.sum, p1);
   p1 = fmaf(-c1.w, xh.sum, p1);
-  return make_float2(p0, p1);
+  // ea carries the 2^14 of the coefficients' d sc 2^-14
+  float e0 = c0.x * xl.ea;
+  e0 = fmaf(c0.y, xh.ea, e0);
+  e0 = fmaf(c0.z, xl.eb, e0);
+  e0 = fmaf(c0.w, xh.eb, e0);
+  float e1 = c1.x * xl.ea;
+  e1 = fmaf(c1.y, xh.ea, e1);
+  e1 = fmaf(c1.z, xl.eb, e1);
+  e1 = fmaf(c1.w, xh.eb, e1);
+  return make_float4(p0, p1, fmaf(-kCertTau, fabsf(p0), e0), fmaf(-kCertTau, fabsf(p1), e1));
 }
 
 // Round to the nearest integer with the fp32 magic constant 1.5 * 2^23
@@ -608,31 +624,6 @@ __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
   return v;
-}
-
-// Sum each of the 8 per-lane values over the warp: afterwards lane l holds the
-// total of slot (l >> 2) & 7 (4 + 2 + 1 exchanging levels, then 2 plain).
-__device__ __forceinline__ float reduce8(float (&v)[8], int lane) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const bool up = lane & 16;
-    const float send = up ? v[i] : v[i + 4], keep = up ? v[i + 4] : v[i];
-    v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const bool up = lane & 8;
-    const float send = up ? v[i] : v[i + 2], keep = up ? v[i + 2] : v[i];
-    v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
-  }
-  {
-    const bool up = lane & 4;
-    const float send = up ? v[0] : v[1], keep = up ? v[1] : v[0];
-    v[0] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 4);
-  }
-  v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], 2);
-  v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], 1);
-  return v[0];
 }
 
 // Shared-memory layout of the x planes: per 64-weight unit u, 208 bytes:
@@ -659,8 +650,13 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
   const int nsub2 = (nsub + 1) & ~1;  // keeps the barriers 8-byte aligned
   float* xscale = reinterpret_cast<float*>(planes + U * kPlaneStride);  // nsub2
   float* xsum = xscale + nsub2;                                        // nsub2
-  uint64_t* bars = reinterpret_cast<uint64_t*>(xsum + nsub2);
-  float* acc = reinterpret_cast<float*>(bars + 2 * a.stages);
+  float* xa = xsum + nsub2;                                            // nsub2
+  float* xb = xa + nsub2;                                              // nsub2
+  uint64_t* bars = reinterpret_cast<uint64_t*>(xb + nsub2);
+  float* acc = reinterpret_cast<float*>(bars + 2 * a.stages);          // max_rows
+  float* dacc = acc + a.max_rows;                                      // max_rows
+  int* flist = reinterpret_cast<int*>(dacc + a.max_rows);              // max_rows
+  int* nfail = flist + a.max_rows;
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + a.stages);
 
   const int compute_warps = a.teams * a.team_warps;
@@ -672,8 +668,9 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
   const int iters = (rows + rps - 1) / rps;
   const int first = iters < a.stages ? iters : a.stages;
 
-  for (int i = threadIdx.x; i < rows; i += blockDim.x) acc[i] = 0.f;
+  for (int i = threadIdx.x; i < rows; i += blockDim.x) acc[i] = dacc[i] = 0.f;
   if (threadIdx.x == 0) {
+    *nfail = 0;
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, compute_warps);
@@ -741,11 +738,12 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
         nb = __ldg(px + 1);
       }
       const float v[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
-      float mx = 0.f, sm = 0.f;
+      float mx = 0.f, sm = 0.f, sa = 0.f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         mx = fmaxf(mx, fabsf(v[i]));
         sm += v[i];
+        sa += fabsf(v[i]);
       }
       mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
@@ -753,6 +751,7 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
       sm += __shfl_xor_sync(0xFFFFFFFFu, sm, 2);
       const float inv = mx > 0.f ? 127.0f / mx : 0.0f;
       uint32_t b1[2] = {0, 0}, b2[2] = {0, 0}, b3[2] = {0, 0};
+      float rs = 0.f;  // third-plane residuals, in units of s / 16384
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float t = fminf(fmaxf(v[i] * inv, -127.0f), 127.0f);
@@ -760,19 +759,29 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
         const float f1 = round_magic(t, i1);
         const float u2 = (t - f1) * 128.0f;
         const float f2 = round_magic(u2, i2);
-        round_magic((u2 - f2) * 128.0f, i3);
+        const float u3 = (u2 - f2) * 128.0f;
+        rs += fabsf(u3 - round_magic(u3, i3));
         const int sh8 = 8 * (i & 3);
         b1[i >> 2] |= ((uint32_t)i1 & 0xFFu) << sh8;
         b2[i >> 2] |= ((uint32_t)i2 & 0xFFu) << sh8;
         b3[i >> 2] |= ((uint32_t)i3 & 0xFFu) << sh8;
       }
+      sa += __shfl_xor_sync(0xFFFFFFFFu, sa, 1);
+      sa += __shfl_xor_sync(0xFFFFFFFFu, sa, 2);
+      rs += __shfl_xor_sync(0xFFFFFFFFu, rs, 1);
+      rs += __shfl_xor_sync(0xFFFFFFFFu, rs, 2);
       uint8_t* pl = planes + (sb32 >> 1) * kPlaneStride + (sb32 & 1) * 32 + 8 * q;
       *reinterpret_cast<uint2*>(pl) = make_uint2(b1[0], b1[1]);
       *reinterpret_cast<uint2*>(pl + 64) = make_uint2(b2[0], b2[1]);
       *reinterpret_cast<uint2*>(pl + 128) = make_uint2(b3[0], b3[1]);
       if (q == 0) {
-        xscale[sb32] = mx > 0.f ? mx / 127.0f : 1.0f;
+        const float sc = mx > 0.f ? mx / 127.0f : 1.0f;
+        float ea, eb;
+        q4k_cert_consts(sc, rs, sa, mx, ea, eb);
+        xscale[sb32] = sc;
         xsum[sb32] = sm;
+        xa[sb32] = ea * 16384.0f;
+        xb[sb32] = eb;
       }
     }
   }
@@ -809,6 +818,8 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
         }
         xs.scale = xscale[2 * u + h];
         xs.sum = xsum[2 * u + h];
+        xs.ea = xa[2 * u + h];
+        xs.eb = xb[2 * u + h];
       }
     } else {
 #pragma unroll
@@ -817,13 +828,15 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
       }
       xsl.scale = xsh.scale = 1.f;
       xsl.sum = xsh.sum = 0.f;
+      xsl.ea = xsh.ea = xsl.eb = xsh.eb = 0.f;
     }
     const int off_h = sb * kQ4KBytes, off_a = off_h + 16 + 32 * g;
     bool ok = true;
     for (int it0 = 0; it0 < iters && ok; it0 += SPB) {
-      float pa[8];
+      // slots 0..7: the row sums of 8 rows, 8..15: their certificate terms
+      float pa[16];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) pa[i] = 0.f;
+      for (int i = 0; i < 16; ++i) pa[i] = 0.f;
 #pragma unroll
       for (int q = 0; q < SPB; ++q) {
         const int it = it0 + q;
@@ -839,11 +852,13 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
               const int ra = team * RPT + j;
               if (active && ra < nr) {
                 const bool two = ra + 1 < nr;
-                const float2 p2 = q4_group_dot2i(stage + j * rowbytes,
+                const float4 p2 = q4_group_dot2i(stage + j * rowbytes,
                                                  stage + (two ? j + 1 : j) * rowbytes, off_h,
                                                  off_a, sh, upper, xsl, xsh);
                 pa[q * RPT + j] = p2.x;
                 pa[q * RPT + j + 1] = two ? p2.y : 0.f;
+                pa[8 + q * RPT + j] = p2.z;
+                pa[8 + q * RPT + j + 1] = two ? p2.w : 0.f;
               }
             }
             __syncwarp();
@@ -851,31 +866,49 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
           }
         }
       }
-      // slot (lane >> 2) & 7 of this warp's 8 rows: stage it0 + slot / RPT,
-      // team row slot % RPT
-      const float tot = reduce8(pa, lane);
-      const int slot = (lane >> 2) & 7;
+      // slot (lane >> 1) & 15: kind (sum / certificate) and row slot of this
+      // warp's 8 rows (stage it0 + slot / RPT, team row slot % RPT)
+      const float tot = reduce16(pa, lane);
+      const int slot = (lane >> 1) & 7;
       const int it = it0 + slot / RPT;
-      if ((lane & 3) == 0 && it < iters) {
+      if ((lane & 1) == 0 && it < iters) {
         const int rr = team * RPT + slot % RPT;
-        if (rr < min(rps, rows - it * rps)) atomicAdd(&acc[it * rps + rr], tot);
+        if (rr < min(rps, rows - it * rps)) atomicAdd((lane & 16 ? dacc : acc) + it * rps + rr, tot);
       }
     }
   }
   __syncthreads();
-  if (a.ksplit == 2) {
-    m1_cluster_sync();  // both halves of every row are in their CTAs' acc
-    if (h == 0)
-      for (int i = threadIdx.x; i < rows; i += blockDim.x) {
-        const int sg = m1_seg(a, r0 + i);
-        a.seg_y[sg][r0 + i - a.seg_start[sg]] = acc[i] + m1_ld_peer(acc + i, 1);
+  // Outputs whose certificate holds are stored; the others are listed and
+  // recomputed exactly, one warp per output (rows split between the CTAs of
+  // a cluster: rank 0 adds rank 1's partial sums and certificates first).
+  if (a.ksplit == 2) m1_cluster_sync();  // both halves of every row are in their CTAs' acc
+  if (h == 0)
+    for (int i = threadIdx.x; i < rows; i += blockDim.x) {
+      float y = acc[i], D = dacc[i];
+      if (a.ksplit == 2) {
+        y += m1_ld_peer(acc + i, 1);
+        D += m1_ld_peer(dacc + i, 1);
       }
-    m1_cluster_sync();  // rank 1's shared memory stays until rank 0 has read it
-    return;
-  }
-  for (int i = threadIdx.x; i < rows; i += blockDim.x) {
-    const int sg = m1_seg(a, r0 + i);
-    a.seg_y[sg][r0 + i - a.seg_start[sg]] = acc[i];
+      if (cert_fails(D)) {
+        flist[atomicAdd(nfail, 1)] = i;
+      } else {
+        const int sg = m1_seg(a, r0 + i);
+        a.seg_y[sg][r0 + i - a.seg_start[sg]] = y;
+      }
+    }
+  if (a.ksplit == 2) m1_cluster_sync();  // rank 1's shared memory stays until rank 0 has read it
+  if (h != 0) return;
+  __syncthreads();
+  const int nwarps = blockDim.x >> 5;
+  for (int f = warp; f < *nfail; f += nwarps) {
+    const int row = r0 + flist[f];
+    const int sg = m1_seg(a, row);
+    const float y = (float)q4k_row_exact(a.seg_w[sg] + (size_t)(row - a.seg_start[sg]) * rowstride,
+                                         a.x, a.K, lane);
+    if (lane == 0) {
+      a.seg_y[sg][row - a.seg_start[sg]] = y;
+      atomicAdd(&g_gemv_exact_outputs, 1ull);
+    }
   }
 }
 
@@ -904,8 +937,26 @@ __global__ void __launch_bounds__(544, 1) q4k_gemv_m1_kernel(const M1Args a) {
 
 struct XSplit16 {
   int p1[4], p2[4], p3[4];  // planes of one 16-weight sub-block
-  float scale, sum;
+  float sc14;               // s / 16384: one unit of the combined plane value
+  int pc;                   // sum over the sub-block of 16384 p1 + 128 p2 + p3
+  float ec;                 // error-bound constant of the sub-block (q6k_cert)
 };
+
+// Error bound of one lane's 64 Q6_K weights (q6k_cert).  The offset -32 is
+// applied in integers: for quarter i the lane forms
+//   I_i = sum_k q_k (16384 p1 + 128 p2 + p3)_k - 32 pc_i = 16384 sum_k (q_k - 32) t_k
+// exactly (|.| < 2^31), so every later fp32 rounding is relative to
+// sum_k |q_k - 32| |x_k| and thus to sum_k |x_k w_k|.  The only other error
+// is that of the planes: |t_k - x_k / s| <= r_k / 16384 with the third-plane
+// residual r_k <= 1/2, so quarter i contributes at most
+//   |d scale_i| * 32 s_i sum_k r_k / 16384 = |d scale_i| * ec_i
+// (|q - 32| <= 32; the constant adds a factor 1 + 2^-7).
+// `finite`: every x of the sub-block is finite.
+__device__ __forceinline__ float q6k_cert_const(float s, float rs, float mx, bool finite) {
+  // planes not valid (tiny maximum) or x not finite: exact path
+  if ((mx > 0.0f && mx < kCertTinyMax) || !finite) return INFINITY;
+  return 32.0f * s * rs * (1.0f / 16384.0f) * (1.0f + 0x1p-7f);
+}
 
 // 16 bytes at a 2-byte aligned shared-memory address (the word after the
 // field is read and discarded; it lies inside the CTA's shared memory).
@@ -920,10 +971,10 @@ __device__ __forceinline__ void lds16u(const uint8_t* p, uint32_t (&w)[4]) {
   w[3] = __funnelshift_r(v3, v4, sh);
 }
 
-// One row's dot product over a lane's unit.  blk: the super-block in shared
-// memory.
-__device__ __forceinline__ float q6_unit_dot(const uint8_t* blk, int hh, int lq,
-                                             const XSplit16 (&xs)[4]) {
+// One row's dot product over a lane's unit, with its certificate term:
+// returns (p, D).  blk: the super-block in shared memory.
+__device__ __forceinline__ float2 q6_unit_dot(const uint8_t* blk, int hh, int lq,
+                                              const XSplit16 (&xs)[4]) {
   uint32_t qa[4], qb[4], qh[4], sc[4];
   lds16u(blk + 64 * hh + 16 * lq, qa);
   lds16u(blk + 64 * hh + 32 + 16 * lq, qb);
@@ -953,15 +1004,18 @@ __device__ __forceinline__ float q6_unit_dot(const uint8_t* blk, int hh, int lq,
   }
   // scale of sub-block 8hh + 2i + lq: byte 8hh + lq + 2i of the 16
   const uint32_t sw0 = hh ? sc[2] : sc[0], sw1 = hh ? sc[3] : sc[1];
-  float r = 0.f;
+  float r = 0.f, e = 0.f;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const uint32_t word = i < 2 ? sw0 : sw1;
     const int bsel = lq + 2 * (i & 1);
     const float s8 = i2f_small((int)(word << (24 - 8 * bsel)) >> 24);  // signed byte
-    r = fmaf(s8, dot3_value(t[i], xs[i].scale) - 32.0f * xs[i].sum, r);
+    const int I = t[i].a1 * 16384 + t[i].a2 * 128 + t[i].a3 - 32 * xs[i].pc;
+    r = fmaf(s8, __int2float_rn(I) * xs[i].sc14, r);
+    e = fmaf(fabsf(s8), xs[i].ec, e);
   }
-  return d * r;
+  const float p = d * r;
+  return make_float2(p, fmaf(-kCertTau, fabsf(p), fabsf(d) * e));
 }
 
 // Shared-memory layout of the Q6_K x planes: per unit u, 208 bytes: plane p
@@ -978,10 +1032,14 @@ __device__ __forceinline__ void q6k_m1_body(const M1Args& a, const int bid, cons
   const uint32_t stage_bytes = (uint32_t)(rps * rowbytes);
   uint8_t* ring = smem_q6;
   uint8_t* planes = ring + a.ring_bytes;                              // U * 208
-  float* xscale = reinterpret_cast<float*>(planes + U * kPlaneStride);  // nsub16
-  float* xsum = xscale + nsub16;                                       // nsub16
-  uint64_t* bars = reinterpret_cast<uint64_t*>(xsum + nsub16);
-  float* acc = reinterpret_cast<float*>(bars + 2 * a.stages);
+  float* xsc14 = reinterpret_cast<float*>(planes + U * kPlaneStride);  // nsub16
+  int* xpc = reinterpret_cast<int*>(xsc14 + nsub16);                   // nsub16
+  float* xec = reinterpret_cast<float*>(xpc + nsub16);                 // nsub16
+  uint64_t* bars = reinterpret_cast<uint64_t*>(xec + nsub16 + (nsub16 & 1));
+  float* acc = reinterpret_cast<float*>(bars + 2 * a.stages);          // max_rows
+  float* dacc = acc + a.max_rows;                                      // max_rows
+  int* flist = reinterpret_cast<int*>(dacc + a.max_rows);              // max_rows
+  int* nfail = flist + a.max_rows;
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + a.stages);
 
   const int compute_warps = a.teams * a.team_warps;
@@ -994,8 +1052,9 @@ __device__ __forceinline__ void q6k_m1_body(const M1Args& a, const int bid, cons
   const int iters = (rows + rps - 1) / rps;
   const int first = iters < a.stages ? iters : a.stages;
 
-  for (int i = threadIdx.x; i < rows; i += blockDim.x) acc[i] = 0.f;
+  for (int i = threadIdx.x; i < rows; i += blockDim.x) acc[i] = dacc[i] = 0.f;
   if (threadIdx.x == 0) {
+    *nfail = 0;
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, compute_warps);
@@ -1041,16 +1100,19 @@ __device__ __forceinline__ void q6k_m1_body(const M1Args& a, const int bid, cons
       const float4* px = reinterpret_cast<const float4*>(a.x + 16 * s16 + 8 * half);
       const float4 va = __ldg(px), vb = __ldg(px + 1);
       const float v[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
-      float mx = 0.f, sm = 0.f;
+      float mx = 0.f;
+      int nonfin = 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         mx = fmaxf(mx, fabsf(v[i]));
-        sm += v[i];
+        nonfin |= !isfinite(v[i]);
       }
       mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-      sm += __shfl_xor_sync(0xFFFFFFFFu, sm, 1);
+      nonfin |= __shfl_xor_sync(0xFFFFFFFFu, nonfin, 1);
       const float inv = mx > 0.f ? 127.0f / mx : 0.0f;
       uint32_t b1[2] = {0, 0}, b2[2] = {0, 0}, b3[2] = {0, 0};
+      int pc = 0;
+      float rs = 0.f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float t = fminf(fmaxf(v[i] * inv, -127.0f), 127.0f);
@@ -1058,12 +1120,16 @@ __device__ __forceinline__ void q6k_m1_body(const M1Args& a, const int bid, cons
         const float f1 = round_magic(t, i1);
         const float u2 = (t - f1) * 128.0f;
         const float f2 = round_magic(u2, i2);
-        round_magic((u2 - f2) * 128.0f, i3);
+        const float u3 = (u2 - f2) * 128.0f;
+        rs += fabsf(u3 - round_magic(u3, i3));
+        pc += i1 * 16384 + i2 * 128 + i3;
         const int sh8 = 8 * (i & 3);
         b1[i >> 2] |= ((uint32_t)i1 & 0xFFu) << sh8;
         b2[i >> 2] |= ((uint32_t)i2 & 0xFFu) << sh8;
         b3[i >> 2] |= ((uint32_t)i3 & 0xFFu) << sh8;
       }
+      pc += __shfl_xor_sync(0xFFFFFFFFu, pc, 1);
+      rs += __shfl_xor_sync(0xFFFFFFFFu, rs, 1);
       // sub-block s16 = 16 sb + 8 hh + 2 i + lq belongs to unit 4 sb + 2 hh + lq
       const int t16 = s16 & 15;
       const int u = 4 * (s16 >> 4) + 2 * (t16 >> 3) + (t16 & 1), qi = (t16 >> 1) & 3;
@@ -1072,8 +1138,10 @@ __device__ __forceinline__ void q6k_m1_body(const M1Args& a, const int bid, cons
       *reinterpret_cast<uint2*>(pl + 64) = make_uint2(b2[0], b2[1]);
       *reinterpret_cast<uint2*>(pl + 128) = make_uint2(b3[0], b3[1]);
       if (half == 0) {
-        xscale[4 * u + qi] = mx > 0.f ? mx / 127.0f : 1.0f;
-        xsum[4 * u + qi] = sm;
+        const float sc = mx > 0.f ? mx / 127.0f : 1.0f;
+        xsc14[4 * u + qi] = sc * (1.0f / 16384.0f);
+        xpc[4 * u + qi] = pc;
+        xec[4 * u + qi] = q6k_cert_const(sc, rs, mx, nonfin == 0);
       }
     }
   }
@@ -1099,21 +1167,23 @@ __device__ __forceinline__ void q6k_m1_body(const M1Args& a, const int bid, cons
         xs[i].p1[0] = v1.x; xs[i].p1[1] = v1.y; xs[i].p1[2] = v1.z; xs[i].p1[3] = v1.w;
         xs[i].p2[0] = v2.x; xs[i].p2[1] = v2.y; xs[i].p2[2] = v2.z; xs[i].p2[3] = v2.w;
         xs[i].p3[0] = v3.x; xs[i].p3[1] = v3.y; xs[i].p3[2] = v3.z; xs[i].p3[3] = v3.w;
-        xs[i].scale = xscale[4 * u + i];
-        xs[i].sum = xsum[4 * u + i];
+        xs[i].sc14 = xsc14[4 * u + i];
+        xs[i].pc = xpc[4 * u + i];
+        xs[i].ec = xec[4 * u + i];
       } else {
 #pragma unroll
         for (int w = 0; w < 4; ++w) xs[i].p1[w] = xs[i].p2[w] = xs[i].p3[w] = 0;
-        xs[i].scale = 1.f;
-        xs[i].sum = 0.f;
+        xs[i].sc14 = 0.f;
+        xs[i].pc = 0;
+        xs[i].ec = 0.f;
       }
     }
     const int off = sb * kQ6KBytes;
     bool ok = true;
     for (int it0 = 0; it0 < iters && ok; it0 += SPB) {
-      float pa[8];
+      float pa[16];  // slots 0..7: row sums, 8..15: their certificate terms
 #pragma unroll
-      for (int i = 0; i < 8; ++i) pa[i] = 0.f;
+      for (int i = 0; i < 16; ++i) pa[i] = 0.f;
 #pragma unroll
       for (int qq = 0; qq < SPB; ++qq) {
         const int it = it0 + qq;
@@ -1126,24 +1196,41 @@ __device__ __forceinline__ void q6k_m1_body(const M1Args& a, const int bid, cons
             const uint8_t* stage = ring + s * stage_bytes + (size_t)team * RPT * rowbytes;
 #pragma unroll
             for (int j = 0; j < RPT; ++j)
-              if (active && team * RPT + j < nr)
-                pa[qq * RPT + j] = q6_unit_dot(stage + j * rowbytes + off, hh, lq, xs);
+              if (active && team * RPT + j < nr) {
+                const float2 pd = q6_unit_dot(stage + j * rowbytes + off, hh, lq, xs);
+                pa[qq * RPT + j] = pd.x;
+                pa[8 + qq * RPT + j] = pd.y;
+              }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * s);
           }
         }
       }
-      const float tot = reduce8(pa, lane);
-      const int slot = (lane >> 2) & 7;
+      const float tot = reduce16(pa, lane);
+      const int slot = (lane >> 1) & 7;
       const int it = it0 + slot / RPT;
-      if ((lane & 3) == 0 && it < iters) {
+      if ((lane & 1) == 0 && it < iters) {
         const int rr = team * RPT + slot % RPT;
-        if (rr < min(rps, rows - it * rps)) atomicAdd(&acc[it * rps + rr], tot);
+        if (rr < min(rps, rows - it * rps)) atomicAdd((lane & 16 ? dacc : acc) + it * rps + rr, tot);
       }
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < rows; i += blockDim.x) a.y[r0 + i] = acc[i];
+  // certified outputs are stored, the others recomputed exactly (one warp each)
+  for (int i = threadIdx.x; i < rows; i += blockDim.x) {
+    if (cert_fails(dacc[i])) flist[atomicAdd(nfail, 1)] = i;
+    else a.y[r0 + i] = acc[i];
+  }
+  __syncthreads();
+  const int nwarps = blockDim.x >> 5;
+  for (int f = warp; f < *nfail; f += nwarps) {
+    const int row = r0 + flist[f];
+    const float y = (float)q6k_row_exact(a.W + (size_t)row * rowbytes, a.x, a.K, lane);
+    if (lane == 0) {
+      a.y[row] = y;
+      atomicAdd(&g_gemv_exact_outputs, 1ull);
+    }
+  }
 }
 
 template <int RPT>
@@ -1188,10 +1275,14 @@ __global__ void __launch_bounds__(544, 1) q6k_gemv_mt_kernel(const M1Args a) {
   const uint32_t stage_bytes = (uint32_t)(rps * rowbytes);
   uint8_t* ring = smem_q6t;
   uint8_t* planes = ring + a.ring_bytes;                                    // M * U * 208
-  float* xscale = reinterpret_cast<float*>(planes + (size_t)M * U * kPlaneStride);  // M * nsub16
-  float* xsum = xscale + M * nsub16;                                         // M * nsub16
-  uint64_t* bars = reinterpret_cast<uint64_t*>(xsum + M * nsub16);
-  float* acc = reinterpret_cast<float*>(bars + 2 * a.stages);               // rows * M
+  float* xsc14 = reinterpret_cast<float*>(planes + (size_t)M * U * kPlaneStride);  // M * nsub16
+  int* xpc = reinterpret_cast<int*>(xsc14 + M * nsub16);                    // M * nsub16
+  float* xec = reinterpret_cast<float*>(xpc + M * nsub16);                  // M * nsub16
+  uint64_t* bars = reinterpret_cast<uint64_t*>(xec + M * nsub16);
+  float* acc = reinterpret_cast<float*>(bars + 2 * a.stages);               // max_rows * M
+  float* dacc = acc + a.max_rows * M;                                       // max_rows * M
+  int* flist = reinterpret_cast<int*>(dacc + a.max_rows * M);               // max_rows * M
+  int* nfail = flist + a.max_rows * M;
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + a.stages);
 
   const int compute_warps = a.teams * a.team_warps;
@@ -1205,8 +1296,9 @@ __global__ void __launch_bounds__(544, 1) q6k_gemv_mt_kernel(const M1Args a) {
   const int iters = (rows + rps - 1) / rps;
   const int first = iters < a.stages ? iters : a.stages;
 
-  for (int i = threadIdx.x; i < rows * M; i += blockDim.x) acc[i] = 0.f;
+  for (int i = threadIdx.x; i < rows * M; i += blockDim.x) acc[i] = dacc[i] = 0.f;
   if (threadIdx.x == 0) {
+    *nfail = 0;
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, compute_warps);
@@ -1251,16 +1343,19 @@ __global__ void __launch_bounds__(544, 1) q6k_gemv_mt_kernel(const M1Args a) {
           reinterpret_cast<const float4*>(a.x + (size_t)m * a.K + 256 * sb0 + 16 * s16 + 8 * half);
       const float4 va = __ldg(px), vb = __ldg(px + 1);
       const float v[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
-      float mx = 0.f, sm = 0.f;
+      float mx = 0.f;
+      int nonfin = 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         mx = fmaxf(mx, fabsf(v[i]));
-        sm += v[i];
+        nonfin |= !isfinite(v[i]);
       }
       mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-      sm += __shfl_xor_sync(0xFFFFFFFFu, sm, 1);
+      nonfin |= __shfl_xor_sync(0xFFFFFFFFu, nonfin, 1);
       const float inv = mx > 0.f ? 127.0f / mx : 0.0f;
       uint32_t b1[2] = {0, 0}, b2[2] = {0, 0}, b3[2] = {0, 0};
+      int pc = 0;
+      float rs = 0.f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float t = fminf(fmaxf(v[i] * inv, -127.0f), 127.0f);
@@ -1268,12 +1363,16 @@ __global__ void __launch_bounds__(544, 1) q6k_gemv_mt_kernel(const M1Args a) {
         const float f1 = round_magic(t, i1);
         const float u2 = (t - f1) * 128.0f;
         const float f2 = round_magic(u2, i2);
-        round_magic((u2 - f2) * 128.0f, i3);
+        const float u3 = (u2 - f2) * 128.0f;
+        rs += fabsf(u3 - round_magic(u3, i3));
+        pc += i1 * 16384 + i2 * 128 + i3;
         const int sh8 = 8 * (i & 3);
         b1[i >> 2] |= ((uint32_t)i1 & 0xFFu) << sh8;
         b2[i >> 2] |= ((uint32_t)i2 & 0xFFu) << sh8;
         b3[i >> 2] |= ((uint32_t)i3 & 0xFFu) << sh8;
       }
+      pc += __shfl_xor_sync(0xFFFFFFFFu, pc, 1);
+      rs += __shfl_xor_sync(0xFFFFFFFFu, rs, 1);
       const int t16 = s16 & 15;
       const int u = 4 * (s16 >> 4) + 2 * (t16 >> 3) + (t16 & 1), qi = (t16 >> 1) & 3;
       uint8_t* pl = planes + ((size_t)m * U + u) * kPlaneStride + qi * 16 + 8 * half;
@@ -1281,8 +1380,11 @@ __global__ void __launch_bounds__(544, 1) q6k_gemv_mt_kernel(const M1Args a) {
       *reinterpret_cast<uint2*>(pl + 64) = make_uint2(b2[0], b2[1]);
       *reinterpret_cast<uint2*>(pl + 128) = make_uint2(b3[0], b3[1]);
       if (half == 0) {
-        xscale[m * nsub16 + 4 * u + qi] = mx > 0.f ? mx / 127.0f : 1.0f;
-        xsum[m * nsub16 + 4 * u + qi] = sm;
+        const float sc = mx > 0.f ? mx / 127.0f : 1.0f;
+        const int at = m * nsub16 + 4 * u + qi;
+        xsc14[at] = sc * (1.0f / 16384.0f);
+        xpc[at] = pc;
+        xec[at] = q6k_cert_const(sc, rs, mx, nonfin == 0);
       }
     }
   }
@@ -1310,9 +1412,9 @@ __global__ void __launch_bounds__(544, 1) q6k_gemv_mt_kernel(const M1Args a) {
       const uint8_t* stage = ring + s * stage_bytes;
       for (int j = 0; j < rpt; ++j) {
         const int rr = team * rpt + j;
-        float pa[8];
+        float pa[16];  // slots 0..7: the token sums, 8..15: their certificate terms
 #pragma unroll
-        for (int m = 0; m < 8; ++m) pa[m] = 0.f;
+        for (int m = 0; m < 16; ++m) pa[m] = 0.f;
         if (active && rr < nr) {
           const uint8_t* blk = stage + (size_t)rr * rowbytes + off;
           uint32_t qa[4], qb[4], qh[4], sc[4];
@@ -1337,15 +1439,19 @@ __global__ void __launch_bounds__(544, 1) q6k_gemv_mt_kernel(const M1Args a) {
           for (int i = 0; i < 4; ++i) {
             const uint32_t word = i < 2 ? sw0 : sw1;
             const int bsel = lq + 2 * (i & 1);
-            s8[i] = d * i2f_small((int)(word << (24 - 8 * bsel)) >> 24);
+            s8[i] = i2f_small((int)(word << (24 - 8 * bsel)) >> 24);
           }
 #pragma unroll
           for (int m = 0; m < 8; ++m) {
             if (m < M) {
               const uint8_t* pu = planes + ((size_t)m * U + u) * kPlaneStride;
-              const float* xsc = xscale + m * nsub16 + 4 * u;
-              const float* xsm = xsum + m * nsub16 + 4 * u;
-              float r = 0.f;
+              const float4 xsc = *reinterpret_cast<const float4*>(xsc14 + m * nsub16 + 4 * u);
+              const int4 xp = *reinterpret_cast<const int4*>(xpc + m * nsub16 + 4 * u);
+              const float4 xe = *reinterpret_cast<const float4*>(xec + m * nsub16 + 4 * u);
+              const float sc14[4] = {xsc.x, xsc.y, xsc.z, xsc.w};
+              const int pcs[4] = {xp.x, xp.y, xp.z, xp.w};
+              const float ecs[4] = {xe.x, xe.y, xe.z, xe.w};
+              float r = 0.f, e = 0.f;
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 const uint4 v1 = lds128(pu + 16 * i), v2 = lds128(pu + 64 + 16 * i);
@@ -1360,17 +1466,22 @@ __global__ void __launch_bounds__(544, 1) q6k_gemv_mt_kernel(const M1Args a) {
                   t.a2 = __dp4a(q[i][w], p2[w], t.a2);
                   t.a3 = __dp4a(q[i][w], p3[w], t.a3);
                 }
-                r = fmaf(s8[i], dot3_value(t, xsc[i]) - 32.0f * xsm[i], r);
+                // offset -32 in integers, as in the one-token kernel (q6k_cert)
+                const int I = t.a1 * 16384 + t.a2 * 128 + t.a3 - 32 * pcs[i];
+                r = fmaf(s8[i], __int2float_rn(I) * sc14[i], r);
+                e = fmaf(fabsf(s8[i]), ecs[i], e);
               }
-              pa[m] = r;
+              const float pm = d * r;
+              pa[m] = pm;
+              pa[8 + m] = fmaf(-kCertTau, fabsf(pm), fabsf(d) * e);
             }
           }
         }
-        // slot (lane >> 2) & 7 of the warp's 8 token sums
-        const float tot = reduce8(pa, lane);
-        const int slot = (lane >> 2) & 7;
-        if ((lane & 3) == 0 && slot < M && rr < nr)
-          atomicAdd(&acc[(it * rps + rr) * M + slot], tot);
+        // slot (lane >> 1) & 15: kind (sum / certificate) and token
+        const float tot = reduce16(pa, lane);
+        const int slot = (lane >> 1) & 7;
+        if ((lane & 1) == 0 && slot < M && rr < nr)
+          atomicAdd((lane & 16 ? dacc : acc) + (it * rps + rr) * M + slot, tot);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * s);
@@ -1381,11 +1492,28 @@ __global__ void __launch_bounds__(544, 1) q6k_gemv_mt_kernel(const M1Args a) {
   if (h == 0)
     for (int i = threadIdx.x; i < rows * M; i += blockDim.x) {
       const int row = i / M, m = i - row * M;
-      float v = acc[i];
-      for (int r = 1; r < ks; ++r) v += m1_ld_peer(acc + i, (uint32_t)r);
-      a.y[(size_t)m * a.N + r0 + row] = v;
+      float v = acc[i], D = dacc[i];
+      for (int r = 1; r < ks; ++r) {
+        v += m1_ld_peer(acc + i, (uint32_t)r);
+        D += m1_ld_peer(dacc + i, (uint32_t)r);
+      }
+      if (cert_fails(D)) flist[atomicAdd(nfail, 1)] = i;
+      else a.y[(size_t)m * a.N + r0 + row] = v;
     }
   if (ks > 1) m1_cluster_sync();  // no CTA leaves while rank 0 may read its memory
+  if (h != 0) return;
+  __syncthreads();
+  // outputs whose certificate fails: exact recomputation, one warp each
+  const int nwarps = blockDim.x >> 5;
+  for (int f = warp; f < *nfail; f += nwarps) {
+    const int row = flist[f] / M, m = flist[f] - row * M;
+    const float y = (float)q6k_row_exact(a.W + (size_t)(r0 + row) * rowbytes,
+                                         a.x + (size_t)m * a.K, a.K, lane);
+    if (lane == 0) {
+      a.y[(size_t)m * a.N + r0 + row] = y;
+      atomicAdd(&g_gemv_exact_outputs, 1ull);
+    }
+  }
 }
 
 // ---------------------------------------------------------------- launch --
@@ -1424,40 +1552,24 @@ void gemv_log(const char* kernel, int M, int N, int K, int grid) {
 template <int M, int R>
 rq_status run_q4k(const uint8_t* w, const float* x, float* y, int N, int K,
                   cudaStream_t st) {
-  const size_t smem = (size_t)M * (K / 32) * sizeof(float);
   auto kern = q4k_gemv_kernel<M, R>;
-  static size_t smem_set = 48 * 1024;
-  if (smem > smem_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-      return RQ_ERR_CUDA;
-    smem_set = smem;
-  }
-  const int grid = persistent_grid(kern, smem, (N + R - 1) / R);
+  const int grid = persistent_grid(kern, 0, (N + R - 1) / R);
   // launched without programmatic serialization: measured on GB300, this
   // small persistent grid launched early slows its neighbours down
   gemv_log("q4k_generic", M, N, K, grid);
-  kern<<<grid, kThreads, smem, st>>>(w, x, y, N, K);
+  kern<<<grid, kThreads, 0, st>>>(w, x, y, N, K);
   return launch_status();
 }
 
 template <int M, int R>
 rq_status run_q6k(const uint8_t* w, const float* x, float* y, int N, int K,
                   cudaStream_t st) {
-  const size_t smem = (size_t)M * (K / 8) * sizeof(float);
   auto kern = q6k_gemv_kernel<M, R>;
-  static size_t smem_set = 48 * 1024;
-  if (smem > smem_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-      return RQ_ERR_CUDA;
-    smem_set = smem;
-  }
-  const int grid = persistent_grid(kern, smem, (N + R - 1) / R);
+  const int grid = persistent_grid(kern, 0, (N + R - 1) / R);
   // launched without programmatic serialization: measured on GB300, this
   // small persistent grid launched early slows its neighbours down
   gemv_log("q6k_generic", M, N, K, grid);
-  kern<<<grid, kThreads, smem, st>>>(w, x, y, N, K);
+  kern<<<grid, kThreads, 0, st>>>(w, x, y, N, K);
   return launch_status();
 }
 
@@ -1538,8 +1650,10 @@ rq_status plan_q4k_m1(int nseg, const int* starts, const uint8_t* const* ws, flo
   const int rowbytes = (Kc / kQK) * kQ4KBytes;
   const int stage_bytes = a.rows_per_stage * rowbytes;
   const size_t nsub2 = (size_t)((nsub + 1) & ~1);
-  const size_t fixed = (size_t)U * kPlaneStride + 8 * nsub2 +
-                       16 * (size_t)max_stages + 4 * (size_t)max_rows;
+  // planes; per sub-block: scale, sum, two error-bound constants; barriers;
+  // per row: sum, certificate, exact-path list; the list's count
+  const size_t fixed = (size_t)U * kPlaneStride + 16 * nsub2 + 16 * (size_t)max_stages +
+                       12 * (size_t)max_rows + 16;
   const size_t limit = 227 * 1024;
   if (fixed + 2 * (size_t)stage_bytes > limit) return RQ_ERR_SHAPE;
   size_t ring = (size_t)ring_kb * 1024;
@@ -1549,8 +1663,9 @@ rq_status plan_q4k_m1(int nseg, const int* starts, const uint8_t* const* ws, flo
   a.stages = stages;
   a.ring_bytes = (uint32_t)(stages * stage_bytes);
   a.wait_limit_ns = kWaitLimitNs;
-  p->smem = a.ring_bytes + (size_t)U * kPlaneStride + 8 * nsub2 + 16 * (size_t)stages +
-            4 * (size_t)max_rows;
+  a.max_rows = max_rows;
+  p->smem = a.ring_bytes + (size_t)U * kPlaneStride + 16 * nsub2 + 16 * (size_t)stages +
+            12 * (size_t)max_rows + 16;
   p->threads = (a.teams * a.team_warps + 1) * 32;
   p->grid = grid;
   p->rpt = rpt;
@@ -1642,8 +1757,10 @@ rq_status plan_q6k_m1(const uint8_t* w, const float* x, float* y, int M, int N, 
   a.rows_per_stage = rpt * a.teams;
   if (a.rows_per_stage % ra != 0) return RQ_ERR_SHAPE;
   const int stage_bytes = a.rows_per_stage * rowbytes;
-  const size_t fixed = (size_t)M * U * kPlaneStride + 8 * (size_t)M * nsub16 +
-                       16 * (size_t)max_stages + 4 * (size_t)M * max_rows;
+  // planes; per token and sub-block: scale, offset sum, error-bound constant;
+  // barriers; per output: sum, certificate, exact-path list; the list's count
+  const size_t fixed = (size_t)M * U * kPlaneStride + 12 * (size_t)M * nsub16 +
+                       16 * (size_t)max_stages + 12 * (size_t)M * max_rows + 16;
   const size_t limit = 227 * 1024;
   if (fixed + 2 * (size_t)stage_bytes > limit) return RQ_ERR_SHAPE;
   size_t ring = (size_t)ring_kb * 1024;
@@ -1653,8 +1770,9 @@ rq_status plan_q6k_m1(const uint8_t* w, const float* x, float* y, int M, int N, 
   a.stages = stages;
   a.ring_bytes = (uint32_t)(stages * stage_bytes);
   a.wait_limit_ns = kWaitLimitNs;
-  p->smem = a.ring_bytes + (size_t)M * U * kPlaneStride + 8 * (size_t)M * nsub16 +
-            16 * (size_t)stages + 4 * (size_t)M * max_rows;
+  a.max_rows = max_rows;
+  p->smem = a.ring_bytes + (size_t)M * U * kPlaneStride + 12 * (size_t)M * nsub16 +
+            16 * (size_t)stages + 12 * (size_t)M * max_rows + 16;
   p->threads = (a.teams * a.team_warps + 1) * 32;
   p->grid = grid;
   p->rpt = rpt;
@@ -1703,39 +1821,44 @@ rq_status read_and_clear_gemv_error() {
   return RQ_ERR_TIMEOUT;
 }
 
+rq_status read_and_clear_gemv_exact_outputs(int64_t* out) {
+  unsigned long long v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_gemv_exact_outputs, sizeof(v)) != cudaSuccess)
+    return RQ_ERR_CUDA;
+  const unsigned long long zero = 0;
+  if (v != 0 && cudaMemcpyToSymbol(g_gemv_exact_outputs, &zero, sizeof(zero)) != cudaSuccess)
+    return RQ_ERR_CUDA;
+  if (out != nullptr) *out = (int64_t)v;
+  return RQ_OK;
+}
+
 rq_status launch_q4k_gemv(const uint8_t* w, const float* x, float* y, int M,
                           int N, int K, cudaStream_t st) {
-  switch (M) {
-    case 1:
-      // the one-token kernel keeps 64 x values per lane in registers; its
-      // team of ceil(K/2048) warps plus the producer warp fit 544 threads
-      if (K <= 32 * 2048) {
-        // RQ_ERR_SHAPE here means the launch shape does not fit the kernel
-        // or its shared memory; nothing was launched, so the generic
-        // kernel takes it
-        const int starts[2] = {0, N};
-        const rq_status s1 = run_q4k_m1(1, starts, &w, &y, x, K, st);
-        if (s1 != RQ_ERR_SHAPE) return s1;
-      }
-      return run_q4k<1, 2>(w, x, y, N, K, st);
-    default:
-      break;
-  }
-  if (M >= 2 && M <= 8 && std::getenv("RQ_GEMV_NO_MMA") == nullptr) {
-    // RQ_ERR_SHAPE: the shape does not fit the tensor-core kernel and
-    // nothing was launched
-    const rq_status s2 = launch_q4k_gemv_mma(w, x, y, M, N, K, st);
-    if (s2 != RQ_ERR_SHAPE) return s2;
+  if (M < 1 || M > 8) return RQ_ERR_SHAPE;
+  // the one-token kernel keeps 64 x values per lane in registers; its team
+  // of ceil(K/2048) warps plus the producer warp fit 544 threads.  Several
+  // tokens take one launch each (the weight is read once per token).
+  if (K <= 32 * 2048 && std::getenv("RQ_GEMV_GENERIC") == nullptr) {
+    const int starts[2] = {0, N};
+    for (int m = 0; m < M; ++m) {
+      float* ym = y + (size_t)m * N;
+      // RQ_ERR_SHAPE: the shape does not fit the kernel or its shared
+      // memory and nothing was launched, so the generic kernel takes it
+      const rq_status s1 = run_q4k_m1(1, starts, &w, &ym, x + (size_t)m * K, K, st);
+      if (s1 == RQ_ERR_SHAPE && m == 0) break;
+      if (s1 != RQ_OK) return s1;
+      if (m == M - 1) return RQ_OK;
+    }
   }
   switch (M) {
+    case 1: return run_q4k<1, 2>(w, x, y, N, K, st);
     case 2: return run_q4k<2, 2>(w, x, y, N, K, st);
     case 3: return run_q4k<3, 2>(w, x, y, N, K, st);
     case 4: return run_q4k<4, 2>(w, x, y, N, K, st);
     case 5: return run_q4k<5, 1>(w, x, y, N, K, st);
     case 6: return run_q4k<6, 1>(w, x, y, N, K, st);
     case 7: return run_q4k<7, 1>(w, x, y, N, K, st);
-    case 8: return run_q4k<8, 1>(w, x, y, N, K, st);
-    default: return RQ_ERR_SHAPE;
+    default: return run_q4k<8, 1>(w, x, y, N, K, st);
   }
 }
 

@@ -94,18 +94,9 @@ rq_status launch_gemv_m1_dual(int count, const int* starts, const uint8_t* const
                               const float* x, int K, cudaStream_t st);
 // Read and clear the GEMV kernels' device error word (after a sync).
 rq_status read_and_clear_gemv_error();
-
-// rq_gemv_mma.cu ------------------------------------------------------------
-// Q4_K GEMV for M = 2..8 tokens on the tensor cores.  RQ_ERR_SHAPE (nothing
-// launched) when the shape does not fit the kernel.
-rq_status launch_q4k_gemv_mma(const uint8_t* w, const float* x, float* y, int M, int N, int K,
-                              cudaStream_t st);
-// The same for several Q4_K weights that share x (member i: ws[i] with Ns[i]
-// rows into ys[i] [M x Ns[i]]) in one launch.
-rq_status launch_q4k_gemv_mma_group(int count, const uint8_t* const* ws, const int* Ns,
-                                    float* const* ys, const float* x, int M, int K,
-                                    cudaStream_t st);
-rq_status read_and_clear_gemv_mma_error();
+// Read (into *out, if non-null) and clear the count of GEMV outputs that took
+// the exact fp64 path (after a sync).
+rq_status read_and_clear_gemv_exact_outputs(int64_t* out);
 
 // rq_wcache.cu --------------------------------------------------------------
 // Decode the packed weight (fixed fp32 order) and reduce its absmax into

@@ -394,8 +394,8 @@ def test_linear_group_mixed_formats_ragged(rq, K, N4, N6):
 @pytest.mark.parametrize("M", [4, 8])
 def test_linear_group_decoder_shapes_few_tokens(rq, monkeypatch, M):
     """q + k and gate + up of the decoder at a few tokens (GEMV route, the
-    threshold raised above M): each group's Q4_K members in one tensor-core
-    launch; sampled rows of every member against the oracle."""
+    threshold raised above M): each group's Q4_K members in one launch per
+    token; sampled rows of every member against the oracle."""
     K = 3584
     ctx = rq.Context(gemm_threshold=9)
     for seed, Ns in ((3, (3584, 512)), (4, (18944, 18944))):
@@ -406,7 +406,7 @@ def test_linear_group_decoder_shapes_few_tokens(rq, monkeypatch, M):
         ctx.rq_ctx_trace_begin(16)
         ctx.rq_linear_group([Q4K] * len(Ns), [to_dev(W) for W in Ws], to_dev(x), ys, list(Ns),
                             M, K)
-        assert ctx.rq_ctx_trace_end()["gemv"][0] == 1
+        assert ctx.rq_ctx_trace_end()["gemv"][0] == M
         assert rq.rq_get_device_status() == 0
         for W, y, N in zip(Ws, ys, Ns):
             rows = np.array([0, 1, 15, 16, N // 2, N - 17, N - 16, N - 1])
@@ -415,12 +415,12 @@ def test_linear_group_decoder_shapes_few_tokens(rq, monkeypatch, M):
     ctx.close()
 
 
-@pytest.mark.parametrize("M,kernels", [(1, ["dual_q4k_q6k_m1"]), (4, ["q4k_ft", "q6k_mt"]),
-                                       (8, ["q4k_ft", "q6k_mt_ksplit"])])
+@pytest.mark.parametrize("M,kernels", [(1, ["dual_q4k_q6k_m1"]),
+                                       (4, ["dual_q4k_q6k_m1"] * 4),
+                                       (8, ["dual_q4k_q6k_m1"] * 8)])
 def test_decoder_qkv_group_launches(rq, monkeypatch, capfd, M, kernels):
-    """q/k/v of the decoder as one group call: one launch for a token (the
-    Q4_K and Q6_K members share it), the grouped tensor-core launch plus the
-    Q6_K member's own at a few tokens."""
+    """q/k/v of the decoder as one group call: one launch per token, which
+    the Q4_K and Q6_K members share."""
     monkeypatch.setenv("RQ_GEMV_LOG", "1")
     K = 3584
     members = [(Q4K, 3584), (Q4K, 512), (Q6K, 512)]

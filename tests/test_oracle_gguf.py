@@ -21,56 +21,7 @@ def test_half_to_float_exhaustive_vs_numpy(orc):
     assert np.array_equal(ours[~nan].view(np.uint32), ref[~nan].view(np.uint32))
 
 
-# --------------------------------------------------------------- packers --
-
-def pack_scale_min(sc, mn):
-    """8 six-bit scales and mins -> the 12 packed bytes of a Q4_K block."""
-    b = np.zeros(12, dtype=np.int64)
-    for j in range(4):
-        b[j] = (sc[j] & 63) | ((sc[j + 4] >> 4) << 6)
-        b[j + 4] = (mn[j] & 63) | ((mn[j + 4] >> 4) << 6)
-        b[j + 8] = (sc[j + 4] & 15) | ((mn[j + 4] & 15) << 4)
-    return b.astype(np.uint8)
-
-
-def pack_q4k(d, dmin, sc, mn, q):
-    """Block from fp16 d/dmin, 8 scales, 8 mins, 256 quants (0..15)."""
-    blk = np.zeros(144, dtype=np.uint8)
-    blk[0:2] = np.array([d], np.float16).view(np.uint8)
-    blk[2:4] = np.array([dmin], np.float16).view(np.uint8)
-    blk[4:16] = pack_scale_min(sc, mn)
-    qs = np.zeros(128, dtype=np.int64)
-    for c in range(4):
-        for l in range(32):
-            qs[32 * c + l] = q[64 * c + l] | (q[64 * c + 32 + l] << 4)
-    blk[16:144] = qs.astype(np.uint8)
-    return blk
-
-
-def pack_q6k(d, scales, q):
-    """Block from fp16 d, 16 int8 scales, 256 quants (0..63)."""
-    ql = np.zeros(128, np.int64)
-    qh = np.zeros(64, np.int64)
-    for h in range(2):
-        for l in range(32):
-            q0, q1, q2, q3 = (q[128 * h + l], q[128 * h + 32 + l],
-                              q[128 * h + 64 + l], q[128 * h + 96 + l])
-            ql[64 * h + l] = (q0 & 15) | ((q2 & 15) << 4)
-            ql[64 * h + 32 + l] = (q1 & 15) | ((q3 & 15) << 4)
-            qh[32 * h + l] = ((q0 >> 4) | ((q1 >> 4) << 2) | ((q2 >> 4) << 4)
-                              | ((q3 >> 4) << 6))
-    blk = np.zeros(210, np.uint8)
-    blk[0:128] = ql.astype(np.uint8)
-    blk[128:192] = qh.astype(np.uint8)
-    blk[192:208] = np.asarray(scales, np.int8).view(np.uint8)
-    blk[208:210] = np.array([d], np.float16).view(np.uint8)
-    return blk
-
-
-def q6_scale_slot(i):
-    h, r = divmod(i, 128)
-    quarter, l = divmod(r, 32)
-    return 8 * h + l // 16 + 2 * quarter
+from gguf_pack import pack_q4k, pack_q6k, pack_scale_min, q6_scale_slot  # noqa: E402
 
 
 # ------------------------------------------------------------------ Q4_K --
@@ -215,3 +166,27 @@ def test_synthetic_q6k_fields_in_range():
     W = synthetic.q6k_matrix(1, 64, 1024).reshape(-1, 210)
     sc = W[:, 192:208].view(np.int8)
     assert sc.min() == -32 and sc.max() == 31
+
+
+def test_matrix_packers_match_block_packers():
+    """The vectorised packers the GPU tests use build the same bytes as the
+    block packers pinned above."""
+    from gguf_pack import pack_q4k_matrix, pack_q6k_matrix
+    rng = np.random.default_rng(5)
+    N, nsb = 3, 2
+    d = rng.uniform(1e-3, 1e-2, (N, nsb))
+    dmin = rng.uniform(1e-3, 1e-2, (N, nsb))
+    sc = rng.integers(0, 64, (N, nsb, 8))
+    mn = rng.integers(0, 64, (N, nsb, 8))
+    q = rng.integers(0, 16, (N, nsb, 256))
+    W = pack_q4k_matrix(d, dmin, sc, mn, q)
+    for r in range(N):
+        for b in range(nsb):
+            assert np.array_equal(W[r, 144 * b:144 * (b + 1)],
+                                  pack_q4k(d[r, b], dmin[r, b], sc[r, b], mn[r, b], q[r, b]))
+    scales = rng.integers(-32, 32, (N, nsb, 16))
+    q6 = rng.integers(0, 64, (N, nsb, 256))
+    W6 = pack_q6k_matrix(d, scales, q6)
+    for r in range(N):
+        for b in range(nsb):
+            assert np.array_equal(W6[r, 210 * b:210 * (b + 1)], pack_q6k(d[r, b], scales[r, b], q6[r, b]))
