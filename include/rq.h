@@ -273,16 +273,19 @@ rq_status rq_linear_group(rq_ctx *ctx, int count, const rq_qtype *qtypes,
  *   w_dequant: one device float.  y: f32 [M x N].
  * The quantized activation (M_pad x K bytes, M_pad = M rounded up to 16) and
  * two device scalars live in one fixed array inside the library, of
- * RQ_NOALLOC_MAX_ACT_BYTES + 256 bytes, which every GPU that loads the
- * library holds until the process exits.  No call allocates: no cudaMalloc,
- * cudaFree or allocating library routine.
- *   - The first call on a device looks up that array's device address (once
- *     per device, with that device current); make that first call before
- *     any stream capture.
- *   - Each GPU has its own copy of the array.  All calls on a GPU share it,
- *     and it keeps the last call's contents; each call re-zeroes what must
- *     start at zero.  Calls whose work overlaps on the same GPU (on two
- *     streams, say) race on the array: serialise them.
+ * RQ_NOALLOC_MAX_ACT_BYTES + 256 bytes, which the GPU holds until the process
+ * exits.  No call allocates: no cudaMalloc, cudaFree or allocating library
+ * routine.
+ *   - The first call looks up the array's device address (with the device
+ *     current).  Under CUDA's lazy module loading that lookup may also be
+ *     what loads the library's module and reserves the array, so the first
+ *     call may take device memory once: make it a warm-up call before
+ *     serving or any stream capture, and before fixing a memory budget.
+ *   - The library serves one device per process (see the conventions at
+ *     the top).  All calls share the array, and it keeps the last call's
+ *     contents; each call re-zeroes what must start at zero.  Calls whose
+ *     work overlaps on the GPU (on two streams, say) race on the array:
+ *     serialise them.
  * Errors: RQ_ERR_NULL; RQ_ERR_SHAPE for M, N < 1, K < 128, K % 128 != 0,
  * misaligned pointers, or M_pad * K > RQ_NOALLOC_MAX_ACT_BYTES (the array
  * is too small for this activation); RQ_ERR_CUDA. */

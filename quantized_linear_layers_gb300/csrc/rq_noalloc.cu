@@ -16,15 +16,18 @@ namespace rq {
 namespace {
 
 // Scratch layout: absmax word at byte 0, activation dequant scale at byte
-// 128, activation E4M3 bytes (M_pad x K) from byte 256.  Every GPU that loads
-// the library holds this array until the process exits.
+// 128, activation E4M3 bytes (M_pad x K) from byte 256.  The GPU holds this
+// array until the process exits (it may be reserved only when the module is
+// loaded, which lazy loading defers to the first call).
 constexpr size_t kActOffset = 256;
 constexpr size_t kScratchBytes = kActOffset + RQ_NOALLOC_MAX_ACT_BYTES;
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kScratchBytes];
 
-// Device address of the array, looked up once per device with that device
-// current (in host code the array's name is only a host-side stand-in).
+// Device address of the array, looked up on the first call with the device
+// current (in host code the array's name is only a host-side stand-in).  The
+// library serves one device per process; the table is indexed by device only
+// so that the lookup never returns another device's address.
 uint8_t* scratch_address() {
   static std::mutex mu;
   static uint8_t* addr[64] = {nullptr};

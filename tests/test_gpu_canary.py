@@ -56,7 +56,7 @@ def check_result(qtype, W, x, N, K, got):
 @pytest.mark.parametrize("qtype,M,N,K", [
     (Q4K, 1, 300, 512),      # one-token kernel, a few rows per CTA
     (Q4K, 1, 300, 18944),    # one-token kernel, rows split between two CTAs
-    (Q4K, 3, 1000, 1024),    # few-token tensor-core kernel
+    (Q4K, 3, 1000, 1024),    # three tokens: one launch of the one-token kernel each
     (Q6K, 1, 301, 512),      # one-token Q6_K kernel, odd row count
     (Q6K, 3, 300, 1024),     # few-token Q6_K kernel
     (Q4K, 4, 300, 512),      # FP8 route at the threshold

@@ -496,3 +496,59 @@ def test_linear_group_rejects_bad_counts(rq):
     with pytest.raises(rq.RqError):
         ctx.rq_linear_group([], [], empty((1, 256), torch.float32), [], [], 1, 256)
     ctx.close()
+
+
+# ------------------------------------------------- a full decoder layer --
+
+LAYER_CALLS = (("q", "k", "v"), ("o",), ("gate", "up"), ("down",))
+LAYER_SOURCE = {"q": "x", "k": "x", "v": "x", "o": "a", "gate": "h", "up": "h", "down": "g"}
+
+
+@pytest.fixture(scope="module")
+def decoder_layer():
+    """One decoder layer's seven weights (full shapes) and the oracle's FP8
+    weight caches of them."""
+    layer = {}
+    for i, (name, qt, N, K) in enumerate(synthetic.LAYER_LINEARS):
+        W = synthetic.weight_matrix(synthetic.layer_seed(77, 0, i), qt, N, K)
+        layer[name] = (qt, N, K, W, oracle.fp8_weight_cache(qt, W, N, K))
+    return layer
+
+
+@pytest.mark.parametrize("M,rows", [
+    (16, [0, 7, 15]),
+    (128, [0, 45, 77, 109, 127]),
+    (4096, [256 * b + (97 * b) % 256 for b in range(16)] + [4095])])
+def test_full_decoder_layer_fp8_route(rq, decoder_layer, M, rows):
+    """The prefill stack's four calls for one layer at M tokens, as the
+    benchmark makes them (rq_linear_group for q/k/v and gate/up, rq_linear
+    for o and down): every member's sampled token rows (full output rows,
+    one in every band of M/16 tokens and the last) against the oracle's FP8
+    route -- its weight caches, the activation's absmax and E4M3 bytes, exact
+    FP8 dot products."""
+    ctx = rq.Context()
+    acts = {kind: synthetic.activation(5000 + 10 * M + j, M, K, outlier_frac=1e-3)
+            for j, (kind, K) in enumerate((("x", 3584), ("a", 3584), ("h", 3584),
+                                           ("g", 18944)))}
+    dacts = {k: to_dev(v) for k, v in acts.items()}
+    ys = {name: empty((M, N), torch.float32) for name, (_, N, _, _, _) in decoder_layer.items()}
+    Wd = {name: to_dev(v[3]) for name, v in decoder_layer.items()}
+    for grp in LAYER_CALLS:
+        K = decoder_layer[grp[0]][2]
+        x = dacts[LAYER_SOURCE[grp[0]]]
+        if len(grp) == 1:
+            qt, N = decoder_layer[grp[0]][:2]
+            ctx.rq_linear(qt, Wd[grp[0]], x, ys[grp[0]], M, N, K)
+        else:
+            ctx.rq_linear_group([decoder_layer[n][0] for n in grp], [Wd[n] for n in grp], x,
+                                [ys[n] for n in grp], [decoder_layer[n][1] for n in grp], M, K)
+    assert rq.rq_get_device_status() == 0
+    quant = {k: oracle.quant_e4m3(v, oracle.absmax_bits(v)) for k, v in acts.items()}
+    for name, (qt, N, K, W, (wb, wd)) in decoder_layer.items():
+        xb, xd = quant[LAYER_SOURCE[name]]
+        ms = np.repeat(np.asarray(rows), N)
+        ns = np.tile(np.arange(N), len(rows))
+        ref = oracle.fp8_gemm_pairs(xb, xd, wb, wd, ms, ns).reshape(len(rows), N)
+        got = ys[name].cpu().numpy()[rows]
+        check_gemm(got, ref)
+    ctx.close()

@@ -138,3 +138,57 @@ def test_large_scaled_variant_bit_exact(rq):
     ob, od = oracle.quant_e4m3(x, a)
     assert bits == a and deq == od
     assert np.array_equal(out, ob.ravel())
+
+
+CHUNK = 1 << 27  # fp32 patterns per GPU launch
+
+
+def gpu_chunk_checksums(rq, start, bits, out, deq):
+    """Encode patterns start .. start + CHUNK - 1 on the GPU with the absmax
+    word `bits`; the checksums of encode_sweep.checksums over the codes."""
+    t = torch.arange(start, start + CHUNK, dtype=torch.int64, device="cuda")
+    t = t - (t >= 2 ** 31).to(torch.int64) * 2 ** 32  # low 32 bits, as signed
+    x = t.to(torch.int32).view(torch.float32)
+    rq.rq_quant_e4m3(x, CHUNK, bits, out, deq)
+    w = out.view(torch.int64)
+    v = torch.arange(w.numel(), dtype=torch.int64, device="cuda") * 2 + 1
+    c1 = int((w * v).sum().item()) & 0xFFFFFFFFFFFFFFFF
+    c2 = int(w.sum().item()) & 0xFFFFFFFFFFFFFFFF
+    return c1, c2
+
+
+@pytest.mark.parametrize("absmax", [448.0, 3.0])
+def test_device_encoder_every_fp32_pattern(rq, absmax):
+    """All 2^32 fp32 bit patterns through rq_quant_e4m3 with the absmax word
+    fixed at `absmax` (scale exactly 1 for 448, 448/3 otherwise), against the
+    oracle's encoder in chunks of 2^27 (one process per host core): the codes
+    agree bit for bit, compared through position-weighted checksums; a
+    mismatching chunk is recomputed in full to name its first differing
+    patterns."""
+    import multiprocessing as mp
+    import os
+
+    import encode_sweep
+    a_bits = int(np.array([absmax], np.float32).view(np.uint32)[0])
+    scale = oracle.scales(a_bits)[0]
+    bits = to_dev(np.array([a_bits], np.uint32).view(np.int32))
+    out = empty(CHUNK, torch.uint8)
+    deq = empty(1, torch.float32)
+    starts = list(range(0, 1 << 32, CHUNK))
+    with mp.get_context("spawn").Pool(os.cpu_count() or 1) as pool:
+        pending = pool.map_async(encode_sweep.oracle_chunk,
+                                 [(s, CHUNK, float(scale)) for s in starts], chunksize=1)
+        gpu = [gpu_chunk_checksums(rq, s, bits, out, deq) for s in starts]
+        want = pending.get(timeout=1800)
+    assert rq.rq_get_device_status() == 0
+    assert np.float32(deq.item()) == oracle.scales(a_bits)[1]
+    bad = [s for s, g, o in zip(starts, gpu, want) if g != o]
+    if bad:
+        s = bad[0]
+        gpu_chunk_checksums(rq, s, bits, out, deq)
+        got = out.cpu().numpy()
+        ref = oracle.encode_scaled(encode_sweep.patterns(s, CHUNK), scale)
+        idx = np.flatnonzero(got != ref)[:8]
+        pytest.fail("chunks %s differ; first patterns %s: gpu %s oracle %s" % (
+            [hex(b) for b in bad[:4]], [hex(s + int(i)) for i in idx],
+            got[idx].tolist(), ref[idx].tolist()))

@@ -190,3 +190,57 @@ def test_matrix_packers_match_block_packers():
     for r in range(N):
         for b in range(nsb):
             assert np.array_equal(W6[r, 210 * b:210 * (b + 1)], pack_q6k(d[r, b], scales[r, b], q6[r, b]))
+
+
+def q6k_one_hot_effect(byte, bit):
+    """From the Q6_K layout alone: the weights that change when bit `bit` of
+    byte `byte` is set in a block with d = 1, every scale 1 and every quant
+    0 (every weight -32), and their new values.  Layout: ql[128] (low 4 bits
+    of the quants), qh[64] (top 2 bits), int8 scales[16], fp16 d; half h
+    holds weights 128h .. 128h+127; for l < 32 the low nibble of ql[64h+l]
+    is quant 128h+l, of ql[64h+32+l] quant 128h+32+l, their high nibbles
+    quants 128h+64+l and 128h+96+l; bits 2i..2i+1 of qh[32h+l] are the top
+    bits of quant 128h+32i+l; weight 128h+32i+l uses scale 8h+l//16+2i."""
+    if byte < 128:
+        h, r = divmod(byte, 64)
+        quarter = (0 if r < 32 else 1) + (2 if bit >= 4 else 0)
+        q = 1 << (bit % 4)
+        return {128 * h + 32 * quarter + r % 32: float(q - 32)}
+    if byte < 192:
+        h, l = divmod(byte - 128, 32)
+        quarter, top = divmod(bit, 2)
+        return {128 * h + 32 * quarter + l: float((16 << top) - 32)}
+    if byte < 208:
+        j = byte - 192
+        h, r = divmod(j, 8)
+        quarter, half = divmod(r, 2)
+        scale = int(np.array([1 | (1 << bit)], np.uint8).view(np.int8)[0])
+        if scale == 1:
+            return {}
+        return {128 * h + 32 * quarter + 16 * half + l: -32.0 * scale for l in range(16)}
+    d = float(np.array([0x3C00 ^ (1 << (bit + 8 * (byte - 208)))], np.uint16).view(np.float16)[0])
+    return {k: -32.0 * d for k in range(256)}
+
+
+def test_q6k_one_hot_bytes(orc):
+    """Every bit of every byte of a Q6_K block, set alone on a base block,
+    changes exactly the weights the layout description predicts, to the
+    predicted values (a table written independently of the packers)."""
+    base = np.zeros(210, np.uint8)
+    base[192:208] = 1
+    base[208:210] = np.array([1.0], np.float16).view(np.uint8)
+    w0 = orc.decode_block(Q6K, base)
+    assert np.all(w0 == -32.0)
+    for byte in range(210):
+        for bit in range(8):
+            blk = base.copy()
+            blk[byte] |= np.uint8(1 << bit)
+            if blk[byte] == base[byte]:
+                continue
+            w = orc.decode_block(Q6K, blk)
+            want = q6k_one_hot_effect(byte, bit)
+            changed = {int(k): float(w[k]) for k in np.flatnonzero(w != w0)}
+            if byte >= 208 and not np.isfinite(list(want.values())[0]):
+                continue  # d bits that make d Inf/NaN: checked by the half tests
+            want = {k: v for k, v in want.items() if v != -32.0}
+            assert changed == want, (byte, bit, changed, want)
