@@ -20,6 +20,9 @@
 //    to sum_k |x_k w_k| (well inside the 1e-4 bound); an output that comes
 //    out non-finite (overflow, non-finite x) is recomputed exactly in fp64.
 //  * fp32 accumulation, one warp-shuffle reduction per row.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <cstdio>
 #include <cstdlib>
 #include <map>
@@ -404,7 +407,23 @@ q6k_gemv_kernel(const uint8_t* __restrict__ W, const float* __restrict__ x,
 
 __device__ unsigned int g_gemv_error;  // bit 0: a pipeline wait timed out
 
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
 struct M1Args {
+  // One-token Q4_K with rows split between two CTAs of a single weight: a
+  // 3-D view [N rows][K/256 super-blocks][144 B] of it whose box is one
+  // stage (rows_per_stage rows x this CTA's super-blocks); tma = 1 loads
+  // each stage with one copy of it.
+  CUtensorMap map;
+  int tma;
+  uint32_t stage_stride;  // bytes between stages in the ring (128-byte multiple)
   const uint8_t* W;
   const float* x;
   float* y;
@@ -690,18 +709,24 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
       return;
     }
     const int nr = min(rps, rows - it * rps);
-    const uint32_t bytes = (uint32_t)(nr * rowbytes);
-    mbar_arrive_expect_tx(full0 + 8 * s, bytes);
-    // one copy per segment the stage's rows fall in (per row when the rows
-    // are split between the CTAs of a cluster)
-    for (int v = r0 + it * rps, done = 0; done < nr;) {
-      const int sg = m1_seg(a, v);
-      const int take = a.ksplit == 1 ? min(nr - done, a.seg_start[sg + 1] - v) : 1;
-      bulk_g2s(smem_u32(ring + s * stage_bytes + (size_t)done * rowbytes),
-               a.seg_w[sg] + (size_t)(v - a.seg_start[sg]) * rowstride + (size_t)h * rowbytes,
-               (uint32_t)(take * rowbytes), full0 + 8 * s);
-      v += take;
-      done += take;
+    if (a.tma) {
+      // the whole box, rows past N read as zero (and count as bytes)
+      mbar_arrive_expect_tx(full0 + 8 * s, stage_bytes);
+      tma_load_3d(smem_u32(ring + s * a.stage_stride), &a.map, full0 + 8 * s, 0, h * nsb,
+                  r0 + it * rps);
+    } else {
+      mbar_arrive_expect_tx(full0 + 8 * s, (uint32_t)(nr * rowbytes));
+      // one copy per segment the stage's rows fall in (per row when the rows
+      // are split between the CTAs of a cluster)
+      for (int v = r0 + it * rps, done = 0; done < nr;) {
+        const int sg = m1_seg(a, v);
+        const int take = a.ksplit == 1 ? min(nr - done, a.seg_start[sg + 1] - v) : 1;
+        bulk_g2s(smem_u32(ring + s * a.stage_stride + (size_t)done * rowbytes),
+                 a.seg_w[sg] + (size_t)(v - a.seg_start[sg]) * rowstride + (size_t)h * rowbytes,
+                 (uint32_t)(take * rowbytes), full0 + 8 * s);
+        v += take;
+        done += take;
+      }
     }
     issued |= 1u << s;
     parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
@@ -846,7 +871,7 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
           ok = __all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * s, ph, a.wait_limit_ns, &g_gemv_error));
           if (ok) {
             const int nr = min(rps, rows - it * rps);
-            const uint8_t* stage = ring + s * stage_bytes + (size_t)team * RPT * rowbytes;
+            const uint8_t* stage = ring + s * a.stage_stride + (size_t)team * RPT * rowbytes;
 #pragma unroll
             for (int j = 0; j < RPT; j += 2) {
               const int ra = team * RPT + j;
@@ -912,8 +937,10 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
   }
 }
 
-template <int RPT>
-__global__ void __launch_bounds__(544, 1) q4k_gemv_m1_kernel(const M1Args a) {
+// MAXT: the most threads a launch of the instance has (17 warps: 96
+// registers a thread; 16 warps: 128).
+template <int RPT, int MAXT>
+__global__ void __launch_bounds__(MAXT, 1) q4k_gemv_m1_kernel(const __grid_constant__ M1Args a) {
   q4k_m1_body<RPT>(a, blockIdx.x, gridDim.x);
 }
 
@@ -1234,7 +1261,7 @@ __device__ __forceinline__ void q6k_m1_body(const M1Args& a, const int bid, cons
 }
 
 template <int RPT>
-__global__ void __launch_bounds__(544, 1) q6k_gemv_m1_kernel(const M1Args a) {
+__global__ void __launch_bounds__(544, 1) q6k_gemv_m1_kernel(const __grid_constant__ M1Args a) {
   q6k_m1_body<RPT>(a, blockIdx.x, gridDim.x);
 }
 
@@ -1243,7 +1270,8 @@ __global__ void __launch_bounds__(544, 1) q6k_gemv_m1_kernel(const M1Args a) {
 // members' rows, the others the Q6_K body, each with its own arguments and
 // its own layout of the (shared) dynamic shared memory.
 template <int R4, int R6>
-__global__ void __launch_bounds__(544, 1) gemv_m1_dual_kernel(const M1Args a4, const M1Args a6,
+__global__ void __launch_bounds__(544, 1) gemv_m1_dual_kernel(const __grid_constant__ M1Args a4,
+                                                              const __grid_constant__ M1Args a6,
                                                               int g4) {
   if ((int)blockIdx.x < g4)
     q4k_m1_body<R4>(a4, blockIdx.x, g4);
@@ -1260,7 +1288,7 @@ __global__ void __launch_bounds__(544, 1) gemv_m1_dual_kernel(const M1Args a4, c
 // products; the M per-token sums of a row are reduced across the warp at
 // once with the 8-slot transpose pattern (slot = token).
 
-__global__ void __launch_bounds__(544, 1) q6k_gemv_mt_kernel(const M1Args a) {
+__global__ void __launch_bounds__(544, 1) q6k_gemv_mt_kernel(const __grid_constant__ M1Args a) {
   extern __shared__ __align__(128) uint8_t smem_q6t[];
   const int M = a.M;
   // with ksplit CTAs per cluster, CTA rank h computes super-blocks
@@ -1518,6 +1546,37 @@ __global__ void __launch_bounds__(544, 1) q6k_gemv_mt_kernel(const M1Args a) {
 
 // ---------------------------------------------------------------- launch --
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 3-D view [N rows][K/256 super-blocks][144 B] of a Q4_K weight with a box of
+// `rows` rows x `sbs` super-blocks; rows past N read as zero.
+bool q4k_stage_map(CUtensorMap* map, const uint8_t* w, int N, int K, int sbs, int rows) {
+  auto fn = tensor_map_encoder();
+  if (fn == nullptr) return false;
+  const int nsb = K / kQK;
+  const cuuint64_t dims[3] = {(cuuint64_t)kQ4KBytes, (cuuint64_t)nsb, (cuuint64_t)N};
+  const cuuint64_t strides[2] = {(cuuint64_t)kQ4KBytes, (cuuint64_t)nsb * kQ4KBytes};
+  const cuuint32_t box[3] = {(cuuint32_t)kQ4KBytes, (cuuint32_t)sbs, (cuuint32_t)rows};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(w), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 // Resident CTAs per SM for a kernel at a dynamic shared-memory size; the
 // occupancy query is cached per (kernel, smem) since it costs host time.
 template <typename KernelT>
@@ -1649,19 +1708,25 @@ rq_status plan_q4k_m1(int nseg, const int* starts, const uint8_t* const* ws, flo
   a.rows_per_stage = rpt * a.teams;
   const int rowbytes = (Kc / kQK) * kQ4KBytes;
   const int stage_bytes = a.rows_per_stage * rowbytes;
+  // split rows of a single weight: one 3-D copy per stage (RQ_GEMV_TMA3D=0:
+  // one bulk copy per half-row instead); TMA destinations 128-byte aligned
+  a.tma = (ksplit == 2 && nseg == 1 && m1_knob("RQ_GEMV_TMA3D", 1, 0, 1) == 1 &&
+           a.rows_per_stage <= 256 && Kc / kQK <= 256) ? 1 : 0;
+  if (a.tma && !q4k_stage_map(&a.map, ws[0], N, K, Kc / kQK, a.rows_per_stage)) a.tma = 0;
+  a.stage_stride = a.tma ? (uint32_t)((stage_bytes + 127) & ~127) : (uint32_t)stage_bytes;
   const size_t nsub2 = (size_t)((nsub + 1) & ~1);
   // planes; per sub-block: scale, sum, two error-bound constants; barriers;
   // per row: sum, certificate, exact-path list; the list's count
   const size_t fixed = (size_t)U * kPlaneStride + 16 * nsub2 + 16 * (size_t)max_stages +
                        12 * (size_t)max_rows + 16;
   const size_t limit = 227 * 1024;
-  if (fixed + 2 * (size_t)stage_bytes > limit) return RQ_ERR_SHAPE;
+  if (fixed + 2 * (size_t)a.stage_stride > limit) return RQ_ERR_SHAPE;
   size_t ring = (size_t)ring_kb * 1024;
   if (ring > limit - fixed) ring = limit - fixed;
-  int stages = (int)(ring / stage_bytes);
+  int stages = (int)(ring / a.stage_stride);
   stages = stages > max_stages ? max_stages : (stages < 2 ? 2 : stages);
   a.stages = stages;
-  a.ring_bytes = (uint32_t)(stages * stage_bytes);
+  a.ring_bytes = (uint32_t)stages * a.stage_stride;
   a.wait_limit_ns = kWaitLimitNs;
   a.max_rows = max_rows;
   p->smem = a.ring_bytes + (size_t)U * kPlaneStride + 16 * nsub2 + 16 * (size_t)stages +
@@ -1677,10 +1742,15 @@ rq_status run_q4k_m1(int nseg, const int* starts, const uint8_t* const* ws, floa
   M1Plan p;
   const rq_status s = plan_q4k_m1(nseg, starts, ws, ys, x, K, 0, true, &p);
   if (s != RQ_OK) return s;
-  auto kern = p.rpt == 8 ? q4k_gemv_m1_kernel<8>
-                         : (p.rpt == 4 ? q4k_gemv_m1_kernel<4> : q4k_gemv_m1_kernel<2>);
-  static size_t smem_set[3] = {48 * 1024, 48 * 1024, 48 * 1024};
-  const rq_status sa = m1_allow_smem(kern, p.smem, smem_set[p.rpt == 8 ? 2 : (p.rpt == 4 ? 1 : 0)]);
+  // launches of up to 16 warps take the instance compiled for 512 threads
+  // (128 registers a thread, where 17 warps allow 96)
+  const bool w16 = p.threads <= 512;
+  auto kern = p.rpt == 8 ? (w16 ? q4k_gemv_m1_kernel<8, 512> : q4k_gemv_m1_kernel<8, 544>)
+            : p.rpt == 4 ? (w16 ? q4k_gemv_m1_kernel<4, 512> : q4k_gemv_m1_kernel<4, 544>)
+                         : (w16 ? q4k_gemv_m1_kernel<2, 512> : q4k_gemv_m1_kernel<2, 544>);
+  static size_t smem_set[6] = {48 * 1024, 48 * 1024, 48 * 1024, 48 * 1024, 48 * 1024, 48 * 1024};
+  const rq_status sa = m1_allow_smem(
+      kern, p.smem, smem_set[(p.rpt == 8 ? 2 : (p.rpt == 4 ? 1 : 0)) + (w16 ? 3 : 0)]);
   if (sa != RQ_OK) return sa;
   gemv_log(p.a.ksplit == 1 ? "q4k_m1" : "q4k_m1_ksplit", 1, p.a.N, K, p.grid);
   if (p.a.ksplit == 1) return launch_kernel(kern, p.grid, p.threads, p.smem, st, p.a);
@@ -1745,6 +1815,7 @@ rq_status plan_q6k_m1(const uint8_t* w, const float* x, float* y, int M, int N, 
   a.row_align = ra;
   a.M = M;
   a.ksplit = ks;
+  a.tma = 0;
   a.nseg = 1;
   a.seg_start[0] = 0;
   for (int i = 1; i <= RQ_MAX_GROUP; ++i) a.seg_start[i] = N;
@@ -1769,6 +1840,7 @@ rq_status plan_q6k_m1(const uint8_t* w, const float* x, float* y, int M, int N, 
   stages = stages > max_stages ? max_stages : (stages < 2 ? 2 : stages);
   a.stages = stages;
   a.ring_bytes = (uint32_t)(stages * stage_bytes);
+  a.stage_stride = (uint32_t)stage_bytes;
   a.wait_limit_ns = kWaitLimitNs;
   a.max_rows = max_rows;
   p->smem = a.ring_bytes + (size_t)M * U * kPlaneStride + 12 * (size_t)M * nsub16 +
