@@ -467,16 +467,14 @@ __device__ __forceinline__ void m1_cluster_sync() {
                    : "memory");
 }
 
-// A float in the shared memory of CTA `rank` of the cluster, at the offset
-// of `local` in this CTA.
-__device__ __forceinline__ float m1_ld_peer(const float* local, uint32_t rank) {
+// Store v into the shared memory of CTA `rank` of the cluster, at the offset
+// of `local` in this CTA (a posted store: no round trip).
+__device__ __forceinline__ void m1_st_peer(float* local, uint32_t rank, float v) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
                : "=r"(remote)
                : "r"(smem_u32(local)), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
@@ -675,7 +673,9 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
   float* acc = reinterpret_cast<float*>(bars + 2 * a.stages);          // max_rows
   float* dacc = acc + a.max_rows;                                      // max_rows
   int* flist = reinterpret_cast<int*>(dacc + a.max_rows);              // max_rows
-  int* nfail = flist + a.max_rows;
+  int* nfail = flist + a.max_rows;                                     // 4 words
+  float* racc = reinterpret_cast<float*>(nfail + 4);                   // max_rows (rank 0: rank 1's
+  float* rdacc = racc + a.max_rows;                                    // max_rows  sums, certificates)
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + a.stages);
 
   const int compute_warps = a.teams * a.team_warps;
@@ -904,25 +904,31 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
   }
   __syncthreads();
   // Outputs whose certificate holds are stored; the others are listed and
-  // recomputed exactly, one warp per output (rows split between the CTAs of
-  // a cluster: rank 0 adds rank 1's partial sums and certificates first).
-  if (a.ksplit == 2) m1_cluster_sync();  // both halves of every row are in their CTAs' acc
-  if (h == 0)
-    for (int i = threadIdx.x; i < rows; i += blockDim.x) {
-      float y = acc[i], D = dacc[i];
-      if (a.ksplit == 2) {
-        y += m1_ld_peer(acc + i, 1);
-        D += m1_ld_peer(dacc + i, 1);
+  // recomputed exactly, one warp per output.  Rows split between the CTAs of
+  // a cluster: rank 1 posts its partial sums and certificates into rank 0's
+  // receive buffers, and rank 0 adds them after the cluster barrier.
+  if (a.ksplit == 2) {
+    if (h == 1)
+      for (int i = threadIdx.x; i < rows; i += blockDim.x) {
+        m1_st_peer(racc + i, 0, acc[i]);
+        m1_st_peer(rdacc + i, 0, dacc[i]);
       }
-      if (cert_fails(D)) {
-        flist[atomicAdd(nfail, 1)] = i;
-      } else {
-        const int sg = m1_seg(a, r0 + i);
-        a.seg_y[sg][r0 + i - a.seg_start[sg]] = y;
-      }
+    m1_cluster_sync();  // rank 1's stores are visible to rank 0
+    if (h != 0) return;
+  }
+  for (int i = threadIdx.x; i < rows; i += blockDim.x) {
+    float y = acc[i], D = dacc[i];
+    if (a.ksplit == 2) {
+      y += racc[i];
+      D += rdacc[i];
     }
-  if (a.ksplit == 2) m1_cluster_sync();  // rank 1's shared memory stays until rank 0 has read it
-  if (h != 0) return;
+    if (cert_fails(D)) {
+      flist[atomicAdd(nfail, 1)] = i;
+    } else {
+      const int sg = m1_seg(a, r0 + i);
+      a.seg_y[sg][r0 + i - a.seg_start[sg]] = y;
+    }
+  }
   __syncthreads();
   const int nwarps = blockDim.x >> 5;
   for (int f = warp; f < *nfail; f += nwarps) {
@@ -1310,7 +1316,9 @@ __global__ void __launch_bounds__(544, 1) q6k_gemv_mt_kernel(const __grid_consta
   float* acc = reinterpret_cast<float*>(bars + 2 * a.stages);               // max_rows * M
   float* dacc = acc + a.max_rows * M;                                       // max_rows * M
   int* flist = reinterpret_cast<int*>(dacc + a.max_rows * M);               // max_rows * M
-  int* nfail = flist + a.max_rows * M;
+  int* nfail = flist + a.max_rows * M;                                      // 4 words
+  float* racc = reinterpret_cast<float*>(nfail + 4);                        // max_rows * M
+  float* rdacc = racc + a.max_rows * M;                                     // max_rows * M
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + a.stages);
 
   const int compute_warps = a.teams * a.team_warps;
@@ -1516,20 +1524,27 @@ __global__ void __launch_bounds__(544, 1) q6k_gemv_mt_kernel(const __grid_consta
     }
   }
   __syncthreads();
-  if (ks > 1) m1_cluster_sync();  // every rank's sums are in its acc
-  if (h == 0)
-    for (int i = threadIdx.x; i < rows * M; i += blockDim.x) {
-      const int row = i / M, m = i - row * M;
-      float v = acc[i], D = dacc[i];
-      for (int r = 1; r < ks; ++r) {
-        v += m1_ld_peer(acc + i, (uint32_t)r);
-        D += m1_ld_peer(dacc + i, (uint32_t)r);
+  // two CTAs per row block: rank 1 posts its sums and certificates into rank
+  // 0's receive buffers before the cluster barrier
+  if (ks > 1) {
+    if (h == 1)
+      for (int i = threadIdx.x; i < rows * M; i += blockDim.x) {
+        m1_st_peer(racc + i, 0, acc[i]);
+        m1_st_peer(rdacc + i, 0, dacc[i]);
       }
-      if (cert_fails(D)) flist[atomicAdd(nfail, 1)] = i;
-      else a.y[(size_t)m * a.N + r0 + row] = v;
+    m1_cluster_sync();  // rank 1's stores are visible to rank 0
+    if (h != 0) return;
+  }
+  for (int i = threadIdx.x; i < rows * M; i += blockDim.x) {
+    const int row = i / M, m = i - row * M;
+    float v = acc[i], D = dacc[i];
+    if (ks > 1) {
+      v += racc[i];
+      D += rdacc[i];
     }
-  if (ks > 1) m1_cluster_sync();  // no CTA leaves while rank 0 may read its memory
-  if (h != 0) return;
+    if (cert_fails(D)) flist[atomicAdd(nfail, 1)] = i;
+    else a.y[(size_t)m * a.N + r0 + row] = v;
+  }
   __syncthreads();
   // outputs whose certificate fails: exact recomputation, one warp each
   const int nwarps = blockDim.x >> 5;
@@ -1718,7 +1733,7 @@ rq_status plan_q4k_m1(int nseg, const int* starts, const uint8_t* const* ws, flo
   // planes; per sub-block: scale, sum, two error-bound constants; barriers;
   // per row: sum, certificate, exact-path list; the list's count
   const size_t fixed = (size_t)U * kPlaneStride + 16 * nsub2 + 16 * (size_t)max_stages +
-                       12 * (size_t)max_rows + 16;
+                       20 * (size_t)max_rows + 16;
   const size_t limit = 227 * 1024;
   if (fixed + 2 * (size_t)a.stage_stride > limit) return RQ_ERR_SHAPE;
   size_t ring = (size_t)ring_kb * 1024;
@@ -1730,7 +1745,7 @@ rq_status plan_q4k_m1(int nseg, const int* starts, const uint8_t* const* ws, flo
   a.wait_limit_ns = kWaitLimitNs;
   a.max_rows = max_rows;
   p->smem = a.ring_bytes + (size_t)U * kPlaneStride + 16 * nsub2 + 16 * (size_t)stages +
-            12 * (size_t)max_rows + 16;
+            20 * (size_t)max_rows + 16;
   p->threads = (a.teams * a.team_warps + 1) * 32;
   p->grid = grid;
   p->rpt = rpt;
@@ -1831,7 +1846,7 @@ rq_status plan_q6k_m1(const uint8_t* w, const float* x, float* y, int M, int N, 
   // planes; per token and sub-block: scale, offset sum, error-bound constant;
   // barriers; per output: sum, certificate, exact-path list; the list's count
   const size_t fixed = (size_t)M * U * kPlaneStride + 12 * (size_t)M * nsub16 +
-                       16 * (size_t)max_stages + 12 * (size_t)M * max_rows + 16;
+                       16 * (size_t)max_stages + 20 * (size_t)M * max_rows + 16;
   const size_t limit = 227 * 1024;
   if (fixed + 2 * (size_t)stage_bytes > limit) return RQ_ERR_SHAPE;
   size_t ring = (size_t)ring_kb * 1024;
@@ -1844,7 +1859,7 @@ rq_status plan_q6k_m1(const uint8_t* w, const float* x, float* y, int M, int N, 
   a.wait_limit_ns = kWaitLimitNs;
   a.max_rows = max_rows;
   p->smem = a.ring_bytes + (size_t)M * U * kPlaneStride + 12 * (size_t)M * nsub16 +
-            16 * (size_t)stages + 12 * (size_t)M * max_rows + 16;
+            16 * (size_t)stages + 20 * (size_t)M * max_rows + 16;
   p->threads = (a.teams * a.team_warps + 1) * 32;
   p->grid = grid;
   p->rpt = rpt;

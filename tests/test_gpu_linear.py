@@ -552,3 +552,66 @@ def test_full_decoder_layer_fp8_route(rq, decoder_layer, M, rows):
         got = ys[name].cpu().numpy()[rows]
         check_gemm(got, ref)
     ctx.close()
+
+
+@pytest.mark.parametrize("M", [1, 512])
+def test_decoder_layer_replayed_from_a_cuda_graph(rq, decoder_layer, M):
+    """One layer's four calls (q/k/v and gate/up grouped, o and down alone)
+    captured once in a CUDA graph and replayed twice with new activations
+    copied into the captured buffers in between, at one token (GEMV route)
+    and at 512 (FP8 route, the weight caches built before the capture):
+    every member's sampled rows of each replay against the oracle."""
+    ctx = rq.Context()
+    kinds = (("x", 3584), ("a", 3584), ("h", 3584), ("g", 18944))
+    bufs = {k: empty((M, K), torch.float32) for k, K in kinds}
+    ys = {name: empty((M, N), torch.float32) for name, (_, N, _, _, _) in decoder_layer.items()}
+    Wd = {name: to_dev(v[3]) for name, v in decoder_layer.items()}
+
+    def layer(stream=None):
+        if M >= ctx.gemm_threshold:
+            ctx.rq_act_cache_invalidate()  # the activations are rewritten in place
+        for grp in LAYER_CALLS:
+            K = decoder_layer[grp[0]][2]
+            x = bufs[LAYER_SOURCE[grp[0]]]
+            if len(grp) == 1:
+                qt, N = decoder_layer[grp[0]][:2]
+                ctx.rq_linear(qt, Wd[grp[0]], x, ys[grp[0]], M, N, K, stream)
+            else:
+                ctx.rq_linear_group([decoder_layer[n][0] for n in grp], [Wd[n] for n in grp],
+                                    x, [ys[n] for n in grp],
+                                    [decoder_layer[n][1] for n in grp], M, K, stream)
+
+    for k, K in kinds:  # warm call: caches and launch settings before capture
+        bufs[k].copy_(to_dev(synthetic.activation(6000 + K, M, K)))
+    layer()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            layer(s)
+    torch.cuda.synchronize()
+    rows = [0] if M == 1 else [0, 255, 511]
+    for rep in range(2):
+        acts = {k: synthetic.activation(6100 + 10 * rep + j, M, K, outlier_frac=1e-3)
+                for j, (k, K) in enumerate(kinds)}
+        for k, _ in kinds:
+            bufs[k].copy_(to_dev(acts[k]))
+        for y in ys.values():
+            y.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert rq.rq_get_device_status() == 0
+        for name, (qt, N, K, W, (wb, wd)) in decoder_layer.items():
+            x = acts[LAYER_SOURCE[name]]
+            got = ys[name].cpu().numpy()[rows]
+            if M == 1:
+                ref, absdot = oracle.gemv(qt, W, x, N, K)
+                assert gemv_ok(got, ref, absdot)[0], (rep, name)
+            else:
+                xb, xd = oracle.quant_e4m3(x, oracle.absmax_bits(x))
+                ms = np.repeat(np.asarray(rows), N)
+                ns = np.tile(np.arange(N), len(rows))
+                check_gemm(got, oracle.fp8_gemm_pairs(xb, xd, wb, wd, ms, ns).reshape(len(rows), N))
+    ctx.close()
