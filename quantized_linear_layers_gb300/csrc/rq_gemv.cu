@@ -1740,6 +1740,9 @@ rq_status plan_q4k_m1(int nseg, const int* starts, const uint8_t* const* ws, flo
   if (ring > limit - fixed) ring = limit - fixed;
   int stages = (int)(ring / a.stage_stride);
   stages = stages > max_stages ? max_stages : (stages < 2 ? 2 : stages);
+  // no more stages than a CTA has iterations
+  const int iters_max = (max_rows + a.rows_per_stage - 1) / a.rows_per_stage;
+  if (stages > iters_max) stages = iters_max < 1 ? 1 : iters_max;
   a.stages = stages;
   a.ring_bytes = (uint32_t)stages * a.stage_stride;
   a.wait_limit_ns = kWaitLimitNs;
@@ -1853,6 +1856,9 @@ rq_status plan_q6k_m1(const uint8_t* w, const float* x, float* y, int M, int N, 
   if (ring > limit - fixed) ring = limit - fixed;
   int stages = (int)(ring / stage_bytes);
   stages = stages > max_stages ? max_stages : (stages < 2 ? 2 : stages);
+  // no more stages than a CTA has iterations
+  const int iters_max = (max_rows + a.rows_per_stage - 1) / a.rows_per_stage;
+  if (stages > iters_max) stages = iters_max < 1 ? 1 : iters_max;
   a.stages = stages;
   a.ring_bytes = (uint32_t)(stages * stage_bytes);
   a.stage_stride = (uint32_t)stage_bytes;
