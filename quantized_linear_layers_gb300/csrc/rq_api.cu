@@ -100,7 +100,6 @@ struct rq_ctx {
   size_t act_cap = 0;
   uint32_t* absmax = nullptr;  // device word
   float* act_deq = nullptr;    // device float
-  unsigned int* fused = nullptr;  // one-pass quantization state (4 device words)
   bool fused_ok = true;           // RQ_ONE_PASS_QUANT=0 keeps the two-kernel path
   int64_t fused_min = 1 << 20;    // fewer elements: two kernels (RQ_ONE_PASS_MIN)
   // at most this many elements: one cluster, one launch (RQ_CLUSTER_QUANT_MAX;
@@ -108,6 +107,7 @@ struct rq_ctx {
   // the 57 K elements of 16 tokens x 3584 and loses from ~230 K on)
   int64_t cluster_max = 1 << 17;
   uint32_t* slots = nullptr;      // per-CTA partial maxima of the two-kernel path
+  unsigned long long* fused = nullptr;  // one-pass quantization barrier word
   // activation cache key
   bool act_valid = false;
   const float* act_x = nullptr;
@@ -194,7 +194,7 @@ rq_status rq_ctx_create(rq_ctx** out) {
   }
   c->absmax = static_cast<uint32_t*>(p);
   c->act_deq = reinterpret_cast<float*>(static_cast<uint8_t*>(p) + 128);
-  c->fused = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(p) + 192);
+  c->fused = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(p) + 192);
   if (cudaMemset(p, 0, 256) != cudaSuccess) {
     cudaFree(p);
     delete c;
@@ -388,7 +388,7 @@ rq_status rq_fp8_act_cache(rq_ctx* ctx, const float* x, int M, int K,
     } else if (ctx->fused_ok && n >= ctx->fused_min && act_quant_fused_fits(x, n, ctx->act)) {
       TraceScope ts(ctx, RQ_TRACE_QUANT, st);
       s = launch_act_quant_fused(x, n, (int64_t)need, ctx->act, ctx->absmax, ctx->act_deq,
-                                 ctx->fused, st);
+                                 ctx->fused, ctx->slots, act_quant_slots(), st);
       if (s == RQ_ERR_SHAPE) ts.kernels(0);
     }
     // RQ_ERR_SHAPE from the one-cluster or one-pass launcher: nothing was

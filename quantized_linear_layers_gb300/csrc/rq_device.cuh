@@ -68,6 +68,13 @@ __device__ __forceinline__ uint32_t e4m3_scaled4(float4 v, float s) {
   return r;
 }
 
+// The same for four finite values (no non-finite fix-ups).
+__device__ __forceinline__ uint32_t e4m3_scaled4_finite(float4 v, float s) {
+  const float a = flush_small(__fmul_rn(v.x, s)), b = flush_small(__fmul_rn(v.y, s));
+  const float c = flush_small(__fmul_rn(v.z, s)), d = flush_small(__fmul_rn(v.w, s));
+  return cvt_e4m3x2(b, a) | (cvt_e4m3x2(d, c) << 16);
+}
+
 // Quantization scale from the absmax word: A' = (A == 0 ? 1 : A),
 // s = 448 / A' (IEEE division), dequant = A' / 448.
 __device__ __forceinline__ float absmax_prime(uint32_t absmax_bits) {

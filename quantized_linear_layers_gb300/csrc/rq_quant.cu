@@ -122,34 +122,65 @@ quant_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
 // Same arithmetic as absmax_kernel + quant_kernel, so the bytes are
 // identical.
 //
-// state[0..1]: absmax words, used alternately by consecutive launches (the
-//              one for launch g is zero when it starts);
-// state[2]:    arrival count (zero between launches);
-// state[3]:    launch generation g.
-// Launches that share a state word block run one after another (one stream).
+// state: one 64-bit word, (launch generation << 32) | CTAs of the current
+//        launch that have published their maximum; zero before the first
+//        launch.  Every CTA adds one arrival; the last also adds
+//        2^32 - grid, which clears the count and starts the next generation,
+//        the signal the others wait for.
+// slots: one word per CTA, its maximum (read by every CTA once all arrived).
+// Launches that share a state word and slots run one after another (one
+// stream), so no launch's arrivals mix with another's.
 
 __device__ unsigned int g_quant_error;
 
 constexpr int kFusedThreads = 1024;
-constexpr int kFusedParts = 4;               // bulk copies (and barriers) per CTA
+constexpr int kFusedParts = 1;               // bulk copies (and barriers) per CTA
 constexpr int64_t kFusedMinChunk = 4096;     // floats: fewer CTAs for small tensors
 constexpr int64_t kFusedSmemMax = 220 * 1024;
 
-__device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned int* p) {
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
   uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+__device__ __forceinline__ uint64_t ld_acquire_u64(const unsigned long long* p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint64_t atom_add_acq_rel_u64(unsigned long long* p, uint64_t v) {
+  uint64_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;"
+               : "=l"(old)
+               : "l"(p), "l"(v)
+               : "memory");
+  return old;
+}
+__device__ __forceinline__ void red_add_release_u64(unsigned long long* p, uint64_t v) {
+  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Running max |x| over four values, NaN skipped (fmaxf returns the other
+// operand; no flush of subnormals in this build, so the bits of the result
+// are the largest non-NaN |x| bits), and a running sum of x * 0, which
+// stays zero while every value is finite and is NaN once one is not.
+__device__ __forceinline__ void max4_f(float& mf, float& nf, float4 v) {
+  mf = fmaxf(mf, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  nf = fmaf(v.x, 0.0f, nf);
+  nf = fmaf(v.y, 0.0f, nf);
+  nf = fmaf(v.z, 0.0f, nf);
+  nf = fmaf(v.w, 0.0f, nf);
 }
 
 __global__ void __launch_bounds__(kFusedThreads, 1)
 act_quant_fused_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
                        int64_t chunk, int64_t stash4, uint8_t* __restrict__ out,
                        uint32_t* __restrict__ absmax_out, float* __restrict__ dequant_out,
-                       unsigned int* state) {
+                       unsigned long long* state, uint32_t* slots) {
   extern __shared__ __align__(128) float4 stash[];
   __shared__ __align__(8) uint64_t bars[kFusedParts];
-  __shared__ uint32_t warp_max[kFusedThreads / 32];
-  __shared__ uint32_t gen_s, absmax_s;
+  __shared__ uint32_t warp_max[kFusedThreads / 32], warp_nf[kFusedThreads / 32];
+  __shared__ uint32_t absmax_s, nonfinite_s;
 
   const int64_t begin = (int64_t)blockIdx.x * chunk;
   const int64_t len = min(chunk, n - begin);
@@ -158,11 +189,11 @@ act_quant_fused_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
   const int64_t h4 = cnt4 - s4;                // the head: streamed twice
   const float4* xb4 = reinterpret_cast<const float4*>(x + begin);
   const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
 
   pdl_wait();
   pdl_trigger();
   if (tid == 0) {
-    gen_s = ld_acquire_u32(state + 3);
     for (int p = 0; p < kFusedParts; ++p) mbar_init(smem_u32(&bars[p]), 1);
     mbar_fence_init();
     for (int p = 0; p < kFusedParts; ++p) {
@@ -174,52 +205,63 @@ act_quant_fused_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
   }
   __syncthreads();
 
-  uint32_t m = 0;
+  float mf = 0.0f, nf = 0.0f;
   {
     int64_t i = tid;
     for (; i + 3 * kFusedThreads < h4; i += 4 * kFusedThreads) {
       const float4 v0 = __ldg(xb4 + i), v1 = __ldg(xb4 + i + kFusedThreads);
       const float4 v2 = __ldg(xb4 + i + 2 * kFusedThreads), v3 = __ldg(xb4 + i + 3 * kFusedThreads);
-      m = max4(max4(max4(max4(m, v0), v1), v2), v3);
+      max4_f(mf, nf, v0);
+      max4_f(mf, nf, v1);
+      max4_f(mf, nf, v2);
+      max4_f(mf, nf, v3);
     }
-    for (; i < h4; i += kFusedThreads) m = max4(m, __ldg(xb4 + i));
+    for (; i < h4; i += kFusedThreads) max4_f(mf, nf, __ldg(xb4 + i));
   }
   for (int p = 0; p < kFusedParts; ++p) {
     mbar_wait(smem_u32(&bars[p]), 0, kWaitLimitNs, &g_quant_error);
     const int64_t lo = s4 * p / kFusedParts, hi = s4 * (p + 1) / kFusedParts;
-    for (int64_t i = lo + tid; i < hi; i += kFusedThreads) m = max4(m, stash[i]);
+    for (int64_t i = lo + tid; i < hi; i += kFusedThreads) max4_f(mf, nf, stash[i]);
   }
-  for (int64_t i = (cnt4 << 2) + tid; i < len; i += kFusedThreads)
-    m = max(m, abs_bits_skip_nan(__ldg(x + begin + i)));
-  m = __reduce_max_sync(0xFFFFFFFFu, m);
-  const int lane = tid & 31, warp = tid >> 5;
-  if (lane == 0) warp_max[warp] = m;
+  for (int64_t i = (cnt4 << 2) + tid; i < len; i += kFusedThreads) {
+    const float v = __ldg(x + begin + i);
+    mf = fmaxf(mf, fabsf(v));
+    nf = fmaf(v, 0.0f, nf);
+  }
+  uint32_t m = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(mf));
+  const uint32_t bad = __any_sync(0xFFFFFFFFu, !(nf == 0.0f)) ? 1u : 0u;
+  if (lane == 0) {
+    warp_max[warp] = m;
+    warp_nf[warp] = bad;
+  }
   __syncthreads();
 
   if (warp == 0) {
     m = __reduce_max_sync(0xFFFFFFFFu, warp_max[lane]);
+    const uint32_t any_bad = __reduce_or_sync(0xFFFFFFFFu, warp_nf[lane]);
+    // publish this CTA's maximum, arrive, and wait for the generation to
+    // change (the last CTA to arrive changes it); every lane waits with its
+    // own acquiring load, so every lane then sees every CTA's slot
+    uint64_t old = 0;
     if (lane == 0) {
-      const uint32_t g = gen_s;
-      unsigned int* word = state + (g & 1u);
-      if (m != 0u) atomicMax(word, m);
-      __threadfence();
-      const unsigned int arrived = atomicAdd(state + 2, 1u);
-      if (arrived == gridDim.x - 1) {
-        state[2] = 0u;
-        state[(g + 1u) & 1u] = 0u;
-        __threadfence();
-        atomicExch(state + 3, g + 1u);
-      } else {
-        const uint64_t t0 = globaltimer();
-        while (ld_acquire_u32(state + 3) == g) {
-          if (globaltimer() - t0 > kWaitLimitNs) {
-            atomicOr(&g_quant_error, 2u);
-            break;
-          }
-        }
-      }
-      absmax_s = ld_acquire_u32(word);
+      nonfinite_s = any_bad;
+      slots[blockIdx.x] = m;
+      old = atom_add_acq_rel_u64(state, 1ull);
+      if ((uint32_t)old == gridDim.x - 1u) red_add_release_u64(state, (1ull << 32) - gridDim.x);
     }
+    old = __shfl_sync(0xFFFFFFFFu, old, 0);
+    const uint32_t gen = (uint32_t)(old >> 32);
+    const uint64_t t0 = globaltimer();
+    while ((uint32_t)(ld_acquire_u64(state) >> 32) == gen) {
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        if (lane == 0) atomicOr(&g_quant_error, 2u);
+        break;
+      }
+    }
+    uint32_t all = 0;
+    for (int i = lane; i < (int)gridDim.x; i += 32) all = max(all, ld_relaxed_u32(slots + i));
+    all = __reduce_max_sync(0xFFFFFFFFu, all);
+    if (lane == 0) absmax_s = all;
   }
   __syncthreads();
 
@@ -230,8 +272,15 @@ act_quant_fused_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
     if (dequant_out != nullptr) *dequant_out = __fdiv_rn(a, 448.0f);
   }
   uint32_t* o4 = reinterpret_cast<uint32_t*>(out + begin);
-  for (int64_t i = h4 - 1 - tid; i >= 0; i -= kFusedThreads) o4[i] = pack4(__ldg(xb4 + i), s);
-  for (int64_t i = tid; i < s4; i += kFusedThreads) o4[h4 + i] = pack4(stash[i], s);
+  if (nonfinite_s == 0u) {
+    // every value of the chunk is finite
+    for (int64_t i = h4 - 1 - tid; i >= 0; i -= kFusedThreads)
+      o4[i] = e4m3_scaled4_finite(__ldg(xb4 + i), s);
+    for (int64_t i = tid; i < s4; i += kFusedThreads) o4[h4 + i] = e4m3_scaled4_finite(stash[i], s);
+  } else {
+    for (int64_t i = h4 - 1 - tid; i >= 0; i -= kFusedThreads) o4[i] = pack4(__ldg(xb4 + i), s);
+    for (int64_t i = tid; i < s4; i += kFusedThreads) o4[h4 + i] = pack4(stash[i], s);
+  }
   for (int64_t i = (cnt4 << 2) + tid; i < len; i += kFusedThreads)
     out[begin + i] = (uint8_t)e4m3_scaled(__ldg(x + begin + i), s);
   const int64_t stride = (int64_t)gridDim.x * kFusedThreads;
@@ -610,8 +659,8 @@ bool act_quant_fused_fits(const float* x, int64_t n, const uint8_t* out) {
 
 rq_status launch_act_quant_fused(const float* x, int64_t n, int64_t n_out,
                                  uint8_t* out, uint32_t* absmax_out,
-                                 float* dequant_out, unsigned int* state,
-                                 cudaStream_t st) {
+                                 float* dequant_out, unsigned long long* state,
+                                 uint32_t* slots, int nslots, cudaStream_t st) {
   if (!act_quant_fused_fits(x, n, out)) return RQ_ERR_SHAPE;
   static bool attr_set = false;
   if (!attr_set) {
@@ -623,6 +672,7 @@ rq_status launch_act_quant_fused(const float* x, int64_t n, int64_t n_out,
   }
   int64_t chunk = fused_chunk(n);
   const int grid = (int)((n + chunk - 1) / chunk);
+  if (grid > nslots) return RQ_ERR_SHAPE;
   const int64_t stash4 = fused_stash4(chunk);
   const size_t smem = (size_t)stash4 * 16;
   cudaLaunchConfig_t cfg = {};
@@ -638,7 +688,7 @@ rq_status launch_act_quant_fused(const float* x, int64_t n, int64_t n_out,
   cfg.attrs = attr;
   cfg.numAttrs = pdl_enabled() ? 2 : 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, act_quant_fused_kernel, x, n, n_out, chunk,
-                                           stash4, out, absmax_out, dequant_out, state);
+                                           stash4, out, absmax_out, dequant_out, state, slots);
   if (e == cudaErrorCooperativeLaunchTooLarge) {
     cudaGetLastError();
     return RQ_ERR_SHAPE;

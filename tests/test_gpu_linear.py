@@ -218,6 +218,31 @@ def test_activation_cache_infinite_max(rq, monkeypatch, one_pass, M, K):
     ctx.close()
 
 
+def test_one_pass_launches_of_different_grids_on_one_context(rq, monkeypatch):
+    """One-pass launches in a row on one context with 1, 152, 33, 1, 152 and
+    152 CTAs: each publishes its CTAs' maxima and meets at its own grid
+    barrier, whose arrival count every launch leaves at zero.  The maxima
+    differ by up to 10^4 from one launch to the next, so a stale one would
+    change the bytes."""
+    set_act_quant_mode(monkeypatch, "1")
+    ctx = rq.Context()
+    shapes = [(5, 256, 1.0), (2048, 3584, 1e-3), (37, 3584, 10.0), (5, 256, 1e-2),
+              (611, 1024, 1.0), (2048, 3584, 1e2)]
+    for i, (M, K, scale) in enumerate(shapes):
+        x = (synthetic.activation(7100 + i, M, K, outlier_frac=1e-3) *
+             np.float32(scale)).astype(np.float32)
+        ctx.rq_act_cache_invalidate()
+        ctx.rq_ctx_trace_begin(8)
+        got, gd = act_cache_bytes(ctx, to_dev(x), M, K)
+        tr = ctx.rq_ctx_trace_end()
+        assert rq.rq_get_device_status() == 0
+        assert tr["quant"][0] == 1
+        want, wd = oracle_act_bytes(x, M, K)
+        assert gd == wd
+        assert np.array_equal(got, want), (i, np.flatnonzero(got != want)[:8])
+    ctx.close()
+
+
 def test_activation_cache_rejects_unaligned_x(rq):
     """The activation cache takes x on a 16-byte boundary only: RQ_ERR_SHAPE
     before anything is launched."""
