@@ -320,12 +320,14 @@ __device__ __forceinline__ float4 ldg_f4_policy(const float4* p, uint64_t pol) {
   return v;
 }
 
+// Each slot: the CTA's maximum |x| bits (NaN skipped) in bits 0..30, and
+// bit 31 set when its part of x holds a NaN or an infinity.
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads)
 absmax_slots_kernel(const float* __restrict__ x, int64_t n, uint32_t* __restrict__ slots) {
   pdl_wait();
   pdl_trigger();
-  uint32_t m = 0;
+  float mf = 0.0f, nf = 0.0f;
   const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
   const int64_t nthreads = (int64_t)gridDim.x * kThreads;
   int64_t done = 0;
@@ -342,21 +344,27 @@ absmax_slots_kernel(const float* __restrict__ x, int64_t n, uint32_t* __restrict
 #pragma unroll
       for (int u = 0; u < kSlotUnroll; ++u) v[u] = ldg_f4_policy(x4 + i + u * nthreads, pol);
 #pragma unroll
-      for (int u = 0; u < kSlotUnroll; ++u) m = max4(m, v[u]);
+      for (int u = 0; u < kSlotUnroll; ++u) max4_f(mf, nf, v[u]);
     }
-    for (; i < n4; i += nthreads) m = max4(m, __ldg(x4 + i));
+    for (; i < n4; i += nthreads) max4_f(mf, nf, __ldg(x4 + i));
     done = n4 << 2;
   }
-  for (int64_t i = done + tid; i < n; i += nthreads) m = max(m, abs_bits_skip_nan(__ldg(x + i)));
+  for (int64_t i = done + tid; i < n; i += nthreads) {
+    const float v = __ldg(x + i);
+    mf = fmaxf(mf, fabsf(v));
+    nf = fmaf(v, 0.0f, nf);
+  }
   __shared__ uint32_t warp_max[kThreads / 32];
-  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  uint32_t m = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(mf));
+  if (__any_sync(0xFFFFFFFFu, !(nf == 0.0f))) m |= 0x80000000u;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) warp_max[warp] = m;
   __syncthreads();
   if (warp == 0) {
     m = lane < kThreads / 32 ? warp_max[lane] : 0u;
-    m = __reduce_max_sync(0xFFFFFFFFu, m);
-    if (lane == 0) slots[blockIdx.x] = m;
+    const uint32_t bad = __reduce_or_sync(0xFFFFFFFFu, m) & 0x80000000u;
+    m = __reduce_max_sync(0xFFFFFFFFu, m & 0x7FFFFFFFu);
+    if (lane == 0) slots[blockIdx.x] = m | bad;
   }
 }
 
@@ -368,17 +376,25 @@ quant_slots_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
   pdl_wait();
   pdl_trigger();
   __shared__ uint32_t warp_max[kThreads / 32];
-  __shared__ uint32_t absmax_s;
-  uint32_t m = 0;
-  for (int i = threadIdx.x; i < nslots; i += kThreads) m = max(m, slots[i]);
-  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  __shared__ uint32_t absmax_s, bad_s;
+  uint32_t m = 0, bad = 0;
+  for (int i = threadIdx.x; i < nslots; i += kThreads) {
+    const uint32_t v = slots[i];
+    m = max(m, v & 0x7FFFFFFFu);
+    bad |= v;
+  }
+  m = __reduce_max_sync(0xFFFFFFFFu, m) | (__reduce_or_sync(0xFFFFFFFFu, bad) & 0x80000000u);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) warp_max[warp] = m;
   __syncthreads();
   if (warp == 0) {
     m = lane < kThreads / 32 ? warp_max[lane] : 0u;
-    m = __reduce_max_sync(0xFFFFFFFFu, m);
-    if (lane == 0) absmax_s = m;
+    bad = __reduce_or_sync(0xFFFFFFFFu, m) >> 31;
+    m = __reduce_max_sync(0xFFFFFFFFu, m & 0x7FFFFFFFu);
+    if (lane == 0) {
+      absmax_s = m;
+      bad_s = bad;
+    }
   }
   __syncthreads();
   const uint32_t bits = absmax_s;
@@ -399,6 +415,7 @@ quant_slots_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
     // first, then backwards
     const int64_t per_round = kSlotUnroll * nthreads;
     const uint64_t last_use = l2_policy_evict_first();
+    const bool finite = bad_s == 0u;  // no NaN or infinity anywhere in x
     for (int64_t base = ((n4 - 1) / per_round) * per_round; base >= 0 && n4 > 0;
          base -= per_round) {
       float4 v[kSlotUnroll];
@@ -407,10 +424,18 @@ quant_slots_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
         const int64_t i = base + u * nthreads + tid;
         if (i < n4) v[u] = ldg_f4_policy(x4 + i, last_use);
       }
+      if (finite) {
 #pragma unroll
-      for (int u = 0; u < kSlotUnroll; ++u) {
-        const int64_t i = base + u * nthreads + tid;
-        if (i < n4) o4[i] = pack4(v[u], s);
+        for (int u = 0; u < kSlotUnroll; ++u) {
+          const int64_t i = base + u * nthreads + tid;
+          if (i < n4) o4[i] = e4m3_scaled4_finite(v[u], s);
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < kSlotUnroll; ++u) {
+          const int64_t i = base + u * nthreads + tid;
+          if (i < n4) o4[i] = pack4(v[u], s);
+        }
       }
     }
     done = n4 << 2;

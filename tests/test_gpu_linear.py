@@ -167,8 +167,9 @@ def set_act_quant_mode(monkeypatch, mode):
 def test_activation_cache_bytes_bit_exact(rq, monkeypatch, one_pass, M, K):
     """The FP8 activation (one-cluster kernel, one-pass kernel or absmax +
     quant kernels) is the oracle's bytes, pad rows zero, over three
-    successive misses with different maxima (the one-pass kernel alternates
-    its absmax words)."""
+    successive misses with different maxima; the second x has no NaN, so
+    the kernels' path for all-finite inputs is checked as well as the one
+    with fix-ups."""
     set_act_quant_mode(monkeypatch, one_pass)
     ctx = rq.Context()
     x = synthetic.activation(5000 + M + K, M, K, outlier_frac=1e-3)
@@ -176,6 +177,9 @@ def test_activation_cache_bytes_bit_exact(rq, monkeypatch, one_pass, M, K):
     xd = to_dev(x)
     for scale in (1.0, 0.25, 3.0):
         xs = (x * np.float32(scale)).astype(np.float32)
+        if scale == 0.25:
+            xs.ravel()[min(4, x.size - 1)] = np.float32(0.75)
+            assert np.isfinite(xs).all()
         xd.copy_(to_dev(xs))
         ctx.rq_act_cache_invalidate()
         ctx.rq_ctx_trace_begin(8)
