@@ -107,7 +107,8 @@ struct rq_ctx {
   // the 57 K elements of 16 tokens x 3584 and loses from ~230 K on)
   int64_t cluster_max = 1 << 17;
   uint32_t* slots = nullptr;      // per-CTA partial maxima of the two-kernel path
-  unsigned long long* fused = nullptr;  // one-pass quantization barrier word
+  unsigned long long* fused = nullptr;        // one-pass quantization barrier word
+  unsigned long long* fused_slots = nullptr;  // and its per-CTA words (SM count)
   // activation cache key
   bool act_valid = false;
   const float* act_x = nullptr;
@@ -215,6 +216,22 @@ rq_status rq_ctx_create(rq_ctx** out) {
     return RQ_ERR_ALLOC;
   }
   c->slots = static_cast<uint32_t*>(sl);
+  void* fs = nullptr;
+  const size_t fs_bytes = sizeof(unsigned long long) * (size_t)device_sm_count();
+  if (cudaMalloc(&fs, fs_bytes) != cudaSuccess) {
+    cudaFree(sl);
+    cudaFree(p);
+    delete c;
+    return RQ_ERR_ALLOC;
+  }
+  if (cudaMemset(fs, 0, fs_bytes) != cudaSuccess) {
+    cudaFree(fs);
+    cudaFree(sl);
+    cudaFree(p);
+    delete c;
+    return RQ_ERR_CUDA;
+  }
+  c->fused_slots = static_cast<unsigned long long*>(fs);
   *out = c;
   return RQ_OK;
 }
@@ -230,6 +247,7 @@ void rq_ctx_destroy(rq_ctx* ctx) {
   if (ctx->act) cudaFree(ctx->act);
   if (ctx->absmax) cudaFree(ctx->absmax);
   if (ctx->slots) cudaFree(ctx->slots);
+  if (ctx->fused_slots) cudaFree(ctx->fused_slots);
   delete ctx;
 }
 
@@ -388,7 +406,7 @@ rq_status rq_fp8_act_cache(rq_ctx* ctx, const float* x, int M, int K,
     } else if (ctx->fused_ok && n >= ctx->fused_min && act_quant_fused_fits(x, n, ctx->act)) {
       TraceScope ts(ctx, RQ_TRACE_QUANT, st);
       s = launch_act_quant_fused(x, n, (int64_t)need, ctx->act, ctx->absmax, ctx->act_deq,
-                                 ctx->fused, ctx->slots, act_quant_slots(), st);
+                                 ctx->fused, ctx->fused_slots, device_sm_count(), st);
       if (s == RQ_ERR_SHAPE) ts.kernels(0);
     }
     // RQ_ERR_SHAPE from the one-cluster or one-pass launcher: nothing was

@@ -51,15 +51,15 @@ rq_status launch_quant(const float* x, int64_t n, int64_t n_out,
 // Absmax + encode in one cooperative wave (each CTA's chunk staged in shared
 // memory as far as it fits, the rest, at most 16 MB in all, read twice).
 // Needs x 16-byte and out 4-byte aligned; RQ_ERR_SHAPE (nothing launched) if
-// the wave does not fit the GPU.  `state` is one 64-bit device word, zero
-// before the first launch; `slots` holds `nslots` words (at least the SM
-// count); both are used by one stream at a time.  absmax_out / dequant_out
-// may be null.
+// the wave does not fit the GPU.  `state` is one 64-bit device word and
+// `slots` `nslots` of them (at least the SM count), all zero before the
+// first launch and used by this kernel only, on one stream at a time.
+// absmax_out / dequant_out may be null.
 bool act_quant_fused_fits(const float* x, int64_t n, const uint8_t* out);
 rq_status launch_act_quant_fused(const float* x, int64_t n, int64_t n_out,
                                  uint8_t* out, uint32_t* absmax_out,
                                  float* dequant_out, unsigned long long* state,
-                                 uint32_t* slots, int nslots, cudaStream_t st);
+                                 unsigned long long* slots, int nslots, cudaStream_t st);
 // Two kernels, no zeroing: per-CTA partial maxima into `slots` (at least
 // act_quant_slots() words), then the encoding, which reduces the slots and
 // walks x backwards (what the first pass read last may still be in L2).

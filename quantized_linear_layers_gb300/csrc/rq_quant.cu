@@ -122,14 +122,18 @@ quant_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
 // Same arithmetic as absmax_kernel + quant_kernel, so the bytes are
 // identical.
 //
-// state: one 64-bit word, (launch generation << 32) | CTAs of the current
-//        launch that have published their maximum; zero before the first
-//        launch.  Every CTA adds one arrival; the last also adds
-//        2^32 - grid, which clears the count and starts the next generation,
-//        the signal the others wait for.
-// slots: one word per CTA, its maximum (read by every CTA once all arrived).
-// Launches that share a state word and slots run one after another (one
-// stream), so no launch's arrivals mix with another's.
+// Grid barrier of the one-pass kernel, on 64-bit words that each carry a
+// launch tag (high half) and a maximum |x| bits (low half), written and read
+// whole, so no fences or atomics are needed:
+// state: the tag of the last launch and its tensor maximum (zero before the
+//        first launch); a launch's tag is that tag + 1, read by every CTA
+//        at its start;
+// slots: one word per SM; CTA i of a launch writes (tag, its maximum) to
+//        slot i.  CTA 0 waits until the slots of all CTAs carry the tag,
+//        then writes (tag, tensor maximum) to `state`, which the other CTAs
+//        wait for.  (Every CTA has read `state` before CTA 0 can write it,
+//        since CTA 0 first waits for every CTA's slot.)
+// Launches that share the words run one after another (one stream).
 
 __device__ unsigned int g_quant_error;
 
@@ -138,26 +142,13 @@ constexpr int kFusedParts = 1;               // bulk copies (and barriers) per C
 constexpr int64_t kFusedMinChunk = 4096;     // floats: fewer CTAs for small tensors
 constexpr int64_t kFusedSmemMax = 220 * 1024;
 
-__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ uint64_t ld_acquire_u64(const unsigned long long* p) {
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const unsigned long long* p) {
   uint64_t v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ uint64_t atom_add_acq_rel_u64(unsigned long long* p, uint64_t v) {
-  uint64_t old;
-  asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;"
-               : "=l"(old)
-               : "l"(p), "l"(v)
-               : "memory");
-  return old;
-}
-__device__ __forceinline__ void red_add_release_u64(unsigned long long* p, uint64_t v) {
-  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 // Running max |x| over four values, NaN skipped (fmaxf returns the other
@@ -176,11 +167,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 act_quant_fused_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
                        int64_t chunk, int64_t stash4, uint8_t* __restrict__ out,
                        uint32_t* __restrict__ absmax_out, float* __restrict__ dequant_out,
-                       unsigned long long* state, uint32_t* slots) {
+                       unsigned long long* state, unsigned long long* slots) {
   extern __shared__ __align__(128) float4 stash[];
   __shared__ __align__(8) uint64_t bars[kFusedParts];
   __shared__ uint32_t warp_max[kFusedThreads / 32], warp_nf[kFusedThreads / 32];
-  __shared__ uint32_t absmax_s, nonfinite_s;
+  __shared__ uint32_t absmax_s, nonfinite_s, tag_s;
 
   const int64_t begin = (int64_t)blockIdx.x * chunk;
   const int64_t len = min(chunk, n - begin);
@@ -203,6 +194,7 @@ act_quant_fused_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
       if (bytes != 0) bulk_g2s(smem_u32(stash + lo), xb4 + h4 + lo, bytes, smem_u32(&bars[p]));
     }
   }
+  if (tid == 32) tag_s = (uint32_t)(ld_relaxed_u64(state) >> 32) + 1u;
   __syncthreads();
 
   float mf = 0.0f, nf = 0.0f;
@@ -239,28 +231,42 @@ act_quant_fused_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
   if (warp == 0) {
     m = __reduce_max_sync(0xFFFFFFFFu, warp_max[lane]);
     const uint32_t any_bad = __reduce_or_sync(0xFFFFFFFFu, warp_nf[lane]);
-    // publish this CTA's maximum, arrive, and wait for the generation to
-    // change (the last CTA to arrive changes it); every lane waits with its
-    // own acquiring load, so every lane then sees every CTA's slot
-    uint64_t old = 0;
+    const uint32_t tag = tag_s;
     if (lane == 0) {
       nonfinite_s = any_bad;
-      slots[blockIdx.x] = m;
-      old = atom_add_acq_rel_u64(state, 1ull);
-      if ((uint32_t)old == gridDim.x - 1u) red_add_release_u64(state, (1ull << 32) - gridDim.x);
-    }
-    old = __shfl_sync(0xFFFFFFFFu, old, 0);
-    const uint32_t gen = (uint32_t)(old >> 32);
-    const uint64_t t0 = globaltimer();
-    while ((uint32_t)(ld_acquire_u64(state) >> 32) == gen) {
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        if (lane == 0) atomicOr(&g_quant_error, 2u);
-        break;
-      }
+      st_relaxed_u64(slots + blockIdx.x, ((uint64_t)tag << 32) | m);
     }
     uint32_t all = 0;
-    for (int i = lane; i < (int)gridDim.x; i += 32) all = max(all, ld_relaxed_u32(slots + i));
-    all = __reduce_max_sync(0xFFFFFFFFu, all);
+    const uint64_t t0 = globaltimer();
+    if (blockIdx.x == 0) {
+      // every CTA's maximum, then the tensor's for the others
+      while (true) {
+        bool done = true;
+        uint32_t mm = 0;
+        for (int i = lane; i < (int)gridDim.x; i += 32) {
+          const uint64_t v = ld_relaxed_u64(slots + i);
+          done = done && (uint32_t)(v >> 32) == tag;
+          mm = max(mm, (uint32_t)v);
+        }
+        all = __reduce_max_sync(0xFFFFFFFFu, mm);
+        if (__all_sync(0xFFFFFFFFu, done)) break;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+          if (lane == 0) atomicOr(&g_quant_error, 2u);
+          break;
+        }
+      }
+      if (lane == 0) st_relaxed_u64(state, ((uint64_t)tag << 32) | all);
+    } else {
+      uint64_t v = ld_relaxed_u64(state);
+      while ((uint32_t)(v >> 32) != tag) {
+        if (globaltimer() - t0 > kWaitLimitNs) {
+          if (lane == 0) atomicOr(&g_quant_error, 2u);
+          break;
+        }
+        v = ld_relaxed_u64(state);
+      }
+      all = (uint32_t)v;
+    }
     if (lane == 0) absmax_s = all;
   }
   __syncthreads();
@@ -685,7 +691,7 @@ bool act_quant_fused_fits(const float* x, int64_t n, const uint8_t* out) {
 rq_status launch_act_quant_fused(const float* x, int64_t n, int64_t n_out,
                                  uint8_t* out, uint32_t* absmax_out,
                                  float* dequant_out, unsigned long long* state,
-                                 uint32_t* slots, int nslots, cudaStream_t st) {
+                                 unsigned long long* slots, int nslots, cudaStream_t st) {
   if (!act_quant_fused_fits(x, n, out)) return RQ_ERR_SHAPE;
   static bool attr_set = false;
   if (!attr_set) {
