@@ -173,6 +173,13 @@ __device__ __noinline__ inline bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// mbar_wait with its first test inline: the call is made only when the
+// phase has not completed yet (for waits in loops that are bound by issue).
+__device__ __forceinline__ bool mbar_wait_fast(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                               unsigned int* err) {
+  return mbar_try_wait(bar, parity) || mbar_wait(bar, parity, limit_ns, err);
+}
+
 // 1-D bulk copy global -> shared, completing `bytes` of transaction on bar.
 // Both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,

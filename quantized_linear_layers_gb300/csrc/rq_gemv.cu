@@ -868,7 +868,7 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
         if (it < iters && ok) {
           const int s = it % a.stages;
           const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
-          ok = __all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * s, ph, a.wait_limit_ns, &g_gemv_error));
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait_fast(full0 + 8 * s, ph, a.wait_limit_ns, &g_gemv_error));
           if (ok) {
             const int nr = min(rps, rows - it * rps);
             const uint8_t* stage = ring + s * a.stage_stride + (size_t)team * RPT * rowbytes;
@@ -1223,7 +1223,7 @@ __device__ __forceinline__ void q6k_m1_body(const M1Args& a, const int bid, cons
         if (it < iters && ok) {
           const int s = it % a.stages;
           const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
-          ok = __all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * s, ph, a.wait_limit_ns, &g_gemv_error));
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait_fast(full0 + 8 * s, ph, a.wait_limit_ns, &g_gemv_error));
           if (ok) {
             const int nr = min(rps, rows - it * rps);
             const uint8_t* stage = ring + s * stage_bytes + (size_t)team * RPT * rowbytes;
@@ -1442,7 +1442,7 @@ __global__ void __launch_bounds__(544, 1) q6k_gemv_mt_kernel(const __grid_consta
     for (int it = 0; it < iters && ok; ++it) {
       const int s = it % a.stages;
       const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * s, ph, a.wait_limit_ns, &g_gemv_error));
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait_fast(full0 + 8 * s, ph, a.wait_limit_ns, &g_gemv_error));
       if (!ok) break;
       const int nr = min(rps, rows - it * rps);
       const uint8_t* stage = ring + s * stage_bytes;
