@@ -857,6 +857,8 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
     }
     const int off_h = sb * kQ4KBytes, off_a = off_h + 16 + 32 * g;
     bool ok = true;
+    int cs = 0;          // ring slot of the next iteration
+    uint32_t cph = 0u;   // and the parity of its phase
     for (int it0 = 0; it0 < iters && ok; it0 += SPB) {
       // slots 0..7: the row sums of 8 rows, 8..15: their certificate terms
       float pa[16];
@@ -866,8 +868,12 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
       for (int q = 0; q < SPB; ++q) {
         const int it = it0 + q;
         if (it < iters && ok) {
-          const int s = it % a.stages;
-          const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
+          const int s = cs;
+          const uint32_t ph = cph;
+          if (++cs == a.stages) {
+            cs = 0;
+            cph ^= 1u;
+          }
           ok = __all_sync(0xFFFFFFFFu, mbar_wait_fast(full0 + 8 * s, ph, a.wait_limit_ns, &g_gemv_error));
           if (ok) {
             const int nr = min(rps, rows - it * rps);
@@ -1213,6 +1219,8 @@ __device__ __forceinline__ void q6k_m1_body(const M1Args& a, const int bid, cons
     }
     const int off = sb * kQ6KBytes;
     bool ok = true;
+    int cs = 0;          // ring slot of the next iteration
+    uint32_t cph = 0u;   // and the parity of its phase
     for (int it0 = 0; it0 < iters && ok; it0 += SPB) {
       float pa[16];  // slots 0..7: row sums, 8..15: their certificate terms
 #pragma unroll
@@ -1221,8 +1229,12 @@ __device__ __forceinline__ void q6k_m1_body(const M1Args& a, const int bid, cons
       for (int qq = 0; qq < SPB; ++qq) {
         const int it = it0 + qq;
         if (it < iters && ok) {
-          const int s = it % a.stages;
-          const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
+          const int s = cs;
+          const uint32_t ph = cph;
+          if (++cs == a.stages) {
+            cs = 0;
+            cph ^= 1u;
+          }
           ok = __all_sync(0xFFFFFFFFu, mbar_wait_fast(full0 + 8 * s, ph, a.wait_limit_ns, &g_gemv_error));
           if (ok) {
             const int nr = min(rps, rows - it * rps);
@@ -1439,9 +1451,15 @@ __global__ void __launch_bounds__(544, 1) q6k_gemv_mt_kernel(const __grid_consta
     const int sb = u >> 2, hh = (u >> 1) & 1, lq = u & 1;
     const int off = (sb0 + sb) * kQ6KBytes;
     bool ok = true;
+    int cs = 0;          // ring slot of the next iteration
+    uint32_t cph = 0u;   // and the parity of its phase
     for (int it = 0; it < iters && ok; ++it) {
-      const int s = it % a.stages;
-      const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
+      const int s = cs;
+      const uint32_t ph = cph;
+      if (++cs == a.stages) {
+        cs = 0;
+        cph ^= 1u;
+      }
       ok = __all_sync(0xFFFFFFFFu, mbar_wait_fast(full0 + 8 * s, ph, a.wait_limit_ns, &g_gemv_error));
       if (!ok) break;
       const int nr = min(rps, rows - it * rps);
