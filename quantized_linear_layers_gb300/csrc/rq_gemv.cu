@@ -1773,14 +1773,48 @@ rq_status plan_q4k_m1(int nseg, const int* starts, const uint8_t* const* ws, flo
   return RQ_OK;
 }
 
+// Dynamic shared memory the mixed-launch kernel instances have been allowed
+// (index (R4 == 4 ? 2 : 0) + (R6 == 4 ? 1 : 0)), shared by its launchers.
+size_t g_dual_smem_set[4] = {48 * 1024, 48 * 1024, 48 * 1024, 48 * 1024};
+
 rq_status run_q4k_m1(int nseg, const int* starts, const uint8_t* const* ws, float* const* ys,
                      const float* x, int K, cudaStream_t st) {
   M1Plan p;
   const rq_status s = plan_q4k_m1(nseg, starts, ws, ys, x, K, 0, true, &p);
   if (s != RQ_OK) return s;
+  // One-token Q4_K launches with 2 or 4 rows per team per stage run the
+  // kernel of the mixed q/k/v launch, every CTA on its Q4_K side: a decode
+  // pass then launches a single kernel, whose code stays in the SMs'
+  // instruction caches from one launch to the next (measured on GB300: the
+  // 28-layer decode pass 1.332 ms with three kernels, 1.263 ms with two,
+  // RQ_GEMV_ONE_KERNEL=0 keeps the separate instances).
+  if ((p.rpt == 4 || p.rpt == 2) && m1_knob("RQ_GEMV_ONE_KERNEL", 1, 0, 1) == 1) {
+    auto dk = p.rpt == 4 ? gemv_m1_dual_kernel<4, 4> : gemv_m1_dual_kernel<2, 2>;
+    const rq_status sd = m1_allow_smem(dk, p.smem, g_dual_smem_set[p.rpt == 4 ? 3 : 0]);
+    if (sd != RQ_OK) return sd;
+    gemv_log(p.a.ksplit == 1 ? "q4k_m1 (mixed kernel)" : "q4k_m1_ksplit (mixed kernel)", 1, p.a.N,
+             K, p.grid);
+    if (p.a.ksplit == 1)
+      return launch_kernel(dk, p.grid, p.threads, p.smem, st, p.a, p.a, p.grid);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.grid);
+    cfg.blockDim = dim3(p.threads);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, dk, p.a, p.a, p.grid));
+  }
   // launches of up to 16 warps take the instance compiled for 512 threads
   // (128 registers a thread, where 17 warps allow 96)
-  const bool w16 = p.threads <= 512;
+  const bool w16 = p.threads <= 512 && m1_knob("RQ_GEMV_W16", 1, 0, 1) == 1;
   auto kern = p.rpt == 8 ? (w16 ? q4k_gemv_m1_kernel<8, 512> : q4k_gemv_m1_kernel<8, 544>)
             : p.rpt == 4 ? (w16 ? q4k_gemv_m1_kernel<4, 512> : q4k_gemv_m1_kernel<4, 544>)
                          : (w16 ? q4k_gemv_m1_kernel<2, 512> : q4k_gemv_m1_kernel<2, 544>);
@@ -1999,8 +2033,7 @@ rq_status launch_gemv_m1_dual(int count, const int* starts, const uint8_t* const
                           : (p6.rpt == 4 ? gemv_m1_dual_kernel<2, 4> : gemv_m1_dual_kernel<2, 2>);
   const size_t smem = p4.smem > p6.smem ? p4.smem : p6.smem;
   const int threads = p4.threads > p6.threads ? p4.threads : p6.threads;
-  static size_t smem_set[4] = {48 * 1024, 48 * 1024, 48 * 1024, 48 * 1024};
-  s = m1_allow_smem(kern, smem, smem_set[(p4.rpt == 4 ? 2 : 0) + (p6.rpt == 4 ? 1 : 0)]);
+  s = m1_allow_smem(kern, smem, g_dual_smem_set[(p4.rpt == 4 ? 2 : 0) + (p6.rpt == 4 ? 1 : 0)]);
   if (s != RQ_OK) return s;
   gemv_log("dual_q4k_q6k_m1", 1, starts[count] + n6, K, p4.grid + p6.grid);
   return launch_kernel(kern, p4.grid + p6.grid, threads, smem, st, p4.a, p6.a, p4.grid);
