@@ -416,6 +416,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar, int c0, int c1, int c2,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 struct M1Args {
   // One-token Q4_K with rows split between two CTAs of a single weight: a
   // 3-D view [N rows][K/256 super-blocks][144 B] of it whose box is one
@@ -437,6 +447,7 @@ struct M1Args {
   int row_align;        // Q6_K: rows per 16-byte-aligned group of rows
   int M;                // tokens (the multi-token Q6_K kernel)
   int max_rows;         // most rows any CTA owns (sizes the row accumulators)
+  int evict_first;      // weight copies ask L2 to evict their lines first
   // One-token Q4_K: 2 = clusters of two CTAs share a block of rows, CTA
   // rank h taking super-blocks [h*nsb/2, (h+1)*nsb/2) of each row (rank 0
   // adds rank 1's partial sums and writes y); 1 = one CTA per row block.
@@ -712,8 +723,12 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
     if (a.tma) {
       // the whole box, rows past N read as zero (and count as bytes)
       mbar_arrive_expect_tx(full0 + 8 * s, stage_bytes);
-      tma_load_3d(smem_u32(ring + s * a.stage_stride), &a.map, full0 + 8 * s, 0, h * nsb,
-                  r0 + it * rps);
+      if (a.evict_first)
+        tma_load_3d_hint(smem_u32(ring + s * a.stage_stride), &a.map, full0 + 8 * s, 0, h * nsb,
+                         r0 + it * rps, l2_policy_evict_first());
+      else
+        tma_load_3d(smem_u32(ring + s * a.stage_stride), &a.map, full0 + 8 * s, 0, h * nsb,
+                    r0 + it * rps);
     } else {
       mbar_arrive_expect_tx(full0 + 8 * s, (uint32_t)(nr * rowbytes));
       // one copy per segment the stage's rows fall in (per row when the rows
@@ -721,9 +736,14 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
       for (int v = r0 + it * rps, done = 0; done < nr;) {
         const int sg = m1_seg(a, v);
         const int take = a.ksplit == 1 ? min(nr - done, a.seg_start[sg + 1] - v) : 1;
-        bulk_g2s(smem_u32(ring + s * a.stage_stride + (size_t)done * rowbytes),
-                 a.seg_w[sg] + (size_t)(v - a.seg_start[sg]) * rowstride + (size_t)h * rowbytes,
-                 (uint32_t)(take * rowbytes), full0 + 8 * s);
+        const uint32_t dst = smem_u32(ring + s * a.stage_stride + (size_t)done * rowbytes);
+        const uint8_t* src =
+            a.seg_w[sg] + (size_t)(v - a.seg_start[sg]) * rowstride + (size_t)h * rowbytes;
+        if (a.evict_first)
+          bulk_g2s_hint(dst, src, (uint32_t)(take * rowbytes), full0 + 8 * s,
+                        l2_policy_evict_first());
+        else
+          bulk_g2s(dst, src, (uint32_t)(take * rowbytes), full0 + 8 * s);
         v += take;
         done += take;
       }
@@ -1121,7 +1141,12 @@ __device__ __forceinline__ void q6k_m1_body(const M1Args& a, const int bid, cons
     for (uint32_t b = bulk; b < bytes; b += 2)
       *reinterpret_cast<unsigned short*>(dst + b) = (unsigned short)ldg_nc_u16(src + b);
     mbar_arrive_expect_tx(full0 + 8 * s, bulk);
-    if (bulk != 0) bulk_g2s(smem_u32(dst), src, bulk, full0 + 8 * s);
+    if (bulk != 0) {
+      if (a.evict_first)
+        bulk_g2s_hint(smem_u32(dst), src, bulk, full0 + 8 * s, l2_policy_evict_first());
+      else
+        bulk_g2s(smem_u32(dst), src, bulk, full0 + 8 * s);
+    }
     issued |= 1u << s;
     parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
   };
@@ -1372,7 +1397,12 @@ __global__ void __launch_bounds__(544, 1) q6k_gemv_mt_kernel(const __grid_consta
     for (uint32_t b = bulk; b < bytes; b += 2)
       *reinterpret_cast<unsigned short*>(dst + b) = (unsigned short)ldg_nc_u16(src + b);
     mbar_arrive_expect_tx(full0 + 8 * s, bulk);
-    if (bulk != 0) bulk_g2s(smem_u32(dst), src, bulk, full0 + 8 * s);
+    if (bulk != 0) {
+      if (a.evict_first)
+        bulk_g2s_hint(smem_u32(dst), src, bulk, full0 + 8 * s, l2_policy_evict_first());
+      else
+        bulk_g2s(smem_u32(dst), src, bulk, full0 + 8 * s);
+    }
     issued |= 1u << s;
     parity_bits = (parity_bits & ~(1u << s)) | (ph << s);
   };
@@ -1765,6 +1795,10 @@ rq_status plan_q4k_m1(int nseg, const int* starts, const uint8_t* const* ws, flo
   a.ring_bytes = (uint32_t)stages * a.stage_stride;
   a.wait_limit_ns = kWaitLimitNs;
   a.max_rows = max_rows;
+  // weights are read once per pass: their copies go to L2 with priority
+  // evict_first, which keeps x, y and the kernel's code there (measured on
+  // GB300: decode pass 1.198 -> 1.181 ms; RQ_GEMV_EVICT_FIRST=0 turns it off)
+  a.evict_first = m1_knob("RQ_GEMV_EVICT_FIRST", 1, 0, 1);
   p->smem = a.ring_bytes + (size_t)U * kPlaneStride + 16 * nsub2 + 16 * (size_t)stages +
             20 * (size_t)max_rows + 16;
   p->threads = (a.teams * a.team_warps + 1) * 32;
@@ -1916,6 +1950,10 @@ rq_status plan_q6k_m1(const uint8_t* w, const float* x, float* y, int M, int N, 
   a.stage_stride = (uint32_t)stage_bytes;
   a.wait_limit_ns = kWaitLimitNs;
   a.max_rows = max_rows;
+  // weights are read once per pass: their copies go to L2 with priority
+  // evict_first, which keeps x, y and the kernel's code there (measured on
+  // GB300: decode pass 1.198 -> 1.181 ms; RQ_GEMV_EVICT_FIRST=0 turns it off)
+  a.evict_first = m1_knob("RQ_GEMV_EVICT_FIRST", 1, 0, 1);
   p->smem = a.ring_bytes + (size_t)M * U * kPlaneStride + 12 * (size_t)M * nsub16 +
             16 * (size_t)stages + 20 * (size_t)M * max_rows + 16;
   p->threads = (a.teams * a.team_warps + 1) * 32;

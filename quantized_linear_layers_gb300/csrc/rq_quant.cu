@@ -312,12 +312,6 @@ int64_t fused_chunk(int64_t n) {
 
 constexpr int kSlotUnroll = 4;  // float4 loads in flight per thread
 
-// L2 eviction priorities as cache policies for the loads below.
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
 __device__ __forceinline__ float4 ldg_f4_policy(const float4* p, uint64_t pol) {
   float4 v;
   asm volatile("ld.global.nc.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
