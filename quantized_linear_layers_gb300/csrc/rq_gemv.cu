@@ -898,18 +898,33 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
           if (ok) {
             const int nr = min(rps, rows - it * rps);
             const uint8_t* stage = ring + s * a.stage_stride + (size_t)team * RPT * rowbytes;
+            if (nr == rps) {
+              // a full stage: every row of the team is there
+              if (active) {
 #pragma unroll
-            for (int j = 0; j < RPT; j += 2) {
-              const int ra = team * RPT + j;
-              if (active && ra < nr) {
-                const bool two = ra + 1 < nr;
-                const float4 p2 = q4_group_dot2i(stage + j * rowbytes,
-                                                 stage + (two ? j + 1 : j) * rowbytes, off_h,
-                                                 off_a, sh, upper, xsl, xsh);
-                pa[q * RPT + j] = p2.x;
-                pa[q * RPT + j + 1] = two ? p2.y : 0.f;
-                pa[8 + q * RPT + j] = p2.z;
-                pa[8 + q * RPT + j + 1] = two ? p2.w : 0.f;
+                for (int j = 0; j < RPT; j += 2) {
+                  const float4 p2 = q4_group_dot2i(stage + j * rowbytes, stage + (j + 1) * rowbytes,
+                                                   off_h, off_a, sh, upper, xsl, xsh);
+                  pa[q * RPT + j] = p2.x;
+                  pa[q * RPT + j + 1] = p2.y;
+                  pa[8 + q * RPT + j] = p2.z;
+                  pa[8 + q * RPT + j + 1] = p2.w;
+                }
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < RPT; j += 2) {
+                const int ra = team * RPT + j;
+                if (active && ra < nr) {
+                  const bool two = ra + 1 < nr;
+                  const float4 p2 = q4_group_dot2i(stage + j * rowbytes,
+                                                   stage + (two ? j + 1 : j) * rowbytes, off_h,
+                                                   off_a, sh, upper, xsl, xsh);
+                  pa[q * RPT + j] = p2.x;
+                  pa[q * RPT + j + 1] = two ? p2.y : 0.f;
+                  pa[8 + q * RPT + j] = p2.z;
+                  pa[8 + q * RPT + j + 1] = two ? p2.w : 0.f;
+                }
               }
             }
             __syncwarp();
