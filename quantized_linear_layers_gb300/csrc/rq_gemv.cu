@@ -554,14 +554,24 @@ __device__ __forceinline__ float dot3_hi_int(const Dot3& d, float scale) {
 // Group coefficients from a header for sub-blocks 2g, 2g+1, with the 2^-14
 // of dot3_lo_int / dot3_hi_int: (d sc_lo 2^-14, d sc_hi 2^-14, dmin m_lo,
 // dmin m_hi); no underflow (d >= 2^-24 and sc >= 1 when it is non-zero).
-__device__ __forceinline__ float4 q4_coeffs(const uint4& h, int sh, bool upper) {
-  const uint32_t a16 = h.y >> sh, b16 = h.z >> sh, c16 = h.w >> sh;
-  const uint32_t scp = upper ? ((c16 & 0x0F0Fu) | ((a16 >> 2) & 0x3030u)) : (a16 & 0x3F3Fu);
-  const uint32_t mp = upper ? (((c16 >> 4) & 0x0F0Fu) | ((b16 >> 2) & 0x3030u)) : (b16 & 0x3F3Fu);
+// The 6-bit scales and mins of all four byte positions are assembled at
+// once (byte k of scw is the scale of sub-block k, k + 4 for the upper
+// lanes; mw likewise for the mins), and the lane's two are moved into the
+// mantissa of 2^23 by a byte permute with the selectors sel0 / sel1
+// (0x7440 | byte index of sub-block 2g resp. 2g + 1 within its word).
+__device__ __forceinline__ float4 q4_coeffs(const uint4& h, uint32_t sel0, uint32_t sel1,
+                                            bool upper) {
+  const uint32_t scw = upper ? ((h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u))
+                             : (h.y & 0x3F3F3F3Fu);
+  const uint32_t mw = upper ? (((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u))
+                            : (h.z & 0x3F3F3F3Fu);
   const float2 dd = half_pair(h.x);
   const float d14 = dd.x * (1.0f / 16384.0f);
-  return make_float4(d14 * byte_to_float(scp, 0), d14 * byte_to_float(scp, 1),
-                     dd.y * byte_to_float(mp, 0), dd.y * byte_to_float(mp, 1));
+  const float s0 = __uint_as_float(__byte_perm(scw, 0x4B000000u, sel0)) - 8388608.0f;
+  const float s1 = __uint_as_float(__byte_perm(scw, 0x4B000000u, sel1)) - 8388608.0f;
+  const float m0 = __uint_as_float(__byte_perm(mw, 0x4B000000u, sel0)) - 8388608.0f;
+  const float m1 = __uint_as_float(__byte_perm(mw, 0x4B000000u, sel1)) - 8388608.0f;
+  return make_float4(d14 * s0, d14 * s1, dd.y * m0, dd.y * m1);
 }
 
 // Error bound of one lane's 64-weight dot product (q4k_cert).  For
@@ -591,7 +601,8 @@ __device__ __forceinline__ void q4k_cert_consts(float s, float rs, float sa, flo
 // Two rows' 64-weight dot products (integer path), interleaved, with their
 // certificate terms: returns (p0, p1, D0, D1).
 __device__ __forceinline__ float4 q4_group_dot2i(const uint8_t* r0, const uint8_t* r1,
-                                                 int off_h, int off_a, int sh, bool upper,
+                                                 int off_h, int off_a, uint32_t sel0,
+                                                 uint32_t sel1, bool upper,
                                                  const XSplit& xl, const XSplit& xh) {
   const uint4 h0 = lds128(r0 + off_h), h1 = lds128(r1 + off_h);
   const uint4 a0 = lds128(r0 + off_a), a1 = lds128(r1 + off_a);
@@ -617,7 +628,7 @@ __device__ __forceinline__ float4 q4_group_dot2i(const uint8_t* r0, const uint8_
     g0.a3 = dp4a_us(hi0, xh.p3[w], g0.a3);
     g1.a3 = dp4a_us(hi1, xh.p3[w], g1.a3);
   }
-  const float4 c0 = q4_coeffs(h0, sh, upper), c1 = q4_coeffs(h1, sh, upper);
+  const float4 c0 = q4_coeffs(h0, sel0, sel1, upper), c1 = q4_coeffs(h1, sel0, sel1, upper);
   const float dl0 = dot3_lo_int(l0, xl.scale), dh0 = dot3_hi_int(g0, xh.scale);
   const float dl1 = dot3_lo_int(l1, xl.scale), dh1 = dot3_hi_int(g1, xh.scale);
   float p0 = c0.x * dl0;
@@ -844,7 +855,8 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
     const int u = wt * 32 + lane;
     const bool active = u < U;
     const int sb = u >> 2, g = u & 3;
-    const int sh = (g & 1) * 16;
+    // byte permute selectors of the lane's two sub-blocks' scale bytes
+    const uint32_t sel0 = 0x7440u | (uint32_t)((g & 1) * 2), sel1 = sel0 + 1u;
     const bool upper = g >= 2;
     XSplit xsl, xsh;
     if (active) {
@@ -904,7 +916,7 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
 #pragma unroll
                 for (int j = 0; j < RPT; j += 2) {
                   const float4 p2 = q4_group_dot2i(stage + j * rowbytes, stage + (j + 1) * rowbytes,
-                                                   off_h, off_a, sh, upper, xsl, xsh);
+                                                   off_h, off_a, sel0, sel1, upper, xsl, xsh);
                   pa[q * RPT + j] = p2.x;
                   pa[q * RPT + j + 1] = p2.y;
                   pa[8 + q * RPT + j] = p2.z;
@@ -919,7 +931,7 @@ __device__ __forceinline__ void q4k_m1_body(const M1Args& a, const int bid, cons
                   const bool two = ra + 1 < nr;
                   const float4 p2 = q4_group_dot2i(stage + j * rowbytes,
                                                    stage + (two ? j + 1 : j) * rowbytes, off_h,
-                                                   off_a, sh, upper, xsl, xsh);
+                                                   off_a, sel0, sel1, upper, xsl, xsh);
                   pa[q * RPT + j] = p2.x;
                   pa[q * RPT + j + 1] = two ? p2.y : 0.f;
                   pa[8 + q * RPT + j] = p2.z;
