@@ -191,7 +191,10 @@ act_quant_fused_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
       const int64_t lo = s4 * p / kFusedParts, hi = s4 * (p + 1) / kFusedParts;
       const uint32_t bytes = (uint32_t)((hi - lo) * 16);
       mbar_arrive_expect_tx(smem_u32(&bars[p]), bytes);
-      if (bytes != 0) bulk_g2s(smem_u32(stash + lo), xb4 + h4 + lo, bytes, smem_u32(&bars[p]));
+      // read once: evict_first
+      if (bytes != 0)
+        bulk_g2s_hint(smem_u32(stash + lo), xb4 + h4 + lo, bytes, smem_u32(&bars[p]),
+                      l2_policy_evict_first());
     }
   }
   if (tid == 32) tag_s = (uint32_t)(ld_relaxed_u64(state) >> 32) + 1u;
@@ -199,16 +202,20 @@ act_quant_fused_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
 
   float mf = 0.0f, nf = 0.0f;
   {
+    // the head is read again after the barrier: ask L2 to keep it
+    const uint64_t keep = l2_policy_evict_last();
     int64_t i = tid;
     for (; i + 3 * kFusedThreads < h4; i += 4 * kFusedThreads) {
-      const float4 v0 = __ldg(xb4 + i), v1 = __ldg(xb4 + i + kFusedThreads);
-      const float4 v2 = __ldg(xb4 + i + 2 * kFusedThreads), v3 = __ldg(xb4 + i + 3 * kFusedThreads);
+      const float4 v0 = ldg_f4_policy(xb4 + i, keep);
+      const float4 v1 = ldg_f4_policy(xb4 + i + kFusedThreads, keep);
+      const float4 v2 = ldg_f4_policy(xb4 + i + 2 * kFusedThreads, keep);
+      const float4 v3 = ldg_f4_policy(xb4 + i + 3 * kFusedThreads, keep);
       max4_f(mf, nf, v0);
       max4_f(mf, nf, v1);
       max4_f(mf, nf, v2);
       max4_f(mf, nf, v3);
     }
-    for (; i < h4; i += kFusedThreads) max4_f(mf, nf, __ldg(xb4 + i));
+    for (; i < h4; i += kFusedThreads) max4_f(mf, nf, ldg_f4_policy(xb4 + i, keep));
   }
   for (int p = 0; p < kFusedParts; ++p) {
     mbar_wait(smem_u32(&bars[p]), 0, kWaitLimitNs, &g_quant_error);
@@ -278,13 +285,15 @@ act_quant_fused_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
     if (dequant_out != nullptr) *dequant_out = __fdiv_rn(a, 448.0f);
   }
   uint32_t* o4 = reinterpret_cast<uint32_t*>(out + begin);
+  const uint64_t last_use = l2_policy_evict_first();
   if (nonfinite_s == 0u) {
     // every value of the chunk is finite
     for (int64_t i = h4 - 1 - tid; i >= 0; i -= kFusedThreads)
-      o4[i] = e4m3_scaled4_finite(__ldg(xb4 + i), s);
+      o4[i] = e4m3_scaled4_finite(ldg_f4_policy(xb4 + i, last_use), s);
     for (int64_t i = tid; i < s4; i += kFusedThreads) o4[h4 + i] = e4m3_scaled4_finite(stash[i], s);
   } else {
-    for (int64_t i = h4 - 1 - tid; i >= 0; i -= kFusedThreads) o4[i] = pack4(__ldg(xb4 + i), s);
+    for (int64_t i = h4 - 1 - tid; i >= 0; i -= kFusedThreads)
+      o4[i] = pack4(ldg_f4_policy(xb4 + i, last_use), s);
     for (int64_t i = tid; i < s4; i += kFusedThreads) o4[h4 + i] = pack4(stash[i], s);
   }
   for (int64_t i = (cnt4 << 2) + tid; i < len; i += kFusedThreads)
@@ -312,13 +321,6 @@ int64_t fused_chunk(int64_t n) {
 
 constexpr int kSlotUnroll = 4;  // float4 loads in flight per thread
 
-__device__ __forceinline__ float4 ldg_f4_policy(const float4* p, uint64_t pol) {
-  float4 v;
-  asm volatile("ld.global.nc.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "l"(p), "l"(pol));
-  return v;
-}
 
 // Each slot: the CTA's maximum |x| bits (NaN skipped) in bits 0..30, and
 // bit 31 set when its part of x holds a NaN or an infinity.
@@ -660,13 +662,21 @@ rq_status launch_act_quant_cluster(const float* x, int64_t n, int64_t n_out, uin
 }
 
 // Heads (the parts of the chunks beyond shared memory) up to this many bytes
-// in all: measured on GB300, the one kernel beats the two while its heads
-// stay in L2 between its passes (512 x 18944, 5 MB of heads: 16.3 against
-// 18.9 us alone, and the 28-layer stack at 512 tokens 1 % faster) and loses
-// once they do not (2048 x 18944, 121 MB: 62 against 55 us); with 25 MB of
-// heads (4096 x 3584) it wins alone (22 against 25 us) but the stack at 4096
-// tokens, whose weights share L2, is 3-5 % slower than with two kernels.
+// in all.  The heads are loaded with L2 priority evict_last on the first
+// pass and evict_first on the second, the on-chip parts with evict_first.
+// Measured on GB300 (graph-replayed, alone; one kernel against two): 512 x
+// 18944, 5 MB of heads: 11.9 against 17.9 us; 1024 x 18944, 54 MB: 22.6
+// against 30.4; 4096 x 3584, 25 MB: 17.4 against 24.3; 2048 x 18944,
+// 121 MB: 55.7 against 54.2.  In the 28-layer stack, whose weights share L2
+// (eager ms per pass, 16 MB cap against 128 MB): 1024 tokens 6.84 / 6.67,
+// 2048 tokens 12.53 / 12.44, but 4096 tokens 23.4 / 23.8, the 25 MB heads
+// of its 4096 x 3584 activations costing the GEMMs after them more than
+// they save.  So up to 16 MB of heads in general, up to 128 MB for tensors
+// of at least 2^24 elements; RQ_ONE_PASS_HEAD_MB sets one cap for all
+// (tuning).
 constexpr int64_t kFusedHeadMax = 16ll << 20;
+constexpr int64_t kFusedHeadMaxLarge = 128ll << 20;
+constexpr int64_t kFusedLargeElems = 1ll << 24;
 
 int64_t fused_stash4(int64_t chunk) {
   return std::min<int64_t>(chunk / 4, kFusedSmemMax / 16);
@@ -679,7 +689,13 @@ bool act_quant_fused_fits(const float* x, int64_t n, const uint8_t* out) {
   const int64_t chunk = fused_chunk(n);
   const int64_t grid = (n + chunk - 1) / chunk;
   const int64_t head_bytes = 4 * n - 16 * grid * fused_stash4(chunk);
-  return head_bytes <= kFusedHeadMax;
+  static int64_t cap = -2;
+  if (cap == -2) {
+    const char* e = std::getenv("RQ_ONE_PASS_HEAD_MB");
+    cap = e != nullptr ? (int64_t)std::atoll(e) << 20 : -1;
+  }
+  if (cap >= 0) return head_bytes <= cap;
+  return head_bytes <= (n >= kFusedLargeElems ? kFusedHeadMaxLarge : kFusedHeadMax);
 }
 
 rq_status launch_act_quant_fused(const float* x, int64_t n, int64_t n_out,

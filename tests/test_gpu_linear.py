@@ -136,7 +136,8 @@ def act_quant_kernels(mode, n):
     """Kernels the activation cache launches for n elements: the one-cluster
     kernel up to 2^17 elements; the one-pass kernel from 2^20 elements on
     while what does not fit one wave of shared memory (220 KB per SM) is at
-    most 16 MB; else the two kernels."""
+    most 16 MB (128 MB for tensors of 2^24 elements or more); else the two
+    kernels."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     chunk = max(4096, ((n + sms - 1) // sms + 3) & ~3)
     grid = (n + chunk - 1) // chunk
@@ -144,7 +145,8 @@ def act_quant_kernels(mode, n):
     if mode == "cluster" or (mode == "default" and n <= 1 << 17):
         return 1
     least = {"1": 0, "0": None, "default": 1 << 20}[mode]
-    return 1 if least is not None and n >= least and head <= 16 << 20 else 2
+    cap = (128 << 20) if n >= 1 << 24 else (16 << 20)
+    return 1 if least is not None and n >= least and head <= cap else 2
 
 
 def set_act_quant_mode(monkeypatch, mode):
