@@ -1795,6 +1795,13 @@ rq_status plan_q4k_m1(int nseg, const int* starts, const uint8_t* const* ws, flo
   a.team_warps = (U + 31) / 32;
   if (a.team_warps > 16) return RQ_ERR_SHAPE;
   a.teams = a.team_warps >= warps_per_cta ? 1 : warps_per_cta / a.team_warps;
+  {
+    // no more teams than a CTA's rows keep busy in one stage (measured on
+    // GB300: o 3584 x 3584, 24 rows a CTA, 6 teams instead of 8: 4.95 ->
+    // 4.73 us; RQ_GEMV_TEAM_CAP=0 keeps every team)
+    const int busy = (max_rows + rpt - 1) / rpt;
+    if (m1_knob("RQ_GEMV_TEAM_CAP", 1, 0, 1) == 1 && a.teams > busy) a.teams = busy;
+  }
   a.rows_per_stage = rpt * a.teams;
   const int rowbytes = (Kc / kQK) * kQ4KBytes;
   const int stage_bytes = a.rows_per_stage * rowbytes;
