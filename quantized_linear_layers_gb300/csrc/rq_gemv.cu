@@ -1338,7 +1338,9 @@ __global__ void __launch_bounds__(544, 1) q6k_gemv_m1_kernel(const __grid_consta
 // One launch for a token's Q4_K members and one Q6_K member that share x
 // (the decoder's q, k and v): CTAs [0, g4) run the Q4_K body over its
 // members' rows, the others the Q6_K body, each with its own arguments and
-// its own layout of the (shared) dynamic shared memory.
+// its own layout of the (shared) dynamic shared memory.  The other
+// one-token Q4_K launches run it too, with g4 = the grid (every CTA on the
+// Q4_K side), so that a decode pass launches this one kernel throughout.
 template <int R4, int R6>
 __global__ void __launch_bounds__(544, 1) gemv_m1_dual_kernel(const __grid_constant__ M1Args a4,
                                                               const __grid_constant__ M1Args a6,
