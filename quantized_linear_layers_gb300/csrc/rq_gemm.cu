@@ -234,7 +234,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
         for (int kb = 0; kb < kblocks; ++kb, ++unit) {
           const uint32_t fb = full0 + 8 * stage;
           if (unit >= early) {
-            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, args.wait_limit_ns,
+            if (!mbar_wait_fast(empty0 + 8 * stage, phase ^ 1, args.wait_limit_ns,
                            &g_rq_device_error)) {
               ok = false;
               break;
@@ -251,7 +251,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
       // Drain: every issued copy has landed before the CTA can exit.
       for (int s = 0; s < nst; ++s)
         if (issued_mask & (1u << s))
-          mbar_wait(full0 + 8 * s, (last_parity >> s) & 1u, args.wait_limit_ns,
+          mbar_wait_fast(full0 + 8 * s, (last_parity >> s) & 1u, args.wait_limit_ns,
                     &g_rq_device_error);
     }
   } else if (warp == 1) {
@@ -264,11 +264,11 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-        if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, args.wait_limit_ns, &g_rq_device_error)) break;
+        if (!mbar_wait_fast(tempty0 + 8 * acc, acc_phase ^ 1, args.wait_limit_ns, &g_rq_device_error)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * bn);
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(full0 + 8 * stage, phase, args.wait_limit_ns, &g_rq_device_error)) {
+          if (!mbar_wait_fast(full0 + 8 * stage, phase, args.wait_limit_ns, &g_rq_device_error)) {
             ok = false;
             break;
           }
@@ -288,7 +288,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
       }
       // Drain: all issued MMAs have completed before TMEM is released.
       mma_commit(done_bar);
-      mbar_wait(done_bar, 0, args.wait_limit_ns, &g_rq_device_error);
+      mbar_wait_fast(done_bar, 0, args.wait_limit_ns, &g_rq_device_error);
     }
   } else {
     // --------------------------------------------------------- epilogue --
@@ -301,7 +301,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
       // every lane polls; the outcome is made warp-uniform before the
       // .sync.aligned TMEM loads below
       const bool ready =
-          mbar_wait(tfull0 + 8 * acc, acc_phase, args.wait_limit_ns, &g_rq_device_error);
+          mbar_wait_fast(tfull0 + 8 * acc, acc_phase, args.wait_limit_ns, &g_rq_device_error);
       if (!__all_sync(0xFFFFFFFFu, ready)) break;
       tc_fence_after();
       const int n = tn * kBM + quad * 32 + lane;
@@ -512,7 +512,7 @@ fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
         for (int kb = 0; kb < kblocks; ++kb, ++unit) {
           const uint32_t lead_full = peer_addr(full0 + 8 * stage, 0);
           if (unit >= early) {
-            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, args.wait_limit_ns,
+            if (!mbar_wait_fast(empty0 + 8 * stage, phase ^ 1, args.wait_limit_ns,
                            &g_rq_device_error)) {
               ok = false;
               break;
@@ -527,7 +527,7 @@ fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
       // Drain: this CTA's last copies have landed once the leader's MMAs
       // that consume them have freed the stages (seen on our own "empty").
       for (int i = 0; i < nst && ok; ++i) {
-        if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, args.wait_limit_ns, &g_rq_device_error))
+        if (!mbar_wait_fast(empty0 + 8 * stage, phase ^ 1, args.wait_limit_ns, &g_rq_device_error))
           break;
         if (++stage == nst) { stage = 0; phase ^= 1; }
       }
@@ -542,12 +542,12 @@ fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int t = pair; t < ntiles && ok; t += npairs) {
-        if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, args.wait_limit_ns, &g_rq_device_error))
+        if (!mbar_wait_fast(tempty0 + 8 * acc, acc_phase ^ 1, args.wait_limit_ns, &g_rq_device_error))
           break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * bn);
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(full0 + 8 * stage, phase, args.wait_limit_ns, &g_rq_device_error)) {
+          if (!mbar_wait_fast(full0 + 8 * stage, phase, args.wait_limit_ns, &g_rq_device_error)) {
             ok = false;
             break;
           }
@@ -566,7 +566,7 @@ fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
         if (++acc == 2) { acc = 0; acc_phase ^= 1; }
       }
       mma_commit_pair_local(done_bar);
-      mbar_wait(done_bar, 0, args.wait_limit_ns, &g_rq_device_error);
+      mbar_wait_fast(done_bar, 0, args.wait_limit_ns, &g_rq_device_error);
     }
   } else {
     // --------------------------------------------------- epilogue (both)
@@ -579,7 +579,7 @@ fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
     for (int t = pair; t < ntiles; t += npairs) {
       const int tn = t / args.tiles_m, tm = t - tn * args.tiles_m;
       const bool ready =
-          mbar_wait(tfull0 + 8 * acc, acc_phase, args.wait_limit_ns, &g_rq_device_error);
+          mbar_wait_fast(tfull0 + 8 * acc, acc_phase, args.wait_limit_ns, &g_rq_device_error);
       if (!__all_sync(0xFFFFFFFFu, ready)) break;
       tc_fence_after();
       const int n = tn * 256 + (int)rank * kBM + quad * 32 + lane;
@@ -733,7 +733,7 @@ fp8_gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmap_w,
       for (int kb = kb0; kb < kb1; ++kb) {
         const uint32_t fb = full0 + 8 * stage;
         if (kb - kb0 >= early) {
-          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, args.wait_limit_ns, &g_rq_device_error))
+          if (!mbar_wait_fast(empty0 + 8 * stage, phase ^ 1, args.wait_limit_ns, &g_rq_device_error))
             break;
           mbar_arrive_expect_tx(fb, stage_tx);
           tma_load_2d(smem_u32(sA + stage * kABytes), &tmap_w, fb, kb * kBK, tn * kBM);
@@ -745,7 +745,7 @@ fp8_gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmap_w,
       }
       for (int s = 0; s < nst; ++s)
         if (issued_mask & (1u << s))
-          mbar_wait(full0 + 8 * s, (last_parity >> s) & 1u, args.wait_limit_ns,
+          mbar_wait_fast(full0 + 8 * s, (last_parity >> s) & 1u, args.wait_limit_ns,
                     &g_rq_device_error);
     }
   } else if (warp == 1) {
@@ -755,7 +755,7 @@ fp8_gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmap_w,
       int stage = 0;
       uint32_t phase = 0;
       for (int kb = kb0; kb < kb1; ++kb) {
-        if (!mbar_wait(full0 + 8 * stage, phase, args.wait_limit_ns, &g_rq_device_error)) break;
+        if (!mbar_wait_fast(full0 + 8 * stage, phase, args.wait_limit_ns, &g_rq_device_error)) break;
         tc_fence_after();
         const uint32_t a_addr = smem_u32(sA + stage * kABytes);
         const uint32_t b_addr = smem_u32(sB + stage * b_stride);
@@ -774,7 +774,7 @@ fp8_gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmap_w,
     // ------------------------------------ epilogue: partial tile to smem --
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
-    const bool ready = mbar_wait(tfull, 0, args.wait_limit_ns, &g_rq_device_error);
+    const bool ready = mbar_wait_fast(tfull, 0, args.wait_limit_ns, &g_rq_device_error);
     if (__all_sync(0xFFFFFFFFu, ready)) {
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16);
@@ -865,7 +865,7 @@ __global__ void wait_timeout_kernel(uint64_t limit_ns) {
     const uint32_t b = smem_u32(&bar);
     mbar_init(b, 1);
     mbar_fence_init();
-    mbar_wait(b, 0, limit_ns, &g_rq_device_error);
+    mbar_wait_fast(b, 0, limit_ns, &g_rq_device_error);
   }
 }
 
