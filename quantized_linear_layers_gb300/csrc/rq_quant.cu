@@ -173,14 +173,23 @@ act_quant_fused_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
   __shared__ uint32_t warp_max[kFusedThreads / 32], warp_nf[kFusedThreads / 32];
   __shared__ uint32_t absmax_s, nonfinite_s, tag_s;
 
-  const int64_t begin = (int64_t)blockIdx.x * chunk;
-  const int64_t len = min(chunk, n - begin);
-  const int64_t cnt4 = len >> 2;               // whole float4s of the chunk
-  const int64_t s4 = min(cnt4, stash4);        // the last s4 of them: shared memory
-  const int64_t h4 = cnt4 - s4;                // the head: streamed twice
-  const float4* xb4 = reinterpret_cast<const float4*>(x + begin);
+  // The whole float4s of x: the last G * S of them are the CTAs' stashes
+  // (CTA i holds [hs + i*S, hs + (i+1)*S) in shared memory, the last one
+  // possibly fewer); the first hs, the head, are streamed by all CTAs
+  // together (thread g of the grid takes float4s g, g + T, ...), once for
+  // the max and once to encode.  The n % 4 last values go to the last CTA.
+  (void)chunk;
+  const int64_t n4 = n >> 2;
+  const int64_t G = gridDim.x;
+  const int64_t S = min(stash4, (n4 + G - 1) / G);
+  const int64_t hs = n4 - min(n4, G * S);
+  const int64_t s_lo = min(n4, hs + (int64_t)blockIdx.x * S);
+  const int64_t s4 = min(n4, s_lo + S) - s_lo;  // this CTA's stash
+  const float4* x4 = reinterpret_cast<const float4*>(x);
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
+  const int64_t g = (int64_t)blockIdx.x * kFusedThreads + tid, T = G * kFusedThreads;
+  const bool last_cta = blockIdx.x == gridDim.x - 1;
 
   pdl_wait();
   pdl_trigger();
@@ -193,7 +202,7 @@ act_quant_fused_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
       mbar_arrive_expect_tx(smem_u32(&bars[p]), bytes);
       // read once: evict_first
       if (bytes != 0)
-        bulk_g2s_hint(smem_u32(stash + lo), xb4 + h4 + lo, bytes, smem_u32(&bars[p]),
+        bulk_g2s_hint(smem_u32(stash + lo), x4 + s_lo + lo, bytes, smem_u32(&bars[p]),
                       l2_policy_evict_first());
     }
   }
@@ -204,29 +213,30 @@ act_quant_fused_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
   {
     // the head is read again after the barrier: ask L2 to keep it
     const uint64_t keep = l2_policy_evict_last();
-    int64_t i = tid;
-    for (; i + 3 * kFusedThreads < h4; i += 4 * kFusedThreads) {
-      const float4 v0 = ldg_f4_policy(xb4 + i, keep);
-      const float4 v1 = ldg_f4_policy(xb4 + i + kFusedThreads, keep);
-      const float4 v2 = ldg_f4_policy(xb4 + i + 2 * kFusedThreads, keep);
-      const float4 v3 = ldg_f4_policy(xb4 + i + 3 * kFusedThreads, keep);
+    int64_t i = g;
+    for (; i + 3 * T < hs; i += 4 * T) {
+      const float4 v0 = ldg_f4_policy(x4 + i, keep);
+      const float4 v1 = ldg_f4_policy(x4 + i + T, keep);
+      const float4 v2 = ldg_f4_policy(x4 + i + 2 * T, keep);
+      const float4 v3 = ldg_f4_policy(x4 + i + 3 * T, keep);
       max4_f(mf, nf, v0);
       max4_f(mf, nf, v1);
       max4_f(mf, nf, v2);
       max4_f(mf, nf, v3);
     }
-    for (; i < h4; i += kFusedThreads) max4_f(mf, nf, ldg_f4_policy(xb4 + i, keep));
+    for (; i < hs; i += T) max4_f(mf, nf, ldg_f4_policy(x4 + i, keep));
   }
   for (int p = 0; p < kFusedParts; ++p) {
     mbar_wait(smem_u32(&bars[p]), 0, kWaitLimitNs, &g_quant_error);
     const int64_t lo = s4 * p / kFusedParts, hi = s4 * (p + 1) / kFusedParts;
     for (int64_t i = lo + tid; i < hi; i += kFusedThreads) max4_f(mf, nf, stash[i]);
   }
-  for (int64_t i = (cnt4 << 2) + tid; i < len; i += kFusedThreads) {
-    const float v = __ldg(x + begin + i);
-    mf = fmaxf(mf, fabsf(v));
-    nf = fmaf(v, 0.0f, nf);
-  }
+  if (last_cta)
+    for (int64_t i = (n4 << 2) + tid; i < n; i += kFusedThreads) {
+      const float v = __ldg(x + i);
+      mf = fmaxf(mf, fabsf(v));
+      nf = fmaf(v, 0.0f, nf);
+    }
   uint32_t m = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(mf));
   const uint32_t bad = __any_sync(0xFFFFFFFFu, !(nf == 0.0f)) ? 1u : 0u;
   if (lane == 0) {
@@ -284,20 +294,34 @@ act_quant_fused_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
     if (absmax_out != nullptr) *absmax_out = absmax_s;
     if (dequant_out != nullptr) *dequant_out = __fdiv_rn(a, 448.0f);
   }
-  uint32_t* o4 = reinterpret_cast<uint32_t*>(out + begin);
+  uint32_t* o4 = reinterpret_cast<uint32_t*>(out);
   const uint64_t last_use = l2_policy_evict_first();
-  if (nonfinite_s == 0u) {
-    // every value of the chunk is finite
-    for (int64_t i = h4 - 1 - tid; i >= 0; i -= kFusedThreads)
-      o4[i] = e4m3_scaled4_finite(ldg_f4_policy(xb4 + i, last_use), s);
-    for (int64_t i = tid; i < s4; i += kFusedThreads) o4[h4 + i] = e4m3_scaled4_finite(stash[i], s);
+  // this thread's head float4s again, the last rounds first (the lines read
+  // last are the likeliest to be in L2)
+  const bool finite = nonfinite_s == 0u;  // every value this CTA read is finite
+  if (hs > 0)
+    for (int64_t base = ((hs - 1) / (4 * T)) * (4 * T); base >= 0; base -= 4 * T) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 3; u >= 0; --u) {
+        const int64_t i = base + u * T + g;
+        if (i < hs) v[u] = ldg_f4_policy(x4 + i, last_use);
+      }
+#pragma unroll
+      for (int u = 3; u >= 0; --u) {
+        const int64_t i = base + u * T + g;
+        if (i < hs) o4[i] = finite ? e4m3_scaled4_finite(v[u], s) : pack4(v[u], s);
+      }
+    }
+  if (finite) {
+    for (int64_t i = tid; i < s4; i += kFusedThreads)
+      o4[s_lo + i] = e4m3_scaled4_finite(stash[i], s);
   } else {
-    for (int64_t i = h4 - 1 - tid; i >= 0; i -= kFusedThreads)
-      o4[i] = pack4(ldg_f4_policy(xb4 + i, last_use), s);
-    for (int64_t i = tid; i < s4; i += kFusedThreads) o4[h4 + i] = pack4(stash[i], s);
+    for (int64_t i = tid; i < s4; i += kFusedThreads) o4[s_lo + i] = pack4(stash[i], s);
   }
-  for (int64_t i = (cnt4 << 2) + tid; i < len; i += kFusedThreads)
-    out[begin + i] = (uint8_t)e4m3_scaled(__ldg(x + begin + i), s);
+  if (last_cta)
+    for (int64_t i = (n4 << 2) + tid; i < n; i += kFusedThreads)
+      out[i] = (uint8_t)e4m3_scaled(__ldg(x + i), s);
   const int64_t stride = (int64_t)gridDim.x * kFusedThreads;
   for (int64_t i = n + (int64_t)blockIdx.x * kFusedThreads + tid; i < n_out; i += stride)
     out[i] = 0;
