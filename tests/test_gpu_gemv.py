@@ -149,6 +149,33 @@ def test_one_token_q4k_rows_split_between_two_ctas(rq, monkeypatch, force, N, K)
     assert ok, "worst error / bound = %.3g" % worst
 
 
+@pytest.mark.parametrize("env", [{}, {"RQ_GEMV_ONE_KERNEL": "0"},
+                                 {"RQ_GEMV_ONE_KERNEL": "0", "RQ_GEMV_W16": "0"},
+                                 {"RQ_GEMV_TEAM_CAP": "0"}, {"RQ_GEMV_EVICT_FIRST": "0"}])
+@pytest.mark.parametrize("N,K", [(3584, 3584), (512, 3584), (3584, 18944), (1001, 2560)])
+def test_one_token_q4k_launch_variants(rq, monkeypatch, capfd, env, N, K):
+    """One-token Q4_K launches run the kernel of the mixed q/k/v launch with
+    every CTA on its Q4_K side by default (the log says so), their own
+    kernel instances with RQ_GEMV_ONE_KERNEL=0 (those compiled for 512
+    threads unless RQ_GEMV_W16=0), every team with RQ_GEMV_TEAM_CAP=0 and
+    weight copies without the L2 hint with RQ_GEMV_EVICT_FIRST=0: every
+    output of each against the oracle (1001 x 2560: few rows a CTA, two rows
+    per team and stage)."""
+    monkeypatch.setenv("RQ_GEMV_LOG", "1")
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    W = synthetic.q4k_matrix(4000 + N + K, N, K)
+    x = synthetic.activation(4001 + K, 1, K, outlier_frac=1e-3)
+    capfd.readouterr()
+    got = gpu_gemv(rq, Q4K, W, x, N, K)
+    lines = [l for l in capfd.readouterr().err.splitlines() if l.startswith("rq_gemv:")]
+    ref, absdot = oracle.gemv(Q4K, W, x, N, K)
+    ok, worst = gemv_ok(got, ref, absdot)
+    assert ok, "worst error / bound = %.3g" % worst
+    assert len(lines) == 1, lines
+    assert ("(mixed kernel)" in lines[0]) == (env.get("RQ_GEMV_ONE_KERNEL") != "0"), lines
+
+
 @pytest.mark.parametrize("qtype,N,K,M,kernel", [
     (Q4K, 3584, 3584, 1, "q4k_m1"), (Q4K, 18944, 3584, 1, "q4k_m1"),
     (Q4K, 3584, 18944, 1, "q4k_m1_ksplit"), (Q6K, 512, 3584, 1, "q6k_m1"),
