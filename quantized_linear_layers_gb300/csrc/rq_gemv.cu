@@ -1861,8 +1861,8 @@ rq_status run_q4k_m1(int nseg, const int* starts, const uint8_t* const* ws, floa
   // kernel of the mixed q/k/v launch, every CTA on its Q4_K side: a decode
   // pass then launches a single kernel, whose code stays in the SMs'
   // instruction caches from one launch to the next (measured on GB300: the
-  // 28-layer decode pass 1.332 ms with three kernels, 1.263 ms with two,
-  // RQ_GEMV_ONE_KERNEL=0 keeps the separate instances).
+  // 28-layer decode pass 1.323 ms with three kernels, 1.256 with two, 1.197
+  // with one; RQ_GEMV_ONE_KERNEL=0 keeps the separate instances).
   if ((p.rpt == 4 || p.rpt == 2) && m1_knob("RQ_GEMV_ONE_KERNEL", 1, 0, 1) == 1) {
     auto dk = p.rpt == 4 ? gemv_m1_dual_kernel<4, 4> : gemv_m1_dual_kernel<2, 2>;
     const rq_status sd = m1_allow_smem(dk, p.smem, g_dual_smem_set[p.rpt == 4 ? 3 : 0]);

@@ -110,17 +110,17 @@ quant_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
 
 // ------------------------------------------------------ one-pass variant --
 //
-// One wave of CTAs (one per SM), each owning a chunk of x.  A CTA keeps the
-// last `stash4` float4s of its chunk in shared memory (bulk copies) and
-// streams the rest, the head, through registers while the copies land,
-// reducing the max of both; all CTAs meet at a grid barrier that publishes
-// the tensor max; each CTA then encodes the head, read again newest lines
-// first (they are the likeliest to be in L2), and the stash from shared
-// memory.  When the chunks fit in shared memory (the activations of 2048
-// tokens x 3584) x is read from HBM once; the launcher takes this kernel
-// only while the heads are small enough to stay in L2 between the passes.
-// Same arithmetic as absmax_kernel + quant_kernel, so the bytes are
-// identical.
+// One wave of CTAs (one per SM).  Each CTA holds a stash of up to `stash4`
+// float4s of x in shared memory (one bulk copy; the stashes are the last
+// float4s of x), and the CTAs stream the rest, the head at the front of x,
+// together through registers while the copies land, reducing the max of
+// both; all CTAs meet at a grid barrier that publishes the tensor max; the
+// head is then read again, newest lines first (they are the likeliest to be
+// in L2), and encoded with each CTA's stash from shared memory.  When the
+// stashes hold all of x (the activations of 2048 tokens x 3584) x is read
+// from HBM once; the launcher takes this kernel only while the head is
+// small enough to stay largely in L2 between the passes.  Same arithmetic
+// as absmax_kernel + quant_kernel, so the bytes are identical.
 //
 // Grid barrier of the one-pass kernel, on 64-bit words that each carry a
 // launch tag (high half) and a maximum |x| bits (low half), written and read
