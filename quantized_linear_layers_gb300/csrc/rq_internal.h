@@ -48,10 +48,11 @@ rq_status launch_quant(const float* x, int64_t n, int64_t n_out,
                        const uint32_t* absmax_bits, uint8_t* out,
                        float* dequant_out, cudaStream_t st);
 
-// Absmax + encode in one cooperative wave (up to 220 KB per CTA of x staged
-// in shared memory; the rest, at the front of x and at most 16 MB -- 128 MB
-// for tensors of 2^24 elements or more -- streamed by all CTAs and read
-// twice).
+// Absmax + encode in one cooperative wave: x held in registers when it fits
+// one wave of them (up to 512 x 24 float4 per CTA), else up to 220 KB per
+// CTA of x staged in shared memory and the rest, at the front of x and at
+// most 16 MB -- 128 MB for tensors of 2^24 elements or more -- streamed by
+// all CTAs and read twice.
 // Needs x 16-byte and out 4-byte aligned; RQ_ERR_SHAPE (nothing launched) if
 // the wave does not fit the GPU.  `state` is one 64-bit device word and
 // `slots` `nslots` of them (at least the SM count), all zero before the

@@ -163,6 +163,71 @@ __device__ __forceinline__ void max4_f(float& mf, float& nf, float4 v) {
   nf = fmaf(v.w, 0.0f, nf);
 }
 
+// Block maximum and non-finite flag of the threads' running values (mf, nf
+// of max4_f), then the grid barrier on the tagged words described above.
+// On return (after a block barrier) absmax_s holds the tensor's maximum |x|
+// bits and nonfinite_s whether this CTA's part of x held a NaN or an
+// infinity.  tag_s: this launch's tag, read from `state` before the call.
+// NW: warps of the block.
+template <int NW>
+__device__ __forceinline__ void one_pass_grid_max(float mf, float nf, uint32_t (&warp_max)[NW],
+                                                  uint32_t (&warp_nf)[NW], const uint32_t& tag_s,
+                                                  unsigned long long* state,
+                                                  unsigned long long* slots, uint32_t& absmax_s,
+                                                  uint32_t& nonfinite_s) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t m = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(mf));
+  const uint32_t bad = __any_sync(0xFFFFFFFFu, !(nf == 0.0f)) ? 1u : 0u;
+  if (lane == 0) {
+    warp_max[warp] = m;
+    warp_nf[warp] = bad;
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    m = __reduce_max_sync(0xFFFFFFFFu, lane < NW ? warp_max[lane] : 0u);
+    const uint32_t any_bad = __reduce_or_sync(0xFFFFFFFFu, lane < NW ? warp_nf[lane] : 0u);
+    const uint32_t tag = tag_s;
+    if (lane == 0) {
+      nonfinite_s = any_bad;
+      st_relaxed_u64(slots + blockIdx.x, ((uint64_t)tag << 32) | m);
+    }
+    uint32_t all = 0;
+    const uint64_t t0 = globaltimer();
+    if (blockIdx.x == 0) {
+      // every CTA's maximum, then the tensor's for the others
+      while (true) {
+        bool done = true;
+        uint32_t mm = 0;
+        for (int i = lane; i < (int)gridDim.x; i += 32) {
+          const uint64_t v = ld_relaxed_u64(slots + i);
+          done = done && (uint32_t)(v >> 32) == tag;
+          mm = max(mm, (uint32_t)v);
+        }
+        all = __reduce_max_sync(0xFFFFFFFFu, mm);
+        if (__all_sync(0xFFFFFFFFu, done)) break;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+          if (lane == 0) atomicOr(&g_quant_error, 2u);
+          break;
+        }
+      }
+      if (lane == 0) st_relaxed_u64(state, ((uint64_t)tag << 32) | all);
+    } else {
+      uint64_t v = ld_relaxed_u64(state);
+      while ((uint32_t)(v >> 32) != tag) {
+        if (globaltimer() - t0 > kWaitLimitNs) {
+          if (lane == 0) atomicOr(&g_quant_error, 2u);
+          break;
+        }
+        v = ld_relaxed_u64(state);
+      }
+      all = (uint32_t)v;
+    }
+    if (lane == 0) absmax_s = all;
+  }
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(kFusedThreads, 1)
 act_quant_fused_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
                        int64_t chunk, int64_t stash4, uint8_t* __restrict__ out,
@@ -187,7 +252,6 @@ act_quant_fused_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
   const int64_t s4 = min(n4, s_lo + S) - s_lo;  // this CTA's stash
   const float4* x4 = reinterpret_cast<const float4*>(x);
   const int tid = threadIdx.x;
-  const int lane = tid & 31, warp = tid >> 5;
   const int64_t g = (int64_t)blockIdx.x * kFusedThreads + tid, T = G * kFusedThreads;
   const bool last_cta = blockIdx.x == gridDim.x - 1;
 
@@ -237,56 +301,8 @@ act_quant_fused_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
       mf = fmaxf(mf, fabsf(v));
       nf = fmaf(v, 0.0f, nf);
     }
-  uint32_t m = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(mf));
-  const uint32_t bad = __any_sync(0xFFFFFFFFu, !(nf == 0.0f)) ? 1u : 0u;
-  if (lane == 0) {
-    warp_max[warp] = m;
-    warp_nf[warp] = bad;
-  }
-  __syncthreads();
-
-  if (warp == 0) {
-    m = __reduce_max_sync(0xFFFFFFFFu, warp_max[lane]);
-    const uint32_t any_bad = __reduce_or_sync(0xFFFFFFFFu, warp_nf[lane]);
-    const uint32_t tag = tag_s;
-    if (lane == 0) {
-      nonfinite_s = any_bad;
-      st_relaxed_u64(slots + blockIdx.x, ((uint64_t)tag << 32) | m);
-    }
-    uint32_t all = 0;
-    const uint64_t t0 = globaltimer();
-    if (blockIdx.x == 0) {
-      // every CTA's maximum, then the tensor's for the others
-      while (true) {
-        bool done = true;
-        uint32_t mm = 0;
-        for (int i = lane; i < (int)gridDim.x; i += 32) {
-          const uint64_t v = ld_relaxed_u64(slots + i);
-          done = done && (uint32_t)(v >> 32) == tag;
-          mm = max(mm, (uint32_t)v);
-        }
-        all = __reduce_max_sync(0xFFFFFFFFu, mm);
-        if (__all_sync(0xFFFFFFFFu, done)) break;
-        if (globaltimer() - t0 > kWaitLimitNs) {
-          if (lane == 0) atomicOr(&g_quant_error, 2u);
-          break;
-        }
-      }
-      if (lane == 0) st_relaxed_u64(state, ((uint64_t)tag << 32) | all);
-    } else {
-      uint64_t v = ld_relaxed_u64(state);
-      while ((uint32_t)(v >> 32) != tag) {
-        if (globaltimer() - t0 > kWaitLimitNs) {
-          if (lane == 0) atomicOr(&g_quant_error, 2u);
-          break;
-        }
-        v = ld_relaxed_u64(state);
-      }
-      all = (uint32_t)v;
-    }
-    if (lane == 0) absmax_s = all;
-  }
-  __syncthreads();
+  one_pass_grid_max<kFusedThreads / 32>(mf, nf, warp_max, warp_nf, tag_s, state, slots, absmax_s,
+                                        nonfinite_s);
 
   const float a = absmax_prime(absmax_s);
   const float s = __fdiv_rn(448.0f, a);
@@ -324,6 +340,86 @@ act_quant_fused_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
       out[i] = (uint8_t)e4m3_scaled(__ldg(x + i), s);
   const int64_t stride = (int64_t)gridDim.x * kFusedThreads;
   for (int64_t i = n + (int64_t)blockIdx.x * kFusedThreads + tid; i < n_out; i += stride)
+    out[i] = 0;
+}
+
+// ------------------------------------------- one-pass, register variant --
+//
+// For tensors whose float4s fit the register files of one wave (up to
+// 512 threads x 24 float4 per SM: 7.47 M values on 152 SMs, the 2048 x 3584
+// activations included): each thread loads its float4s of x straight into
+// registers (all loads in flight at once, read once: evict_first), takes
+// the maximum as they land, meets the other CTAs at the same grid barrier
+// as act_quant_fused_kernel, and encodes from its registers.  Unlike the
+// shared-memory stash, x is not read from shared memory twice (once for the
+// maximum, once to encode).  CTA i owns float4s [i*per4, (i+1)*per4);
+// thread t of it takes float4s t, t + 512, ...  Same arithmetic as
+// absmax_kernel + quant_kernel, so the bytes are identical.
+
+constexpr int kRegThreads = 512;
+constexpr int kRegVec = 24;  // float4s of x per thread
+
+__global__ void __launch_bounds__(kRegThreads, 1)
+act_quant_reg_kernel(const float* __restrict__ x, int64_t n, int64_t n_out, int64_t per4,
+                     uint8_t* __restrict__ out, uint32_t* __restrict__ absmax_out,
+                     float* __restrict__ dequant_out, unsigned long long* state,
+                     unsigned long long* slots) {
+  __shared__ uint32_t warp_max[kRegThreads / 32], warp_nf[kRegThreads / 32];
+  __shared__ uint32_t absmax_s, nonfinite_s, tag_s;
+  const int64_t n4 = n >> 2;
+  const int64_t lo = min(n4, (int64_t)blockIdx.x * per4);
+  const int64_t cnt = min(n4, lo + per4) - lo;  // this CTA's float4s, <= kRegThreads * kRegVec
+  const float4* x4 = reinterpret_cast<const float4*>(x) + lo;
+  const int tid = threadIdx.x;
+  const bool last_cta = blockIdx.x == gridDim.x - 1;
+
+  pdl_wait();
+  pdl_trigger();
+  if (tid == 32) tag_s = (uint32_t)(ld_relaxed_u64(state) >> 32) + 1u;
+  const uint64_t once = l2_policy_evict_first();
+  float4 v[kRegVec];
+#pragma unroll
+  for (int k = 0; k < kRegVec; ++k) {
+    const int64_t i = tid + (int64_t)k * kRegThreads;
+    v[k] = i < cnt ? ldg_f4_policy(x4 + i, once) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  float mf = 0.0f, nf = 0.0f;  // the zeros of absent float4s change neither
+#pragma unroll
+  for (int k = 0; k < kRegVec; ++k) max4_f(mf, nf, v[k]);
+  if (last_cta)
+    for (int64_t i = (n4 << 2) + tid; i < n; i += kRegThreads) {
+      const float w = __ldg(x + i);
+      mf = fmaxf(mf, fabsf(w));
+      nf = fmaf(w, 0.0f, nf);
+    }
+  one_pass_grid_max<kRegThreads / 32>(mf, nf, warp_max, warp_nf, tag_s, state, slots, absmax_s,
+                                      nonfinite_s);
+
+  const float a = absmax_prime(absmax_s);
+  const float s = __fdiv_rn(448.0f, a);
+  if (blockIdx.x == 0 && tid == 0) {
+    if (absmax_out != nullptr) *absmax_out = absmax_s;
+    if (dequant_out != nullptr) *dequant_out = __fdiv_rn(a, 448.0f);
+  }
+  uint32_t* o4 = reinterpret_cast<uint32_t*>(out) + lo;
+  if (nonfinite_s == 0u) {  // every value this CTA read is finite
+#pragma unroll
+    for (int k = 0; k < kRegVec; ++k) {
+      const int64_t i = tid + (int64_t)k * kRegThreads;
+      if (i < cnt) o4[i] = e4m3_scaled4_finite(v[k], s);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < kRegVec; ++k) {
+      const int64_t i = tid + (int64_t)k * kRegThreads;
+      if (i < cnt) o4[i] = pack4(v[k], s);
+    }
+  }
+  if (last_cta)
+    for (int64_t i = (n4 << 2) + tid; i < n; i += kRegThreads)
+      out[i] = (uint8_t)e4m3_scaled(__ldg(x + i), s);
+  const int64_t stride = (int64_t)gridDim.x * kRegThreads;
+  for (int64_t i = n + (int64_t)blockIdx.x * kRegThreads + tid; i < n_out; i += stride)
     out[i] = 0;
 }
 
@@ -727,6 +823,38 @@ rq_status launch_act_quant_fused(const float* x, int64_t n, int64_t n_out,
                                  float* dequant_out, unsigned long long* state,
                                  unsigned long long* slots, int nslots, cudaStream_t st) {
   if (!act_quant_fused_fits(x, n, out)) return RQ_ERR_SHAPE;
+  {
+    // x held in registers when it fits one wave of them (at least one
+    // float4 per thread).  Measured on GB300 (graph-replayed): 2048 x 3584
+    // 10.15 -> 9.41 us; the 28-layer stack at 2048 tokens 11.98 -> 11.93 ms
+    // eager, at 512 tokens 4.59 -> 4.54 ms.  RQ_QUANT_REG=0 keeps the
+    // shared-memory stash.
+    const int g = std::min(device_sm_count(), nslots);
+    const int64_t n4 = n >> 2;
+    const int64_t per4 = (n4 + g - 1) / g;
+    const char* reg = std::getenv("RQ_QUANT_REG");
+    if ((reg == nullptr || std::atoi(reg) != 0) && g > 0 && n4 >= (int64_t)g * kRegThreads &&
+        per4 <= (int64_t)kRegThreads * kRegVec) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)((n4 + per4 - 1) / per4));
+      cfg.blockDim = dim3(kRegThreads);
+      cfg.stream = st;
+      cudaLaunchAttribute attr[2];
+      attr[0].id = cudaLaunchAttributeCooperative;
+      attr[0].val.cooperative = 1;
+      attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[1].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = pdl_enabled() ? 2 : 1;
+      const cudaError_t e = cudaLaunchKernelEx(&cfg, act_quant_reg_kernel, x, n, n_out, per4,
+                                               out, absmax_out, dequant_out, state, slots);
+      if (e == cudaErrorCooperativeLaunchTooLarge) {
+        cudaGetLastError();
+        return RQ_ERR_SHAPE;
+      }
+      return cuda_status(e);
+    }
+  }
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(act_quant_fused_kernel,

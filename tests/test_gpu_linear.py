@@ -163,7 +163,7 @@ def set_act_quant_mode(monkeypatch, mode):
 
 
 @pytest.mark.parametrize("one_pass", ["cluster", "1", "0", "default"])
-@pytest.mark.parametrize("M,K", [(2048, 3584), (611, 1024), (37, 3584), (5, 256),
+@pytest.mark.parametrize("M,K", [(2048, 3584), (611, 1024), (611, 1023), (37, 3584), (5, 256),
                                  (16, 128), (3, 4101), (2048, 18944), (1001, 18947),
                                  (512, 18944), (509, 18947), (16, 18944), (128, 3584)])
 def test_activation_cache_bytes_bit_exact(rq, monkeypatch, one_pass, M, K):
@@ -221,6 +221,33 @@ def test_activation_cache_infinite_max(rq, monkeypatch, one_pass, M, K):
     assert np.array_equal(got, want), np.flatnonzero(got != want)[:8]
     assert got[x.size // 2] == 0xFE and np.count_nonzero(got) == 1
     assert tr["quant"][0] == act_quant_kernels(one_pass, M * K)
+    ctx.close()
+
+
+@pytest.mark.parametrize("reg", ["1", "0"])
+@pytest.mark.parametrize("M,K", [(2048, 3584), (611, 1023), (128, 3584), (300, 18944)])
+def test_one_pass_register_and_shared_memory_forms(rq, monkeypatch, reg, M, K):
+    """Tensors that fit one wave of registers take the register form of the
+    one-pass kernel by default, the shared-memory form with RQ_QUANT_REG=0;
+    both give the oracle's bytes, with a NaN in x (fix-up path) and without
+    (all-finite path), n % 4 != 0 included."""
+    set_act_quant_mode(monkeypatch, "1")
+    monkeypatch.setenv("RQ_QUANT_REG", reg)
+    ctx = rq.Context()
+    x = synthetic.activation(7300 + M + K, M, K, outlier_frac=1e-3)
+    for nan in (False, True):
+        xs = x.copy()
+        if nan:
+            xs.ravel()[xs.size // 2 + 1] = np.nan
+        ctx.rq_act_cache_invalidate()
+        ctx.rq_ctx_trace_begin(8)
+        got, gd = act_cache_bytes(ctx, to_dev(xs), M, K)
+        tr = ctx.rq_ctx_trace_end()
+        assert rq.rq_get_device_status() == 0
+        assert tr["quant"][0] == 1
+        want, wd = oracle_act_bytes(xs, M, K)
+        assert gd == wd
+        assert np.array_equal(got, want), (nan, np.flatnonzero(got != want)[:8])
     ctx.close()
 
 
