@@ -345,15 +345,18 @@ act_quant_fused_kernel(const float* __restrict__ x, int64_t n, int64_t n_out,
 
 // ------------------------------------------- one-pass, register variant --
 //
-// For tensors whose float4s fit the register files of one wave (up to
-// 512 threads x 24 float4 per SM: 7.47 M values on 152 SMs, the 2048 x 3584
-// activations included): each thread loads its float4s of x straight into
-// registers (all loads in flight at once, read once: evict_first), takes
-// the maximum as they land, meets the other CTAs at the same grid barrier
-// as act_quant_fused_kernel, and encodes from its registers.  Unlike the
-// shared-memory stash, x is not read from shared memory twice (once for the
-// maximum, once to encode).  CTA i owns float4s [i*per4, (i+1)*per4);
-// thread t of it takes float4s t, t + 512, ...  Same arithmetic as
+// For tensors that fit on chip in one wave: each CTA holds up to 512 x 24
+// float4s of x in its threads' registers (7.47 M values on 152 SMs, the
+// 2048 x 3584 activations included) and up to 220 KB more in shared memory
+// (63 MB in all: the 4096 x 3584 activations).  Each thread loads its
+// float4s straight into registers (all loads in flight at once, read once:
+// evict_first), the rest of the CTA's part arrives by one bulk copy; the
+// maximum is taken as they land, the CTAs meet at the same grid barrier as
+// act_quant_fused_kernel, and each encodes from its registers and shared
+// memory.  The register part is not read from shared memory twice (once for
+// the maximum, once to encode) as the shared-memory stash is.  CTA i owns
+// float4s [i*per4, (i+1)*per4): thread t takes float4s t, t + 512, ... of
+// its first 512 * 24, the bulk copy the rest.  Same arithmetic as
 // absmax_kernel + quant_kernel, so the bytes are identical.
 
 constexpr int kRegThreads = 512;
@@ -364,28 +367,44 @@ act_quant_reg_kernel(const float* __restrict__ x, int64_t n, int64_t n_out, int6
                      uint8_t* __restrict__ out, uint32_t* __restrict__ absmax_out,
                      float* __restrict__ dequant_out, unsigned long long* state,
                      unsigned long long* slots) {
+  extern __shared__ __align__(128) float4 rstash[];
+  __shared__ __align__(8) uint64_t rbar;
   __shared__ uint32_t warp_max[kRegThreads / 32], warp_nf[kRegThreads / 32];
   __shared__ uint32_t absmax_s, nonfinite_s, tag_s;
   const int64_t n4 = n >> 2;
   const int64_t lo = min(n4, (int64_t)blockIdx.x * per4);
-  const int64_t cnt = min(n4, lo + per4) - lo;  // this CTA's float4s, <= kRegThreads * kRegVec
+  const int64_t cnt = min(n4, lo + per4) - lo;  // this CTA's float4s
+  const int64_t rcnt = min(cnt, (int64_t)kRegThreads * kRegVec);  // in registers
+  const int64_t scnt = cnt - rcnt;  // in shared memory, <= kFusedSmemMax / 16
   const float4* x4 = reinterpret_cast<const float4*>(x) + lo;
   const int tid = threadIdx.x;
   const bool last_cta = blockIdx.x == gridDim.x - 1;
 
   pdl_wait();
   pdl_trigger();
+  if (tid == 0 && scnt > 0) {
+    const uint32_t b = smem_u32(&rbar);
+    mbar_init(b, 1);
+    mbar_fence_init();
+    mbar_arrive_expect_tx(b, (uint32_t)(scnt * 16));
+    bulk_g2s_hint(smem_u32(rstash), x4 + rcnt, (uint32_t)(scnt * 16), b, l2_policy_evict_first());
+  }
   if (tid == 32) tag_s = (uint32_t)(ld_relaxed_u64(state) >> 32) + 1u;
   const uint64_t once = l2_policy_evict_first();
   float4 v[kRegVec];
 #pragma unroll
   for (int k = 0; k < kRegVec; ++k) {
     const int64_t i = tid + (int64_t)k * kRegThreads;
-    v[k] = i < cnt ? ldg_f4_policy(x4 + i, once) : make_float4(0.f, 0.f, 0.f, 0.f);
+    v[k] = i < rcnt ? ldg_f4_policy(x4 + i, once) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   float mf = 0.0f, nf = 0.0f;  // the zeros of absent float4s change neither
 #pragma unroll
   for (int k = 0; k < kRegVec; ++k) max4_f(mf, nf, v[k]);
+  __syncthreads();  // the barrier's initialization is visible to every thread
+  if (scnt > 0) {
+    mbar_wait(smem_u32(&rbar), 0, kWaitLimitNs, &g_quant_error);
+    for (int64_t i = tid; i < scnt; i += kRegThreads) max4_f(mf, nf, rstash[i]);
+  }
   if (last_cta)
     for (int64_t i = (n4 << 2) + tid; i < n; i += kRegThreads) {
       const float w = __ldg(x + i);
@@ -406,14 +425,17 @@ act_quant_reg_kernel(const float* __restrict__ x, int64_t n, int64_t n_out, int6
 #pragma unroll
     for (int k = 0; k < kRegVec; ++k) {
       const int64_t i = tid + (int64_t)k * kRegThreads;
-      if (i < cnt) o4[i] = e4m3_scaled4_finite(v[k], s);
+      if (i < rcnt) o4[i] = e4m3_scaled4_finite(v[k], s);
     }
+    for (int64_t i = tid; i < scnt; i += kRegThreads)
+      o4[rcnt + i] = e4m3_scaled4_finite(rstash[i], s);
   } else {
 #pragma unroll
     for (int k = 0; k < kRegVec; ++k) {
       const int64_t i = tid + (int64_t)k * kRegThreads;
-      if (i < cnt) o4[i] = pack4(v[k], s);
+      if (i < rcnt) o4[i] = pack4(v[k], s);
     }
+    for (int64_t i = tid; i < scnt; i += kRegThreads) o4[rcnt + i] = pack4(rstash[i], s);
   }
   if (last_cta)
     for (int64_t i = (n4 << 2) + tid; i < n; i += kRegThreads)
@@ -802,10 +824,25 @@ int64_t fused_stash4(int64_t chunk) {
   return std::min<int64_t>(chunk / 4, kFusedSmemMax / 16);
 }
 
+// The register form of the one-pass kernel takes x when every CTA of one
+// wave of g keeps its part on chip (at least one float4 per thread, at most
+// 512 x 24 in registers plus 220 KB in shared memory); *per4 gets the
+// float4s per CTA.  RQ_QUANT_REG=0 turns it off (tuning).
+bool act_quant_reg_fits(int64_t n, int g, int64_t* per4) {
+  const char* e = std::getenv("RQ_QUANT_REG");
+  if (g <= 0 || (e != nullptr && std::atoi(e) == 0)) return false;
+  const int64_t n4 = n >> 2;
+  *per4 = (n4 + g - 1) / g;
+  return n4 >= (int64_t)g * kRegThreads &&
+         *per4 <= (int64_t)kRegThreads * kRegVec + kFusedSmemMax / 16;
+}
+
 bool act_quant_fused_fits(const float* x, int64_t n, const uint8_t* out) {
   if (n <= 0 || (reinterpret_cast<uintptr_t>(x) & 15) != 0 ||
       (reinterpret_cast<uintptr_t>(out) & 3) != 0)
     return false;
+  int64_t per4 = 0;
+  if (act_quant_reg_fits(n, device_sm_count(), &per4)) return true;
   const int64_t chunk = fused_chunk(n);
   const int64_t grid = (n + chunk - 1) / chunk;
   const int64_t head_bytes = 4 * n - 16 * grid * fused_stash4(chunk);
@@ -824,20 +861,25 @@ rq_status launch_act_quant_fused(const float* x, int64_t n, int64_t n_out,
                                  unsigned long long* slots, int nslots, cudaStream_t st) {
   if (!act_quant_fused_fits(x, n, out)) return RQ_ERR_SHAPE;
   {
-    // x held in registers when it fits one wave of them (at least one
-    // float4 per thread).  Measured on GB300 (graph-replayed): 2048 x 3584
-    // 10.15 -> 9.41 us; the 28-layer stack at 2048 tokens 11.98 -> 11.93 ms
-    // eager, at 512 tokens 4.59 -> 4.54 ms.  RQ_QUANT_REG=0 keeps the
-    // shared-memory stash.
-    const int g = std::min(device_sm_count(), nslots);
-    const int64_t n4 = n >> 2;
-    const int64_t per4 = (n4 + g - 1) / g;
-    const char* reg = std::getenv("RQ_QUANT_REG");
-    if ((reg == nullptr || std::atoi(reg) != 0) && g > 0 && n4 >= (int64_t)g * kRegThreads &&
-        per4 <= (int64_t)kRegThreads * kRegVec) {
+    // x held on chip in registers (and shared memory) when it fits one wave.
+    // Measured on GB300 (graph-replayed): 2048 x 3584 10.3 -> 9.3 us (all
+    // in registers); the 28-layer stack at 2048 tokens 11.98 -> 11.93 ms
+    // eager, at 512 tokens 4.59 -> 4.54 ms.
+    int64_t per4 = 0;
+    if (act_quant_reg_fits(n, std::min(device_sm_count(), nslots), &per4)) {
+      const int64_t s4 = per4 - (int64_t)kRegThreads * kRegVec;
+      const size_t smem = s4 > 0 ? (size_t)s4 * 16 : 0;
+      static bool reg_attr = false;
+      if (!reg_attr) {
+        if (cudaFuncSetAttribute(act_quant_reg_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kFusedSmemMax) != cudaSuccess)
+          return launch_status();
+        reg_attr = true;
+      }
       cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3((unsigned)((n4 + per4 - 1) / per4));
+      cfg.gridDim = dim3((unsigned)(((n >> 2) + per4 - 1) / per4));
       cfg.blockDim = dim3(kRegThreads);
+      cfg.dynamicSmemBytes = smem;
       cfg.stream = st;
       cudaLaunchAttribute attr[2];
       attr[0].id = cudaLaunchAttributeCooperative;

@@ -132,12 +132,14 @@ def oracle_act_bytes(x, M, K):
     return want, od
 
 
-def act_quant_kernels(mode, n):
+def act_quant_kernels(mode, n, reg=True):
     """Kernels the activation cache launches for n elements: the one-cluster
     kernel up to 2^17 elements; the one-pass kernel from 2^20 elements on
-    while what does not fit one wave of shared memory (220 KB per SM) is at
-    most 16 MB (128 MB for tensors of 2^24 elements or more); else the two
-    kernels."""
+    while x fits on chip in one wave (per SM at least 512 and at most
+    512 x 24 float4 in registers plus 220 KB of shared memory; reg=False:
+    RQ_QUANT_REG=0) or what does not fit one wave of shared memory (220 KB
+    per SM) is at most 16 MB (128 MB for tensors of 2^24 elements or more);
+    else the two kernels."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     chunk = max(4096, ((n + sms - 1) // sms + 3) & ~3)
     grid = (n + chunk - 1) // chunk
@@ -145,8 +147,14 @@ def act_quant_kernels(mode, n):
     if mode == "cluster" or (mode == "default" and n <= 1 << 17):
         return 1
     least = {"1": 0, "0": None, "default": 1 << 20}[mode]
+    if least is None or n < least:
+        return 2
+    n4 = n // 4
+    per4 = (n4 + sms - 1) // sms
+    if reg and n4 >= sms * 512 and per4 <= 512 * 24 + 220 * 1024 // 16:
+        return 1
     cap = (128 << 20) if n >= 1 << 24 else (16 << 20)
-    return 1 if least is not None and n >= least and head <= cap else 2
+    return 1 if head <= cap else 2
 
 
 def set_act_quant_mode(monkeypatch, mode):
@@ -225,12 +233,15 @@ def test_activation_cache_infinite_max(rq, monkeypatch, one_pass, M, K):
 
 
 @pytest.mark.parametrize("reg", ["1", "0"])
-@pytest.mark.parametrize("M,K", [(2048, 3584), (611, 1023), (128, 3584), (300, 18944)])
+@pytest.mark.parametrize("M,K", [(2048, 3584), (611, 1023), (128, 3584), (300, 18944),
+                                 (4096, 3584), (512, 18944), (3000, 4101)])
 def test_one_pass_register_and_shared_memory_forms(rq, monkeypatch, reg, M, K):
-    """Tensors that fit one wave of registers take the register form of the
-    one-pass kernel by default, the shared-memory form with RQ_QUANT_REG=0;
-    both give the oracle's bytes, with a NaN in x (fix-up path) and without
-    (all-finite path), n % 4 != 0 included."""
+    """Tensors that fit on chip take the register form of the one-pass
+    kernel by default (all in registers, or registers plus shared memory:
+    4096 x 3584, 512 x 18944, 3000 x 4101), the shared-memory form (or the
+    two kernels) with RQ_QUANT_REG=0; every form gives the oracle's bytes,
+    with a NaN in x (fix-up path) and without (all-finite path), n % 4 != 0
+    included."""
     set_act_quant_mode(monkeypatch, "1")
     monkeypatch.setenv("RQ_QUANT_REG", reg)
     ctx = rq.Context()
@@ -244,7 +255,7 @@ def test_one_pass_register_and_shared_memory_forms(rq, monkeypatch, reg, M, K):
         got, gd = act_cache_bytes(ctx, to_dev(xs), M, K)
         tr = ctx.rq_ctx_trace_end()
         assert rq.rq_get_device_status() == 0
-        assert tr["quant"][0] == 1
+        assert tr["quant"][0] == act_quant_kernels("1", M * K, reg=reg == "1")
         want, wd = oracle_act_bytes(xs, M, K)
         assert gd == wd
         assert np.array_equal(got, want), (nan, np.flatnonzero(got != want)[:8])
