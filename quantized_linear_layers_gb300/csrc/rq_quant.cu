@@ -862,9 +862,10 @@ rq_status launch_act_quant_fused(const float* x, int64_t n, int64_t n_out,
   if (!act_quant_fused_fits(x, n, out)) return RQ_ERR_SHAPE;
   {
     // x held on chip in registers (and shared memory) when it fits one wave.
-    // Measured on GB300 (graph-replayed): 2048 x 3584 10.3 -> 9.3 us (all
-    // in registers); the 28-layer stack at 2048 tokens 11.98 -> 11.93 ms
-    // eager, at 512 tokens 4.59 -> 4.54 ms.
+    // Measured on GB300 (graph-replayed, against the shared-memory form or,
+    // where that does not take x, the two kernels): 2048 x 3584 10.3 -> 9.3
+    // us (all in registers), 4096 x 3584 24.4 -> 15.6 us; the 28-layer stack
+    // at 4096 tokens ~22.1 -> 21.5 ms eager, at 512 tokens 4.57 -> 4.51 ms.
     int64_t per4 = 0;
     if (act_quant_reg_fits(n, std::min(device_sm_count(), nslots), &per4)) {
       const int64_t s4 = per4 - (int64_t)kRegThreads * kRegVec;
