@@ -262,6 +262,32 @@ def test_one_pass_register_and_shared_memory_forms(rq, monkeypatch, reg, M, K):
     ctx.close()
 
 
+@pytest.mark.parametrize("offset", [4, 8])
+def test_one_pass_head_at_16_and_32_byte_alignment(rq, monkeypatch, offset):
+    """A tensor larger than the wave holds (1001 x 18947, n % 4 = 3: a
+    head streamed twice by all CTAs) at an x that is 16-byte but not
+    32-byte aligned (offset 4 floats) and at one that is 32-byte aligned
+    (offset 8): the stash boundaries and the tail fall differently; the
+    oracle's bytes either way."""
+    set_act_quant_mode(monkeypatch, "1")
+    M, K = 1001, 18947
+    ctx = rq.Context()
+    x = synthetic.activation(7400 + offset, M, K, outlier_frac=1e-3)
+    buf = empty((M * K + 8,), torch.float32)
+    assert buf.data_ptr() % 32 == 0
+    xv = buf[offset:offset + M * K]
+    xv.copy_(to_dev(x.ravel()))
+    ctx.rq_ctx_trace_begin(8)
+    got, gd = act_cache_bytes(ctx, xv, M, K)
+    tr = ctx.rq_ctx_trace_end()
+    assert rq.rq_get_device_status() == 0
+    assert tr["quant"][0] == act_quant_kernels("1", M * K)
+    want, wd = oracle_act_bytes(x, M, K)
+    assert gd == wd
+    assert np.array_equal(got, want), np.flatnonzero(got != want)[:8]
+    ctx.close()
+
+
 def test_one_pass_launches_of_different_grids_on_one_context(rq, monkeypatch):
     """One-pass launches in a row on one context with 1, 152, 33, 1, 152 and
     152 CTAs: each publishes its CTAs' maxima and meets at its own grid
