@@ -11,8 +11,9 @@
 //
 // Roles (192 threads, one CTA per SM, persistent over output tiles):
 //   warp 0      TMA producer: 128 x 128 B tiles of W and BN x 128 B tiles of
-//               X (SWIZZLE_128B) into a shared-memory ring (4 stages by
-//               default; RQ_GEMM_STAGES sets another depth for tuning);
+//               X (SWIZZLE_128B) into a shared-memory ring (8 stages by
+//               default, fewer where they do not fit; RQ_GEMM_STAGES sets
+//               another depth for tuning);
 //   warp 1      allocates TMEM, and one thread issues tcgen05.mma
 //               (kind::f8f6f4, E4M3 x E4M3 -> f32, M = 128, N = BN, K = 32)
 //               into one of two TMEM accumulators (2 x BN columns);
@@ -40,7 +41,15 @@ namespace {
 
 constexpr int kBM = 128;               // weight rows per tile (MMA M)
 constexpr int kBK = 128;               // K bytes per stage = one swizzle row
-constexpr int kStages = 4;             // default ring depth, one-CTA and split-K kernels
+constexpr int kStages = 4;             // default ring depth, split-K kernel
+// Default ring depth of the one-CTA kernel (capped by what fits).  Measured
+// on GB300 at 16 tokens (graph-replayed, weights from HBM): the 37888 x 3584
+// gate/up group 26.1 us with 4 stages, 24.3 with 6 to 10.  The split-K
+// kernel keeps 4: 8 stages made its long splits (the 3584 x 18944 down
+// projection) faster alone (16 tokens 16.7 -> 15.9 us) but the 28-layer
+// stack at 32 tokens slower (2.34 -> 2.49 ms per pass), its larger shared
+// memory keeping the next launch from starting beside it.
+constexpr int kStagesSingle = 8;
 constexpr int kMaxStages = 16;
 constexpr int kMaxBN = 256;
 constexpr int kMaxSegs = RQ_MAX_GROUP;  // members of a grouped launch
@@ -1183,7 +1192,7 @@ rq_status launch_fp8_gemm_group(const uint8_t* x_fp8, const float* x_deq,
       return RQ_ERR_CUDA;
     attr_done = true;
   }
-  a.stages = gemm_stages(bn * kBK, kStages, 0);
+  a.stages = gemm_stages(bn * kBK, kStagesSingle, 0);
   const int grid = tiles < sms ? tiles : sms;
   if (std::getenv("RQ_GEMM_LOG") != nullptr)
     std::fprintf(stderr, "rq_gemm: single M=%d N=%d K=%d bn=%d tiles=%d grid=%d stages=%d\n", M,
