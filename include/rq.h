@@ -218,10 +218,12 @@ rq_status rq_fp8_act_cache(rq_ctx *ctx, const float *x, int M, int K,
  *                   then the FP8 GEMM.  Up to 2^17 elements, absmax and
  *                   quantization are one launch of one thread-block
  *                   cluster (x read twice, the second time from L2); from
- *                   2^20 elements on, while what does not fit the shared
- *                   memory of one wave of CTAs (about 220 KB per SM) is at
- *                   most 16 MB, one cooperative kernel (x read once when it
- *                   fits, otherwise only the rest read twice); otherwise
+ *                   2^20 elements on, one cooperative kernel while x fits
+ *                   on chip in one wave of CTAs (per SM 512 x 24 float4
+ *                   in registers plus about 220 KB of shared memory: x
+ *                   read once) or, with x held in shared memory, while
+ *                   what does not fit is at most 16 MB (128 MB from 2^24
+ *                   elements on; only that rest read twice); otherwise
  *                   two kernels, the second reading x backwards (the same
  *                   bytes every way; at ctx creation the environment
  *                   variables RQ_CLUSTER_QUANT_MAX (elements, 0 = never)
